@@ -1,0 +1,69 @@
+"""Oracle of the variant-selection rules -- TEST INFRASTRUCTURE ONLY.
+
+Source [LBG]: "Leveraging Large-Scale Data for Efficient Low-Bit CUTLASS GEMM
+Optimization via Neural Networks" (press summary page).  Section 2: the
+search space is three tile sizes (large, medium, small) times three pipeline
+stage counts (2, 3, 4), nine templates; each (M, N, K) sample of the dataset is
+labelled with the index of the fastest template.  Section 3: the selector's
+inputs are M, N, K and the SM count.  Section 4: the selected template is
+compared with a default template.
+
+Readings where the page is silent:
+  - variant index = 3 * tile + (stages - 2), tile 0 = small, 1 = medium,
+    2 = large; so index 0 is small/2 stages and index 8 is large/4 stages.
+  - the default template (not named on the page) is large tile, 3 stages,
+    index 7.
+  - label: the argmin of the measured times, the lowest index on exact ties.
+  - the library's stored choice adds a no-regression guard: keep the default
+    unless the label beats it by more than ``keep_within`` (2 %).
+  - a shape missing from the table takes the entry of the nearest swept
+    shape of the same bit width and SM count, distance = sum over M, N, K of
+    |log2(x) - log2(x')|, ties to the earlier entry in (M, N, K) order; an
+    empty table gives the default.
+"""
+from __future__ import annotations
+
+import math
+
+NUM_VARIANTS = 9
+TILES = ("small", "medium", "large")
+STAGES = (2, 3, 4)
+DEFAULT_VARIANT = 3 * 2 + (3 - 2)  # large tile, 3 stages
+
+
+def variant_index(tile: int, stages: int) -> int:
+    return 3 * tile + (stages - 2)
+
+
+def variant_of(index: int) -> tuple[int, int]:
+    return index // 3, index % 3 + 2
+
+
+def label(times) -> int:
+    """Index of the fastest variant; lowest index on exact ties (section 2)."""
+    if len(times) != NUM_VARIANTS:
+        raise ValueError("need one time per variant")
+    best = 0
+    for i, t in enumerate(times):
+        if t < times[best]:
+            best = i
+    return best
+
+
+def table_choice(times, default: int = DEFAULT_VARIANT, keep_within: float = 0.02) -> int:
+    """The stored choice: the label, unless the default is within keep_within of it."""
+    lab = label(times)
+    if times[default] <= times[lab] * (1.0 + keep_within):
+        return default
+    return lab
+
+
+def nearest(entries, M: int, N: int, K: int, default: int = DEFAULT_VARIANT) -> int:
+    """Variant for (M, N, K) from a list of ((M', N', K'), variant) entries."""
+    best, best_d = default, None
+    for (m, n, k), v in sorted(entries, key=lambda e: e[0]):
+        d = abs(math.log2(M) - math.log2(m)) + abs(math.log2(N) - math.log2(n)) + \
+            abs(math.log2(K) - math.log2(k))
+        if best_d is None or d < best_d - 1e-12:
+            best, best_d = v, d
+    return best
