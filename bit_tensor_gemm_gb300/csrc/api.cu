@@ -1,0 +1,690 @@
+// api.cu -- the C ABI (include/lbgemm.h): argument checks, variant
+// selection, scratch management, TMA descriptors and kernel dispatch.
+//
+// Method: "Leveraging Large-Scale Data for Efficient Low-Bit CUTLASS GEMM
+// Optimization via Neural Networks" (press summary page).  Intro and section 3:
+// the selector maps (M, N, K, SM count) to one of the templates at run time;
+// section 2: nine templates (three tile sizes x 2/3/4 stages), each dataset
+// sample labelled with its fastest one; section 4: comparison with a default
+// template.  Here the selector is a table filled by a timing sweep on the
+// device itself, with a nearest-shape fallback.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <string>
+#include <tuple>
+#include <vector>
+
+#include "lbgemm.h"
+#include "simt.h"
+#include "tc_params.h"
+
+// Device status word: kernels OR error bits into it (see lbgemm_device_status).
+__device__ int g_lbgemm_status_word;
+
+namespace {
+
+using lbg::TcKernel;
+using lbg::TcParams;
+
+constexpr int kNumVariants = 9;
+constexpr int kDefaultVariant = 7;  // large tile, 3 stages
+constexpr int kMaxDevices = 64;
+constexpr int kSkinnyMaxM = 16;
+constexpr int kGroupM = 8;
+
+thread_local std::string t_last_error;
+std::atomic<int64_t> g_launches{0};
+std::atomic<int> g_chunk_s8{512};
+std::atomic<int> g_chunk_s4{2048};
+
+lbgemm_status fail(lbgemm_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  t_last_error = buf;
+  return st;
+}
+
+lbgemm_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(LBGEMM_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+// ---- per-device state ------------------------------------------------------------
+
+struct Scratch {
+  void* ptr = nullptr;
+  size_t bytes = 0;
+  cudaEvent_t done = nullptr;  // recorded after the last use
+  bool used = false;
+};
+
+struct DeviceState {
+  bool ready = false;
+  bool supported = false;
+  int sm_count = 0;
+  int* status = nullptr;
+  Scratch ws;           // operand re-encoding scratch
+  Scratch host_stage;   // device staging for lbgemm_run_host
+  std::map<const void*, int> occupancy;
+};
+
+std::mutex g_mu;     // device state
+std::mutex g_ws_mu;  // the internal re-encoding scratch
+DeviceState g_dev[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+lbgemm_status device_state(DeviceState** out) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(LBGEMM_ERR_UNSUPPORTED, "device %d", dev);
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState& d = g_dev[dev];
+  if (!d.ready) {
+    int major = 0, minor = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev);
+    d.supported = (major == 10 && minor == 3);
+    if (d.supported) {
+      e = cudaGetSymbolAddress(reinterpret_cast<void**>(&d.status), g_lbgemm_status_word);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(status word)");
+      if (!g_encode) {
+        cudaDriverEntryPointQueryResult q;
+        void* fn = nullptr;
+        e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                             cudaEnableDefault, &q);
+        if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
+          return fail(LBGEMM_ERR_CUDA, "cuTensorMapEncodeTiled entry point not found");
+        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+      }
+    }
+    d.ready = true;
+  }
+  if (!d.supported)
+    return fail(LBGEMM_ERR_UNSUPPORTED, "device %d is not an sm_103 GPU (this library is built "
+                "for sm_103a only)", dev);
+  *out = &d;
+  return LBGEMM_OK;
+}
+
+// Grows `s` to at least `bytes` (synchronising the device when it must
+// reallocate) and orders this use after the previous one on another stream.
+lbgemm_status scratch_acquire(Scratch& s, size_t bytes, cudaStream_t stream) {
+  if (s.bytes < bytes) {
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize (scratch growth)");
+    if (s.ptr) cudaFree(s.ptr);
+    s.ptr = nullptr;
+    s.bytes = 0;
+    size_t want = std::max<size_t>(bytes, size_t(1) << 20);
+    e = cudaMalloc(&s.ptr, want);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc (scratch)");
+    s.bytes = want;
+    s.used = false;
+  }
+  if (!s.done) {
+    cudaError_t e = cudaEventCreateWithFlags(&s.done, cudaEventDisableTiming);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaEventCreate");
+  }
+  if (s.used) {
+    cudaError_t e = cudaStreamWaitEvent(stream, s.done, 0);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamWaitEvent");
+  }
+  return LBGEMM_OK;
+}
+
+lbgemm_status scratch_release(Scratch& s, cudaStream_t stream) {
+  cudaError_t e = cudaEventRecord(s.done, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+  s.used = true;
+  return LBGEMM_OK;
+}
+
+// ---- shapes, checks, variants ----------------------------------------------------------
+
+int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+lbgemm_status check_gemm_args(int bits, int64_t M, int64_t N, int64_t K, const void* A,
+                              const void* B, const void* C) {
+  if (bits != 8 && bits != 4 && bits != 1)
+    return fail(LBGEMM_ERR_INVALID_ARG, "bits must be 8, 4 or 1 (got %d)", bits);
+  if (M < 0 || N < 0) return fail(LBGEMM_ERR_INVALID_ARG, "negative M or N");
+  if (K < 1) return fail(LBGEMM_ERR_INVALID_ARG, "K must be >= 1");
+  if (M > INT32_MAX || N > INT32_MAX)
+    return fail(LBGEMM_ERR_INVALID_ARG, "M and N must be below 2^31");
+  const int64_t kmax = bits == 8 ? 131071 : bits == 4 ? (int64_t(1) << 25) - 1 : INT32_MAX - 1;
+  if (K > kmax)
+    return fail(LBGEMM_ERR_INVALID_ARG, "K=%lld can overflow int32 for %d-bit operands (max %lld)",
+                (long long)K, bits, (long long)kmax);
+  if (bits == 4 && K % 2) return fail(LBGEMM_ERR_ALIGNMENT, "4-bit rows need an even K");
+  if (bits == 1 && K % 32) return fail(LBGEMM_ERR_ALIGNMENT, "1-bit rows need K %% 32 == 0");
+  if (M == 0 || N == 0) return LBGEMM_OK;
+  if (!A || !B || !C) return fail(LBGEMM_ERR_INVALID_ARG, "null operand pointer");
+  if (!aligned16(A) || !aligned16(B) || !aligned16(C))
+    return fail(LBGEMM_ERR_ALIGNMENT, "operand pointers must be 16-byte aligned");
+  return LBGEMM_OK;
+}
+
+TcKernel tc_kernel(int variant, bool f8, bool linear) {
+  const int tile = variant / 3, stages = variant % 3 + 2;
+  switch (tile) {
+    case 0: return lbg::tc_kernel_small(stages, f8, linear);
+    case 1: return lbg::tc_kernel_medium(stages, f8, linear);
+    default: return lbg::tc_kernel_large(stages, f8, linear);
+  }
+}
+
+// Padded K of the re-encoded operands (row strides stay multiples of 16 bytes).
+int64_t enc_kp(int bits, int64_t K) { return bits == 8 ? round_up(K, 8) : round_up(K, 16); }
+
+size_t enc_bytes(int bits, int64_t rows, int64_t K) {
+  const int64_t kp = enc_kp(bits, K);
+  return (size_t)round_up(rows * kp * (bits == 8 ? 2 : 1), 256);
+}
+
+bool skinny_ok(int64_t M, int64_t K, const void* A, const void* B) {
+  return M <= kSkinnyMaxM && K % 16 == 0 && aligned16(A) && aligned16(B);
+}
+
+// ---- selection table --------------------------------------------------------------------
+
+using Key = std::tuple<int, int, int64_t, int64_t, int64_t>;  // sm, bits, M, N, K
+std::mutex g_table_mu;
+std::map<Key, int> g_table;
+
+int table_select(int sm, int bits, int64_t M, int64_t N, int64_t K) {
+  std::lock_guard<std::mutex> lock(g_table_mu);
+  auto it = g_table.find(Key{sm, bits, M, N, K});
+  if (it != g_table.end()) return it->second;
+  int best = kDefaultVariant;
+  double best_d = 0;
+  bool have = false;
+  const double lm = std::log2((double)std::max<int64_t>(M, 1));
+  const double ln = std::log2((double)std::max<int64_t>(N, 1));
+  const double lk = std::log2((double)std::max<int64_t>(K, 1));
+  for (auto lo = g_table.lower_bound(Key{sm, bits, 0, 0, 0}); lo != g_table.end(); ++lo) {
+    if (std::get<0>(lo->first) != sm || std::get<1>(lo->first) != bits) break;
+    const double d = std::fabs(lm - std::log2((double)std::get<2>(lo->first))) +
+                     std::fabs(ln - std::log2((double)std::get<3>(lo->first))) +
+                     std::fabs(lk - std::log2((double)std::get<4>(lo->first)));
+    if (!have || d < best_d - 1e-12) {
+      best = lo->second;
+      best_d = d;
+      have = true;
+    }
+  }
+  return best;
+}
+
+// ---- TMA descriptors -----------------------------------------------------------------------
+
+lbgemm_status encode_kmajor(CUtensorMap* map, const void* base, int64_t rows, int64_t kp,
+                            bool f16, int box_rows) {
+  const int esize = f16 ? 2 : 1;
+  cuuint64_t dims[2] = {(cuuint64_t)kp, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)(kp * esize)};
+  cuuint32_t box[2] = {(cuuint32_t)(128 / esize), (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(map, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8,
+                        2, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(LBGEMM_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return LBGEMM_OK;
+}
+
+int occupancy(DeviceState& d, const TcKernel& k) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  auto it = d.occupancy.find(k.func);
+  if (it != d.occupancy.end()) return it->second;
+  cudaFuncSetAttribute(k.func, cudaFuncAttributeMaxDynamicSharedMemorySize, k.smem);
+  int occ = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k.func, 320, k.smem) != cudaSuccess)
+    occ = 1;
+  occ = std::max(1, std::min(occ, 512 / k.tmem_cols));
+  d.occupancy[k.func] = occ;
+  return occ;
+}
+
+// ---- the tensor-core path (bits 8 and 4, and the linear layer) --------------------------------
+
+lbgemm_status run_tc(DeviceState& d, int bits, int64_t M, int64_t N, int64_t K, const void* A,
+                     const void* B, int32_t* C, const float* sx, const float* sw, void* Y,
+                     int variant, void* ws, cudaStream_t stream) {
+  const bool f8 = bits == 4;
+  const bool linear = Y != nullptr;
+  TcKernel k = tc_kernel(variant, f8, linear);
+  if (!k.launch) return fail(LBGEMM_ERR_UNSUPPORTED, "no kernel for variant %d", variant);
+  const int64_t kp = enc_kp(bits, K);
+  uint8_t* encA = static_cast<uint8_t*>(ws);
+  uint8_t* encB = encA + enc_bytes(bits, M, K);
+  cudaError_t e;
+  if (!f8) {
+    e = lbg::launch_cvt_s8_f16(static_cast<const int8_t*>(A), M, K, encA, kp, d.sm_count, stream);
+    if (e == cudaSuccess)
+      e = lbg::launch_cvt_s8_f16(static_cast<const int8_t*>(B), N, K, encB, kp, d.sm_count, stream);
+  } else {
+    e = lbg::launch_cvt_s4_e4m3(static_cast<const uint8_t*>(A), M, K, encA, kp, d.sm_count,
+                                stream);
+    if (e == cudaSuccess)
+      e = lbg::launch_cvt_s4_e4m3(static_cast<const uint8_t*>(B), N, K, encB, kp, d.sm_count,
+                                  stream);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "operand re-encoding launch");
+  CUtensorMap ma, mb;
+  lbgemm_status st = encode_kmajor(&ma, encA, M, kp, !f8, 128);
+  if (st != LBGEMM_OK) return st;
+  st = encode_kmajor(&mb, encB, N, kp, !f8, k.tile_n);
+  if (st != LBGEMM_OK) return st;
+
+  TcParams p{};
+  p.M = (int)M;
+  p.N = (int)N;
+  p.K = (int)K;
+  const int bk = f8 ? 128 : 64;
+  p.num_kb = (int)((kp + bk - 1) / bk);
+  const int chunk_elems = f8 ? g_chunk_s4.load() : g_chunk_s8.load();
+  p.chunk_kb = std::max(1, chunk_elems / bk);
+  p.tiles_m = (int)((M + 127) / 128);
+  p.tiles_n = (int)((N + k.tile_n - 1) / k.tile_n);
+  p.num_tiles = p.tiles_m * p.tiles_n;
+  p.group_m = kGroupM;
+  p.C = C;
+  p.sx = sx;
+  p.sw = sw;
+  p.Y = static_cast<__nv_bfloat16*>(Y);
+  p.status = d.status;
+  if (linear)
+    p.vec_ok = (N % 8 == 0) && aligned16(Y);
+  else
+    p.vec_ok = (N % 4 == 0) && aligned16(C);
+  const int grid = (int)std::min<int64_t>(p.num_tiles, (int64_t)d.sm_count * occupancy(d, k));
+  e = k.launch(&ma, &mb, &p, grid, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "tensor-core GEMM launch");
+  g_launches += 3;
+  return LBGEMM_OK;
+}
+
+lbgemm_status run_any(int bits, int64_t M, int64_t N, int64_t K, const void* A, const void* B,
+                      int32_t* C, int variant, void* ws, size_t ws_bytes, bool internal_ws,
+                      cudaStream_t stream) {
+  lbgemm_status st = check_gemm_args(bits, M, N, K, A, B, C);
+  if (st != LBGEMM_OK) return st;
+  if (variant < -1 || variant >= kNumVariants)
+    return fail(LBGEMM_ERR_INVALID_ARG, "variant %d out of range", variant);
+  if (M == 0 || N == 0) return LBGEMM_OK;
+  DeviceState* d = nullptr;
+  st = device_state(&d);
+  if (st != LBGEMM_OK) return st;
+  const bool auto_pick = variant < 0;
+  if (auto_pick) variant = table_select(d->sm_count, bits, M, N, K);
+  cudaError_t e;
+  if (bits == 1) {
+    e = lbg::launch_b1_popc(variant / 3, variant % 3 + 2, static_cast<const uint32_t*>(A),
+                            static_cast<const uint32_t*>(B), M, N, K, C, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "1-bit GEMM launch");
+    g_launches += 1;
+    return LBGEMM_OK;
+  }
+  if (bits == 8 && auto_pick && skinny_ok(M, K, A, B)) {
+    e = lbg::launch_skinny_s8(static_cast<const int8_t*>(A), static_cast<const int8_t*>(B), (int)M,
+                              (int)N, (int)K, C, nullptr, nullptr, nullptr, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "skinny GEMM launch");
+    g_launches += 1;
+    return LBGEMM_OK;
+  }
+  const size_t need = enc_bytes(bits, M, K) + enc_bytes(bits, N, K);
+  if (!internal_ws) {
+    if (!ws || ws_bytes < need)
+      return fail(LBGEMM_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need, ws_bytes);
+    if ((reinterpret_cast<uintptr_t>(ws) & 255) != 0)
+      return fail(LBGEMM_ERR_ALIGNMENT, "workspace must be 256-byte aligned");
+    return run_tc(*d, bits, M, N, K, A, B, C, nullptr, nullptr, nullptr, variant, ws, stream);
+  }
+  std::lock_guard<std::mutex> lock(g_ws_mu);
+  st = scratch_acquire(d->ws, need, stream);
+  if (st != LBGEMM_OK) return st;
+  st = run_tc(*d, bits, M, N, K, A, B, C, nullptr, nullptr, nullptr, variant, d->ws.ptr, stream);
+  lbgemm_status st2 = scratch_release(d->ws, stream);
+  return st != LBGEMM_OK ? st : st2;
+}
+
+lbgemm_status run_linear(int64_t M, int64_t N, int64_t K, const int8_t* X, const float* sx,
+                         const int8_t* W, const float* sw, void* Y, int variant,
+                         cudaStream_t stream) {
+  lbgemm_status st = check_gemm_args(8, M, N, K, X, W, Y);
+  if (st != LBGEMM_OK) return st;
+  if (variant < -1 || variant >= kNumVariants)
+    return fail(LBGEMM_ERR_INVALID_ARG, "variant %d out of range", variant);
+  if (M == 0 || N == 0) return LBGEMM_OK;
+  if (!sx || !sw) return fail(LBGEMM_ERR_INVALID_ARG, "null scale pointer");
+  DeviceState* d = nullptr;
+  st = device_state(&d);
+  if (st != LBGEMM_OK) return st;
+  const bool auto_pick = variant < 0;
+  if (auto_pick && skinny_ok(M, K, X, W)) {
+    cudaError_t e = lbg::launch_skinny_s8(X, W, (int)M, (int)N, (int)K, nullptr, sx, sw, Y, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "skinny linear launch");
+    g_launches += 1;
+    return LBGEMM_OK;
+  }
+  if (auto_pick) variant = table_select(d->sm_count, 8, M, N, K);
+  std::lock_guard<std::mutex> lock(g_ws_mu);
+  const size_t need = enc_bytes(8, M, K) + enc_bytes(8, N, K);
+  st = scratch_acquire(d->ws, need, stream);
+  if (st != LBGEMM_OK) return st;
+  st = run_tc(*d, 8, M, N, K, X, W, nullptr, sx, sw, Y, variant, d->ws.ptr, stream);
+  lbgemm_status st2 = scratch_release(d->ws, stream);
+  return st != LBGEMM_OK ? st : st2;
+}
+
+cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
+
+}  // namespace
+
+// =============================================================================================
+extern "C" {
+
+int lbgemm_num_variants(void) { return kNumVariants; }
+int lbgemm_default_variant(void) { return kDefaultVariant; }
+
+lbgemm_status lbgemm_variant_info(int bits, int variant, int* tile_m, int* tile_n, int* tile_k,
+                                  int* stages) {
+  if ((bits != 8 && bits != 4 && bits != 1) || variant < 0 || variant >= kNumVariants)
+    return fail(LBGEMM_ERR_INVALID_ARG, "unknown bits/variant");
+  const int tile = variant / 3;
+  int bm, bn, bk;
+  if (bits == 1) {
+    lbg::b1_tile_shape(tile, &bm, &bn);
+    bk = 32 * 32;
+  } else {
+    bm = 128;
+    bn = 64 << tile;
+    bk = bits == 8 ? 64 : 128;
+  }
+  if (tile_m) *tile_m = bm;
+  if (tile_n) *tile_n = bn;
+  if (tile_k) *tile_k = bk;
+  if (stages) *stages = variant % 3 + 2;
+  return LBGEMM_OK;
+}
+
+lbgemm_status lbgemm_run(int bits, int64_t M, int64_t N, int64_t K, const void* A, const void* B,
+                         int32_t* C, void* stream) {
+  try {
+    return run_any(bits, M, N, K, A, B, C, -1, nullptr, 0, true, as_stream(stream));
+  } catch (...) {
+    return fail(LBGEMM_ERR_CUDA, "internal error");
+  }
+}
+
+lbgemm_status lbgemm_run_variant(int bits, int64_t M, int64_t N, int64_t K, const void* A,
+                                 const void* B, int32_t* C, int variant, void* stream) {
+  try {
+    return run_any(bits, M, N, K, A, B, C, variant, nullptr, 0, true, as_stream(stream));
+  } catch (...) {
+    return fail(LBGEMM_ERR_CUDA, "internal error");
+  }
+}
+
+size_t lbgemm_workspace_size(int bits, int64_t M, int64_t N, int64_t K) {
+  if ((bits != 8 && bits != 4) || M <= 0 || N <= 0 || K <= 0) return 0;
+  return enc_bytes(bits, M, K) + enc_bytes(bits, N, K);
+}
+
+lbgemm_status lbgemm_run_ws(int bits, int64_t M, int64_t N, int64_t K, const void* A,
+                            const void* B, int32_t* C, int variant, void* workspace,
+                            size_t workspace_bytes, void* stream) {
+  try {
+    return run_any(bits, M, N, K, A, B, C, variant, workspace, workspace_bytes, false,
+                   as_stream(stream));
+  } catch (...) {
+    return fail(LBGEMM_ERR_CUDA, "internal error");
+  }
+}
+
+lbgemm_status lbgemm_linear(int64_t M, int64_t N, int64_t K, const int8_t* X, const float* sx,
+                            const int8_t* W, const float* sw, void* Y, void* stream) {
+  try {
+    return run_linear(M, N, K, X, sx, W, sw, Y, -1, as_stream(stream));
+  } catch (...) {
+    return fail(LBGEMM_ERR_CUDA, "internal error");
+  }
+}
+
+lbgemm_status lbgemm_linear_variant(int64_t M, int64_t N, int64_t K, const int8_t* X,
+                                    const float* sx, const int8_t* W, const float* sw, void* Y,
+                                    int variant, void* stream) {
+  try {
+    return run_linear(M, N, K, X, sx, W, sw, Y, variant, as_stream(stream));
+  } catch (...) {
+    return fail(LBGEMM_ERR_CUDA, "internal error");
+  }
+}
+
+int lbgemm_select_for(int sm_count, int bits, int64_t M, int64_t N, int64_t K) {
+  if ((bits != 8 && bits != 4 && bits != 1) || M < 1 || N < 1 || K < 1) return -1;
+  return table_select(sm_count, bits, M, N, K);
+}
+
+int lbgemm_select(int bits, int64_t M, int64_t N, int64_t K) {
+  DeviceState* d = nullptr;
+  if (device_state(&d) != LBGEMM_OK) return -1;
+  return lbgemm_select_for(d->sm_count, bits, M, N, K);
+}
+
+lbgemm_status lbgemm_table_set_for(int sm_count, int bits, int64_t M, int64_t N, int64_t K,
+                                   int variant) {
+  if ((bits != 8 && bits != 4 && bits != 1) || M < 1 || N < 1 || K < 1 || sm_count < 1 ||
+      variant < 0 || variant >= kNumVariants)
+    return fail(LBGEMM_ERR_INVALID_ARG, "bad table entry");
+  std::lock_guard<std::mutex> lock(g_table_mu);
+  g_table[Key{sm_count, bits, M, N, K}] = variant;
+  return LBGEMM_OK;
+}
+
+lbgemm_status lbgemm_table_set(int bits, int64_t M, int64_t N, int64_t K, int variant) {
+  DeviceState* d = nullptr;
+  lbgemm_status st = device_state(&d);
+  if (st != LBGEMM_OK) return st;
+  return lbgemm_table_set_for(d->sm_count, bits, M, N, K, variant);
+}
+
+lbgemm_status lbgemm_table_clear(void) {
+  std::lock_guard<std::mutex> lock(g_table_mu);
+  g_table.clear();
+  return LBGEMM_OK;
+}
+
+int64_t lbgemm_table_size(void) {
+  std::lock_guard<std::mutex> lock(g_table_mu);
+  return (int64_t)g_table.size();
+}
+
+lbgemm_status lbgemm_table_load(const char* path) {
+  if (!path) return fail(LBGEMM_ERR_INVALID_ARG, "null path");
+  FILE* f = fopen(path, "r");
+  if (!f) return fail(LBGEMM_ERR_INVALID_ARG, "cannot open %s", path);
+  std::vector<std::pair<Key, int>> rows;
+  char line[256];
+  int lineno = 0;
+  while (fgets(line, sizeof line, f)) {
+    ++lineno;
+    const char* s = line;
+    while (*s == ' ' || *s == '\t') ++s;
+    if (*s == '#' || *s == '\n' || *s == '\0') continue;
+    int sm, bits, v;
+    long long M, N, K;
+    if (sscanf(s, "%d %d %lld %lld %lld %d", &sm, &bits, &M, &N, &K, &v) != 6 || sm < 1 ||
+        (bits != 8 && bits != 4 && bits != 1) || M < 1 || N < 1 || K < 1 || v < 0 ||
+        v >= kNumVariants) {
+      fclose(f);
+      return fail(LBGEMM_ERR_INVALID_ARG, "%s:%d: malformed table line", path, lineno);
+    }
+    rows.push_back({Key{sm, bits, M, N, K}, v});
+  }
+  fclose(f);
+  std::lock_guard<std::mutex> lock(g_table_mu);
+  for (auto& r : rows) g_table[r.first] = r.second;
+  return LBGEMM_OK;
+}
+
+lbgemm_status lbgemm_table_save(const char* path) {
+  if (!path) return fail(LBGEMM_ERR_INVALID_ARG, "null path");
+  FILE* f = fopen(path, "w");
+  if (!f) return fail(LBGEMM_ERR_INVALID_ARG, "cannot write %s", path);
+  fprintf(f, "# sm_count bits M N K variant\n");
+  {
+    std::lock_guard<std::mutex> lock(g_table_mu);
+    for (auto& kv : g_table)
+      fprintf(f, "%d %d %lld %lld %lld %d\n", std::get<0>(kv.first), std::get<1>(kv.first),
+              (long long)std::get<2>(kv.first), (long long)std::get<3>(kv.first),
+              (long long)std::get<4>(kv.first), kv.second);
+  }
+  fclose(f);
+  return LBGEMM_OK;
+}
+
+int lbgemm_choose(const float* times, int default_variant, float keep_within) {
+  if (!times || default_variant < 0 || default_variant >= kNumVariants || keep_within < 0)
+    return -1;
+  int best = 0;
+  for (int i = 0; i < kNumVariants; ++i) {
+    if (!(times[i] >= 0)) return -1;  // rejects NaN and negatives
+    if (times[i] < times[best]) best = i;
+  }
+  if (times[default_variant] <= times[best] * (1.0f + keep_within)) return default_variant;
+  return best;
+}
+
+lbgemm_status lbgemm_time_variants(int bits, int64_t M, int64_t N, int64_t K, const void* A,
+                                   const void* B, int32_t* C, int warmup, int reps, float* times,
+                                   void* stream) {
+  if (!times || reps < 1 || warmup < 0) return fail(LBGEMM_ERR_INVALID_ARG, "bad timing args");
+  cudaStream_t s = as_stream(stream);
+  cudaEvent_t e0, e1;
+  if (cudaEventCreate(&e0) != cudaSuccess || cudaEventCreate(&e1) != cudaSuccess)
+    return fail(LBGEMM_ERR_CUDA, "cudaEventCreate");
+  lbgemm_status st = LBGEMM_OK;
+  std::vector<float> samples(reps);
+  for (int v = 0; v < kNumVariants && st == LBGEMM_OK; ++v) {
+    for (int w = 0; w < warmup && st == LBGEMM_OK; ++w)
+      st = lbgemm_run_variant(bits, M, N, K, A, B, C, v, stream);
+    for (int r = 0; r < reps && st == LBGEMM_OK; ++r) {
+      cudaEventRecord(e0, s);
+      st = lbgemm_run_variant(bits, M, N, K, A, B, C, v, stream);
+      cudaEventRecord(e1, s);
+      if (st != LBGEMM_OK) break;
+      cudaError_t e = cudaEventSynchronize(e1);
+      if (e != cudaSuccess) {
+        st = cuda_fail(e, "timing");
+        break;
+      }
+      cudaEventElapsedTime(&samples[r], e0, e1);
+    }
+    if (st == LBGEMM_OK) {
+      std::sort(samples.begin(), samples.end());
+      times[v] = samples[reps / 2];
+    }
+  }
+  cudaEventDestroy(e0);
+  cudaEventDestroy(e1);
+  return st;
+}
+
+lbgemm_status lbgemm_run_host(int bits, int64_t M, int64_t N, int64_t K, const void* A_host,
+                              const void* B_host, int32_t* C_host, int variant, void* stream) {
+  try {
+    lbgemm_status st = check_gemm_args(bits, M, N, K, A_host, B_host, C_host);
+    if (st != LBGEMM_OK) return st;
+    if (M == 0 || N == 0) return LBGEMM_OK;
+    DeviceState* d = nullptr;
+    st = device_state(&d);
+    if (st != LBGEMM_OK) return st;
+    cudaStream_t s = as_stream(stream);
+    const int64_t row_bytes = bits == 8 ? K : bits == 4 ? K / 2 : K / 8;
+    const size_t a_bytes = (size_t)round_up(M * row_bytes, 256);
+    const size_t b_bytes = (size_t)round_up(N * row_bytes, 256);
+    const size_t c_bytes = (size_t)(M * N * 4);
+    static std::mutex host_mu;
+    std::lock_guard<std::mutex> lock(host_mu);
+    st = scratch_acquire(d->host_stage, a_bytes + b_bytes + round_up(c_bytes, 256), s);
+    if (st != LBGEMM_OK) return st;
+    uint8_t* dA = static_cast<uint8_t*>(d->host_stage.ptr);
+    uint8_t* dB = dA + a_bytes;
+    int32_t* dC = reinterpret_cast<int32_t*>(dB + b_bytes);
+    cudaError_t e = cudaMemcpyAsync(dA, A_host, (size_t)(M * row_bytes), cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(dB, B_host, (size_t)(N * row_bytes), cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return cuda_fail(e, "host-to-device copy");
+    st = run_any(bits, M, N, K, dA, dB, dC, variant, nullptr, 0, true, s);
+    if (st != LBGEMM_OK) return st;
+    e = cudaMemcpyAsync(C_host, dC, c_bytes, cudaMemcpyDeviceToHost, s);
+    if (e != cudaSuccess) return cuda_fail(e, "device-to-host copy");
+    st = scratch_release(d->host_stage, s);
+    if (st != LBGEMM_OK) return st;
+    e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    return LBGEMM_OK;
+  } catch (...) {
+    return fail(LBGEMM_ERR_CUDA, "internal error");
+  }
+}
+
+lbgemm_status lbgemm_set_exact_chunk(int bits, int k_elems) {
+  if (bits == 8) {
+    if (k_elems < 64 || k_elems > 1024 || k_elems % 64)
+      return fail(LBGEMM_ERR_INVALID_ARG, "8-bit chunk must be a multiple of 64 in [64, 1024]");
+    g_chunk_s8 = k_elems;
+    return LBGEMM_OK;
+  }
+  if (bits == 4) {
+    if (k_elems < 128 || k_elems > 262144 || k_elems % 128)
+      return fail(LBGEMM_ERR_INVALID_ARG, "4-bit chunk must be a multiple of 128 in [128, 262144]");
+    g_chunk_s4 = k_elems;
+    return LBGEMM_OK;
+  }
+  return fail(LBGEMM_ERR_INVALID_ARG, "exact chunks exist for bits 8 and 4 only");
+}
+
+int lbgemm_get_exact_chunk(int bits) {
+  return bits == 8 ? g_chunk_s8.load() : bits == 4 ? g_chunk_s4.load() : -1;
+}
+
+lbgemm_status lbgemm_device_status(void* stream) {
+  DeviceState* d = nullptr;
+  lbgemm_status st = device_state(&d);
+  if (st != LBGEMM_OK) return st;
+  cudaError_t e = cudaStreamSynchronize(as_stream(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  int word = 0;
+  e = cudaMemcpy(&word, d->status, sizeof word, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the status word");
+  if (word != 0) {
+    const int zero = 0;
+    cudaMemcpy(d->status, &zero, sizeof zero, cudaMemcpyHostToDevice);
+    return fail(LBGEMM_ERR_TIMEOUT, "a device-side wait ran out of time (status %d)", word);
+  }
+  return LBGEMM_OK;
+}
+
+const char* lbgemm_last_error(void) { return t_last_error.c_str(); }
+
+int64_t lbgemm_launch_count(void) { return g_launches.load(); }
+
+}  // extern "C"

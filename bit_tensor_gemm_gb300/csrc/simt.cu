@@ -1,0 +1,399 @@
+// simt.cu -- the CUDA-core kernels of the library:
+//   * exact operand re-encoding for the tensor-core path (int8 -> fp16,
+//     packed int4 -> e4m3), HBM-bound streaming passes;
+//   * the skinny 8-bit GEMM (M <= 16) on dp4a, which streams B once from HBM
+//     instead of re-encoding it;
+//   * the 1-bit GEMM on XOR + popcount.
+//
+// Method: "Leveraging Large-Scale Data for Efficient Low-Bit CUTLASS GEMM
+// Optimization via Neural Networks" (press summary page), intro (1-, 4-,
+// 8-bit GEMM) and section 1 (tiles of C looping over K with a multi-stage
+// load pipeline).
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "simt.h"
+
+namespace lbg {
+
+// ---------------------------------------------------------------------------
+// int8 -> fp16, rows of K values into rows of Kp >= K halves (zero padded).
+// Each thread writes 8 halves (16 bytes).
+__global__ void cvt_s8_f16_kernel(const int8_t* __restrict__ in, int64_t rows, int64_t K,
+                                  __half* __restrict__ out, int64_t Kp, int fast) {
+  const int64_t vec_per_row = Kp / 8;
+  const int64_t total = rows * vec_per_row;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = i / vec_per_row;
+    const int64_t c = (i - r * vec_per_row) * 8;
+    const int8_t* src = in + r * K + c;
+    __align__(16) __half h[8];
+    if (fast && c + 8 <= K) {
+      const uint2 w = __ldg(reinterpret_cast<const uint2*>(src));
+      const uint32_t lo = w.x, hi = w.y;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        h[j] = __short2half_rn((short)(int8_t)(lo >> (8 * j)));
+        h[4 + j] = __short2half_rn((short)(int8_t)(hi >> (8 * j)));
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) h[j] = __short2half_rn(c + j < K ? (short)src[j] : (short)0);
+    }
+    *reinterpret_cast<uint4*>(out + r * Kp + c) = *reinterpret_cast<const uint4*>(h);
+  }
+}
+
+// packed int4 (two per byte, low nibble first) -> e4m3 bytes, rows of K
+// values into rows of Kp >= K bytes (zero padded).  K is even.  Each thread
+// writes 16 output bytes from 8 input bytes through a 256-entry table
+// (byte -> two e4m3 codes) built per block with CUDA's fp8 conversion.
+__global__ void cvt_s4_e4m3_kernel(const uint8_t* __restrict__ in, int64_t rows, int64_t K,
+                                   uint8_t* __restrict__ out, int64_t Kp, int fast) {
+  __shared__ uint16_t table[256];
+  for (int b = threadIdx.x; b < 256; b += blockDim.x) {
+    const int lo = (b & 15) >= 8 ? (b & 15) - 16 : (b & 15);
+    const int hi = (b >> 4) >= 8 ? (b >> 4) - 16 : (b >> 4);
+    const uint16_t elo = __nv_cvt_float_to_fp8((float)lo, __NV_SATFINITE, __NV_E4M3);
+    const uint16_t ehi = __nv_cvt_float_to_fp8((float)hi, __NV_SATFINITE, __NV_E4M3);
+    table[b] = (uint16_t)(elo | (ehi << 8));
+  }
+  __syncthreads();
+  const int64_t in_row = K / 2;
+  const int64_t vec_per_row = Kp / 16;
+  const int64_t total = rows * vec_per_row;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = i / vec_per_row;
+    const int64_t cb = (i - r * vec_per_row) * 8;  // input byte column
+    const uint8_t* src = in + r * in_row + cb;
+    uint32_t o[4];
+    if (fast && cb + 8 <= in_row) {
+      const uint2 w = __ldg(reinterpret_cast<const uint2*>(src));
+      o[0] = table[w.x & 0xFF] | ((uint32_t)table[(w.x >> 8) & 0xFF] << 16);
+      o[1] = table[(w.x >> 16) & 0xFF] | ((uint32_t)table[w.x >> 24] << 16);
+      o[2] = table[w.y & 0xFF] | ((uint32_t)table[(w.y >> 8) & 0xFF] << 16);
+      o[3] = table[(w.y >> 16) & 0xFF] | ((uint32_t)table[w.y >> 24] << 16);
+    } else {
+      uint16_t t[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) t[j] = cb + j < in_row ? table[src[j]] : (uint16_t)0;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) o[j] = t[2 * j] | ((uint32_t)t[2 * j + 1] << 16);
+    }
+    *reinterpret_cast<uint4*>(out + r * Kp + 2 * cb) = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Skinny 8-bit GEMM: M <= MT rows of A against all N rows of B.  Each warp
+// owns kSkNR consecutive rows of B and streams them once (16 bytes per lane
+// per step); A rows come through L1.  Partial sums are combined across the
+// warp by a halving butterfly so that each lane ends with its own outputs.
+constexpr int kSkNR = 4;
+constexpr int kSkWarps = 8;
+
+template <int MT, bool LINEAR>
+__global__ void __launch_bounds__(kSkWarps * 32)
+    skinny_s8_kernel(const int8_t* __restrict__ A, const int8_t* __restrict__ B, int M, int N,
+                     int K, int32_t* __restrict__ C, const float* __restrict__ sx,
+                     const float* __restrict__ sw, __nv_bfloat16* __restrict__ Y) {
+  constexpr int NV = MT * kSkNR;
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int n0 = (blockIdx.x * kSkWarps + warp) * kSkNR;
+  if (n0 >= N) return;
+  int acc[NV];
+#pragma unroll
+  for (int i = 0; i < NV; ++i) acc[i] = 0;
+  const int4 zero = make_int4(0, 0, 0, 0);
+  for (int k = lane * 16; k < K; k += 32 * 16) {
+    int4 b[kSkNR];
+#pragma unroll
+    for (int r = 0; r < kSkNR; ++r)
+      b[r] = (n0 + r < N) ? __ldg(reinterpret_cast<const int4*>(B + (int64_t)(n0 + r) * K + k))
+                          : zero;
+#pragma unroll
+    for (int m = 0; m < MT; ++m) {
+      const int4 a = (m < M) ? __ldg(reinterpret_cast<const int4*>(A + (int64_t)m * K + k)) : zero;
+#pragma unroll
+      for (int r = 0; r < kSkNR; ++r) {
+        int s = acc[m * kSkNR + r];
+        s = __dp4a(a.x, b[r].x, s);
+        s = __dp4a(a.y, b[r].y, s);
+        s = __dp4a(a.z, b[r].z, s);
+        s = __dp4a(a.w, b[r].w, s);
+        acc[m * kSkNR + r] = s;
+      }
+    }
+  }
+  // Halving butterfly: at each step a lane keeps half of its values (upper
+  // half if the step's lane bit is set) plus its partner's copy of that half.
+  int n = NV;
+  int idx_base = 0;
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) {
+    if (n > 1) {
+      const bool upper = (lane & off) != 0;
+      const int h = n / 2;
+#pragma unroll
+      for (int i = 0; i < NV / 2; ++i) {
+        if (i < h) {
+          const int send = upper ? acc[i] : acc[i + h];
+          const int keep = upper ? acc[i + h] : acc[i];
+          acc[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+        }
+      }
+      if (upper) idx_base += h;
+      n = h;
+    } else {
+      acc[0] += __shfl_xor_sync(0xffffffffu, acc[0], off);
+    }
+  }
+  // Lanes that share idx_base hold the same totals; the lowest one writes.
+  // n values remain per lane: indices idx_base .. idx_base + n - 1.
+  const int owner_mask = (NV >= 32) ? 0 : (32 / NV) - 1;  // low lane bits summed out
+  if ((lane & owner_mask) == 0) {
+#pragma unroll
+    for (int j = 0; j < (NV >= 32 ? NV / 32 : 1); ++j) {
+      const int idx = idx_base + j;
+      const int m = idx / kSkNR, r = idx % kSkNR;
+      if (m < M && n0 + r < N) {
+        if (LINEAR)
+          Y[(int64_t)m * N + n0 + r] = __float2bfloat16_rn((float)acc[j] * sx[m] * sw[n0 + r]);
+        else
+          C[(int64_t)m * N + n0 + r] = acc[j];
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// 1-bit GEMM on CUDA cores: C[m][n] = K - 2 * sum_w popc(A[m][w] ^ B[n][w]).
+// CTA tile BM x BN, 256 threads as a 16 x 16 grid, thread (ty, tx) owning rows
+// ty + 16 i and columns tx + 16 j; K staged 32 words at a time through a
+// STAGES-deep cp.async ring.  Out-of-range rows and words are zero in both
+// operands, so they add no differing bits.
+constexpr int kB1KW = 32;            // words per stage
+constexpr int kB1Stride = kB1KW + 4;  // padded smem row (16-byte aligned)
+
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, int bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src, int bytes) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+template <int ROWS, bool VEC>
+__device__ __forceinline__ void b1_load_tile(uint32_t* dst, const uint32_t* src, int64_t rows,
+                                             int64_t W, int64_t r0, int64_t w0) {
+  const uint32_t base = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
+  if (VEC) {
+    constexpr int kChunks = ROWS * kB1KW / 4;
+    for (int i = threadIdx.x; i < kChunks; i += 256) {
+      const int r = i / (kB1KW / 4), c = (i % (kB1KW / 4)) * 4;
+      const int64_t gr = r0 + r, gw = w0 + c;
+      const bool ok = gr < rows && gw < W;
+      const uint32_t* g = ok ? src + gr * W + gw : src;
+      cp_async_16(base + (r * kB1Stride + c) * 4, g, ok ? 16 : 0);
+    }
+  } else {
+    constexpr int kWords = ROWS * kB1KW;
+    for (int i = threadIdx.x; i < kWords; i += 256) {
+      const int r = i / kB1KW, c = i % kB1KW;
+      const int64_t gr = r0 + r, gw = w0 + c;
+      const bool ok = gr < rows && gw < W;
+      const uint32_t* g = ok ? src + gr * W + gw : src;
+      cp_async_4(base + (r * kB1Stride + c) * 4, g, ok ? 4 : 0);
+    }
+  }
+}
+
+template <int BM, int BN, int STAGES, bool VEC>
+__global__ void __launch_bounds__(256)
+    b1_popc_kernel(const uint32_t* __restrict__ A, const uint32_t* __restrict__ B, int64_t M,
+                   int64_t N, int64_t K, int32_t* __restrict__ C) {
+  constexpr int TM = BM / 16, TN = BN / 16;
+  extern __shared__ __align__(16) uint32_t b1_smem[];
+  uint32_t* sA = b1_smem;
+  uint32_t* sB = b1_smem + STAGES * BM * kB1Stride;
+  const int64_t W = K / 32;
+  const int64_t m0 = (int64_t)blockIdx.y * BM, n0 = (int64_t)blockIdx.x * BN;
+  const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
+  const int64_t num_kt = (W + kB1KW - 1) / kB1KW;
+
+  int acc[TM][TN];
+#pragma unroll
+  for (int i = 0; i < TM; ++i)
+#pragma unroll
+    for (int j = 0; j < TN; ++j) acc[i][j] = 0;
+
+#pragma unroll
+  for (int s = 0; s < STAGES - 1; ++s) {
+    if (s < num_kt) {
+      b1_load_tile<BM, VEC>(sA + s * BM * kB1Stride, A, M, W, m0, s * kB1KW);
+      b1_load_tile<BN, VEC>(sB + s * BN * kB1Stride, B, N, W, n0, s * kB1KW);
+    }
+    cp_async_commit();
+  }
+  for (int64_t kt = 0; kt < num_kt; ++kt) {
+    cp_async_wait<STAGES - 2>();
+    __syncthreads();
+    {  // prefetch the stage STAGES-1 ahead into the slot freed last iteration
+      const int64_t nk = kt + STAGES - 1;
+      const int slot = (int)(nk % STAGES);
+      if (nk < num_kt) {
+        b1_load_tile<BM, VEC>(sA + slot * BM * kB1Stride, A, M, W, m0, nk * kB1KW);
+        b1_load_tile<BN, VEC>(sB + slot * BN * kB1Stride, B, N, W, n0, nk * kB1KW);
+      }
+      cp_async_commit();
+    }
+    const int slot = (int)(kt % STAGES);
+    const uint32_t* a_s = sA + slot * BM * kB1Stride;
+    const uint32_t* b_s = sB + slot * BN * kB1Stride;
+#pragma unroll 2
+    for (int w = 0; w < kB1KW; w += 4) {
+      uint4 a[TM], b[TN];
+#pragma unroll
+      for (int i = 0; i < TM; ++i)
+        a[i] = *reinterpret_cast<const uint4*>(a_s + (ty + 16 * i) * kB1Stride + w);
+#pragma unroll
+      for (int j = 0; j < TN; ++j)
+        b[j] = *reinterpret_cast<const uint4*>(b_s + (tx + 16 * j) * kB1Stride + w);
+#pragma unroll
+      for (int i = 0; i < TM; ++i)
+#pragma unroll
+        for (int j = 0; j < TN; ++j)
+          acc[i][j] += __popc(a[i].x ^ b[j].x) + __popc(a[i].y ^ b[j].y) +
+                       __popc(a[i].z ^ b[j].z) + __popc(a[i].w ^ b[j].w);
+    }
+  }
+  cp_async_wait<0>();
+#pragma unroll
+  for (int i = 0; i < TM; ++i) {
+    const int64_t m = m0 + ty + 16 * i;
+    if (m >= M) continue;
+#pragma unroll
+    for (int j = 0; j < TN; ++j) {
+      const int64_t n = n0 + tx + 16 * j;
+      if (n < N) C[m * N + n] = (int32_t)(K - 2 * (int64_t)acc[i][j]);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// host launchers
+
+static int grid_for(int64_t work, int threads, int sm_count) {
+  int64_t blocks = (work + threads - 1) / threads;
+  const int64_t cap = (int64_t)sm_count * 16;
+  if (blocks > cap) blocks = cap;
+  return (int)(blocks < 1 ? 1 : blocks);
+}
+
+cudaError_t launch_cvt_s8_f16(const int8_t* in, int64_t rows, int64_t K, void* out, int64_t Kp,
+                              int sm_count, cudaStream_t s) {
+  if (rows == 0) return cudaSuccess;
+  const int fast = (K % 8 == 0) && ((reinterpret_cast<uintptr_t>(in) & 7) == 0);
+  const int64_t work = rows * (Kp / 8);
+  cvt_s8_f16_kernel<<<grid_for(work, 256, sm_count), 256, 0, s>>>(
+      in, rows, K, static_cast<__half*>(out), Kp, fast);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_cvt_s4_e4m3(const uint8_t* in, int64_t rows, int64_t K, void* out, int64_t Kp,
+                               int sm_count, cudaStream_t s) {
+  if (rows == 0) return cudaSuccess;
+  const int fast = ((K / 2) % 8 == 0) && ((reinterpret_cast<uintptr_t>(in) & 7) == 0);
+  const int64_t work = rows * (Kp / 16);
+  cvt_s4_e4m3_kernel<<<grid_for(work, 256, sm_count), 256, 0, s>>>(
+      in, rows, K, static_cast<uint8_t*>(out), Kp, fast);
+  return cudaGetLastError();
+}
+
+template <int MT, bool LINEAR>
+static cudaError_t skinny_go(const int8_t* A, const int8_t* B, int M, int N, int K, int32_t* C,
+                             const float* sx, const float* sw, void* Y, cudaStream_t s) {
+  const int rows_per_block = kSkWarps * kSkNR;
+  const int grid = (N + rows_per_block - 1) / rows_per_block;
+  skinny_s8_kernel<MT, LINEAR><<<grid, kSkWarps * 32, 0, s>>>(
+      A, B, M, N, K, C, sx, sw, static_cast<__nv_bfloat16*>(Y));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_skinny_s8(const int8_t* A, const int8_t* B, int M, int N, int K, int32_t* C,
+                             const float* sx, const float* sw, void* Y, cudaStream_t s) {
+  const bool lin = Y != nullptr;
+  if (M <= 1) return lin ? skinny_go<1, true>(A, B, M, N, K, C, sx, sw, Y, s)
+                         : skinny_go<1, false>(A, B, M, N, K, C, sx, sw, Y, s);
+  if (M <= 2) return lin ? skinny_go<2, true>(A, B, M, N, K, C, sx, sw, Y, s)
+                         : skinny_go<2, false>(A, B, M, N, K, C, sx, sw, Y, s);
+  if (M <= 4) return lin ? skinny_go<4, true>(A, B, M, N, K, C, sx, sw, Y, s)
+                         : skinny_go<4, false>(A, B, M, N, K, C, sx, sw, Y, s);
+  if (M <= 8) return lin ? skinny_go<8, true>(A, B, M, N, K, C, sx, sw, Y, s)
+                         : skinny_go<8, false>(A, B, M, N, K, C, sx, sw, Y, s);
+  return lin ? skinny_go<16, true>(A, B, M, N, K, C, sx, sw, Y, s)
+             : skinny_go<16, false>(A, B, M, N, K, C, sx, sw, Y, s);
+}
+
+template <int BM, int BN, int STAGES>
+static cudaError_t b1_go(const uint32_t* A, const uint32_t* B, int64_t M, int64_t N, int64_t K,
+                         int32_t* C, cudaStream_t s) {
+  const int smem = STAGES * (BM + BN) * kB1Stride * 4;
+  const bool vec = ((K / 32) % 4 == 0) && ((reinterpret_cast<uintptr_t>(A) & 15) == 0) &&
+                   ((reinterpret_cast<uintptr_t>(B) & 15) == 0);
+  const dim3 grid((unsigned)((N + BN - 1) / BN), (unsigned)((M + BM - 1) / BM));
+  if (vec) {
+    auto k = b1_popc_kernel<BM, BN, STAGES, true>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    k<<<grid, 256, smem, s>>>(A, B, M, N, K, C);
+  } else {
+    auto k = b1_popc_kernel<BM, BN, STAGES, false>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    k<<<grid, 256, smem, s>>>(A, B, M, N, K, C);
+  }
+  return cudaGetLastError();
+}
+
+template <int BM, int BN>
+static cudaError_t b1_stages(int stages, const uint32_t* A, const uint32_t* B, int64_t M,
+                             int64_t N, int64_t K, int32_t* C, cudaStream_t s) {
+  switch (stages) {
+    case 2: return b1_go<BM, BN, 2>(A, B, M, N, K, C, s);
+    case 3: return b1_go<BM, BN, 3>(A, B, M, N, K, C, s);
+    default: return b1_go<BM, BN, 4>(A, B, M, N, K, C, s);
+  }
+}
+
+cudaError_t launch_b1_popc(int tile, int stages, const uint32_t* A, const uint32_t* B, int64_t M,
+                           int64_t N, int64_t K, int32_t* C, cudaStream_t s) {
+  if (M == 0 || N == 0) return cudaSuccess;
+  switch (tile) {
+    case 0: return b1_stages<64, 64>(stages, A, B, M, N, K, C, s);
+    case 1: return b1_stages<128, 64>(stages, A, B, M, N, K, C, s);
+    default: return b1_stages<128, 128>(stages, A, B, M, N, K, C, s);
+  }
+}
+
+void b1_tile_shape(int tile, int* bm, int* bn) {
+  *bm = tile == 0 ? 64 : 128;
+  *bn = tile == 2 ? 128 : 64;
+}
+
+}  // namespace lbg

@@ -1,0 +1,24 @@
+// simt.h -- launchers of the CUDA-core kernels (simt.cu).
+#pragma once
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+namespace lbg {
+
+// int8 rows of K -> fp16 rows of Kp (Kp % 8 == 0, Kp >= K), zero padded.
+cudaError_t launch_cvt_s8_f16(const int8_t* in, int64_t rows, int64_t K, void* out, int64_t Kp,
+                              int sm_count, cudaStream_t s);
+// packed int4 rows of K (K even) -> e4m3 rows of Kp (Kp % 16 == 0), zero padded.
+cudaError_t launch_cvt_s4_e4m3(const uint8_t* in, int64_t rows, int64_t K, void* out,
+                               int64_t Kp, int sm_count, cudaStream_t s);
+// M <= 16, K % 16 == 0, A and B 16-byte aligned.  Y != nullptr selects the
+// linear epilogue (bf16 Y with scales sx, sw) instead of int32 C.
+cudaError_t launch_skinny_s8(const int8_t* A, const int8_t* B, int M, int N, int K, int32_t* C,
+                             const float* sx, const float* sw, void* Y, cudaStream_t s);
+// 1-bit GEMM, tile class 0..2 and 2..4 stages; K % 32 == 0.
+cudaError_t launch_b1_popc(int tile, int stages, const uint32_t* A, const uint32_t* B, int64_t M,
+                           int64_t N, int64_t K, int32_t* C, cudaStream_t s);
+void b1_tile_shape(int tile, int* bm, int* bn);
+
+}  // namespace lbg

@@ -1,0 +1,23 @@
+// tc_large.cu -- instantiations of the tensor-core GEMM for the large tile
+// class (128 x 256 outputs per tile), stage counts 2, 3 and 4.
+#include "tc_gemm.cuh"
+
+namespace lbg {
+
+template <int S>
+static TcKernel pick(bool f8, bool linear) {
+  if (linear) return tc_kernel_entry<256, S, false, true>();
+  return f8 ? tc_kernel_entry<256, S, true, false>() : tc_kernel_entry<256, S, false, false>();
+}
+
+TcKernel tc_kernel_large(int stages, bool f8, bool linear) {
+  if (linear && f8) return TcKernel{};
+  switch (stages) {
+    case 2: return pick<2>(f8, linear);
+    case 3: return pick<3>(f8, linear);
+    case 4: return pick<4>(f8, linear);
+    default: return TcKernel{};
+  }
+}
+
+}  // namespace lbg

@@ -1,0 +1,51 @@
+// tc_params.h -- launch parameters and the registry of tensor-core kernel
+// instantiations (one per tile class x stage count x operand kind x epilogue).
+#pragma once
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+namespace lbg {
+
+struct TcParams {
+  int M, N, K;
+  int num_kb;    // 128-byte K slices per tile row
+  int chunk_kb;  // slices per exact fp32 accumulation chunk
+  int tiles_m, tiles_n, num_tiles, group_m;
+  int vec_ok;    // 16-byte vector stores are aligned for every row
+  int32_t* C;
+  const float* sx;
+  const float* sw;
+  __nv_bfloat16* Y;
+  int* status;
+};
+
+typedef cudaError_t (*TcLaunchFn)(const CUtensorMap*, const CUtensorMap*, const TcParams*, int,
+                                  cudaStream_t);
+
+struct TcKernel {
+  TcLaunchFn launch = nullptr;
+  const void* func = nullptr;
+  int smem = 0;
+  int tmem_cols = 0;
+  int tile_n = 0;
+  int stages = 0;
+};
+
+// Dynamic shared memory to request so that the CTAs that fit on one SM by
+// shared memory never need more than the 512 TMEM columns of that SM.
+inline constexpr int tc_smem_request(int used, int tmem_cols) {
+  constexpr int kSmPerSm = 233472;  // 228 KB shared memory per SM
+  const int max_ctas = 512 / tmem_cols;
+  const int min_req = kSmPerSm / (max_ctas + 1) + 1;  // one more CTA cannot fit
+  return used > min_req ? used : min_req;
+}
+
+// tile: 0 small (128 x 64), 1 medium (128 x 128), 2 large (128 x 256).
+TcKernel tc_kernel_small(int stages, bool f8, bool linear);
+TcKernel tc_kernel_medium(int stages, bool f8, bool linear);
+TcKernel tc_kernel_large(int stages, bool f8, bool linear);
+
+}  // namespace lbg

@@ -1,0 +1,239 @@
+"""Python binding of the C ABI in ``include/lbgemm.h`` (argument marshalling only).
+
+Every function has the name of its C entry point.  Pointer arguments accept a
+plain integer address or any object with ``data_ptr()`` (a torch tensor);
+``stream`` accepts an integer handle, an object with ``cuda_stream`` (a
+torch.cuda.Stream), or None for torch's current stream when torch is loaded
+(else the legacy default stream).  A non-OK status raises ``LbgemmError``
+with the library's message.  There is no fallback: if the compiled library
+is missing, the first call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIBRARY = os.path.join(_HERE, "lib", "liblbgemm.so")
+
+OK = 0
+ERR_INVALID_ARG = 1
+ERR_ALIGNMENT = 2
+ERR_UNSUPPORTED = 3
+ERR_CUDA = 4
+ERR_TIMEOUT = 5
+ERR_WORKSPACE = 6
+STATUS_NAMES = {0: "OK", 1: "INVALID_ARG", 2: "ALIGNMENT", 3: "UNSUPPORTED", 4: "CUDA",
+                5: "TIMEOUT", 6: "WORKSPACE"}
+
+
+class LbgemmError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"lbgemm {STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+_i64, _i32, _vp, _f32 = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_float
+_SIGNATURES = {
+    "lbgemm_num_variants": (_i32, []),
+    "lbgemm_default_variant": (_i32, []),
+    "lbgemm_variant_info": (_i32, [_i32, _i32, _vp, _vp, _vp, _vp]),
+    "lbgemm_run": (_i32, [_i32, _i64, _i64, _i64, _vp, _vp, _vp, _vp]),
+    "lbgemm_run_variant": (_i32, [_i32, _i64, _i64, _i64, _vp, _vp, _vp, _i32, _vp]),
+    "lbgemm_workspace_size": (ctypes.c_size_t, [_i32, _i64, _i64, _i64]),
+    "lbgemm_run_ws": (_i32, [_i32, _i64, _i64, _i64, _vp, _vp, _vp, _i32, _vp, ctypes.c_size_t,
+                             _vp]),
+    "lbgemm_linear": (_i32, [_i64, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _vp]),
+    "lbgemm_linear_variant": (_i32, [_i64, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _i32, _vp]),
+    "lbgemm_select": (_i32, [_i32, _i64, _i64, _i64]),
+    "lbgemm_table_set": (_i32, [_i32, _i64, _i64, _i64, _i32]),
+    "lbgemm_select_for": (_i32, [_i32, _i32, _i64, _i64, _i64]),
+    "lbgemm_table_set_for": (_i32, [_i32, _i32, _i64, _i64, _i64, _i32]),
+    "lbgemm_table_clear": (_i32, []),
+    "lbgemm_table_size": (_i64, []),
+    "lbgemm_table_load": (_i32, [ctypes.c_char_p]),
+    "lbgemm_table_save": (_i32, [ctypes.c_char_p]),
+    "lbgemm_choose": (_i32, [_vp, _i32, _f32]),
+    "lbgemm_time_variants": (_i32, [_i32, _i64, _i64, _i64, _vp, _vp, _vp, _i32, _i32, _vp, _vp]),
+    "lbgemm_run_host": (_i32, [_i32, _i64, _i64, _i64, _vp, _vp, _vp, _i32, _vp]),
+    "lbgemm_set_exact_chunk": (_i32, [_i32, _i32]),
+    "lbgemm_get_exact_chunk": (_i32, [_i32]),
+    "lbgemm_device_status": (_i32, [_vp]),
+    "lbgemm_last_error": (ctypes.c_char_p, []),
+    "lbgemm_launch_count": (_i64, []),
+}
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load(path: str | None = None):
+    """Open the compiled library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None or path is not None:
+            p = path or LIBRARY
+            if not os.path.exists(p):
+                raise RuntimeError(
+                    f"{p} is missing: build it first (python -c 'import __graft_entry__ as g; "
+                    "g.build()' or python bit_tensor_gemm_gb300/build.py)")
+            lib = ctypes.CDLL(p)
+            for name, (res, args) in _SIGNATURES.items():
+                f = getattr(lib, name)
+                f.restype = res
+                f.argtypes = args
+            if path is not None:
+                return lib
+            _lib = lib
+    return _lib
+
+
+def exported_symbols():
+    return sorted(_SIGNATURES)
+
+
+def _addr(x) -> int | None:
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    if hasattr(x, "data_ptr"):
+        return x.data_ptr()
+    if hasattr(x, "ctypes"):  # numpy array (host memory)
+        return x.ctypes.data
+    raise TypeError(f"cannot take the address of {type(x).__name__}")
+
+
+def _stream(s) -> int | None:
+    if s is None:
+        try:
+            import torch  # noqa: PLC0415
+            if torch.cuda.is_available() and torch.cuda.is_initialized():
+                return torch.cuda.current_stream().cuda_stream
+        except ImportError:
+            pass
+        return None
+    if isinstance(s, int):
+        return s
+    if hasattr(s, "cuda_stream"):
+        return s.cuda_stream
+    raise TypeError(f"not a stream: {type(s).__name__}")
+
+
+def _check(status: int) -> None:
+    if status != OK:
+        raise LbgemmError(status, (load().lbgemm_last_error() or b"").decode())
+
+
+# ---- entry points -------------------------------------------------------------
+
+def lbgemm_num_variants() -> int:
+    return load().lbgemm_num_variants()
+
+
+def lbgemm_default_variant() -> int:
+    return load().lbgemm_default_variant()
+
+
+def lbgemm_variant_info(bits: int, variant: int) -> dict:
+    vals = [ctypes.c_int() for _ in range(4)]
+    _check(load().lbgemm_variant_info(bits, variant, *[ctypes.addressof(v) for v in vals]))
+    return dict(zip(("tile_m", "tile_n", "tile_k", "stages"), (v.value for v in vals)))
+
+
+def lbgemm_run(bits, M, N, K, A, B, C, stream=None) -> None:
+    _check(load().lbgemm_run(bits, M, N, K, _addr(A), _addr(B), _addr(C), _stream(stream)))
+
+
+def lbgemm_run_variant(bits, M, N, K, A, B, C, variant, stream=None) -> None:
+    _check(load().lbgemm_run_variant(bits, M, N, K, _addr(A), _addr(B), _addr(C), variant,
+                                     _stream(stream)))
+
+
+def lbgemm_workspace_size(bits, M, N, K) -> int:
+    return load().lbgemm_workspace_size(bits, M, N, K)
+
+
+def lbgemm_run_ws(bits, M, N, K, A, B, C, variant, workspace, workspace_bytes, stream=None):
+    _check(load().lbgemm_run_ws(bits, M, N, K, _addr(A), _addr(B), _addr(C), variant,
+                                _addr(workspace), workspace_bytes, _stream(stream)))
+
+
+def lbgemm_linear(M, N, K, X, sx, W, sw, Y, stream=None) -> None:
+    _check(load().lbgemm_linear(M, N, K, _addr(X), _addr(sx), _addr(W), _addr(sw), _addr(Y),
+                                _stream(stream)))
+
+
+def lbgemm_linear_variant(M, N, K, X, sx, W, sw, Y, variant, stream=None) -> None:
+    _check(load().lbgemm_linear_variant(M, N, K, _addr(X), _addr(sx), _addr(W), _addr(sw),
+                                        _addr(Y), variant, _stream(stream)))
+
+
+def lbgemm_select(bits, M, N, K) -> int:
+    return load().lbgemm_select(bits, M, N, K)
+
+
+def lbgemm_select_for(sm_count, bits, M, N, K) -> int:
+    return load().lbgemm_select_for(sm_count, bits, M, N, K)
+
+
+def lbgemm_table_set(bits, M, N, K, variant) -> None:
+    _check(load().lbgemm_table_set(bits, M, N, K, variant))
+
+
+def lbgemm_table_set_for(sm_count, bits, M, N, K, variant) -> None:
+    _check(load().lbgemm_table_set_for(sm_count, bits, M, N, K, variant))
+
+
+def lbgemm_table_clear() -> None:
+    _check(load().lbgemm_table_clear())
+
+
+def lbgemm_table_size() -> int:
+    return load().lbgemm_table_size()
+
+
+def lbgemm_table_load(path: str) -> None:
+    _check(load().lbgemm_table_load(os.fsencode(path)))
+
+
+def lbgemm_table_save(path: str) -> None:
+    _check(load().lbgemm_table_save(os.fsencode(path)))
+
+
+def lbgemm_choose(times, default_variant: int = 7, keep_within: float = 0.02) -> int:
+    arr = (ctypes.c_float * 9)(*[float(t) for t in times])
+    return load().lbgemm_choose(ctypes.addressof(arr), default_variant, keep_within)
+
+
+def lbgemm_time_variants(bits, M, N, K, A, B, C, warmup=2, reps=5, stream=None) -> list:
+    arr = (ctypes.c_float * 9)()
+    _check(load().lbgemm_time_variants(bits, M, N, K, _addr(A), _addr(B), _addr(C), warmup, reps,
+                                       ctypes.addressof(arr), _stream(stream)))
+    return list(arr)
+
+
+def lbgemm_run_host(bits, M, N, K, A_host, B_host, C_host, variant=-1, stream=None) -> None:
+    _check(load().lbgemm_run_host(bits, M, N, K, _addr(A_host), _addr(B_host), _addr(C_host),
+                                  variant, _stream(stream)))
+
+
+def lbgemm_set_exact_chunk(bits: int, k_elems: int) -> None:
+    _check(load().lbgemm_set_exact_chunk(bits, k_elems))
+
+
+def lbgemm_get_exact_chunk(bits: int) -> int:
+    return load().lbgemm_get_exact_chunk(bits)
+
+
+def lbgemm_device_status(stream=None) -> None:
+    _check(load().lbgemm_device_status(_stream(stream)))
+
+
+def lbgemm_last_error() -> str:
+    return (load().lbgemm_last_error() or b"").decode()
+
+
+def lbgemm_launch_count() -> int:
+    return load().lbgemm_launch_count()

@@ -1,0 +1,179 @@
+/*
+ * lbgemm.h -- C ABI of the low-bit integer GEMM library for GB300 (sm_103a).
+ *
+ * Method source, cited below as [LBG]: "Leveraging Large-Scale Data for
+ * Efficient Low-Bit CUTLASS GEMM Optimization via Neural Networks", IEEE
+ * Transactions on Big Data (press summary page).
+ *   intro      : GEMM on 1-, 4- and 8-bit operands; a selector picks the
+ *                kernel template per (M, N, K, SM count) at run time.
+ *   section 1  : C = A x B is split into uniform thread-block tiles, each
+ *                looping over K; tile shape and pipeline stage count are the
+ *                two tuning parameters.
+ *   section 2  : nine templates = {small, medium, large} tile x {2, 3, 4}
+ *                stages; each sample is labelled with its fastest template.
+ *   section 4  : the selected template is compared with a default template,
+ *                for a GEMM and for a linear layer.
+ *
+ * Conventions shared by every entry point
+ *   - Operands: A is M x K, B is N x K, both K-major with dense rows;
+ *     C[m][n] = sum_k A[m][k] * B[n][k] (C = A . B^T), C is M x N row-major
+ *     int32.  K counts logical elements (bits when bits == 1).
+ *   - Element formats by `bits`:
+ *       8 : int8, rows of K bytes, full range [-128, 127].
+ *       4 : signed nibbles, two per byte, element 2j in the low nibble of
+ *           byte j; rows of K/2 bytes; value = (nibble ^ 8) - 8.
+ *       1 : +-1 values, 32 per uint32 word, element k = bit k%32 of word
+ *           k/32, bit 1 = +1, bit 0 = -1; rows of K/32 words;
+ *           C[m][n] = K - 2 * popcount(A[m] XOR B[n]).
+ *   - Pointers: A, B, C (and X, W, sx, sw, Y, workspace) are DEVICE pointers
+ *     of the current CUDA device, owned by the caller, 16-byte aligned.  The
+ *     library keeps no reference to them after the call returns.
+ *   - `stream` is a cudaStream_t passed as void*; NULL is the legacy default
+ *     stream.  Every compute call is asynchronous on that stream.
+ *   - Errors: argument errors are detected on the host and returned before
+ *     anything is launched.  A launch failure returns LBGEMM_ERR_CUDA.  A
+ *     device-side wait that exceeds its time limit (about 2 s) makes the
+ *     kernel stop and sets a device status word that lbgemm_device_status()
+ *     reports.  lbgemm_last_error() gives a message for the last failure on
+ *     the calling thread.
+ *   - Shape limits: M, N >= 0 (0 is a no-op), K >= 1; the result must fit
+ *     int32: K <= 131071 for bits 8, K <= 2^25 - 1 for bits 4, K < 2^31 for
+ *     bits 1.  Alignment: K % 2 == 0 for bits 4 and K % 32 == 0 for bits 1
+ *     (rows must hold whole bytes / words); any K for bits 8.
+ */
+#ifndef LBGEMM_H
+#define LBGEMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  LBGEMM_OK = 0,
+  LBGEMM_ERR_INVALID_ARG = 1, /* null pointer, bad bits, negative size, K out of range  */
+  LBGEMM_ERR_ALIGNMENT = 2,   /* K not a whole number of bytes/words, pointer not 16-B aligned */
+  LBGEMM_ERR_UNSUPPORTED = 3, /* no sm_103a device current, or variant not available     */
+  LBGEMM_ERR_CUDA = 4,        /* a CUDA runtime or driver call failed                      */
+  LBGEMM_ERR_TIMEOUT = 5,     /* a device-side wait ran out (reported by lbgemm_device_status) */
+  LBGEMM_ERR_WORKSPACE = 6    /* caller-supplied workspace smaller than lbgemm_workspace_size */
+} lbgemm_status;
+
+/* Number of tile x stage variants (9) and the index of the default one.
+ * Variant v has tile class v / 3 (0 small, 1 medium, 2 large) and v % 3 + 2
+ * pipeline stages.  [LBG] section 2; the default (large, 3 stages = 7) is
+ * this library's reading of the unnamed "default template" of section 4. */
+int lbgemm_num_variants(void);
+int lbgemm_default_variant(void);
+
+/* Tile shape and stage count of variant v for operands of `bits`
+ * (tile_m x tile_n output tile, tile_k logical elements per pipeline stage).
+ * Returns LBGEMM_ERR_INVALID_ARG for an unknown v or bits. */
+lbgemm_status lbgemm_variant_info(int bits, int variant, int* tile_m, int* tile_n, int* tile_k,
+                                  int* stages);
+
+/* C = A . B^T with the variant the selection table picks for
+ * (bits, M, N, K, SM count).  [LBG] intro, sections 1-2.  Scratch memory
+ * (bits 8 and 4 convert their operands to an exact tensor-core encoding) is
+ * taken from a per-device buffer the library grows with cudaMalloc on demand;
+ * calls from different streams are ordered on it with events.  A call that
+ * grows the buffer synchronises the device, so make the first call of the
+ * largest shape before capturing a CUDA graph, or use lbgemm_run_ws. */
+lbgemm_status lbgemm_run(int bits, int64_t M, int64_t N, int64_t K, const void* A, const void* B,
+                         int32_t* C, void* stream);
+
+/* As lbgemm_run, forcing variant v (0..8); -1 means "use the table". */
+lbgemm_status lbgemm_run_variant(int bits, int64_t M, int64_t N, int64_t K, const void* A,
+                                 const void* B, int32_t* C, int variant, void* stream);
+
+/* Bytes of scratch that lbgemm_run_ws needs for this problem (0 if none). */
+size_t lbgemm_workspace_size(int bits, int64_t M, int64_t N, int64_t K);
+
+/* As lbgemm_run_variant, with caller-owned scratch: `workspace` is a device
+ * buffer of at least lbgemm_workspace_size() bytes, 256-byte aligned, not
+ * used by any other call in flight.  This entry point allocates nothing. */
+lbgemm_status lbgemm_run_ws(int bits, int64_t M, int64_t N, int64_t K, const void* A,
+                            const void* B, int32_t* C, int variant, void* workspace,
+                            size_t workspace_bytes, void* stream);
+
+/* Quantised linear layer, [LBG] section 4 (a linear layer on the low-bit
+ * GEMM): Y[m][n] = bf16_round_nearest_even( (float)acc[m][n] * sx[m] * sw[n] )
+ * with acc = X . W^T exact in int32.  X: int8 M x K (per-token scale sx, fp32
+ * [M]); W: int8 N x K (per-output-channel scale sw, fp32 [N]); Y: bf16 M x N
+ * row-major, passed as void* (2 bytes per element).  The scale product is
+ * formed in fp32, left to right.  K <= 131071. */
+lbgemm_status lbgemm_linear(int64_t M, int64_t N, int64_t K, const int8_t* X, const float* sx,
+                            const int8_t* W, const float* sw, void* Y, void* stream);
+
+/* As lbgemm_linear, forcing variant v (-1 = table). */
+lbgemm_status lbgemm_linear_variant(int64_t M, int64_t N, int64_t K, const int8_t* X,
+                                    const float* sx, const int8_t* W, const float* sw, void* Y,
+                                    int variant, void* stream);
+
+/* ---- selection table: [LBG] sections 2-3 ------------------------------------
+ * The table maps (bits, M, N, K) on this device's SM count to a variant.  A
+ * shape with no entry takes the entry of the nearest one of the same bits and
+ * SM count (distance: sum of |log2| differences of M, N, K; ties to the first
+ * in (M, N, K) order); an empty table gives the default variant. */
+int lbgemm_select(int bits, int64_t M, int64_t N, int64_t K);
+lbgemm_status lbgemm_table_set(int bits, int64_t M, int64_t N, int64_t K, int variant);
+/* The same two for an explicit SM count (no device needed). */
+int lbgemm_select_for(int sm_count, int bits, int64_t M, int64_t N, int64_t K);
+lbgemm_status lbgemm_table_set_for(int sm_count, int bits, int64_t M, int64_t N, int64_t K,
+                                   int variant);
+lbgemm_status lbgemm_table_clear(void);
+int64_t lbgemm_table_size(void);
+/* Text file, one entry per line: "sm_count bits M N K variant". */
+lbgemm_status lbgemm_table_load(const char* path);
+lbgemm_status lbgemm_table_save(const char* path);
+
+/* The stored choice from nine measured times: the fastest variant (lowest
+ * index on ties), unless times[default_variant] is within keep_within
+ * (relative) of it, in which case the default is kept.  -1 on bad input. */
+int lbgemm_choose(const float* times, int default_variant, float keep_within);
+
+/* Timing step of the sweep, [LBG] section 2: runs every variant on the given
+ * operands `warmup` times, then `reps` times, each rep timed with CUDA events
+ * on `stream`, and writes the median milliseconds per variant to times[9].
+ * Uses the internal workspace like lbgemm_run.  Synchronises `stream`. */
+lbgemm_status lbgemm_time_variants(int bits, int64_t M, int64_t N, int64_t K, const void* A,
+                                   const void* B, int32_t* C, int warmup, int reps, float* times,
+                                   void* stream);
+
+/* Host-buffer convenience, for callers whose operands live in host memory:
+ * copies A and B to device staging buffers that the library owns (grown with
+ * cudaMalloc on demand), runs lbgemm_run_variant, copies C back to the host
+ * buffer and synchronises `stream`.  Pinned host memory gives the fastest
+ * copies.  Not for use under stream capture. */
+lbgemm_status lbgemm_run_host(int bits, int64_t M, int64_t N, int64_t K, const void* A_host,
+                              const void* B_host, int32_t* C_host, int variant, void* stream);
+
+/* ---- exactness tuning ----------------------------------------------------------
+ * The tensor-core path sums fp32 products of exact encodings in chunks of
+ * k_elems along K and adds the chunks in int32.  A chunk stays exact while
+ * k_elems * max|a*b| stays below 2^24: max|a*b| = 2^14 for bits 8 (k_elems
+ * <= 1024) and 2^6 for bits 4 (k_elems <= 262144).  Defaults: 512 for bits
+ * 8, 2048 for bits 4.  k_elems must be a multiple of 64 (bits 8) or 128
+ * (bits 4).  Process-wide; affects calls launched afterwards. */
+lbgemm_status lbgemm_set_exact_chunk(int bits, int k_elems);
+int lbgemm_get_exact_chunk(int bits);
+
+/* ---- status ------------------------------------------------------------------ */
+
+/* Synchronises `stream`, then returns LBGEMM_ERR_TIMEOUT if any kernel of this
+ * library on the current device stopped on a wait limit since the last call
+ * (and clears that record), else LBGEMM_OK. */
+lbgemm_status lbgemm_device_status(void* stream);
+
+/* Message for the last failing call on this thread ("" if none). */
+const char* lbgemm_last_error(void);
+
+/* Number of kernels this library has launched in this process (all devices). */
+int64_t lbgemm_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* LBGEMM_H */

@@ -1,0 +1,149 @@
+"""Host-side tests of the C ABI: the library loads, exports every declared
+symbol, and its host logic (argument checks, selection rule, table, chunk
+settings) agrees with the oracle of the selection rules.  No GPU needed."""
+import os
+import re
+
+import numpy as np
+import pytest
+
+from bit_tensor_gemm_gb300 import build as bld
+from bit_tensor_gemm_gb300 import lbgemm as L
+from oracle import select as osel
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",
+                      "lbgemm.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    bld.build()
+    return L.load()
+
+
+def header_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(lbgemm_\w+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = header_functions()
+    assert len(names) >= 20
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in lbgemm.h but not exported"
+
+
+def test_binding_matches_header():
+    assert L.exported_symbols() == header_functions()
+
+
+def test_variant_space(lib):
+    assert L.lbgemm_num_variants() == osel.NUM_VARIANTS == 9
+    assert L.lbgemm_default_variant() == osel.DEFAULT_VARIANT
+    for v in range(9):
+        tile, stages = osel.variant_of(v)
+        info = L.lbgemm_variant_info(8, v)
+        assert info["stages"] == stages
+        assert info["tile_n"] == (64, 128, 256)[tile] and info["tile_m"] == 128
+        assert L.lbgemm_variant_info(4, v)["tile_k"] == 128
+        b1 = L.lbgemm_variant_info(1, v)
+        assert (b1["tile_m"], b1["tile_n"]) == ((64, 64), (128, 64), (128, 128))[tile]
+    with pytest.raises(L.LbgemmError):
+        L.lbgemm_variant_info(8, 9)
+
+
+def test_choose_matches_oracle(lib):
+    g = np.random.default_rng(11)
+    for trial in range(500):
+        t = g.uniform(1.0, 2.0, 9).astype(np.float32)
+        if trial % 3 == 0:  # ties and near-ties around the default
+            t[g.integers(0, 9)] = t.min()
+            t[7] = t.min() * np.float32(1.0 + g.choice([0.0, 0.01, 0.019, 0.03]))
+        want = osel.table_choice([float(x) for x in t], 7, 0.02)
+        assert L.lbgemm_choose(t, 7, 0.02) == want, t
+    assert L.lbgemm_choose([1.0] * 8 + [float("nan")]) == -1
+
+
+def test_select_nearest_matches_oracle(lib):
+    g = np.random.default_rng(12)
+    sm = 4242  # an SM count no real device has, so no other test's entries interfere
+    sizes = [64, 128, 256, 512, 1024, 2048, 4096, 8192, 16384]
+    entries = {}
+    for _ in range(40):
+        key = tuple(int(x) for x in g.choice(sizes, 3))
+        entries[key] = int(g.integers(0, 9))
+    for (m, n, k), v in entries.items():
+        L.lbgemm_table_set_for(sm, 8, m, n, k, v)
+    ent = list(entries.items())
+    for _ in range(300):
+        q = [int(x) for x in g.integers(1, 20000, 3)]
+        assert L.lbgemm_select_for(sm, 8, *q) == osel.nearest(ent, *q), q
+    for (m, n, k), v in ent:
+        assert L.lbgemm_select_for(sm, 8, m, n, k) == v
+    # other bit widths and SM counts see none of these entries
+    assert L.lbgemm_select_for(sm, 4, 64, 64, 64) == osel.DEFAULT_VARIANT
+    assert L.lbgemm_select_for(sm + 1, 8, 64, 64, 64) == osel.DEFAULT_VARIANT
+
+
+def test_table_roundtrip(lib, tmp_path):
+    L.lbgemm_table_clear()
+    L.lbgemm_table_set_for(152, 8, 64, 128, 256, 3)
+    L.lbgemm_table_set_for(152, 1, 8192, 8192, 65536, 8)
+    L.lbgemm_table_set_for(148, 4, 8192, 8192, 8192, 0)
+    p = str(tmp_path / "table.txt")
+    L.lbgemm_table_save(p)
+    L.lbgemm_table_clear()
+    assert L.lbgemm_table_size() == 0
+    L.lbgemm_table_load(p)
+    assert L.lbgemm_table_size() == 3
+    assert L.lbgemm_select_for(152, 8, 64, 128, 256) == 3
+    assert L.lbgemm_select_for(152, 1, 8192, 8192, 65536) == 8
+    assert L.lbgemm_select_for(148, 4, 8192, 8192, 8192) == 0
+    bad = tmp_path / "bad.txt"
+    bad.write_text("152 8 64 64 64 9\n")
+    with pytest.raises(L.LbgemmError):
+        L.lbgemm_table_load(str(bad))
+    L.lbgemm_table_clear()
+
+
+def test_exact_chunk_settings(lib):
+    assert L.lbgemm_get_exact_chunk(8) == 512
+    assert L.lbgemm_get_exact_chunk(4) == 2048
+    for bits, bad in [(8, 1088), (8, 100), (4, 64), (4, 1 << 20), (1, 128)]:
+        with pytest.raises(L.LbgemmError):
+            L.lbgemm_set_exact_chunk(bits, bad)
+    L.lbgemm_set_exact_chunk(8, 1024)
+    assert L.lbgemm_get_exact_chunk(8) == 1024
+    L.lbgemm_set_exact_chunk(8, 512)
+
+
+@pytest.mark.parametrize("args,status", [
+    ((3, 4, 4, 4, 16, 16, 16), L.ERR_INVALID_ARG),           # bits
+    ((8, -1, 4, 4, 16, 16, 16), L.ERR_INVALID_ARG),          # negative M
+    ((8, 4, 4, 0, 16, 16, 16), L.ERR_INVALID_ARG),           # K = 0
+    ((8, 4, 4, 131072, 16, 16, 16), L.ERR_INVALID_ARG),      # int32 overflow possible
+    ((4, 4, 4, 7, 16, 16, 16), L.ERR_ALIGNMENT),             # odd K, 4-bit
+    ((1, 4, 4, 48, 16, 16, 16), L.ERR_ALIGNMENT),            # K % 32, 1-bit
+    ((8, 4, 4, 16, 0, 16, 16), L.ERR_INVALID_ARG),           # null A
+    ((8, 4, 4, 16, 16, 24, 16), L.ERR_ALIGNMENT),            # misaligned B
+])
+def test_argument_errors_need_no_device(lib, args, status):
+    bits, M, N, K, a, b, c = args
+    with pytest.raises(L.LbgemmError) as e:
+        L.lbgemm_run_variant(bits, M, N, K, a or None, b, c, 0, 0)
+    assert e.value.status == status
+    assert L.lbgemm_last_error()
+
+
+def test_empty_problem_is_a_noop(lib):
+    L.lbgemm_run(8, 0, 5, 16, 16, 16, 16, 0)
+    L.lbgemm_run(1, 7, 0, 32, None, None, None, 0)
+
+
+def test_workspace_size(lib):
+    assert L.lbgemm_workspace_size(1, 64, 64, 64) == 0
+    # int8: fp16 copies, rows padded to a multiple of 8 halves, each buffer to 256 bytes
+    assert L.lbgemm_workspace_size(8, 3, 5, 9) == 256 + 256
+    assert L.lbgemm_workspace_size(8, 256, 256, 256) == 2 * 256 * 256 * 2
+    assert L.lbgemm_workspace_size(4, 256, 128, 256) == 256 * 256 + 128 * 256

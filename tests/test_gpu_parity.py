@@ -1,0 +1,203 @@
+"""GPU parity: the library's CUDA kernels against the CPU oracle, element by
+element, through the C ABI.  Integer results must be bit-exact; the bf16
+linear layer must be within 1e-2 relative of the fp64 oracle per element
+(fp32 scaling adds at most a few ulp, bf16 rounding at most 2^-9 relative)
+and exactly zero where the exact accumulator is zero."""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+import oracle  # noqa: E402
+from bit_tensor_gemm_gb300 import build as bld  # noqa: E402
+from bit_tensor_gemm_gb300 import lbgemm as L  # noqa: E402
+from bit_tensor_gemm_gb300 import synth  # noqa: E402
+
+LINEAR_RTOL = 1e-2
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    bld.build()
+    L.load()
+    yield
+
+
+def G():
+    import gpu_util  # noqa: PLC0415
+    return gpu_util
+
+
+def assert_exact(got, want, what):
+    if not np.array_equal(got, want):
+        bad = np.argwhere(got != want)
+        m, n = bad[0]
+        raise AssertionError(f"{what}: {len(bad)} entries differ; first at ({m},{n}): "
+                             f"got {got[m, n]} want {want[m, n]}")
+
+
+# ---- 8-bit ---------------------------------------------------------------------
+
+def test_int8_256_cube_config():
+    """The 256^3 int8 workload, seeded like the benchmark, default dispatch."""
+    A, B = synth.operands(8, 256, 256, 256, synth.config_seed(1))
+    assert_exact(G().gemm(8, A, B, 256), oracle.gemm(8, A, B, 256), "int8 256^3")
+
+
+SHAPES_8 = [(256, 256, 256), (300, 200, 136), (129, 65, 1000), (128, 512, 2048), (1, 1, 1),
+            (17, 333, 24), (257, 129, 4104)]
+
+
+@pytest.mark.parametrize("variant", range(9))
+def test_int8_every_variant(variant):
+    for i, (M, N, K) in enumerate(SHAPES_8):
+        A, B = synth.operands(8, M, N, K, 100 + i)
+        assert_exact(G().gemm(8, A, B, K, variant), oracle.gemm(8, A, B, K),
+                     f"int8 variant {variant} {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("M", [1, 2, 5, 16])
+def test_int8_skinny_path(M):
+    for N, K in [(1000, 4096), (37, 16), (11008, 512)]:
+        A, B = synth.operands(8, M, N, K, 7 * M + N)
+        assert_exact(G().gemm(8, A, B, K), oracle.gemm(8, A, B, K), f"int8 skinny {M}x{N}x{K}")
+
+
+def test_int8_full_range_and_extremes():
+    g = np.random.default_rng(5)
+    M, N, K = 130, 70, 3000
+    A = g.integers(-128, 128, (M, K)).astype(np.int8)
+    B = g.integers(-128, 128, (N, K)).astype(np.int8)
+    A[0] = -128
+    B[0] = -128
+    B[1] = 127
+    assert_exact(G().gemm(8, A, B, K, 7), oracle.gemm(8, A, B, K), "int8 full range")
+
+
+def test_int8_max_k_all_min():
+    """K = 131071 with every value -128: C = 16384 K = 2147467264, the largest
+    result the 8-bit path accepts; every chunk and the int32 sum are at their
+    limits."""
+    K = 131071
+    A = np.full((3, K), -128, np.int8)
+    B = np.full((2, K), -128, np.int8)
+    C = G().gemm(8, A, B, K, 1)
+    assert np.all(C == 16384 * K)
+
+
+def test_int8_exact_accumulation_adversarial():
+    """Large products first, then +-1 terms: a truncating fp32 sum would drop
+    the small terms.  The per-chunk magnitude reaches 2^23."""
+    K = 4096
+    A = np.ones((128, K), np.int8)
+    B = np.ones((64, K), np.int8)
+    A[:, :511] = -128
+    B[:, :511] = -128
+    B[1::2, 600:] = -1
+    assert_exact(G().gemm(8, A, B, K, 4), oracle.gemm(8, A, B, K), "int8 adversarial")
+
+
+def test_int8_workspace_entry_matches():
+    M, N, K = 200, 300, 520
+    A, B = synth.operands(8, M, N, K, 77)
+    need = L.lbgemm_workspace_size(8, M, N, K)
+    ws = torch.empty(need, dtype=torch.uint8, device=G().DEV)
+    dC = torch.empty((M, N), dtype=torch.int32, device=G().DEV)
+    L.lbgemm_run_ws(8, M, N, K, G().to_dev(A), G().to_dev(B), dC, 5, ws, need)
+    L.lbgemm_device_status()
+    assert_exact(dC.cpu().numpy(), oracle.gemm(8, A, B, K), "int8 run_ws")
+    with pytest.raises(L.LbgemmError) as e:
+        L.lbgemm_run_ws(8, M, N, K, G().to_dev(A), G().to_dev(B), dC, 5, ws, need - 1)
+    assert e.value.status == L.ERR_WORKSPACE
+
+
+def test_int8_host_buffers():
+    M, N, K = 96, 160, 640
+    A, B = synth.operands(8, M, N, K, 78)
+    C = np.zeros((M, N), np.int32)
+    L.lbgemm_run_host(8, M, N, K, A, B, C, -1, 0)
+    assert_exact(C, oracle.gemm(8, A, B, K), "int8 host buffers")
+
+
+# ---- 4-bit ---------------------------------------------------------------------
+
+SHAPES_4 = [(256, 256, 256), (300, 200, 138), (129, 65, 1000), (128, 512, 4096), (3, 5, 2)]
+
+
+@pytest.mark.parametrize("variant", range(9))
+def test_int4_every_variant(variant):
+    for i, (M, N, K) in enumerate(SHAPES_4):
+        A, B = synth.operands(4, M, N, K, 200 + i)
+        assert_exact(G().gemm(4, A, B, K, variant), oracle.gemm(4, A, B, K),
+                     f"int4 variant {variant} {M}x{N}x{K}")
+
+
+def test_int4_extremes_long_k():
+    K = 65536
+    A = np.full((2, K // 2), 0x88, np.uint8)   # all -8
+    B = np.full((3, K // 2), 0x88, np.uint8)
+    B[1] = 0x77                                # all 7
+    C = G().gemm(4, A, B, K)
+    assert np.all(C[:, 0] == 64 * K) and np.all(C[:, 1] == -56 * K) and np.all(C[:, 2] == 64 * K)
+
+
+# ---- 1-bit ---------------------------------------------------------------------
+
+SHAPES_1 = [(64, 64, 1024), (100, 70, 4096), (129, 257, 96), (5, 3, 32), (200, 130, 65536)]
+
+
+@pytest.mark.parametrize("variant", range(9))
+def test_b1_every_variant(variant):
+    for i, (M, N, K) in enumerate(SHAPES_1):
+        A, B = synth.operands(1, M, N, K, 300 + i)
+        assert_exact(G().gemm(1, A, B, K, variant), oracle.gemm(1, A, B, K),
+                     f"b1 variant {variant} {M}x{N}x{K}")
+
+
+def test_b1_closed_forms():
+    K = 4096
+    g = np.random.default_rng(9)
+    A = g.integers(0, 1 << 32, (40, K // 32), dtype=np.uint64).astype(np.uint32)
+    B = np.concatenate([A, ~A])
+    C = G().gemm(1, A, B, K)
+    assert np.all(np.diag(C[:, :40]) == K) and np.all(np.diag(C[:, 40:]) == -K)
+
+
+# ---- linear layer -----------------------------------------------------------------
+
+def check_linear(Y, ref, acc_zero, what):
+    assert np.all(np.isfinite(Y)), what
+    err = np.abs(Y - ref)
+    tol = LINEAR_RTOL * np.abs(ref)
+    bad = err > tol
+    assert not bad.any(), f"{what}: {bad.sum()} entries beyond 1e-2 relative"
+    assert np.all(Y[acc_zero] == 0), f"{what}: nonzero output where the accumulator is zero"
+
+
+@pytest.mark.parametrize("M", [1, 16, 128, 200])
+def test_linear_small(M):
+    N, K = 1000, 4096
+    X, sx, W, sw = synth.linear_operands(M, N, K, 400 + M)
+    X[0, :] = 0  # an all-zero token gives exact zeros
+    ref = oracle.linear(X, sx, W, sw)
+    acc = oracle.gemm(8, X, W, K)
+    check_linear(G().linear(X, sx, W, sw), ref, acc == 0, f"linear M={M}")
+
+
+@pytest.mark.parametrize("variant", [0, 4, 8])
+def test_linear_variants(variant):
+    M, N, K = 160, 520, 1024
+    X, sx, W, sw = synth.linear_operands(M, N, K, 500 + variant)
+    ref = oracle.linear(X, sx, W, sw)
+    acc = oracle.gemm(8, X, W, K)
+    check_linear(G().linear(X, sx, W, sw, variant), ref, acc == 0, f"linear v{variant}")
+
+
+# ---- status word ------------------------------------------------------------------
+
+def test_device_status_clean_after_runs():
+    L.lbgemm_device_status()
+    assert L.lbgemm_launch_count() > 0
