@@ -41,11 +41,12 @@ constexpr int kDefaultVariant = 7;  // large tile, 3 stages
 constexpr int kMaxDevices = 64;
 constexpr int kSkinnyMaxM = 16;
 constexpr int kGroupM = 8;
+constexpr size_t kFlushBytes = size_t(256) << 20;  // twice the 129 MB L2
 
 thread_local std::string t_last_error;
 std::atomic<int64_t> g_launches{0};
 std::atomic<int> g_chunk_s8{512};
-std::atomic<int> g_chunk_s4{2048};
+std::atomic<int> g_chunk_s4{131072};
 
 lbgemm_status fail(lbgemm_status st, const char* fmt, ...) {
   char buf[512];
@@ -77,6 +78,7 @@ struct DeviceState {
   int* status = nullptr;
   Scratch ws;           // operand re-encoding scratch
   Scratch host_stage;   // device staging for lbgemm_run_host
+  Scratch flush;        // buffer written between timed runs to evict L2
   std::map<const void*, int> occupancy;
 };
 
@@ -263,29 +265,27 @@ int occupancy(DeviceState& d, const TcKernel& k) {
 
 // ---- the tensor-core path (bits 8 and 4, and the linear layer) --------------------------------
 
-lbgemm_status run_tc(DeviceState& d, int bits, int64_t M, int64_t N, int64_t K, const void* A,
-                     const void* B, int32_t* C, const float* sx, const float* sw, void* Y,
-                     int variant, void* ws, cudaStream_t stream) {
+lbgemm_status encode_operand(DeviceState& d, int bits, const void* src, int64_t rows, int64_t K,
+                             void* dst, cudaStream_t stream) {
+  const int64_t kp = enc_kp(bits, K);
+  cudaError_t e = bits == 8
+      ? lbg::launch_cvt_s8_f16(static_cast<const int8_t*>(src), rows, K, dst, kp, d.sm_count, stream)
+      : lbg::launch_cvt_s4_e4m3(static_cast<const uint8_t*>(src), rows, K, dst, kp, d.sm_count,
+                                stream);
+  if (e != cudaSuccess) return cuda_fail(e, "operand re-encoding launch");
+  g_launches += rows > 0 ? 1 : 0;
+  return LBGEMM_OK;
+}
+
+// The GEMM kernel alone, on encoded operands.
+lbgemm_status run_tc_encoded(DeviceState& d, int bits, int64_t M, int64_t N, int64_t K,
+                             const void* encA, const void* encB, int32_t* C, const float* sx,
+                             const float* sw, void* Y, int variant, cudaStream_t stream) {
   const bool f8 = bits == 4;
   const bool linear = Y != nullptr;
   TcKernel k = tc_kernel(variant, f8, linear);
   if (!k.launch) return fail(LBGEMM_ERR_UNSUPPORTED, "no kernel for variant %d", variant);
   const int64_t kp = enc_kp(bits, K);
-  uint8_t* encA = static_cast<uint8_t*>(ws);
-  uint8_t* encB = encA + enc_bytes(bits, M, K);
-  cudaError_t e;
-  if (!f8) {
-    e = lbg::launch_cvt_s8_f16(static_cast<const int8_t*>(A), M, K, encA, kp, d.sm_count, stream);
-    if (e == cudaSuccess)
-      e = lbg::launch_cvt_s8_f16(static_cast<const int8_t*>(B), N, K, encB, kp, d.sm_count, stream);
-  } else {
-    e = lbg::launch_cvt_s4_e4m3(static_cast<const uint8_t*>(A), M, K, encA, kp, d.sm_count,
-                                stream);
-    if (e == cudaSuccess)
-      e = lbg::launch_cvt_s4_e4m3(static_cast<const uint8_t*>(B), N, K, encB, kp, d.sm_count,
-                                  stream);
-  }
-  if (e != cudaSuccess) return cuda_fail(e, "operand re-encoding launch");
   CUtensorMap ma, mb;
   lbgemm_status st = encode_kmajor(&ma, encA, M, kp, !f8, 128);
   if (st != LBGEMM_OK) return st;
@@ -314,10 +314,21 @@ lbgemm_status run_tc(DeviceState& d, int bits, int64_t M, int64_t N, int64_t K, 
   else
     p.vec_ok = (N % 4 == 0) && aligned16(C);
   const int grid = (int)std::min<int64_t>(p.num_tiles, (int64_t)d.sm_count * occupancy(d, k));
-  e = k.launch(&ma, &mb, &p, grid, stream);
+  cudaError_t e = k.launch(&ma, &mb, &p, grid, stream);
   if (e != cudaSuccess) return cuda_fail(e, "tensor-core GEMM launch");
-  g_launches += 3;
+  g_launches += 1;
   return LBGEMM_OK;
+}
+
+lbgemm_status run_tc(DeviceState& d, int bits, int64_t M, int64_t N, int64_t K, const void* A,
+                     const void* B, int32_t* C, const float* sx, const float* sw, void* Y,
+                     int variant, void* ws, cudaStream_t stream) {
+  uint8_t* encA = static_cast<uint8_t*>(ws);
+  uint8_t* encB = encA + enc_bytes(bits, M, K);
+  lbgemm_status st = encode_operand(d, bits, A, M, K, encA, stream);
+  if (st == LBGEMM_OK) st = encode_operand(d, bits, B, N, K, encB, stream);
+  if (st != LBGEMM_OK) return st;
+  return run_tc_encoded(d, bits, M, N, K, encA, encB, C, sx, sw, Y, variant, stream);
 }
 
 lbgemm_status run_any(int bits, int64_t M, int64_t N, int64_t K, const void* A, const void* B,
@@ -458,6 +469,47 @@ lbgemm_status lbgemm_run_ws(int bits, int64_t M, int64_t N, int64_t K, const voi
   }
 }
 
+size_t lbgemm_encoded_size(int bits, int64_t rows, int64_t K) {
+  if ((bits != 8 && bits != 4) || rows <= 0 || K <= 0) return 0;
+  return enc_bytes(bits, rows, K);
+}
+
+lbgemm_status lbgemm_encode(int bits, int64_t rows, int64_t K, const void* src, void* dst,
+                            void* stream) {
+  try {
+    if (bits != 8 && bits != 4) return fail(LBGEMM_ERR_INVALID_ARG, "encode: bits must be 8 or 4");
+    lbgemm_status st = check_gemm_args(bits, rows, 1, K, src, dst, dst);
+    if (st != LBGEMM_OK || rows == 0) return st;
+    DeviceState* d = nullptr;
+    st = device_state(&d);
+    if (st != LBGEMM_OK) return st;
+    return encode_operand(*d, bits, src, rows, K, dst, as_stream(stream));
+  } catch (...) {
+    return fail(LBGEMM_ERR_CUDA, "internal error");
+  }
+}
+
+lbgemm_status lbgemm_run_encoded(int bits, int64_t M, int64_t N, int64_t K, const void* A_enc,
+                                 const void* B_enc, int32_t* C, int variant, void* stream) {
+  try {
+    if (bits != 8 && bits != 4)
+      return fail(LBGEMM_ERR_INVALID_ARG, "encoded operands exist for bits 8 and 4 only");
+    lbgemm_status st = check_gemm_args(bits, M, N, K, A_enc, B_enc, C);
+    if (st != LBGEMM_OK) return st;
+    if (variant < -1 || variant >= kNumVariants)
+      return fail(LBGEMM_ERR_INVALID_ARG, "variant %d out of range", variant);
+    if (M == 0 || N == 0) return LBGEMM_OK;
+    DeviceState* d = nullptr;
+    st = device_state(&d);
+    if (st != LBGEMM_OK) return st;
+    if (variant < 0) variant = table_select(d->sm_count, bits, M, N, K);
+    return run_tc_encoded(*d, bits, M, N, K, A_enc, B_enc, C, nullptr, nullptr, nullptr, variant,
+                          as_stream(stream));
+  } catch (...) {
+    return fail(LBGEMM_ERR_CUDA, "internal error");
+  }
+}
+
 lbgemm_status lbgemm_linear(int64_t M, int64_t N, int64_t K, const int8_t* X, const float* sx,
                             const int8_t* W, const float* sw, void* Y, void* stream) {
   try {
@@ -573,10 +625,18 @@ int lbgemm_choose(const float* times, int default_variant, float keep_within) {
 }
 
 lbgemm_status lbgemm_time_variants(int bits, int64_t M, int64_t N, int64_t K, const void* A,
-                                   const void* B, int32_t* C, int warmup, int reps, float* times,
-                                   void* stream) {
+                                   const void* B, int32_t* C, int warmup, int reps, int flush_l2,
+                                   float* times, void* stream) {
   if (!times || reps < 1 || warmup < 0) return fail(LBGEMM_ERR_INVALID_ARG, "bad timing args");
   cudaStream_t s = as_stream(stream);
+  DeviceState* d = nullptr;
+  lbgemm_status st0 = device_state(&d);
+  if (st0 != LBGEMM_OK) return st0;
+  if (flush_l2) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    st0 = scratch_acquire(d->flush, kFlushBytes, s);
+    if (st0 != LBGEMM_OK) return st0;
+  }
   cudaEvent_t e0, e1;
   if (cudaEventCreate(&e0) != cudaSuccess || cudaEventCreate(&e1) != cudaSuccess)
     return fail(LBGEMM_ERR_CUDA, "cudaEventCreate");
@@ -586,6 +646,7 @@ lbgemm_status lbgemm_time_variants(int bits, int64_t M, int64_t N, int64_t K, co
     for (int w = 0; w < warmup && st == LBGEMM_OK; ++w)
       st = lbgemm_run_variant(bits, M, N, K, A, B, C, v, stream);
     for (int r = 0; r < reps && st == LBGEMM_OK; ++r) {
+      if (flush_l2) cudaMemsetAsync(d->flush.ptr, r & 0xFF, kFlushBytes, s);
       cudaEventRecord(e0, s);
       st = lbgemm_run_variant(bits, M, N, K, A, B, C, v, stream);
       cudaEventRecord(e1, s);

@@ -317,10 +317,8 @@ template <int BN, int STAGES, bool F8, bool LINEAR>
 cudaError_t tc_launch(const CUtensorMap* a, const CUtensorMap* b, const TcParams* p, int grid,
                       cudaStream_t stream) {
   using L = TcLayout<BN, STAGES>;
+  // The dynamic shared memory limit was raised once per device by the caller.
   auto kern = tc_gemm_kernel<BN, STAGES, F8, LINEAR>;
-  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         tc_smem_request(L::kDynSmem, L::kTmemCols));
-  if (err != cudaSuccess) return err;
   kern<<<grid, kTcThreads, tc_smem_request(L::kDynSmem, L::kTmemCols), stream>>>(*a, *b, *p);
   return cudaGetLastError();
 }

@@ -44,6 +44,9 @@ _SIGNATURES = {
     "lbgemm_workspace_size": (ctypes.c_size_t, [_i32, _i64, _i64, _i64]),
     "lbgemm_run_ws": (_i32, [_i32, _i64, _i64, _i64, _vp, _vp, _vp, _i32, _vp, ctypes.c_size_t,
                              _vp]),
+    "lbgemm_encoded_size": (ctypes.c_size_t, [_i32, _i64, _i64]),
+    "lbgemm_encode": (_i32, [_i32, _i64, _i64, _vp, _vp, _vp]),
+    "lbgemm_run_encoded": (_i32, [_i32, _i64, _i64, _i64, _vp, _vp, _vp, _i32, _vp]),
     "lbgemm_linear": (_i32, [_i64, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _vp]),
     "lbgemm_linear_variant": (_i32, [_i64, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _i32, _vp]),
     "lbgemm_select": (_i32, [_i32, _i64, _i64, _i64]),
@@ -55,7 +58,8 @@ _SIGNATURES = {
     "lbgemm_table_load": (_i32, [ctypes.c_char_p]),
     "lbgemm_table_save": (_i32, [ctypes.c_char_p]),
     "lbgemm_choose": (_i32, [_vp, _i32, _f32]),
-    "lbgemm_time_variants": (_i32, [_i32, _i64, _i64, _i64, _vp, _vp, _vp, _i32, _i32, _vp, _vp]),
+    "lbgemm_time_variants": (_i32, [_i32, _i64, _i64, _i64, _vp, _vp, _vp, _i32, _i32, _i32, _vp,
+                                    _vp]),
     "lbgemm_run_host": (_i32, [_i32, _i64, _i64, _i64, _vp, _vp, _vp, _i32, _vp]),
     "lbgemm_set_exact_chunk": (_i32, [_i32, _i32]),
     "lbgemm_get_exact_chunk": (_i32, [_i32]),
@@ -160,6 +164,19 @@ def lbgemm_run_ws(bits, M, N, K, A, B, C, variant, workspace, workspace_bytes, s
                                 _addr(workspace), workspace_bytes, _stream(stream)))
 
 
+def lbgemm_encoded_size(bits, rows, K) -> int:
+    return load().lbgemm_encoded_size(bits, rows, K)
+
+
+def lbgemm_encode(bits, rows, K, src, dst, stream=None) -> None:
+    _check(load().lbgemm_encode(bits, rows, K, _addr(src), _addr(dst), _stream(stream)))
+
+
+def lbgemm_run_encoded(bits, M, N, K, A_enc, B_enc, C, variant=-1, stream=None) -> None:
+    _check(load().lbgemm_run_encoded(bits, M, N, K, _addr(A_enc), _addr(B_enc), _addr(C), variant,
+                                     _stream(stream)))
+
+
 def lbgemm_linear(M, N, K, X, sx, W, sw, Y, stream=None) -> None:
     _check(load().lbgemm_linear(M, N, K, _addr(X), _addr(sx), _addr(W), _addr(sw), _addr(Y),
                                 _stream(stream)))
@@ -207,10 +224,12 @@ def lbgemm_choose(times, default_variant: int = 7, keep_within: float = 0.02) ->
     return load().lbgemm_choose(ctypes.addressof(arr), default_variant, keep_within)
 
 
-def lbgemm_time_variants(bits, M, N, K, A, B, C, warmup=2, reps=5, stream=None) -> list:
+def lbgemm_time_variants(bits, M, N, K, A, B, C, warmup=2, reps=5, flush_l2=True,
+                         stream=None) -> list:
     arr = (ctypes.c_float * 9)()
     _check(load().lbgemm_time_variants(bits, M, N, K, _addr(A), _addr(B), _addr(C), warmup, reps,
-                                       ctypes.addressof(arr), _stream(stream)))
+                                       int(bool(flush_l2)), ctypes.addressof(arr),
+                                       _stream(stream)))
     return list(arr)
 
 

@@ -98,6 +98,22 @@ lbgemm_status lbgemm_run_ws(int bits, int64_t M, int64_t N, int64_t K, const voi
                             const void* B, int32_t* C, int variant, void* workspace,
                             size_t workspace_bytes, void* stream);
 
+/* ---- pre-encoded operands ------------------------------------------------------
+ * The 8- and 4-bit tensor-core path first re-encodes each operand exactly
+ * (int8 -> fp16, int4 -> e4m3; rows padded with zeros to a multiple of 8
+ * halves / 16 bytes).  A caller that reuses an operand (the weights of a
+ * linear layer) can encode it once and call lbgemm_run_encoded, which runs
+ * the GEMM kernel alone.  The encoded layout is private to this library
+ * version: only lbgemm_encode may write it. */
+size_t lbgemm_encoded_size(int bits, int64_t rows, int64_t K);
+/* dst: device buffer of lbgemm_encoded_size(bits, rows, K) bytes, 16-byte
+ * aligned.  src: rows x K operand in the format of `bits` (8 or 4). */
+lbgemm_status lbgemm_encode(int bits, int64_t rows, int64_t K, const void* src, void* dst,
+                            void* stream);
+/* C = A . B^T from encoded operands (variant -1 = table). */
+lbgemm_status lbgemm_run_encoded(int bits, int64_t M, int64_t N, int64_t K, const void* A_enc,
+                                 const void* B_enc, int32_t* C, int variant, void* stream);
+
 /* Quantised linear layer, [LBG] section 4 (a linear layer on the low-bit
  * GEMM): Y[m][n] = bf16_round_nearest_even( (float)acc[m][n] * sx[m] * sw[n] )
  * with acc = X . W^T exact in int32.  X: int8 M x K (per-token scale sx, fp32
@@ -137,10 +153,13 @@ int lbgemm_choose(const float* times, int default_variant, float keep_within);
 /* Timing step of the sweep, [LBG] section 2: runs every variant on the given
  * operands `warmup` times, then `reps` times, each rep timed with CUDA events
  * on `stream`, and writes the median milliseconds per variant to times[9].
- * Uses the internal workspace like lbgemm_run.  Synchronises `stream`. */
+ * With flush_l2 != 0, a 256 MB library-owned buffer (allocated on first use)
+ * is overwritten before each timed rep, outside the timed interval, so every
+ * rep starts with operands out of L2.  Uses the internal workspace like
+ * lbgemm_run.  Synchronises `stream`. */
 lbgemm_status lbgemm_time_variants(int bits, int64_t M, int64_t N, int64_t K, const void* A,
-                                   const void* B, int32_t* C, int warmup, int reps, float* times,
-                                   void* stream);
+                                   const void* B, int32_t* C, int warmup, int reps, int flush_l2,
+                                   float* times, void* stream);
 
 /* Host-buffer convenience, for callers whose operands live in host memory:
  * copies A and B to device staging buffers that the library owns (grown with
@@ -155,7 +174,7 @@ lbgemm_status lbgemm_run_host(int bits, int64_t M, int64_t N, int64_t K, const v
  * k_elems along K and adds the chunks in int32.  A chunk stays exact while
  * k_elems * max|a*b| stays below 2^24: max|a*b| = 2^14 for bits 8 (k_elems
  * <= 1024) and 2^6 for bits 4 (k_elems <= 262144).  Defaults: 512 for bits
- * 8, 2048 for bits 4.  k_elems must be a multiple of 64 (bits 8) or 128
+ * 8, 131072 for bits 4.  k_elems must be a multiple of 64 (bits 8) or 128
  * (bits 4).  Process-wide; affects calls launched afterwards. */
 lbgemm_status lbgemm_set_exact_chunk(int bits, int k_elems);
 int lbgemm_get_exact_chunk(int bits);
