@@ -746,6 +746,18 @@ lbgemm_status lbgemm_device_status(void* stream) {
 
 const char* lbgemm_last_error(void) { return t_last_error.c_str(); }
 
+}  // extern "C"
+
+// Lets other translation units of the library report a failure through
+// lbgemm_last_error().
+namespace lbg {
+lbgemm_status report_error(lbgemm_status st, const char* message) {
+  return fail(st, "%s", message);
+}
+}  // namespace lbg
+
+extern "C" {
+
 int64_t lbgemm_launch_count(void) { return g_launches.load(); }
 
 }  // extern "C"

@@ -98,6 +98,31 @@ lbgemm_status lbgemm_run_ws(int bits, int64_t M, int64_t N, int64_t K, const voi
                             const void* B, int32_t* C, int variant, void* workspace,
                             size_t workspace_bytes, void* stream);
 
+/* For callers that cannot allocate GPU memory at all -- code running where
+ * cudaMalloc is forbidden or unsafe, such as inside a host callback, a custom
+ * allocator's own hooks, or a plugin whose host process owns every device
+ * allocation -- and that also cannot hand over a workspace of their own.
+ * The paper has no counterpart; this is a convenience of this library.
+ *
+ * Same result as lbgemm_run_variant / lbgemm_run_ws, but the operand
+ * re-encoding scratch is a fixed array of LBGEMM_STATIC_SCRATCH_BYTES (32 MiB)
+ * compiled into the library: every GPU that loads the library holds it until
+ * the process exits, and this call allocates nothing.  The caller still
+ * passes A, B and C.  Problems whose scratch (lbgemm_workspace_size) exceeds
+ * the array are rejected with LBGEMM_ERR_WORKSPACE before anything runs;
+ * for 8-bit operands that is (M + N) * round_up(K, 8) * 2 bytes, e.g. M = N =
+ * 2048 at K = 4096.  1-bit problems use no scratch and have no limit.
+ *
+ * The first call on each device looks up the array's device address (with
+ * that device current); make that first call before any stream capture.
+ * Every call shares the one array: calls that can overlap on the GPU (other
+ * streams, other threads) race on it and must be ordered by the caller.  The
+ * array keeps whatever the last call wrote; each call rewrites every byte its
+ * GEMM reads (zero padding included), so nothing stale is read. */
+#define LBGEMM_STATIC_SCRATCH_BYTES ((size_t)32 << 20)
+lbgemm_status lbgemm_run_static(int bits, int64_t M, int64_t N, int64_t K, const void* A,
+                                const void* B, int32_t* C, int variant, void* stream);
+
 /* ---- pre-encoded operands ------------------------------------------------------
  * The 8- and 4-bit tensor-core path first re-encodes each operand exactly
  * (int8 -> fp16, int4 -> e4m3; rows padded with zeros to a multiple of 8
