@@ -744,6 +744,16 @@ lbgemm_status lbgemm_device_status(void* stream) {
   return LBGEMM_OK;
 }
 
+lbgemm_status lbgemm_selftest_timeout(void* stream) {
+  DeviceState* d = nullptr;
+  lbgemm_status st = device_state(&d);
+  if (st != LBGEMM_OK) return st;
+  cudaError_t e = lbg::launch_wait_selftest(d->status, 100000000ull, as_stream(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "self-test launch");
+  g_launches += 1;
+  return LBGEMM_OK;
+}
+
 const char* lbgemm_last_error(void) { return t_last_error.c_str(); }
 
 }  // extern "C"

@@ -16,6 +16,7 @@
 
 #include <cstdint>
 
+#include "ptx.cuh"
 #include "simt.h"
 
 namespace lbg {
@@ -296,7 +297,28 @@ __global__ void __launch_bounds__(256)
 }
 
 // ---------------------------------------------------------------------------
+// Self-test of the bounded wait: one thread waits on an mbarrier that nothing
+// will ever signal, through the same helper the GEMM kernel uses, with a short
+// limit.  The wait gives up, raises the status word and the kernel returns.
+__global__ void wait_selftest_kernel(int* status, uint64_t limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    const uint32_t b = smem_addr(&bar);
+    mbar_init(b, 1);
+    abort_flag = 0;
+    fence_barrier_init();
+    mbar_wait(b, 0, &abort_flag, status, limit_ns);
+  }
+}
+
+// ---------------------------------------------------------------------------
 // host launchers
+
+cudaError_t launch_wait_selftest(int* status, uint64_t limit_ns, cudaStream_t s) {
+  wait_selftest_kernel<<<1, 32, 0, s>>>(status, limit_ns);
+  return cudaGetLastError();
+}
 
 static int grid_for(int64_t work, int threads, int sm_count) {
   int64_t blocks = (work + threads - 1) / threads;

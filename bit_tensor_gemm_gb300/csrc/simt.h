@@ -20,5 +20,7 @@ cudaError_t launch_skinny_s8(const int8_t* A, const int8_t* B, int M, int N, int
 cudaError_t launch_b1_popc(int tile, int stages, const uint32_t* A, const uint32_t* B, int64_t M,
                            int64_t N, int64_t K, int32_t* C, cudaStream_t s);
 void b1_tile_shape(int tile, int* bm, int* bn);
+// One-thread kernel whose mbarrier wait runs out after limit_ns.
+cudaError_t launch_wait_selftest(int* status, uint64_t limit_ns, cudaStream_t s);
 
 }  // namespace lbg

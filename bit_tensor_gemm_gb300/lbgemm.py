@@ -65,6 +65,7 @@ _SIGNATURES = {
     "lbgemm_set_exact_chunk": (_i32, [_i32, _i32]),
     "lbgemm_get_exact_chunk": (_i32, [_i32]),
     "lbgemm_device_status": (_i32, [_vp]),
+    "lbgemm_selftest_timeout": (_i32, [_vp]),
     "lbgemm_last_error": (ctypes.c_char_p, []),
     "lbgemm_launch_count": (_i64, []),
 }
@@ -258,6 +259,10 @@ def lbgemm_get_exact_chunk(bits: int) -> int:
 
 def lbgemm_device_status(stream=None) -> None:
     _check(load().lbgemm_device_status(_stream(stream)))
+
+
+def lbgemm_selftest_timeout(stream=None) -> None:
+    _check(load().lbgemm_selftest_timeout(_stream(stream)))
 
 
 def lbgemm_last_error() -> str:

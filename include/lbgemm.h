@@ -211,6 +211,13 @@ int lbgemm_get_exact_chunk(int bits);
  * (and clears that record), else LBGEMM_OK. */
 lbgemm_status lbgemm_device_status(void* stream);
 
+/* Diagnostic of the failure path: launches a one-thread kernel that waits on
+ * an mbarrier nothing will signal, through the same bounded-wait code the
+ * GEMM kernels use, with a 0.1 s limit.  The wait gives up, the kernel
+ * returns, and the next lbgemm_device_status() on that stream returns
+ * LBGEMM_ERR_TIMEOUT (and clears it).  Nothing hangs or faults. */
+lbgemm_status lbgemm_selftest_timeout(void* stream);
+
 /* Message for the last failing call on this thread ("" if none). */
 const char* lbgemm_last_error(void);
 

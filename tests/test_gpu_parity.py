@@ -198,6 +198,19 @@ def test_linear_variants(variant):
 
 # ---- status word ------------------------------------------------------------------
 
+def test_wait_timeout_is_reported_and_recovers():
+    """A wait that nothing signals gives up after its limit: the status word
+    reports the time-out once, and the next GEMM runs and is exact."""
+    L.lbgemm_device_status()
+    L.lbgemm_selftest_timeout()
+    with pytest.raises(L.LbgemmError) as e:
+        L.lbgemm_device_status()
+    assert e.value.status == L.ERR_TIMEOUT
+    L.lbgemm_device_status()  # cleared
+    A, B = synth.operands(8, 130, 70, 300, 4242)
+    assert_exact(G().gemm(8, A, B, 300, 7), oracle.gemm(8, A, B, 300), "after time-out")
+
+
 def test_device_status_clean_after_runs():
     L.lbgemm_device_status()
     assert L.lbgemm_launch_count() > 0
