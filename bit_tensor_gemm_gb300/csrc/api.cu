@@ -40,12 +40,12 @@ constexpr int kNumVariants = 9;
 constexpr int kDefaultVariant = 7;  // large tile, 3 stages
 constexpr int kMaxDevices = 64;
 constexpr int kSkinnyMaxM = 16;
-constexpr int kGroupM = 8;
+constexpr int kGroupM = 16;  // M-tiles per group of the tile order (L2 reuse)
 constexpr size_t kFlushBytes = size_t(256) << 20;  // twice the 129 MB L2
 
 thread_local std::string t_last_error;
 std::atomic<int64_t> g_launches{0};
-std::atomic<int> g_chunk_s8{512};
+std::atomic<int> g_chunk_s8{1024};
 std::atomic<int> g_chunk_s4{131072};
 
 lbgemm_status fail(lbgemm_status st, const char* fmt, ...) {
@@ -313,8 +313,21 @@ lbgemm_status run_tc_encoded(DeviceState& d, int bits, int64_t M, int64_t N, int
     p.vec_ok = (N % 8 == 0) && aligned16(Y);
   else
     p.vec_ok = (N % 4 == 0) && aligned16(C);
+  CUtensorMap mc;
+  std::memset(&mc, 0, sizeof mc);
+  if (!linear && p.vec_ok) {
+    cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)M};
+    cuuint64_t strides[1] = {(cuuint64_t)(N * 4)};
+    cuuint32_t box[2] = {32, 32};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(&mc, CU_TENSOR_MAP_DATA_TYPE_INT32, 2, C, dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+      return fail(LBGEMM_ERR_CUDA, "cuTensorMapEncodeTiled (C) failed (%d)", (int)r);
+  }
   const int grid = (int)std::min<int64_t>(p.num_tiles, (int64_t)d.sm_count * occupancy(d, k));
-  cudaError_t e = k.launch(&ma, &mb, &p, grid, stream);
+  cudaError_t e = k.launch(&ma, &mb, &mc, &p, grid, stream);
   if (e != cudaSuccess) return cuda_fail(e, "tensor-core GEMM launch");
   g_launches += 1;
   return LBGEMM_OK;

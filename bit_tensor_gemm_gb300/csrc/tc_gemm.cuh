@@ -22,8 +22,11 @@
 //               128-byte-wide K slice (64 fp16 or 128 e4m3 elements) stored
 //               with the 128-byte swizzle.
 //   warp 1      allocates TMEM; one thread issues tcgen05.mma (4 per stage).
-//   warps 2..9  epilogue: TMEM -> registers -> exact int32 sums -> global
-//               (int32 C, or bf16 Y of the linear layer).
+//   warps 2..9  epilogue: TMEM -> registers -> exact int32 sums -> global.
+//               int32 C goes through a per-warp 32 x 32 staging tile in
+//               shared memory (128-byte swizzle, conflict-free writes) and a
+//               TMA bulk store, so each store is whole 128-byte rows; bf16 Y
+//               of the linear layer is stored from registers.
 // Every mbarrier wait is bounded; a wait that runs out raises the device
 // status word and winds the CTA down (waiting for its own copies in flight
 // and for its MMAs) before TMEM is freed.
@@ -49,9 +52,12 @@ struct TcLayout {
   static constexpr int kBBytes = BN * 128;
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kRingBytes = kStageBytes * STAGES;
+  // epilogue staging: one 32-row x 128-byte tile per epilogue warp
+  static constexpr int kEpiOffset = kRingBytes;
+  static constexpr int kEpiBytes = kTcEpiWarps * 32 * 128;
   // barriers: full[S], empty[S], acc_full[2], acc_empty[2], mma_done
   static constexpr int kNumBars = 2 * STAGES + 5;
-  static constexpr int kBarOffset = kRingBytes;
+  static constexpr int kBarOffset = kEpiOffset + kEpiBytes;
   static constexpr int kTmemSlotOffset = kBarOffset + 8 * kNumBars;
   static constexpr int kAbortOffset = kTmemSlotOffset + 4;
   static constexpr int kUsedBytes = kAbortOffset + 4;
@@ -121,7 +127,7 @@ __device__ __forceinline__ void store_group(const TcParams& p, int m, int n0,
 template <int BN, int STAGES, bool F8, bool LINEAR>
 __global__ void __launch_bounds__(kTcThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const TcParams p) {
+                   const __grid_constant__ CUtensorMap tmC, const TcParams p) {
   using L = TcLayout<BN, STAGES>;
   constexpr int kBkElems = F8 ? 128 : 64;  // elements per 128-byte K slice
   constexpr uint32_t kIdesc = instr_desc(kTcBM, BN);
@@ -263,6 +269,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int row = quarter * 32 + lane;
     const int col0 = (e >> 2) * (BN / 2);
     const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
+    const uint32_t stage_addr = sbase + L::kEpiOffset + e * (32 * 128);
     uint32_t u = 0;
     int32_t acc[kGroups][32];
     bool ok = true;
@@ -295,13 +302,36 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (lane == 0) mbar_arrive(acce_bar(buf));
       }
       if (!ok) break;
-      const int m = tm * kTcBM + row;
-      if (m < p.M) {
+      if (!LINEAR && p.vec_ok) {
+        // Row `lane` of the warp's 32 x 32 staging tile holds this thread's 32
+        // columns; 16-byte chunk q sits at chunk q ^ (row % 8), the layout a
+        // 128-byte-swizzled TMA box has.  The TMA store clips rows >= M and
+        // columns >= N.
 #pragma unroll
-        for (int g = 0; g < kGroups; ++g)
-          store_group<BN, LINEAR>(p, m, tn * BN + col0 + g * 32, acc[g]);
+        for (int g = 0; g < kGroups; ++g) {
+          if (lane == 0) bulk_wait_read_all();  // the previous store has read the tile
+          __syncwarp();
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            st_shared_v4(stage_addr + lane * 128 + ((q ^ (lane & 7)) << 4), acc[g][4 * q],
+                         acc[g][4 * q + 1], acc[g][4 * q + 2], acc[g][4 * q + 3]);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&tmC, stage_addr, tn * BN + col0 + g * 32, tm * kTcBM + quarter * 32);
+            bulk_commit();
+          }
+        }
+      } else {
+        const int m = tm * kTcBM + row;
+        if (m < p.M) {
+#pragma unroll
+          for (int g = 0; g < kGroups; ++g)
+            store_group<BN, LINEAR>(p, m, tn * BN + col0 + g * 32, acc[g]);
+        }
       }
     }
+    if (lane == 0) bulk_wait_all();
   }
 
   __syncthreads();
@@ -314,12 +344,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 }
 
 template <int BN, int STAGES, bool F8, bool LINEAR>
-cudaError_t tc_launch(const CUtensorMap* a, const CUtensorMap* b, const TcParams* p, int grid,
-                      cudaStream_t stream) {
+cudaError_t tc_launch(const CUtensorMap* a, const CUtensorMap* b, const CUtensorMap* c,
+                      const TcParams* p, int grid, cudaStream_t stream) {
   using L = TcLayout<BN, STAGES>;
   // The dynamic shared memory limit was raised once per device by the caller.
   auto kern = tc_gemm_kernel<BN, STAGES, F8, LINEAR>;
-  kern<<<grid, kTcThreads, tc_smem_request(L::kDynSmem, L::kTmemCols), stream>>>(*a, *b, *p);
+  kern<<<grid, kTcThreads, tc_smem_request(L::kDynSmem, L::kTmemCols), stream>>>(*a, *b, *c, *p);
   return cudaGetLastError();
 }
 

@@ -14,7 +14,8 @@ struct TcParams {
   int num_kb;    // 128-byte K slices per tile row
   int chunk_kb;  // slices per exact fp32 accumulation chunk
   int tiles_m, tiles_n, num_tiles, group_m;
-  int vec_ok;    // 16-byte vector stores are aligned for every row
+  int vec_ok;    // rows of C/Y are 16-byte aligned: C goes out by TMA stores,
+                 // Y by 16-byte vector stores
   int32_t* C;
   const float* sx;
   const float* sw;
@@ -22,8 +23,8 @@ struct TcParams {
   int* status;
 };
 
-typedef cudaError_t (*TcLaunchFn)(const CUtensorMap*, const CUtensorMap*, const TcParams*, int,
-                                  cudaStream_t);
+typedef cudaError_t (*TcLaunchFn)(const CUtensorMap*, const CUtensorMap*, const CUtensorMap*,
+                                  const TcParams*, int, cudaStream_t);
 
 struct TcKernel {
   TcLaunchFn launch = nullptr;

@@ -196,11 +196,12 @@ lbgemm_status lbgemm_run_host(int bits, int64_t M, int64_t N, int64_t K, const v
 
 /* ---- exactness tuning ----------------------------------------------------------
  * The tensor-core path sums fp32 products of exact encodings in chunks of
- * k_elems along K and adds the chunks in int32.  A chunk stays exact while
- * k_elems * max|a*b| stays below 2^24: max|a*b| = 2^14 for bits 8 (k_elems
- * <= 1024) and 2^6 for bits 4 (k_elems <= 262144).  Defaults: 512 for bits
- * 8, 131072 for bits 4.  k_elems must be a multiple of 64 (bits 8) or 128
- * (bits 4).  Process-wide; affects calls launched afterwards. */
+ * k_elems along K and adds the chunks in int32.  A chunk is exact while
+ * k_elems * max|a*b| <= 2^24 (every integer of magnitude <= 2^24 is an fp32
+ * value): max|a*b| = 2^14 for bits 8 (k_elems <= 1024) and 2^6 for bits 4
+ * (k_elems <= 262144).  Defaults: 1024 for bits 8, 131072 for bits 4.
+ * k_elems must be a multiple of 64 (bits 8) or 128 (bits 4).  Process-wide;
+ * affects calls launched afterwards. */
 lbgemm_status lbgemm_set_exact_chunk(int bits, int k_elems);
 int lbgemm_get_exact_chunk(int bits);
 

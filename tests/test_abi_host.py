@@ -108,14 +108,14 @@ def test_table_roundtrip(lib, tmp_path):
 
 
 def test_exact_chunk_settings(lib):
-    assert L.lbgemm_get_exact_chunk(8) == 512
+    assert L.lbgemm_get_exact_chunk(8) == 1024
     assert L.lbgemm_get_exact_chunk(4) == 131072
     for bits, bad in [(8, 1088), (8, 100), (4, 64), (4, 1 << 20), (1, 128)]:
         with pytest.raises(L.LbgemmError):
             L.lbgemm_set_exact_chunk(bits, bad)
-    L.lbgemm_set_exact_chunk(8, 1024)
-    assert L.lbgemm_get_exact_chunk(8) == 1024
     L.lbgemm_set_exact_chunk(8, 512)
+    assert L.lbgemm_get_exact_chunk(8) == 512
+    L.lbgemm_set_exact_chunk(8, 1024)
 
 
 @pytest.mark.parametrize("args,status", [

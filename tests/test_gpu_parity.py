@@ -90,13 +90,16 @@ def test_int8_max_k_all_min():
 
 def test_int8_exact_accumulation_adversarial():
     """Large products first, then +-1 terms: a truncating fp32 sum would drop
-    the small terms.  The per-chunk magnitude reaches 2^23."""
+    the small terms.  The per-chunk magnitude reaches 2^23 + 2^9 and, in the
+    second chunk, 2^24 - 2^14 + 1."""
     K = 4096
     A = np.ones((128, K), np.int8)
     B = np.ones((64, K), np.int8)
     A[:, :511] = -128
     B[:, :511] = -128
-    B[1::2, 600:] = -1
+    A[:, 1024:2047] = -128
+    B[:, 1024:2047] = -128
+    B[1::2, 600:1000] = -1
     assert_exact(G().gemm(8, A, B, K, 4), oracle.gemm(8, A, B, K), "int8 adversarial")
 
 
