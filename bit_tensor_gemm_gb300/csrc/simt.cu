@@ -22,40 +22,59 @@
 namespace lbg {
 
 // ---------------------------------------------------------------------------
-// int8 -> fp16, rows of K values into rows of Kp >= K halves (zero padded).
-// Each thread writes 8 halves (16 bytes).
-__global__ void cvt_s8_f16_kernel(const int8_t* __restrict__ in, int64_t rows, int64_t K,
-                                  __half* __restrict__ out, int64_t Kp, int fast) {
+// Exact re-encoding of up to two operands in one launch.  Rows of K values
+// become rows of Kp >= K (zero padded).  The kernel lets a dependent launch
+// (the GEMM, which waits for this grid's completion before its first read)
+// start its prologue early.
+
+struct CvtJob {
+  const void* src;
+  int64_t rows;
+  void* dst;
+  int fast;  // 8-byte aligned source rows
+};
+
+__device__ __forceinline__ void allow_dependent_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// int8 -> fp16; each thread writes 8 halves (16 bytes).
+__global__ void cvt_s8_f16_kernel(CvtJob ja, CvtJob jb, int64_t K, int64_t Kp) {
+  allow_dependent_launch();
   const int64_t vec_per_row = Kp / 8;
-  const int64_t total = rows * vec_per_row;
+  const int64_t total_a = ja.rows * vec_per_row;
+  const int64_t total = total_a + jb.rows * vec_per_row;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
        i += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t r = i / vec_per_row;
-    const int64_t c = (i - r * vec_per_row) * 8;
-    const int8_t* src = in + r * K + c;
+    const bool in_a = i < total_a;
+    const int64_t ii = in_a ? i : i - total_a;
+    const CvtJob& j = in_a ? ja : jb;
+    const int64_t r = ii / vec_per_row;
+    const int64_t c = (ii - r * vec_per_row) * 8;
+    const int8_t* src = static_cast<const int8_t*>(j.src) + r * K + c;
     __align__(16) __half h[8];
-    if (fast && c + 8 <= K) {
+    if (j.fast && c + 8 <= K) {
       const uint2 w = __ldg(reinterpret_cast<const uint2*>(src));
       const uint32_t lo = w.x, hi = w.y;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        h[j] = __short2half_rn((short)(int8_t)(lo >> (8 * j)));
-        h[4 + j] = __short2half_rn((short)(int8_t)(hi >> (8 * j)));
+      for (int q = 0; q < 4; ++q) {
+        h[q] = __short2half_rn((short)(int8_t)(lo >> (8 * q)));
+        h[4 + q] = __short2half_rn((short)(int8_t)(hi >> (8 * q)));
       }
     } else {
 #pragma unroll
-      for (int j = 0; j < 8; ++j) h[j] = __short2half_rn(c + j < K ? (short)src[j] : (short)0);
+      for (int q = 0; q < 8; ++q) h[q] = __short2half_rn(c + q < K ? (short)src[q] : (short)0);
     }
-    *reinterpret_cast<uint4*>(out + r * Kp + c) = *reinterpret_cast<const uint4*>(h);
+    *reinterpret_cast<uint4*>(static_cast<__half*>(j.dst) + r * Kp + c) =
+        *reinterpret_cast<const uint4*>(h);
   }
 }
 
-// packed int4 (two per byte, low nibble first) -> e4m3 bytes, rows of K
-// values into rows of Kp >= K bytes (zero padded).  K is even.  Each thread
-// writes 16 output bytes from 8 input bytes through a 256-entry table
-// (byte -> two e4m3 codes) built per block with CUDA's fp8 conversion.
-__global__ void cvt_s4_e4m3_kernel(const uint8_t* __restrict__ in, int64_t rows, int64_t K,
-                                   uint8_t* __restrict__ out, int64_t Kp, int fast) {
+// packed int4 (two per byte, low nibble first) -> e4m3 bytes; K is even.
+// Each thread writes 16 output bytes from 8 input bytes through a 256-entry
+// table (byte -> two e4m3 codes) built per block with CUDA's fp8 conversion.
+__global__ void cvt_s4_e4m3_kernel(CvtJob ja, CvtJob jb, int64_t K, int64_t Kp) {
+  allow_dependent_launch();
   __shared__ uint16_t table[256];
   for (int b = threadIdx.x; b < 256; b += blockDim.x) {
     const int lo = (b & 15) >= 8 ? (b & 15) - 16 : (b & 15);
@@ -67,14 +86,18 @@ __global__ void cvt_s4_e4m3_kernel(const uint8_t* __restrict__ in, int64_t rows,
   __syncthreads();
   const int64_t in_row = K / 2;
   const int64_t vec_per_row = Kp / 16;
-  const int64_t total = rows * vec_per_row;
+  const int64_t total_a = ja.rows * vec_per_row;
+  const int64_t total = total_a + jb.rows * vec_per_row;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
        i += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t r = i / vec_per_row;
-    const int64_t cb = (i - r * vec_per_row) * 8;  // input byte column
-    const uint8_t* src = in + r * in_row + cb;
+    const bool in_a = i < total_a;
+    const int64_t ii = in_a ? i : i - total_a;
+    const CvtJob& j = in_a ? ja : jb;
+    const int64_t r = ii / vec_per_row;
+    const int64_t cb = (ii - r * vec_per_row) * 8;  // input byte column
+    const uint8_t* src = static_cast<const uint8_t*>(j.src) + r * in_row + cb;
     uint32_t o[4];
-    if (fast && cb + 8 <= in_row) {
+    if (j.fast && cb + 8 <= in_row) {
       const uint2 w = __ldg(reinterpret_cast<const uint2*>(src));
       o[0] = table[w.x & 0xFF] | ((uint32_t)table[(w.x >> 8) & 0xFF] << 16);
       o[1] = table[(w.x >> 16) & 0xFF] | ((uint32_t)table[w.x >> 24] << 16);
@@ -83,11 +106,12 @@ __global__ void cvt_s4_e4m3_kernel(const uint8_t* __restrict__ in, int64_t rows,
     } else {
       uint16_t t[8];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) t[j] = cb + j < in_row ? table[src[j]] : (uint16_t)0;
+      for (int q = 0; q < 8; ++q) t[q] = cb + q < in_row ? table[src[q]] : (uint16_t)0;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) o[j] = t[2 * j] | ((uint32_t)t[2 * j + 1] << 16);
+      for (int q = 0; q < 4; ++q) o[q] = t[2 * q] | ((uint32_t)t[2 * q + 1] << 16);
     }
-    *reinterpret_cast<uint4*>(out + r * Kp + 2 * cb) = make_uint4(o[0], o[1], o[2], o[3]);
+    *reinterpret_cast<uint4*>(static_cast<uint8_t*>(j.dst) + r * Kp + 2 * cb) =
+        make_uint4(o[0], o[1], o[2], o[3]);
   }
 }
 
@@ -327,23 +351,22 @@ static int grid_for(int64_t work, int threads, int sm_count) {
   return (int)(blocks < 1 ? 1 : blocks);
 }
 
-cudaError_t launch_cvt_s8_f16(const int8_t* in, int64_t rows, int64_t K, void* out, int64_t Kp,
-                              int sm_count, cudaStream_t s) {
-  if (rows == 0) return cudaSuccess;
-  const int fast = (K % 8 == 0) && ((reinterpret_cast<uintptr_t>(in) & 7) == 0);
-  const int64_t work = rows * (Kp / 8);
-  cvt_s8_f16_kernel<<<grid_for(work, 256, sm_count), 256, 0, s>>>(
-      in, rows, K, static_cast<__half*>(out), Kp, fast);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_cvt_s4_e4m3(const uint8_t* in, int64_t rows, int64_t K, void* out, int64_t Kp,
+cudaError_t launch_encode_pair(int bits, const void* a, int64_t rows_a, void* enc_a,
+                               const void* b, int64_t rows_b, void* enc_b, int64_t K, int64_t Kp,
                                int sm_count, cudaStream_t s) {
-  if (rows == 0) return cudaSuccess;
-  const int fast = ((K / 2) % 8 == 0) && ((reinterpret_cast<uintptr_t>(in) & 7) == 0);
-  const int64_t work = rows * (Kp / 16);
-  cvt_s4_e4m3_kernel<<<grid_for(work, 256, sm_count), 256, 0, s>>>(
-      in, rows, K, static_cast<uint8_t*>(out), Kp, fast);
+  if (rows_a + rows_b == 0) return cudaSuccess;
+  const int64_t row_bytes = bits == 8 ? K : K / 2;
+  auto fast = [&](const void* p) {
+    return (int)(row_bytes % 8 == 0 && (reinterpret_cast<uintptr_t>(p) & 7) == 0);
+  };
+  CvtJob ja{a, rows_a, enc_a, a ? fast(a) : 0};
+  CvtJob jb{b, rows_b, enc_b, b ? fast(b) : 0};
+  const int64_t vec = bits == 8 ? Kp / 8 : Kp / 16;
+  const int grid = grid_for((rows_a + rows_b) * vec, 256, sm_count);
+  if (bits == 8)
+    cvt_s8_f16_kernel<<<grid, 256, 0, s>>>(ja, jb, K, Kp);
+  else
+    cvt_s4_e4m3_kernel<<<grid, 256, 0, s>>>(ja, jb, K, Kp);
   return cudaGetLastError();
 }
 

@@ -6,12 +6,12 @@
 
 namespace lbg {
 
-// int8 rows of K -> fp16 rows of Kp (Kp % 8 == 0, Kp >= K), zero padded.
-cudaError_t launch_cvt_s8_f16(const int8_t* in, int64_t rows, int64_t K, void* out, int64_t Kp,
-                              int sm_count, cudaStream_t s);
-// packed int4 rows of K (K even) -> e4m3 rows of Kp (Kp % 16 == 0), zero padded.
-cudaError_t launch_cvt_s4_e4m3(const uint8_t* in, int64_t rows, int64_t K, void* out,
-                               int64_t Kp, int sm_count, cudaStream_t s);
+// Exact re-encoding of operand rows (bits 8: int8 -> fp16 rows of Kp halves,
+// Kp % 8 == 0; bits 4: packed int4 -> e4m3 rows of Kp bytes, Kp % 16 == 0),
+// zero padded, for up to two operands in one launch (rows_b may be 0).
+cudaError_t launch_encode_pair(int bits, const void* a, int64_t rows_a, void* enc_a,
+                               const void* b, int64_t rows_b, void* enc_b, int64_t K, int64_t Kp,
+                               int sm_count, cudaStream_t s);
 // M <= 16, K % 16 == 0, A and B 16-byte aligned.  Y != nullptr selects the
 // linear epilogue (bf16 Y with scales sx, sw) instead of int32 C.
 cudaError_t launch_skinny_s8(const int8_t* A, const int8_t* B, int M, int N, int K, int32_t* C,

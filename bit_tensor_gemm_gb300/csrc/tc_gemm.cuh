@@ -178,6 +178,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (lane == 0) {
       tma_prefetch_desc(&tmA);
       tma_prefetch_desc(&tmB);
+      // When launched as a dependent of the re-encoding grid, wait for that
+      // grid to finish (and its writes to be visible) before the first load.
+      asm volatile("griddepcontrol.wait;" ::: "memory");
       int stage = 0;
       uint32_t phase = 0;
       int64_t issued = 0;
@@ -345,12 +348,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
 template <int BN, int STAGES, bool F8, bool LINEAR>
 cudaError_t tc_launch(const CUtensorMap* a, const CUtensorMap* b, const CUtensorMap* c,
-                      const TcParams* p, int grid, cudaStream_t stream) {
+                      const TcParams* p, int grid, bool pdl, cudaStream_t stream) {
   using L = TcLayout<BN, STAGES>;
   // The dynamic shared memory limit was raised once per device by the caller.
-  auto kern = tc_gemm_kernel<BN, STAGES, F8, LINEAR>;
-  kern<<<grid, kTcThreads, tc_smem_request(L::kDynSmem, L::kTmemCols), stream>>>(*a, *b, *c, *p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kTcThreads);
+  cfg.dynamicSmemBytes = tc_smem_request(L::kDynSmem, L::kTmemCols);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<BN, STAGES, F8, LINEAR>, *a, *b, *c, *p);
 }
 
 template <int BN, int STAGES, bool F8, bool LINEAR>

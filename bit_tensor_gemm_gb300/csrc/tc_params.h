@@ -23,8 +23,9 @@ struct TcParams {
   int* status;
 };
 
+// (A map, B map, C map, params, grid, programmatic dependent launch, stream)
 typedef cudaError_t (*TcLaunchFn)(const CUtensorMap*, const CUtensorMap*, const CUtensorMap*,
-                                  const TcParams*, int, cudaStream_t);
+                                  const TcParams*, int, bool, cudaStream_t);
 
 struct TcKernel {
   TcLaunchFn launch = nullptr;
