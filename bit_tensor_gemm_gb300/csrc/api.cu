@@ -40,13 +40,17 @@ constexpr int kNumVariants = 9;
 constexpr int kDefaultVariant = 7;  // large tile, 3 stages
 constexpr int kMaxDevices = 64;
 constexpr int kSkinnyMaxM = 16;
-constexpr int kGroupM = 16;  // M-tiles per group of the tile order (L2 reuse)
+constexpr int kGroupM = 16;
+// 1-bit problems below this many bit-MACs go to the popcount kernel: there
+// the expansion pass and the second launch cost more than they save.
+constexpr double kPopcMaxWork = 1073741824.0;  // M-tiles per group of the tile order (L2 reuse)
 constexpr size_t kFlushBytes = size_t(256) << 20;  // twice the 129 MB L2
 
 thread_local std::string t_last_error;
 std::atomic<int64_t> g_launches{0};
 std::atomic<int> g_chunk_s8{1024};
 std::atomic<int> g_chunk_s4{131072};
+std::atomic<int> g_chunk_b1{1 << 23};
 
 lbgemm_status fail(lbgemm_status st, const char* fmt, ...) {
   char buf[512];
@@ -281,7 +285,7 @@ lbgemm_status run_tc_encoded(DeviceState& d, int bits, int64_t M, int64_t N, int
                              const void* encA, const void* encB, int32_t* C, const float* sx,
                              const float* sw, void* Y, int variant, bool after_encode,
                              cudaStream_t stream) {
-  const bool f8 = bits == 4;
+  const bool f8 = bits != 8;  // 4-bit and 1-bit operands are e4m3-encoded
   const bool linear = Y != nullptr;
   TcKernel k = tc_kernel(variant, f8, linear);
   if (!k.launch) return fail(LBGEMM_ERR_UNSUPPORTED, "no kernel for variant %d", variant);
@@ -298,7 +302,8 @@ lbgemm_status run_tc_encoded(DeviceState& d, int bits, int64_t M, int64_t N, int
   p.K = (int)K;
   const int bk = f8 ? 128 : 64;
   p.num_kb = (int)((kp + bk - 1) / bk);
-  const int chunk_elems = f8 ? g_chunk_s4.load() : g_chunk_s8.load();
+  const int chunk_elems =
+      bits == 8 ? g_chunk_s8.load() : bits == 4 ? g_chunk_s4.load() : g_chunk_b1.load();
   p.chunk_kb = std::max(1, chunk_elems / bk);
   p.tiles_m = (int)((M + 127) / 128);
   p.tiles_n = (int)((N + k.tile_n - 1) / k.tile_n);
@@ -361,10 +366,12 @@ lbgemm_status run_any(int bits, int64_t M, int64_t N, int64_t K, const void* A, 
   const bool auto_pick = variant < 0;
   if (auto_pick) variant = table_select(d->sm_count, bits, M, N, K);
   cudaError_t e;
-  if (bits == 1) {
-    e = lbg::launch_b1_popc(variant / 3, variant % 3 + 2, static_cast<const uint32_t*>(A),
-                            static_cast<const uint32_t*>(B), M, N, K, C, stream);
-    if (e != cudaSuccess) return cuda_fail(e, "1-bit GEMM launch");
+  if (bits == 1 && auto_pick && (double)M * (double)N * (double)K < kPopcMaxWork) {
+    // Small 1-bit problems: XOR + popcount on CUDA cores, no re-encoding.
+    e = lbg::launch_b1_popc(kDefaultVariant / 3, kDefaultVariant % 3 + 2,
+                            static_cast<const uint32_t*>(A), static_cast<const uint32_t*>(B), M, N,
+                            K, C, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "1-bit popcount GEMM launch");
     g_launches += 1;
     return LBGEMM_OK;
   }
@@ -435,15 +442,7 @@ lbgemm_status lbgemm_variant_info(int bits, int variant, int* tile_m, int* tile_
   if ((bits != 8 && bits != 4 && bits != 1) || variant < 0 || variant >= kNumVariants)
     return fail(LBGEMM_ERR_INVALID_ARG, "unknown bits/variant");
   const int tile = variant / 3;
-  int bm, bn, bk;
-  if (bits == 1) {
-    lbg::b1_tile_shape(tile, &bm, &bn);
-    bk = 32 * 32;
-  } else {
-    bm = 128;
-    bn = 64 << tile;
-    bk = bits == 8 ? 64 : 128;
-  }
+  const int bm = 128, bn = 64 << tile, bk = bits == 8 ? 64 : 128;
   if (tile_m) *tile_m = bm;
   if (tile_n) *tile_n = bn;
   if (tile_k) *tile_k = bk;
@@ -469,8 +468,31 @@ lbgemm_status lbgemm_run_variant(int bits, int64_t M, int64_t N, int64_t K, cons
   }
 }
 
+lbgemm_status lbgemm_run_popc(int64_t M, int64_t N, int64_t K, const uint32_t* A,
+                              const uint32_t* B, int32_t* C, int variant, void* stream) {
+  try {
+    lbgemm_status st = check_gemm_args(1, M, N, K, A, B, C);
+    if (st != LBGEMM_OK) return st;
+    if (variant < -1 || variant >= kNumVariants)
+      return fail(LBGEMM_ERR_INVALID_ARG, "variant %d out of range", variant);
+    if (M == 0 || N == 0) return LBGEMM_OK;
+    DeviceState* d = nullptr;
+    st = device_state(&d);
+    if (st != LBGEMM_OK) return st;
+    if (variant < 0) variant = kDefaultVariant;
+    cudaError_t e = lbg::launch_b1_popc(variant / 3, variant % 3 + 2, A, B, M, N, K, C,
+                                        as_stream(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "1-bit popcount GEMM launch");
+    g_launches += 1;
+    return LBGEMM_OK;
+  } catch (...) {
+    return fail(LBGEMM_ERR_CUDA, "internal error");
+  }
+}
+
 size_t lbgemm_workspace_size(int bits, int64_t M, int64_t N, int64_t K) {
-  if ((bits != 8 && bits != 4) || M <= 0 || N <= 0 || K <= 0) return 0;
+  if ((bits != 8 && bits != 4 && bits != 1) || M <= 0 || N <= 0 || K <= 0) return 0;
+  if (bits == 1 && K % 32) return 0;
   return enc_bytes(bits, M, K) + enc_bytes(bits, N, K);
 }
 
@@ -486,14 +508,15 @@ lbgemm_status lbgemm_run_ws(int bits, int64_t M, int64_t N, int64_t K, const voi
 }
 
 size_t lbgemm_encoded_size(int bits, int64_t rows, int64_t K) {
-  if ((bits != 8 && bits != 4) || rows <= 0 || K <= 0) return 0;
+  if ((bits != 8 && bits != 4 && bits != 1) || rows <= 0 || K <= 0) return 0;
   return enc_bytes(bits, rows, K);
 }
 
 lbgemm_status lbgemm_encode(int bits, int64_t rows, int64_t K, const void* src, void* dst,
                             void* stream) {
   try {
-    if (bits != 8 && bits != 4) return fail(LBGEMM_ERR_INVALID_ARG, "encode: bits must be 8 or 4");
+    if (bits != 8 && bits != 4 && bits != 1)
+      return fail(LBGEMM_ERR_INVALID_ARG, "encode: bits must be 8, 4 or 1");
     lbgemm_status st = check_gemm_args(bits, rows, 1, K, src, dst, dst);
     if (st != LBGEMM_OK || rows == 0) return st;
     DeviceState* d = nullptr;
@@ -508,8 +531,8 @@ lbgemm_status lbgemm_encode(int bits, int64_t rows, int64_t K, const void* src, 
 lbgemm_status lbgemm_run_encoded(int bits, int64_t M, int64_t N, int64_t K, const void* A_enc,
                                  const void* B_enc, int32_t* C, int variant, void* stream) {
   try {
-    if (bits != 8 && bits != 4)
-      return fail(LBGEMM_ERR_INVALID_ARG, "encoded operands exist for bits 8 and 4 only");
+    if (bits != 8 && bits != 4 && bits != 1)
+      return fail(LBGEMM_ERR_INVALID_ARG, "bits must be 8, 4 or 1");
     lbgemm_status st = check_gemm_args(bits, M, N, K, A_enc, B_enc, C);
     if (st != LBGEMM_OK) return st;
     if (variant < -1 || variant >= kNumVariants)
@@ -736,11 +759,20 @@ lbgemm_status lbgemm_set_exact_chunk(int bits, int k_elems) {
     g_chunk_s4 = k_elems;
     return LBGEMM_OK;
   }
-  return fail(LBGEMM_ERR_INVALID_ARG, "exact chunks exist for bits 8 and 4 only");
+  if (bits == 1) {
+    if (k_elems < 128 || k_elems > (1 << 24) || k_elems % 128)
+      return fail(LBGEMM_ERR_INVALID_ARG, "1-bit chunk must be a multiple of 128 in [128, 2^24]");
+    g_chunk_b1 = k_elems;
+    return LBGEMM_OK;
+  }
+  return fail(LBGEMM_ERR_INVALID_ARG, "bits must be 8, 4 or 1");
 }
 
 int lbgemm_get_exact_chunk(int bits) {
-  return bits == 8 ? g_chunk_s8.load() : bits == 4 ? g_chunk_s4.load() : -1;
+  return bits == 8 ? g_chunk_s8.load()
+         : bits == 4 ? g_chunk_s4.load()
+         : bits == 1 ? g_chunk_b1.load()
+                     : -1;
 }
 
 lbgemm_status lbgemm_device_status(void* stream) {

@@ -115,6 +115,39 @@ __global__ void cvt_s4_e4m3_kernel(CvtJob ja, CvtJob jb, int64_t K, int64_t Kp) 
   }
 }
 
+// +-1 bits (32 per word, bit 1 = +1) -> e4m3 bytes, one per element: every
+// +-1 is an e4m3 value, so the tensor-core route stays exact.  Rows of W
+// words become rows of 32 W bytes.  Each thread expands one word through a
+// 16-entry table (four bits -> four codes) built per block with CUDA's fp8
+// conversion of +1 and -1.
+__global__ void cvt_b1_e4m3_kernel(CvtJob ja, CvtJob jb, int64_t W) {
+  allow_dependent_launch();
+  __shared__ uint32_t nib[16];
+  if (threadIdx.x < 16) {
+    const uint32_t pos = __nv_cvt_float_to_fp8(1.0f, __NV_SATFINITE, __NV_E4M3);
+    const uint32_t neg = __nv_cvt_float_to_fp8(-1.0f, __NV_SATFINITE, __NV_E4M3);
+    uint32_t v = 0;
+    for (int q = 0; q < 4; ++q) v |= (((threadIdx.x >> q) & 1) ? pos : neg) << (8 * q);
+    nib[threadIdx.x] = v;
+  }
+  __syncthreads();
+  const int64_t total_a = ja.rows * W;
+  const int64_t total = total_a + jb.rows * W;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const bool in_a = i < total_a;
+    const int64_t ii = in_a ? i : i - total_a;
+    const CvtJob& j = in_a ? ja : jb;
+    const uint32_t word = __ldg(static_cast<const uint32_t*>(j.src) + ii);
+    uint32_t o[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) o[q] = nib[(word >> (4 * q)) & 15u];
+    uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(j.dst) + ii * 32);
+    dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+    dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+  }
+}
+
 // ---------------------------------------------------------------------------
 // Skinny 8-bit GEMM: M <= MT rows of A against all N rows of B.  Each warp
 // owns kSkNR consecutive rows of B and streams them once (16 bytes per lane
@@ -355,12 +388,17 @@ cudaError_t launch_encode_pair(int bits, const void* a, int64_t rows_a, void* en
                                const void* b, int64_t rows_b, void* enc_b, int64_t K, int64_t Kp,
                                int sm_count, cudaStream_t s) {
   if (rows_a + rows_b == 0) return cudaSuccess;
-  const int64_t row_bytes = bits == 8 ? K : K / 2;
+  const int64_t row_bytes = bits == 8 ? K : bits == 4 ? K / 2 : K / 8;
   auto fast = [&](const void* p) {
     return (int)(row_bytes % 8 == 0 && (reinterpret_cast<uintptr_t>(p) & 7) == 0);
   };
   CvtJob ja{a, rows_a, enc_a, a ? fast(a) : 0};
   CvtJob jb{b, rows_b, enc_b, b ? fast(b) : 0};
+  if (bits == 1) {  // K % 32 == 0 and Kp == K: rows are contiguous words
+    const int64_t W = K / 32;
+    cvt_b1_e4m3_kernel<<<grid_for((rows_a + rows_b) * W, 256, sm_count), 256, 0, s>>>(ja, jb, W);
+    return cudaGetLastError();
+  }
   const int64_t vec = bits == 8 ? Kp / 8 : Kp / 16;
   const int grid = grid_for((rows_a + rows_b) * vec, 256, sm_count);
   if (bits == 8)

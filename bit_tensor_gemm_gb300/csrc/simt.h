@@ -7,8 +7,9 @@
 namespace lbg {
 
 // Exact re-encoding of operand rows (bits 8: int8 -> fp16 rows of Kp halves,
-// Kp % 8 == 0; bits 4: packed int4 -> e4m3 rows of Kp bytes, Kp % 16 == 0),
-// zero padded, for up to two operands in one launch (rows_b may be 0).
+// Kp % 8 == 0; bits 4: packed int4 -> e4m3 rows of Kp bytes, Kp % 16 == 0;
+// bits 1: +-1 bits -> e4m3 rows of Kp == K bytes), zero padded, for up to two
+// operands in one launch (rows_b may be 0).
 cudaError_t launch_encode_pair(int bits, const void* a, int64_t rows_a, void* enc_a,
                                const void* b, int64_t rows_b, void* enc_b, int64_t K, int64_t Kp,
                                int sm_count, cudaStream_t s);

@@ -44,6 +44,7 @@ _SIGNATURES = {
     "lbgemm_workspace_size": (ctypes.c_size_t, [_i32, _i64, _i64, _i64]),
     "lbgemm_run_ws": (_i32, [_i32, _i64, _i64, _i64, _vp, _vp, _vp, _i32, _vp, ctypes.c_size_t,
                              _vp]),
+    "lbgemm_run_popc": (_i32, [_i64, _i64, _i64, _vp, _vp, _vp, _i32, _vp]),
     "lbgemm_run_static": (_i32, [_i32, _i64, _i64, _i64, _vp, _vp, _vp, _i32, _vp]),
     "lbgemm_encoded_size": (ctypes.c_size_t, [_i32, _i64, _i64]),
     "lbgemm_encode": (_i32, [_i32, _i64, _i64, _vp, _vp, _vp]),
@@ -164,6 +165,11 @@ def lbgemm_workspace_size(bits, M, N, K) -> int:
 def lbgemm_run_ws(bits, M, N, K, A, B, C, variant, workspace, workspace_bytes, stream=None):
     _check(load().lbgemm_run_ws(bits, M, N, K, _addr(A), _addr(B), _addr(C), variant,
                                 _addr(workspace), workspace_bytes, _stream(stream)))
+
+
+def lbgemm_run_popc(M, N, K, A, B, C, variant=-1, stream=None) -> None:
+    _check(load().lbgemm_run_popc(M, N, K, _addr(A), _addr(B), _addr(C), variant,
+                                  _stream(stream)))
 
 
 STATIC_SCRATCH_BYTES = 32 << 20  # LBGEMM_STATIC_SCRATCH_BYTES in lbgemm.h

@@ -68,15 +68,20 @@ typedef enum {
 int lbgemm_num_variants(void);
 int lbgemm_default_variant(void);
 
-/* Tile shape and stage count of variant v for operands of `bits`
- * (tile_m x tile_n output tile, tile_k logical elements per pipeline stage).
+/* Tile shape and stage count of variant v of the tensor-core kernel for
+ * operands of `bits` (tile_m x tile_n output tile, tile_k logical elements
+ * per pipeline stage: 64 for bits 8, 128 for bits 4 and 1).
  * Returns LBGEMM_ERR_INVALID_ARG for an unknown v or bits. */
 lbgemm_status lbgemm_variant_info(int bits, int variant, int* tile_m, int* tile_n, int* tile_k,
                                   int* stages);
 
 /* C = A . B^T with the variant the selection table picks for
- * (bits, M, N, K, SM count).  [LBG] intro, sections 1-2.  Scratch memory
- * (bits 8 and 4 convert their operands to an exact tensor-core encoding) is
+ * (bits, M, N, K, SM count).  [LBG] intro, sections 1-2.  Every bit width
+ * runs on the tensor cores through an exact re-encoding of its operands
+ * (int8 -> fp16, int4 -> e4m3, +-1 -> e4m3), except two shape rules: 8-bit
+ * problems with M <= 16 (and K % 16 == 0) run on a kernel that streams B
+ * once, and 1-bit problems with M*N*K < 2^30 run on the XOR-popcount kernel
+ * of lbgemm_run_popc.  Scratch memory for the re-encoding is
  * taken from a per-device buffer the library grows with cudaMalloc on demand;
  * calls from different streams are ordered on it with events.  A call that
  * grows the buffer synchronises the device, so make the first call of the
@@ -84,11 +89,13 @@ lbgemm_status lbgemm_variant_info(int bits, int variant, int* tile_m, int* tile_
 lbgemm_status lbgemm_run(int bits, int64_t M, int64_t N, int64_t K, const void* A, const void* B,
                          int32_t* C, void* stream);
 
-/* As lbgemm_run, forcing variant v (0..8); -1 means "use the table". */
+/* As lbgemm_run, forcing variant v (0..8) of the tensor-core kernel (no shape
+ * rule applies); -1 means "use the table" (and the shape rules). */
 lbgemm_status lbgemm_run_variant(int bits, int64_t M, int64_t N, int64_t K, const void* A,
                                  const void* B, int32_t* C, int variant, void* stream);
 
-/* Bytes of scratch that lbgemm_run_ws needs for this problem (0 if none). */
+/* Bytes of scratch that lbgemm_run_ws needs for this problem on the
+ * tensor-core route (0 for bad arguments): the re-encoded A and B. */
 size_t lbgemm_workspace_size(int bits, int64_t M, int64_t N, int64_t K);
 
 /* As lbgemm_run_variant, with caller-owned scratch: `workspace` is a device
@@ -111,7 +118,7 @@ lbgemm_status lbgemm_run_ws(int bits, int64_t M, int64_t N, int64_t K, const voi
  * passes A, B and C.  Problems whose scratch (lbgemm_workspace_size) exceeds
  * the array are rejected with LBGEMM_ERR_WORKSPACE before anything runs;
  * for 8-bit operands that is (M + N) * round_up(K, 8) * 2 bytes, e.g. M = N =
- * 2048 at K = 4096.  1-bit problems use no scratch and have no limit.
+ * 2048 at K = 4096; for 1-bit operands (M + N) * K bytes.
  *
  * The first call on each device looks up the array's device address (with
  * that device current); make that first call before any stream capture.
@@ -124,20 +131,29 @@ lbgemm_status lbgemm_run_static(int bits, int64_t M, int64_t N, int64_t K, const
                                 const void* B, int32_t* C, int variant, void* stream);
 
 /* ---- pre-encoded operands ------------------------------------------------------
- * The 8- and 4-bit tensor-core path first re-encodes each operand exactly
- * (int8 -> fp16, int4 -> e4m3; rows padded with zeros to a multiple of 8
- * halves / 16 bytes).  A caller that reuses an operand (the weights of a
+ * The tensor-core path first re-encodes each operand exactly (int8 -> fp16,
+ * int4 -> e4m3, +-1 -> e4m3 one byte per element; rows padded with zeros to
+ * a multiple of 8 halves / 16 bytes).  A caller that reuses an operand (the weights of a
  * linear layer) can encode it once and call lbgemm_run_encoded, which runs
  * the GEMM kernel alone.  The encoded layout is private to this library
  * version: only lbgemm_encode may write it. */
 size_t lbgemm_encoded_size(int bits, int64_t rows, int64_t K);
 /* dst: device buffer of lbgemm_encoded_size(bits, rows, K) bytes, 16-byte
- * aligned.  src: rows x K operand in the format of `bits` (8 or 4). */
+ * aligned.  src: rows x K operand in the format of `bits` (8, 4 or 1). */
 lbgemm_status lbgemm_encode(int bits, int64_t rows, int64_t K, const void* src, void* dst,
                             void* stream);
 /* C = A . B^T from encoded operands (variant -1 = table). */
 lbgemm_status lbgemm_run_encoded(int bits, int64_t M, int64_t N, int64_t K, const void* A_enc,
                                  const void* B_enc, int32_t* C, int variant, void* stream);
+
+/* The 1-bit product on CUDA cores: C[m][n] = K - 2 * sum_w popc(A[m][w] ^
+ * B[n][w]) with XOR and __popc, no re-encoding and no scratch.  [LBG]
+ * intro (1-bit GEMM).  A, B: uint32 words, K/32 per row; K % 32 == 0.
+ * Variant v picks the CTA tile (v / 3: 0 = 64 x 64, 1 = 128 x 64,
+ * 2 = 128 x 128 outputs, 256 threads) and v % 3 + 2 cp.async stages of 32
+ * words of K; -1 = variant 7.  Asynchronous on `stream`. */
+lbgemm_status lbgemm_run_popc(int64_t M, int64_t N, int64_t K, const uint32_t* A,
+                              const uint32_t* B, int32_t* C, int variant, void* stream);
 
 /* Quantised linear layer, [LBG] section 4 (a linear layer on the low-bit
  * GEMM): Y[m][n] = bf16_round_nearest_even( (float)acc[m][n] * sx[m] * sw[n] )
@@ -198,10 +214,10 @@ lbgemm_status lbgemm_run_host(int bits, int64_t M, int64_t N, int64_t K, const v
  * The tensor-core path sums fp32 products of exact encodings in chunks of
  * k_elems along K and adds the chunks in int32.  A chunk is exact while
  * k_elems * max|a*b| <= 2^24 (every integer of magnitude <= 2^24 is an fp32
- * value): max|a*b| = 2^14 for bits 8 (k_elems <= 1024) and 2^6 for bits 4
- * (k_elems <= 262144).  Defaults: 1024 for bits 8, 131072 for bits 4.
- * k_elems must be a multiple of 64 (bits 8) or 128 (bits 4).  Process-wide;
- * affects calls launched afterwards. */
+ * value): max|a*b| = 2^14 for bits 8 (k_elems <= 1024), 2^6 for bits 4
+ * (k_elems <= 262144) and 1 for bits 1 (k_elems <= 2^24).  Defaults: 1024,
+ * 131072 and 2^23.  k_elems must be a multiple of 64 (bits 8) or 128 (bits 4
+ * and 1).  Process-wide; affects calls launched afterwards. */
 lbgemm_status lbgemm_set_exact_chunk(int bits, int k_elems);
 int lbgemm_get_exact_chunk(int bits);
 

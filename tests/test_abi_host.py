@@ -48,7 +48,7 @@ def test_variant_space(lib):
         assert info["tile_n"] == (64, 128, 256)[tile] and info["tile_m"] == 128
         assert L.lbgemm_variant_info(4, v)["tile_k"] == 128
         b1 = L.lbgemm_variant_info(1, v)
-        assert (b1["tile_m"], b1["tile_n"]) == ((64, 64), (128, 64), (128, 128))[tile]
+        assert (b1["tile_m"], b1["tile_n"], b1["tile_k"]) == (128, (64, 128, 256)[tile], 128)
     with pytest.raises(L.LbgemmError):
         L.lbgemm_variant_info(8, 9)
 
@@ -110,7 +110,8 @@ def test_table_roundtrip(lib, tmp_path):
 def test_exact_chunk_settings(lib):
     assert L.lbgemm_get_exact_chunk(8) == 1024
     assert L.lbgemm_get_exact_chunk(4) == 131072
-    for bits, bad in [(8, 1088), (8, 100), (4, 64), (4, 1 << 20), (1, 128)]:
+    assert L.lbgemm_get_exact_chunk(1) == 1 << 23
+    for bits, bad in [(8, 1088), (8, 100), (4, 64), (4, 1 << 20), (1, 64), (1, 1 << 25), (2, 128)]:
         with pytest.raises(L.LbgemmError):
             L.lbgemm_set_exact_chunk(bits, bad)
     L.lbgemm_set_exact_chunk(8, 512)
@@ -142,7 +143,8 @@ def test_empty_problem_is_a_noop(lib):
 
 
 def test_workspace_size(lib):
-    assert L.lbgemm_workspace_size(1, 64, 64, 64) == 0
+    assert L.lbgemm_workspace_size(1, 64, 64, 48) == 0   # K % 32 != 0: not a 1-bit problem
+    assert L.lbgemm_workspace_size(1, 64, 64, 64) == 2 * 64 * 64  # one e4m3 byte per bit
     # int8: fp16 copies, rows padded to a multiple of 8 halves, each buffer to 256 bytes
     assert L.lbgemm_workspace_size(8, 3, 5, 9) == 256 + 256
     assert L.lbgemm_workspace_size(8, 256, 256, 256) == 2 * 256 * 256 * 2

@@ -72,9 +72,14 @@ def test_b1_8192_square_k65536():
     K = 65536
     A, B = synth.operands(1, M, N, K, synth.config_seed(4))
     C = torch.empty((M, N), dtype=torch.int32, device="cuda")
-    L.lbgemm_run(1, M, N, K, _dev(A), _dev(B), C)
+    dA, dB = _dev(A), _dev(B)
+    L.lbgemm_run(1, M, N, K, dA, dB, C)  # tensor-core route
     L.lbgemm_device_status()
     _check_sampled(1, A, B, K, C, 3, count=2048)
+    C.fill_(-1)
+    L.lbgemm_run_popc(M, N, K, dA, dB, C)  # XOR-popcount route
+    L.lbgemm_device_status()
+    _check_sampled(1, A, B, K, C, 4, count=2048)
 
 
 @pytest.mark.parametrize("M", [1, 16, 128, 2048])

@@ -160,6 +160,25 @@ def test_b1_every_variant(variant):
                      f"b1 variant {variant} {M}x{N}x{K}")
 
 
+@pytest.mark.parametrize("variant", range(9))
+def test_b1_popc_every_variant(variant):
+    """The XOR-popcount CUDA-core kernel, each of its tile x stage variants."""
+    for i, (M, N, K) in enumerate(SHAPES_1):
+        A, B = synth.operands(1, M, N, K, 300 + i)
+        dC = torch.full((M, N), -7, dtype=torch.int32, device=G().DEV)
+        L.lbgemm_run_popc(M, N, K, G().to_dev(A), G().to_dev(B), dC, variant)
+        L.lbgemm_device_status()
+        assert_exact(dC.cpu().numpy(), oracle.gemm(1, A, B, K), f"b1 popc v{variant} {M}x{N}x{K}")
+
+
+def test_b1_auto_routes():
+    """Default dispatch: small problems on the popcount kernel, large ones on
+    the tensor cores; both exact."""
+    for M, N, K in [(64, 64, 1024), (256, 256, 32768)]:
+        A, B = synth.operands(1, M, N, K, M + K)
+        assert_exact(G().gemm(1, A, B, K), oracle.gemm(1, A, B, K), f"b1 auto {M}x{N}x{K}")
+
+
 def test_b1_closed_forms():
     K = 4096
     g = np.random.default_rng(9)

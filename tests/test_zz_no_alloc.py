@@ -61,6 +61,6 @@ def test_static_limit_is_enforced_before_running():
     assert "static" in L.lbgemm_last_error()
 
 
-def test_static_needs_no_scratch_for_one_bit():
+def test_static_one_bit():
     got, want = _pair(1, 96, 80, 2048, 905, 2)
     assert np.array_equal(got, want)
