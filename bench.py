@@ -53,6 +53,7 @@ def parse_args():
     p.add_argument("--sweep-reps", type=int, default=3)
     p.add_argument("--shapes", type=int, default=0, help="debug: use only the first N shapes")
     p.add_argument("--no-cpu", action="store_true", help="debug: skip the CPU oracle sample")
+    p.add_argument("--dump", default="", help="write per-shape sweep data (JSON) to this path")
     return p.parse_args()
 
 
@@ -240,9 +241,11 @@ def run_ours(args):
     # -- the sweep: nine variants per shape; the table keeps lbgemm_choose's pick ------------
     t_sweep0 = time.perf_counter()
     L.lbgemm_table_clear()
+    sweep_times = []
     for (m, n, k) in shapes:
         t = L.lbgemm_time_variants(8, m, n, k, A, B, C, warmup=1, reps=args.sweep_reps,
                                    flush_l2=True)
+        sweep_times.append(t)
         L.lbgemm_table_set(8, m, n, k, L.lbgemm_choose(t, L.lbgemm_default_variant(), 0.02))
     sweep_s = time.perf_counter() - t_sweep0
 
@@ -300,6 +303,19 @@ def run_ours(args):
     s_ms = np.median(np.array(s_runs), axis=0)
     speed = d_ms / s_ms
     chosen = [L.lbgemm_select(8, *s) for s in shapes]
+    # Per-shape roofline: the slower of the tensor pipe and the HBM bytes of
+    # the operation (int8 A and B read once, int32 C written once).
+    t_roof = np.array([max(2.0 * m * n * k / (peaks["bf16_tflops_sustained"] * 1e12),
+                           (m * k + n * k + 4.0 * m * n) / (peaks["hbm_gbs"] * 1e9))
+                       for m, n, k in shapes])
+    t_roof8 = np.array([max(2.0 * m * n * k / (peaks["bf16_tflops_sustained"] * 1e12),
+                            (m * k + n * k + 4.0 * m * n) / 8.0e12) for m, n, k in shapes])
+    sweep_roofline = {
+        "frac": float(t_roof.sum() / (s_ms.sum() / 1e3)),
+        "frac_hbm_8tbs": float(t_roof8.sum() / (s_ms.sum() / 1e3)),
+        "roofline_tops": ops_step / t_roof.sum() / 1e12,
+        "definition": "sum over shapes of max(2MNK / sustained bf16 peak, (MK+NK+4MN) bytes / "
+                      "HBM) divided by the sum of measured times (selected variants)"}
     worst = int(np.argmin(speed))
     selection = {
         "shapes": len(shapes),
@@ -442,8 +458,15 @@ def run_ours(args):
                        "timing": "sum of per-GEMM CUDA-event times on the launching stream",
                        "parallelism": "replicas" if world > 1 else "single GPU"},
             "clocks": clk, "gpu_launches": launches, "e2e": e2e, "roofline": roofline,
-            "cpu_baseline": cpu, "selection": selection, "per_config": per_config,
+            "cpu_baseline": cpu, "selection": selection, "sweep_roofline": sweep_roofline,
+            "per_config": per_config,
         }), flush=True)
+        if args.dump:
+            with open(args.dump, "w") as f:
+                json.dump({"shapes": shapes, "variant_times_ms": sweep_times, "chosen": chosen,
+                           "selected_ms": s_ms.tolist(), "default_ms": d_ms.tolist(),
+                           "kernel_only_ms": enc_ms, "roofline_ms": (t_roof * 1e3).tolist(),
+                           "sm_count": None}, f)
 
 
 def main():
