@@ -65,7 +65,8 @@ def build(force: bool = False, jobs: int | None = None, verbose: bool = False) -
     with cf.ThreadPoolExecutor(max_workers=jobs) as ex:
         objs = list(ex.map(_compile, srcs))
     tmp = LIBRARY + f".tmp{os.getpid()}"
-    cmd = [nvcc()] + ARCH + ["-shared", "-cudart", "static", "-o", tmp] + objs
+    # -z defs: an undefined symbol fails the link instead of the first dlopen
+    cmd = [nvcc()] + ARCH + ["-shared", "-cudart", "static", "-Xlinker", "-z,defs", "-o", tmp] + objs
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")

@@ -43,7 +43,11 @@ constexpr int kSkinnyMaxM = 16;
 constexpr int kGroupM = 16;
 // 1-bit problems below this many bit-MACs go to the popcount kernel: there
 // the expansion pass and the second launch cost more than they save.
-constexpr double kPopcMaxWork = 1073741824.0;  // M-tiles per group of the tile order (L2 reuse)
+constexpr double kPopcMaxWork = 1073741824.0;
+// 8-bit problems with K <= kSmallMaxK and at most kSmallMaxWork MACs go to the
+// one-launch dp4a kernel.
+constexpr int64_t kSmallMaxK = 512;
+constexpr double kSmallMaxWork = 268435456.0;  // M-tiles per group of the tile order (L2 reuse)
 constexpr size_t kFlushBytes = size_t(256) << 20;  // twice the 129 MB L2
 
 thread_local std::string t_last_error;
@@ -205,6 +209,15 @@ size_t enc_bytes(int bits, int64_t rows, int64_t K) {
 
 bool skinny_ok(int64_t M, int64_t K, const void* A, const void* B) {
   return M <= kSkinnyMaxM && K % 16 == 0 && aligned16(A) && aligned16(B);
+}
+
+// Problems this small run faster as one dp4a launch than as re-encoding plus
+// a tensor-core launch.  Measured on GB300 over M, N, K in {64..2048}: the
+// dp4a kernel wins for K <= 512 up to 2^28 MACs and loses from K = 1024 on
+// (its K loop is latency-bound, one 64-byte stage per memory round trip).
+bool small_ok(int64_t M, int64_t N, int64_t K, const void* A, const void* B) {
+  return K <= kSmallMaxK && (double)M * (double)N * (double)K <= kSmallMaxWork && K % 16 == 0 &&
+         aligned16(A) && aligned16(B);
 }
 
 // ---- selection table --------------------------------------------------------------------
@@ -377,8 +390,15 @@ lbgemm_status run_any(int bits, int64_t M, int64_t N, int64_t K, const void* A, 
   }
   if (bits == 8 && auto_pick && skinny_ok(M, K, A, B)) {
     e = lbg::launch_skinny_s8(static_cast<const int8_t*>(A), static_cast<const int8_t*>(B), (int)M,
-                              (int)N, (int)K, C, nullptr, nullptr, nullptr, stream);
+                              (int)N, (int)K, C, nullptr, nullptr, nullptr, d->sm_count, stream);
     if (e != cudaSuccess) return cuda_fail(e, "skinny GEMM launch");
+    g_launches += 1;
+    return LBGEMM_OK;
+  }
+  if (bits == 8 && auto_pick && small_ok(M, N, K, A, B)) {
+    e = lbg::launch_small_s8(static_cast<const int8_t*>(A), static_cast<const int8_t*>(B), M, N, K,
+                             C, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "small GEMM launch");
     g_launches += 1;
     return LBGEMM_OK;
   }
@@ -412,7 +432,8 @@ lbgemm_status run_linear(int64_t M, int64_t N, int64_t K, const int8_t* X, const
   if (st != LBGEMM_OK) return st;
   const bool auto_pick = variant < 0;
   if (auto_pick && skinny_ok(M, K, X, W)) {
-    cudaError_t e = lbg::launch_skinny_s8(X, W, (int)M, (int)N, (int)K, nullptr, sx, sw, Y, stream);
+    cudaError_t e =
+        lbg::launch_skinny_s8(X, W, (int)M, (int)N, (int)K, nullptr, sx, sw, Y, d->sm_count, stream);
     if (e != cudaSuccess) return cuda_fail(e, "skinny linear launch");
     g_launches += 1;
     return LBGEMM_OK;

@@ -149,49 +149,34 @@ __global__ void cvt_b1_e4m3_kernel(CvtJob ja, CvtJob jb, int64_t W) {
 }
 
 // ---------------------------------------------------------------------------
-// Skinny 8-bit GEMM: M <= MT rows of A against all N rows of B.  Each warp
-// owns kSkNR consecutive rows of B and streams them once (16 bytes per lane
-// per step); A rows come through L1.  Partial sums are combined across the
-// warp by a halving butterfly so that each lane ends with its own outputs.
-constexpr int kSkNR = 4;
+// Skinny 8-bit GEMM: M <= MT rows of A against all N rows of B, for M <= 16.
+// HBM-bound on B, which is streamed exactly once.  Persistent warps each own
+// groups of NR consecutive rows of B; a lane covers 16 bytes of K per step
+// (512 bytes per warp-step); each batch issues the loads of PF steps for all
+// NR rows before consuming any of them.  A rows come through L1.
 constexpr int kSkWarps = 8;
 
-template <int MT, bool LINEAR>
-__global__ void __launch_bounds__(kSkWarps * 32)
-    skinny_s8_kernel(const int8_t* __restrict__ A, const int8_t* __restrict__ B, int M, int N,
-                     int K, int32_t* __restrict__ C, const float* __restrict__ sx,
-                     const float* __restrict__ sw, __nv_bfloat16* __restrict__ Y) {
-  constexpr int NV = MT * kSkNR;
-  const int lane = threadIdx.x & 31;
-  const int warp = threadIdx.x >> 5;
-  const int n0 = (blockIdx.x * kSkWarps + warp) * kSkNR;
-  if (n0 >= N) return;
-  int acc[NV];
+template <int NR>
+__device__ __forceinline__ void skinny_load_step(int4 (&dst)[NR], const int8_t* __restrict__ B,
+                                                 int K, int N, int n0, int k) {
 #pragma unroll
-  for (int i = 0; i < NV; ++i) acc[i] = 0;
-  const int4 zero = make_int4(0, 0, 0, 0);
-  for (int k = lane * 16; k < K; k += 32 * 16) {
-    int4 b[kSkNR];
-#pragma unroll
-    for (int r = 0; r < kSkNR; ++r)
-      b[r] = (n0 + r < N) ? __ldg(reinterpret_cast<const int4*>(B + (int64_t)(n0 + r) * K + k))
-                          : zero;
-#pragma unroll
-    for (int m = 0; m < MT; ++m) {
-      const int4 a = (m < M) ? __ldg(reinterpret_cast<const int4*>(A + (int64_t)m * K + k)) : zero;
-#pragma unroll
-      for (int r = 0; r < kSkNR; ++r) {
-        int s = acc[m * kSkNR + r];
-        s = __dp4a(a.x, b[r].x, s);
-        s = __dp4a(a.y, b[r].y, s);
-        s = __dp4a(a.z, b[r].z, s);
-        s = __dp4a(a.w, b[r].w, s);
-        acc[m * kSkNR + r] = s;
-      }
-    }
-  }
-  // Halving butterfly: at each step a lane keeps half of its values (upper
-  // half if the step's lane bit is set) plus its partner's copy of that half.
+  for (int r = 0; r < NR; ++r)
+    dst[r] = (k < K && n0 + r < N)
+                 ? __ldg(reinterpret_cast<const int4*>(B + (int64_t)(n0 + r) * K + k))
+                 : make_int4(0, 0, 0, 0);
+}
+
+// Combines a warp's partial sums of one group (halving butterfly: at each
+// step a lane keeps half of its values -- the upper half if the step's lane
+// bit is set -- plus its partner's copy of that half; once one value is left
+// the remaining steps simply add), writes the group's outputs and clears acc.
+template <int MT, int NR, bool LINEAR>
+__device__ __forceinline__ void skinny_finish(int (&acc)[MT * NR], int lane, int M, int N, int n0,
+                                              int32_t* __restrict__ C,
+                                              const float* __restrict__ sx,
+                                              const float* __restrict__ sw,
+                                              __nv_bfloat16* __restrict__ Y) {
+  constexpr int NV = MT * NR;
   int n = NV;
   int idx_base = 0;
 #pragma unroll
@@ -200,7 +185,7 @@ __global__ void __launch_bounds__(kSkWarps * 32)
       const bool upper = (lane & off) != 0;
       const int h = n / 2;
 #pragma unroll
-      for (int i = 0; i < NV / 2; ++i) {
+      for (int i = 0; i < (NV > 1 ? NV / 2 : 1); ++i) {
         if (i < h) {
           const int send = upper ? acc[i] : acc[i + h];
           const int keep = upper ? acc[i + h] : acc[i];
@@ -214,19 +199,143 @@ __global__ void __launch_bounds__(kSkWarps * 32)
     }
   }
   // Lanes that share idx_base hold the same totals; the lowest one writes.
-  // n values remain per lane: indices idx_base .. idx_base + n - 1.
-  const int owner_mask = (NV >= 32) ? 0 : (32 / NV) - 1;  // low lane bits summed out
+  const int owner_mask = (NV >= 32) ? 0 : (32 / NV) - 1;
   if ((lane & owner_mask) == 0) {
 #pragma unroll
     for (int j = 0; j < (NV >= 32 ? NV / 32 : 1); ++j) {
       const int idx = idx_base + j;
-      const int m = idx / kSkNR, r = idx % kSkNR;
+      const int m = idx / NR, r = idx % NR;
       if (m < M && n0 + r < N) {
         if (LINEAR)
           Y[(int64_t)m * N + n0 + r] = __float2bfloat16_rn((float)acc[j] * sx[m] * sw[n0 + r]);
         else
           C[(int64_t)m * N + n0 + r] = acc[j];
       }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < NV; ++i) acc[i] = 0;
+}
+
+template <int MT, int NR, int PF, int MINB, bool LINEAR>
+__global__ void __launch_bounds__(kSkWarps * 32, MINB)
+    skinny_s8_kernel(const int8_t* __restrict__ A, const int8_t* __restrict__ B, int M, int N,
+                     int K, int32_t* __restrict__ C, const float* __restrict__ sx,
+                     const float* __restrict__ sw, __nv_bfloat16* __restrict__ Y) {
+  constexpr int NV = MT * NR;
+  const int lane = threadIdx.x & 31;
+  const int nwarps = gridDim.x * kSkWarps;
+  const int groups = (N + NR - 1) / NR;
+  const int steps = (K + 511) / 512;
+  int acc[NV];
+#pragma unroll
+  for (int i = 0; i < NV; ++i) acc[i] = 0;
+  for (int g = blockIdx.x * kSkWarps + (threadIdx.x >> 5); g < groups; g += nwarps) {
+    const int n0 = g * NR;
+    for (int s0 = 0; s0 < steps; s0 += PF) {
+      // issue every load of this batch of PF steps, then consume them
+      int4 v[PF][NR];
+#pragma unroll
+      for (int q = 0; q < PF; ++q)
+        skinny_load_step<NR>(v[q], B, K, N, n0, (s0 + q) * 512 + lane * 16);
+#pragma unroll
+      for (int q = 0; q < PF; ++q) {
+        const int k = (s0 + q) * 512 + lane * 16;
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+          const int4 a = (m < M && k < K)
+                             ? __ldg(reinterpret_cast<const int4*>(A + (int64_t)m * K + k))
+                             : make_int4(0, 0, 0, 0);
+#pragma unroll
+          for (int r = 0; r < NR; ++r) {
+            int t = acc[m * NR + r];
+            t = __dp4a(a.x, v[q][r].x, t);
+            t = __dp4a(a.y, v[q][r].y, t);
+            t = __dp4a(a.z, v[q][r].z, t);
+            t = __dp4a(a.w, v[q][r].w, t);
+            acc[m * NR + r] = t;
+          }
+        }
+      }
+    }
+    skinny_finish<MT, NR, LINEAR>(acc, lane, M, N, n0, C, sx, sw, Y);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Small 8-bit GEMM on CUDA cores (dp4a), for problems too small to pay for the
+// re-encoding pass and a second launch: one launch, int8 read directly.  CTA
+// tile 64 x 64, 256 threads as a 16 x 16 grid, thread (ty, tx) owning rows
+// ty + 16 i and columns tx + 16 j; K staged 64 bytes at a time through a
+// two-stage cp.async ring.  Out-of-range rows and K bytes load as zero.
+// Requires K % 16 == 0 and 16-byte aligned A and B.
+constexpr int kSmKS = 64;           // bytes of K per stage
+constexpr int kSmStride = kSmKS + 16;  // padded smem row, 16-byte aligned
+
+__device__ __forceinline__ void small_load_tile(int8_t* dst, const int8_t* src, int64_t rows,
+                                                int64_t K, int64_t r0, int64_t k0) {
+  // 64 rows x 64 bytes = 256 chunks of 16 bytes: one per thread
+  const int r = threadIdx.x >> 2, c = (threadIdx.x & 3) * 16;
+  const int64_t gr = r0 + r, gk = k0 + c;
+  const bool ok = gr < rows && gk < K;
+  const int8_t* g = ok ? src + gr * K + gk : src;
+  const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst + r * kSmStride + c));
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(d), "l"(g), "r"(ok ? 16 : 0)
+               : "memory");
+}
+
+__global__ void __launch_bounds__(256)
+    small_s8_kernel(const int8_t* __restrict__ A, const int8_t* __restrict__ B, int64_t M,
+                    int64_t N, int64_t K, int32_t* __restrict__ C) {
+  __shared__ __align__(16) int8_t sA[2][64 * kSmStride];
+  __shared__ __align__(16) int8_t sB[2][64 * kSmStride];
+  const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
+  const int64_t m0 = (int64_t)blockIdx.y * 64, n0 = (int64_t)blockIdx.x * 64;
+  const int64_t num_kt = (K + kSmKS - 1) / kSmKS;
+  int acc[4][4] = {};
+  small_load_tile(sA[0], A, M, K, m0, 0);
+  small_load_tile(sB[0], B, N, K, n0, 0);
+  asm volatile("cp.async.commit_group;" ::: "memory");
+  for (int64_t kt = 0; kt < num_kt; ++kt) {
+    const int cur = (int)(kt & 1);
+    if (kt + 1 < num_kt) {
+      small_load_tile(sA[cur ^ 1], A, M, K, m0, (kt + 1) * kSmKS);
+      small_load_tile(sB[cur ^ 1], B, N, K, n0, (kt + 1) * kSmKS);
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+    asm volatile("cp.async.wait_group 1;" ::: "memory");
+    __syncthreads();
+#pragma unroll
+    for (int c = 0; c < kSmKS; c += 16) {
+      int4 a[4], b[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        a[i] = *reinterpret_cast<const int4*>(sA[cur] + (ty + 16 * i) * kSmStride + c);
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        b[j] = *reinterpret_cast<const int4*>(sB[cur] + (tx + 16 * j) * kSmStride + c);
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          int s = acc[i][j];
+          s = __dp4a(a[i].x, b[j].x, s);
+          s = __dp4a(a[i].y, b[j].y, s);
+          s = __dp4a(a[i].z, b[j].z, s);
+          s = __dp4a(a[i].w, b[j].w, s);
+          acc[i][j] = s;
+        }
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int64_t m = m0 + ty + 16 * i;
+    if (m >= M) continue;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int64_t n = n0 + tx + 16 * j;
+      if (n < N) C[m * N + n] = acc[i][j];
     }
   }
 }
@@ -408,29 +517,43 @@ cudaError_t launch_encode_pair(int bits, const void* a, int64_t rows_a, void* en
   return cudaGetLastError();
 }
 
-template <int MT, bool LINEAR>
+cudaError_t launch_small_s8(const int8_t* A, const int8_t* B, int64_t M, int64_t N, int64_t K,
+                            int32_t* C, cudaStream_t s) {
+  if (M == 0 || N == 0) return cudaSuccess;
+  const dim3 grid((unsigned)((N + 63) / 64), (unsigned)((M + 63) / 64));
+  small_s8_kernel<<<grid, 256, 0, s>>>(A, B, M, N, K, C);
+  return cudaGetLastError();
+}
+
+template <int MT, int NR, int PF, int MINB, bool LINEAR>
 static cudaError_t skinny_go(const int8_t* A, const int8_t* B, int M, int N, int K, int32_t* C,
-                             const float* sx, const float* sw, void* Y, cudaStream_t s) {
-  const int rows_per_block = kSkWarps * kSkNR;
-  const int grid = (N + rows_per_block - 1) / rows_per_block;
-  skinny_s8_kernel<MT, LINEAR><<<grid, kSkWarps * 32, 0, s>>>(
+                             const float* sx, const float* sw, void* Y, int sm_count,
+                             cudaStream_t s) {
+  const int groups = (N + NR - 1) / NR;
+  const int want = (groups + kSkWarps - 1) / kSkWarps;
+  const int grid = want < sm_count * MINB ? want : sm_count * MINB;
+  skinny_s8_kernel<MT, NR, PF, MINB, LINEAR><<<grid, kSkWarps * 32, 0, s>>>(
       A, B, M, N, K, C, sx, sw, static_cast<__nv_bfloat16*>(Y));
   return cudaGetLastError();
 }
 
+template <bool LINEAR>
+static cudaError_t skinny_pick(const int8_t* A, const int8_t* B, int M, int N, int K, int32_t* C,
+                               const float* sx, const float* sw, void* Y, int sm, cudaStream_t s) {
+  // (rows of A, rows of B per warp, steps per load batch, CTAs per SM), the
+  // fastest of a sweep of these on GB300 at N = 11008 and 65536, K = 4096
+  if (M <= 1) return skinny_go<1, 2, 4, 3, LINEAR>(A, B, M, N, K, C, sx, sw, Y, sm, s);
+  if (M <= 2) return skinny_go<2, 2, 4, 3, LINEAR>(A, B, M, N, K, C, sx, sw, Y, sm, s);
+  if (M <= 4) return skinny_go<4, 2, 4, 2, LINEAR>(A, B, M, N, K, C, sx, sw, Y, sm, s);
+  if (M <= 8) return skinny_go<8, 4, 2, 2, LINEAR>(A, B, M, N, K, C, sx, sw, Y, sm, s);
+  return skinny_go<16, 4, 2, 2, LINEAR>(A, B, M, N, K, C, sx, sw, Y, sm, s);
+}
+
 cudaError_t launch_skinny_s8(const int8_t* A, const int8_t* B, int M, int N, int K, int32_t* C,
-                             const float* sx, const float* sw, void* Y, cudaStream_t s) {
-  const bool lin = Y != nullptr;
-  if (M <= 1) return lin ? skinny_go<1, true>(A, B, M, N, K, C, sx, sw, Y, s)
-                         : skinny_go<1, false>(A, B, M, N, K, C, sx, sw, Y, s);
-  if (M <= 2) return lin ? skinny_go<2, true>(A, B, M, N, K, C, sx, sw, Y, s)
-                         : skinny_go<2, false>(A, B, M, N, K, C, sx, sw, Y, s);
-  if (M <= 4) return lin ? skinny_go<4, true>(A, B, M, N, K, C, sx, sw, Y, s)
-                         : skinny_go<4, false>(A, B, M, N, K, C, sx, sw, Y, s);
-  if (M <= 8) return lin ? skinny_go<8, true>(A, B, M, N, K, C, sx, sw, Y, s)
-                         : skinny_go<8, false>(A, B, M, N, K, C, sx, sw, Y, s);
-  return lin ? skinny_go<16, true>(A, B, M, N, K, C, sx, sw, Y, s)
-             : skinny_go<16, false>(A, B, M, N, K, C, sx, sw, Y, s);
+                             const float* sx, const float* sw, void* Y, int sm_count,
+                             cudaStream_t s) {
+  return Y != nullptr ? skinny_pick<true>(A, B, M, N, K, C, sx, sw, Y, sm_count, s)
+                      : skinny_pick<false>(A, B, M, N, K, C, sx, sw, Y, sm_count, s);
 }
 
 template <int BM, int BN, int STAGES>

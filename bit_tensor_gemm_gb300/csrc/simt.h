@@ -16,7 +16,11 @@ cudaError_t launch_encode_pair(int bits, const void* a, int64_t rows_a, void* en
 // M <= 16, K % 16 == 0, A and B 16-byte aligned.  Y != nullptr selects the
 // linear epilogue (bf16 Y with scales sx, sw) instead of int32 C.
 cudaError_t launch_skinny_s8(const int8_t* A, const int8_t* B, int M, int N, int K, int32_t* C,
-                             const float* sx, const float* sw, void* Y, cudaStream_t s);
+                             const float* sx, const float* sw, void* Y, int sm_count,
+                             cudaStream_t s);
+// Small 8-bit GEMM on dp4a, one launch; K % 16 == 0, A and B 16-byte aligned.
+cudaError_t launch_small_s8(const int8_t* A, const int8_t* B, int64_t M, int64_t N, int64_t K,
+                            int32_t* C, cudaStream_t s);
 // 1-bit GEMM, tile class 0..2 and 2..4 stages; K % 32 == 0.
 cudaError_t launch_b1_popc(int tile, int stages, const uint32_t* A, const uint32_t* B, int64_t M,
                            int64_t N, int64_t K, int32_t* C, cudaStream_t s);

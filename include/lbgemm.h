@@ -78,10 +78,11 @@ lbgemm_status lbgemm_variant_info(int bits, int variant, int* tile_m, int* tile_
 /* C = A . B^T with the variant the selection table picks for
  * (bits, M, N, K, SM count).  [LBG] intro, sections 1-2.  Every bit width
  * runs on the tensor cores through an exact re-encoding of its operands
- * (int8 -> fp16, int4 -> e4m3, +-1 -> e4m3), except two shape rules: 8-bit
- * problems with M <= 16 (and K % 16 == 0) run on a kernel that streams B
- * once, and 1-bit problems with M*N*K < 2^30 run on the XOR-popcount kernel
- * of lbgemm_run_popc.  Scratch memory for the re-encoding is
+ * (int8 -> fp16, int4 -> e4m3, +-1 -> e4m3), except three shape rules:
+ * 8-bit problems with M <= 16 run on a kernel that streams B once, 8-bit
+ * problems with K <= 512 and M*N*K <= 2^28 on a one-launch dp4a kernel (both
+ * need K % 16 == 0), and 1-bit problems with M*N*K < 2^30 on the
+ * XOR-popcount kernel of lbgemm_run_popc.  Scratch memory for the re-encoding is
  * taken from a per-device buffer the library grows with cudaMalloc on demand;
  * calls from different streams are ordered on it with events.  A call that
  * grows the buffer synchronises the device, so make the first call of the

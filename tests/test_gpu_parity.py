@@ -66,6 +66,16 @@ def test_int8_skinny_path(M):
         assert_exact(G().gemm(8, A, B, K), oracle.gemm(8, A, B, K), f"int8 skinny {M}x{N}x{K}")
 
 
+def test_int8_small_dp4a_path():
+    """Default dispatch of small problems (K <= 512, M*N*K <= 2^28): the
+    one-launch dp4a kernel, with ragged M, N and K tails."""
+    for M, N, K in [(17, 19, 16), (64, 64, 64), (100, 300, 144), (1000, 250, 512), (65, 4000, 32)]:
+        A, B = synth.operands(8, M, N, K, 13 * M + K)
+        assert_exact(G().gemm(8, A, B, K), oracle.gemm(8, A, B, K), f"int8 small {M}x{N}x{K}")
+    A = np.full((40, 512), -128, np.int8)
+    assert np.all(G().gemm(8, A, A, 512) == 16384 * 512)
+
+
 def test_int8_full_range_and_extremes():
     g = np.random.default_rng(5)
     M, N, K = 130, 70, 3000
