@@ -47,6 +47,11 @@ constexpr double kPopcMaxWork = 1073741824.0;
 // 8-bit problems with K <= kSmallMaxK and at most kSmallMaxWork MACs go to the
 // one-launch dp4a kernel.
 constexpr int64_t kSmallMaxK = 512;
+// Skinny 8-bit problems on the fused-conversion kernel (see fused_route).
+constexpr int64_t kFusedMaxSide = 256;
+constexpr int64_t kFusedMinOther = 2048;
+constexpr int64_t kFusedMinK = 1024;
+constexpr int kFusedTileN = 128;
 constexpr double kSmallMaxWork = 268435456.0;  // M-tiles per group of the tile order (L2 reuse)
 constexpr size_t kFlushBytes = size_t(256) << 20;  // twice the 129 MB L2
 
@@ -273,7 +278,8 @@ int occupancy(DeviceState& d, const TcKernel& k) {
   if (it != d.occupancy.end()) return it->second;
   cudaFuncSetAttribute(k.func, cudaFuncAttributeMaxDynamicSharedMemorySize, k.smem);
   int occ = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k.func, 320, k.smem) != cudaSuccess)
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k.func, k.threads, k.smem) !=
+      cudaSuccess)
     occ = 1;
   occ = std::max(1, std::min(occ, 512 / k.tmem_cols));
   d.occupancy[k.func] = occ;
@@ -365,6 +371,78 @@ lbgemm_status run_tc(DeviceState& d, int bits, int64_t M, int64_t N, int64_t K, 
   return run_tc_encoded(d, bits, M, N, K, encA, encB, C, sx, sw, Y, variant, true, stream);
 }
 
+// Skinny 8-bit problems: only the small operand is re-encoded ahead; the
+// kernel converts the large one from int8 itself (fuse 1: B large, fuse 2: A
+// large).  Requires K % 16 == 0 (16-byte int8 row strides for TMA).
+lbgemm_status run_tc_fused(DeviceState& d, int fuse, int tile_n, int64_t M, int64_t N, int64_t K,
+                           const void* A, const void* B, int32_t* C, const float* sx,
+                           const float* sw, void* Y, void* ws, cudaStream_t stream) {
+  const bool linear = Y != nullptr;
+  TcKernel k = lbg::tc_kernel_fused(fuse, tile_n, linear);
+  if (!k.launch) return fail(LBGEMM_ERR_UNSUPPORTED, "no fused kernel (fuse %d, tile %d)", fuse, tile_n);
+  const int64_t kp = enc_kp(8, K);  // == K when K % 16 == 0
+  lbgemm_status st = fuse == 1 ? encode_operands(d, 8, A, M, ws, nullptr, 0, nullptr, K, stream)
+                               : encode_operands(d, 8, B, N, ws, nullptr, 0, nullptr, K, stream);
+  if (st != LBGEMM_OK) return st;
+  CUtensorMap ma, mb;
+  cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)(fuse == 1 ? N : M)};
+  cuuint64_t strides[1] = {(cuuint64_t)K};
+  cuuint32_t box[2] = {64, (cuuint32_t)(fuse == 1 ? tile_n : 128)};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(fuse == 1 ? &mb : &ma, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
+                        const_cast<void*>(fuse == 1 ? B : A), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(LBGEMM_ERR_CUDA, "cuTensorMapEncodeTiled (int8) failed (%d)", (int)r);
+  st = fuse == 1 ? encode_kmajor(&ma, ws, M, kp, true, 128)
+                 : encode_kmajor(&mb, ws, N, kp, true, tile_n);
+  if (st != LBGEMM_OK) return st;
+  TcParams p{};
+  p.M = (int)M;
+  p.N = (int)N;
+  p.K = (int)K;
+  p.num_kb = (int)((kp + 63) / 64);
+  p.chunk_kb = std::max(1, g_chunk_s8.load() / 64);
+  p.tiles_m = (int)((M + 127) / 128);
+  p.tiles_n = (int)((N + tile_n - 1) / tile_n);
+  p.num_tiles = p.tiles_m * p.tiles_n;
+  p.group_m = kGroupM;
+  p.C = C;
+  p.sx = sx;
+  p.sw = sw;
+  p.Y = static_cast<__nv_bfloat16*>(Y);
+  p.status = d.status;
+  p.vec_ok = linear ? (N % 8 == 0) && aligned16(Y) : (N % 4 == 0) && aligned16(C);
+  CUtensorMap mc;
+  std::memset(&mc, 0, sizeof mc);
+  if (!linear && p.vec_ok) {
+    cuuint64_t cd[2] = {(cuuint64_t)N, (cuuint64_t)M};
+    cuuint64_t cs[1] = {(cuuint64_t)(N * 4)};
+    cuuint32_t cb[2] = {32, 32};
+    r = g_encode(&mc, CU_TENSOR_MAP_DATA_TYPE_INT32, 2, C, cd, cs, cb, estr,
+                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                 CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(LBGEMM_ERR_CUDA, "cuTensorMapEncodeTiled (C) failed (%d)", (int)r);
+  }
+  const int grid = (int)std::min<int64_t>(p.num_tiles, (int64_t)d.sm_count * occupancy(d, k));
+  cudaError_t e = k.launch(&ma, &mb, &mc, &p, grid, true, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "fused tensor-core GEMM launch");
+  g_launches += 1;
+  return LBGEMM_OK;
+}
+
+// Route of the fused kernel for a skinny 8-bit problem (1: B is converted in
+// the kernel, 2: A is), or 0.  Measured on GB300: with one side <= 256, the
+// other >= 2048 and K >= 1024, skipping the large operand's re-encoding pass
+// is 1.1-2x faster (64 x 16384 x 16384: 294 -> 141 us); at 512 rows and up
+// the pre-pass route wins.
+int fused_route(int64_t M, int64_t N, int64_t K, const void* A, const void* B) {
+  if (K % 16 || !aligned16(A) || !aligned16(B)) return 0;
+  const int64_t lo = std::min(M, N), hi = std::max(M, N);
+  if (!(lo <= kFusedMaxSide && hi >= kFusedMinOther && K >= kFusedMinK)) return 0;
+  return M <= N ? 1 : 2;
+}
+
 lbgemm_status run_any(int bits, int64_t M, int64_t N, int64_t K, const void* A, const void* B,
                       int32_t* C, int variant, void* ws, size_t ws_bytes, bool internal_ws,
                       cudaStream_t stream) {
@@ -402,6 +480,25 @@ lbgemm_status run_any(int bits, int64_t M, int64_t N, int64_t K, const void* A, 
     g_launches += 1;
     return LBGEMM_OK;
   }
+  const int fuse = (bits == 8 && auto_pick) ? fused_route(M, N, K, A, B) : 0;
+  const int fuse_tile = kFusedTileN;
+  if (fuse) {
+    const size_t need_f = enc_bytes(8, fuse == 1 ? M : N, K);
+    if (!internal_ws) {
+      if (!ws || ws_bytes < need_f)
+        return fail(LBGEMM_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need_f,
+                    ws_bytes);
+      return run_tc_fused(*d, fuse, fuse_tile, M, N, K, A, B, C, nullptr, nullptr, nullptr, ws,
+                          stream);
+    }
+    std::lock_guard<std::mutex> lock(g_ws_mu);
+    st = scratch_acquire(d->ws, need_f, stream);
+    if (st != LBGEMM_OK) return st;
+    st = run_tc_fused(*d, fuse, fuse_tile, M, N, K, A, B, C, nullptr, nullptr, nullptr, d->ws.ptr,
+                      stream);
+    lbgemm_status st2 = scratch_release(d->ws, stream);
+    return st != LBGEMM_OK ? st : st2;
+  }
   const size_t need = enc_bytes(bits, M, K) + enc_bytes(bits, N, K);
   if (!internal_ws) {
     if (!ws || ws_bytes < need)
@@ -437,6 +534,15 @@ lbgemm_status run_linear(int64_t M, int64_t N, int64_t K, const int8_t* X, const
     if (e != cudaSuccess) return cuda_fail(e, "skinny linear launch");
     g_launches += 1;
     return LBGEMM_OK;
+  }
+  if (auto_pick && fused_route(M, N, K, X, W) == 1) {
+    // small token counts: only X is re-encoded; the kernel converts W itself
+    std::lock_guard<std::mutex> lock(g_ws_mu);
+    st = scratch_acquire(d->ws, enc_bytes(8, M, K), stream);
+    if (st != LBGEMM_OK) return st;
+    st = run_tc_fused(*d, 1, kFusedTileN, M, N, K, X, W, nullptr, sx, sw, Y, d->ws.ptr, stream);
+    lbgemm_status st2 = scratch_release(d->ws, stream);
+    return st != LBGEMM_OK ? st : st2;
   }
   if (auto_pick) variant = table_select(d->sm_count, 8, M, N, K);
   std::lock_guard<std::mutex> lock(g_ws_mu);

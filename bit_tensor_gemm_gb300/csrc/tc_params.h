@@ -34,6 +34,7 @@ struct TcKernel {
   int tmem_cols = 0;
   int tile_n = 0;
   int stages = 0;
+  int threads = 320;
 };
 
 // Dynamic shared memory to request so that the CTAs that fit on one SM by
@@ -49,5 +50,8 @@ inline constexpr int tc_smem_request(int used, int tmem_cols) {
 TcKernel tc_kernel_small(int stages, bool f8, bool linear);
 TcKernel tc_kernel_medium(int stages, bool f8, bool linear);
 TcKernel tc_kernel_large(int stages, bool f8, bool linear);
+// Fused variants (8-bit only, 3 fp16 stages, 8 int8 staging stages): fuse 1 converts B in the kernel,
+// fuse 2 converts A; tile_n 64 or 128.
+TcKernel tc_kernel_fused(int fuse, int tile_n, bool linear);
 
 }  // namespace lbg

@@ -78,11 +78,13 @@ lbgemm_status lbgemm_variant_info(int bits, int variant, int* tile_m, int* tile_
 /* C = A . B^T with the variant the selection table picks for
  * (bits, M, N, K, SM count).  [LBG] intro, sections 1-2.  Every bit width
  * runs on the tensor cores through an exact re-encoding of its operands
- * (int8 -> fp16, int4 -> e4m3, +-1 -> e4m3), except three shape rules:
- * 8-bit problems with M <= 16 run on a kernel that streams B once, 8-bit
- * problems with K <= 512 and M*N*K <= 2^28 on a one-launch dp4a kernel (both
- * need K % 16 == 0), and 1-bit problems with M*N*K < 2^30 on the
- * XOR-popcount kernel of lbgemm_run_popc.  Scratch memory for the re-encoding is
+ * (int8 -> fp16, int4 -> e4m3, +-1 -> e4m3), except four shape rules:
+ * 8-bit problems with M <= 16 run on a kernel that streams B once; 8-bit
+ * problems with K <= 512 and M*N*K <= 2^28 on a one-launch dp4a kernel;
+ * skinny 8-bit problems (min(M, N) <= 256, max(M, N) >= 2048, K >= 1024) on
+ * a tensor-core kernel that converts the large operand itself, with only the
+ * small one re-encoded ahead (these three need K % 16 == 0); and 1-bit
+ * problems with M*N*K < 2^30 on the XOR-popcount kernel of lbgemm_run_popc.  Scratch memory for the re-encoding is
  * taken from a per-device buffer the library grows with cudaMalloc on demand;
  * calls from different streams are ordered on it with events.  A call that
  * grows the buffer synchronises the device, so make the first call of the
@@ -161,7 +163,9 @@ lbgemm_status lbgemm_run_popc(int64_t M, int64_t N, int64_t K, const uint32_t* A
  * with acc = X . W^T exact in int32.  X: int8 M x K (per-token scale sx, fp32
  * [M]); W: int8 N x K (per-output-channel scale sw, fp32 [N]); Y: bf16 M x N
  * row-major, passed as void* (2 bytes per element).  The scale product is
- * formed in fp32, left to right.  K <= 131071. */
+ * formed in fp32, left to right.  K <= 131071.  M <= 16 runs on the kernel
+ * that streams W once, 16 < M <= 256 (N >= 2048, K >= 1024) on the fused
+ * conversion kernel, larger M on the tensor-core variant table. */
 lbgemm_status lbgemm_linear(int64_t M, int64_t N, int64_t K, const int8_t* X, const float* sx,
                             const int8_t* W, const float* sw, void* Y, void* stream);
 

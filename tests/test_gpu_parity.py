@@ -76,6 +76,15 @@ def test_int8_small_dp4a_path():
     assert np.all(G().gemm(8, A, A, 512) == 16384 * 512)
 
 
+@pytest.mark.parametrize("M,N,K", [(64, 4096, 2048), (200, 2500, 1040), (4096, 100, 1024),
+                                   (3000, 256, 2064), (17, 2048, 4096)])
+def test_int8_fused_conversion_path(M, N, K):
+    """Skinny problems (one side <= 256, the other >= 2048, K >= 1024): the
+    kernel converts the large int8 operand itself; ragged tiles included."""
+    A, B = synth.operands(8, M, N, K, 7 * M + N + K)
+    assert_exact(G().gemm(8, A, B, K), oracle.gemm(8, A, B, K), f"int8 fused {M}x{N}x{K}")
+
+
 def test_int8_full_range_and_extremes():
     g = np.random.default_rng(5)
     M, N, K = 130, 70, 3000
@@ -209,7 +218,7 @@ def check_linear(Y, ref, acc_zero, what):
     assert np.all(Y[acc_zero] == 0), f"{what}: nonzero output where the accumulator is zero"
 
 
-@pytest.mark.parametrize("M", [1, 16, 128, 200])
+@pytest.mark.parametrize("M", [1, 16, 128, 200, 40])
 def test_linear_small(M):
     N, K = 1000, 4096
     X, sx, W, sw = synth.linear_operands(M, N, K, 400 + M)
