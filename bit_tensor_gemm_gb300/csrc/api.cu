@@ -300,10 +300,26 @@ lbgemm_status encode_operands(DeviceState& d, int bits, const void* a, int64_t r
 }
 
 // The GEMM kernel alone, on encoded operands.
+// K splits for a problem with few output tiles: when at most half of the
+// CTA slots would get a tile, each tile's K range is cut into pieces (at
+// least 4 K slices each) whose int32 partial sums are added into a zeroed C.
+// Only for int32 C stored by TMA (the linear layer scales the whole sum).
+int plan_splits(DeviceState& d, const TcKernel& k, int bits, int64_t M, int64_t N, int64_t K,
+                bool linear, bool vec_ok) {
+  if (linear || !vec_ok) return 1;
+  const int bk = bits == 8 ? 64 : 128;
+  const int64_t num_kb = (enc_kp(bits, K) + bk - 1) / bk;
+  const int64_t tiles = ((M + 127) / 128) * ((N + k.tile_n - 1) / k.tile_n);
+  const int64_t slots = (int64_t)d.sm_count * occupancy(d, k);
+  if (tiles * 2 > slots) return 1;
+  const int64_t splits = std::min<int64_t>(std::min<int64_t>(slots / tiles, num_kb / 4), 64);
+  return (int)std::max<int64_t>(splits, 1);
+}
+
 lbgemm_status run_tc_encoded(DeviceState& d, int bits, int64_t M, int64_t N, int64_t K,
                              const void* encA, const void* encB, int32_t* C, const float* sx,
                              const float* sw, void* Y, int variant, bool after_encode,
-                             cudaStream_t stream) {
+                             int splits, cudaStream_t stream) {
   const bool f8 = bits != 8;  // 4-bit and 1-bit operands are e4m3-encoded
   const bool linear = Y != nullptr;
   TcKernel k = tc_kernel(variant, f8, linear);
@@ -337,6 +353,15 @@ lbgemm_status run_tc_encoded(DeviceState& d, int bits, int64_t M, int64_t N, int
     p.vec_ok = (N % 8 == 0) && aligned16(Y);
   else
     p.vec_ok = (N % 4 == 0) && aligned16(C);
+  if (splits < 0) {  // not planned by the caller: plan here and clear C now
+    splits = plan_splits(d, k, bits, M, N, K, linear, p.vec_ok);
+    if (splits > 1) {
+      cudaError_t ez = cudaMemsetAsync(C, 0, (size_t)(M * N) * sizeof(int32_t), stream);
+      if (ez != cudaSuccess) return cuda_fail(ez, "cudaMemsetAsync (split K)");
+    }
+  }
+  p.splits = splits;
+  p.num_units = p.num_tiles * splits;
   CUtensorMap mc;
   std::memset(&mc, 0, sizeof mc);
   if (!linear && p.vec_ok) {
@@ -350,7 +375,7 @@ lbgemm_status run_tc_encoded(DeviceState& d, int bits, int64_t M, int64_t N, int
     if (r != CUDA_SUCCESS)
       return fail(LBGEMM_ERR_CUDA, "cuTensorMapEncodeTiled (C) failed (%d)", (int)r);
   }
-  const int grid = (int)std::min<int64_t>(p.num_tiles, (int64_t)d.sm_count * occupancy(d, k));
+  const int grid = (int)std::min<int64_t>(p.num_units, (int64_t)d.sm_count * occupancy(d, k));
   // Right after our own re-encoding launch, the GEMM is a programmatic
   // dependent launch: its prologue (barriers, TMEM, descriptor prefetch)
   // overlaps the encoder's tail and its producer waits for the encoder's
@@ -366,9 +391,21 @@ lbgemm_status run_tc(DeviceState& d, int bits, int64_t M, int64_t N, int64_t K, 
                      int variant, void* ws, cudaStream_t stream) {
   uint8_t* encA = static_cast<uint8_t*>(ws);
   uint8_t* encB = encA + enc_bytes(bits, M, K);
+  // Plan K splits first: C must be cleared before the encoder, so that the
+  // GEMM can still be launched as the encoder's dependent.
+  int splits = 1;
+  const bool linear = Y != nullptr;
+  TcKernel k = tc_kernel(variant, bits != 8, linear);
+  if (k.launch) {
+    splits = plan_splits(d, k, bits, M, N, K, linear, (N % 4 == 0) && aligned16(C));
+    if (splits > 1) {
+      cudaError_t ez = cudaMemsetAsync(C, 0, (size_t)(M * N) * sizeof(int32_t), stream);
+      if (ez != cudaSuccess) return cuda_fail(ez, "cudaMemsetAsync (split K)");
+    }
+  }
   lbgemm_status st = encode_operands(d, bits, A, M, encA, B, N, encB, K, stream);
   if (st != LBGEMM_OK) return st;
-  return run_tc_encoded(d, bits, M, N, K, encA, encB, C, sx, sw, Y, variant, true, stream);
+  return run_tc_encoded(d, bits, M, N, K, encA, encB, C, sx, sw, Y, variant, true, splits, stream);
 }
 
 // Skinny 8-bit problems: only the small operand is re-encoded ahead; the
@@ -407,6 +444,8 @@ lbgemm_status run_tc_fused(DeviceState& d, int fuse, int tile_n, int64_t M, int6
   p.tiles_n = (int)((N + tile_n - 1) / tile_n);
   p.num_tiles = p.tiles_m * p.tiles_n;
   p.group_m = kGroupM;
+  p.splits = 1;
+  p.num_units = p.num_tiles;
   p.C = C;
   p.sx = sx;
   p.sw = sw;
@@ -424,7 +463,7 @@ lbgemm_status run_tc_fused(DeviceState& d, int fuse, int tile_n, int64_t M, int6
                  CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(LBGEMM_ERR_CUDA, "cuTensorMapEncodeTiled (C) failed (%d)", (int)r);
   }
-  const int grid = (int)std::min<int64_t>(p.num_tiles, (int64_t)d.sm_count * occupancy(d, k));
+  const int grid = (int)std::min<int64_t>(p.num_units, (int64_t)d.sm_count * occupancy(d, k));
   cudaError_t e = k.launch(&ma, &mb, &mc, &p, grid, true, stream);
   if (e != cudaSuccess) return cuda_fail(e, "fused tensor-core GEMM launch");
   g_launches += 1;
@@ -670,7 +709,7 @@ lbgemm_status lbgemm_run_encoded(int bits, int64_t M, int64_t N, int64_t K, cons
     if (st != LBGEMM_OK) return st;
     if (variant < 0) variant = table_select(d->sm_count, bits, M, N, K);
     return run_tc_encoded(*d, bits, M, N, K, A_enc, B_enc, C, nullptr, nullptr, nullptr, variant,
-                          false, as_stream(stream));
+                          false, -1, as_stream(stream));
   } catch (...) {
     return fail(LBGEMM_ERR_CUDA, "internal error");
   }

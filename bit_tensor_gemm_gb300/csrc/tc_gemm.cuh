@@ -82,6 +82,15 @@ struct TcLayout {
   static constexpr int kTmemCols = 2 * BN;
 };
 
+// Work unit u = (output tile, K split): split sp of tile t covers the
+// 128-byte K slices [kb0, kb1).  With one split per tile a unit is a tile.
+__device__ __forceinline__ void unit_range(int u, const TcParams& p, int& t, int& kb0, int& kb1) {
+  t = u / p.splits;
+  const int sp = u - t * p.splits;
+  kb0 = (int)((int64_t)sp * p.num_kb / p.splits);
+  kb1 = (int)((int64_t)(sp + 1) * p.num_kb / p.splits);
+}
+
 __device__ __forceinline__ void tile_coords(int t, const TcParams& p, int& tm, int& tn) {
   const int per_group = p.group_m * p.tiles_n;
   const int g = t / per_group;
@@ -222,7 +231,6 @@ __global__ void __launch_bounds__(tc_threads(FUSE), 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  const int num_chunks = (p.num_kb + p.chunk_kb - 1) / p.chunk_kb;
 
   if (warp == 0) {
     // ---------------- TMA producer ----------------
@@ -236,10 +244,11 @@ __global__ void __launch_bounds__(tc_threads(FUSE), 1)
       uint32_t phase = 0;
       int64_t issued = 0;
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
-        int tm, tn;
+      for (int w = blockIdx.x; ok && w < p.num_units; w += gridDim.x) {
+        int t, kbb, kbe, tm, tn;
+        unit_range(w, p, t, kbb, kbe);
         tile_coords(t, p, tm, tn);
-        for (int kb = 0; kb < p.num_kb; ++kb) {
+        for (int kb = kbb; kb < kbe; ++kb) {
           if (FUSE == 0) {
             if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.status)) {
               ok = false;
@@ -292,7 +301,10 @@ __global__ void __launch_bounds__(tc_threads(FUSE), 1)
       uint32_t phase = 0;
       uint32_t u = 0;
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+      for (int w = blockIdx.x; ok && w < p.num_units; w += gridDim.x) {
+        int t, kbb, kbe;
+        unit_range(w, p, t, kbb, kbe);
+        const int num_chunks = (kbe - kbb + p.chunk_kb - 1) / p.chunk_kb;
         for (int c = 0; ok && c < num_chunks; ++c, ++u) {
           const int buf = u & 1;
           if (!mbar_wait(acce_bar(buf), ((u >> 1) & 1u) ^ 1u, abort_flag, p.status)) {
@@ -301,8 +313,8 @@ __global__ void __launch_bounds__(tc_threads(FUSE), 1)
           }
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + buf * BN;
-          const int kb0 = c * p.chunk_kb;
-          const int kb1 = min(kb0 + p.chunk_kb, p.num_kb);
+          const int kb0 = kbb + c * p.chunk_kb;
+          const int kb1 = min(kb0 + p.chunk_kb, kbe);
           for (int kb = kb0; kb < kb1; ++kb) {
             if (!mbar_wait(full_bar(stage), phase, abort_flag, p.status) ||
                 (FUSE && !mbar_wait(conv_bar(stage), phase, abort_flag, p.status))) {
@@ -343,10 +355,11 @@ __global__ void __launch_bounds__(tc_threads(FUSE), 1)
     uint32_t oph = 0, sph = 0;
     int64_t issued = 0;
     bool ok = true;
-    for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
-      int tm, tn;
+    for (int w = blockIdx.x; ok && w < p.num_units; w += gridDim.x) {
+      int t, kbb, kbe, tm, tn;
+      unit_range(w, p, t, kbb, kbe);
       tile_coords(t, p, tm, tn);
-      for (int kb = 0; kb < p.num_kb; ++kb) {
+      for (int kb = kbb; kb < kbe; ++kb) {
         int got = 1;
         if (lane == 0) {
           got = mbar_wait(empty_bar(os), oph ^ 1u, abort_flag, p.status);
@@ -427,9 +440,11 @@ __global__ void __launch_bounds__(tc_threads(FUSE), 1)
     uint32_t u = 0;
     int32_t acc[kGroups][32];
     bool ok = true;
-    for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
-      int tm, tn;
+    for (int w = blockIdx.x; ok && w < p.num_units; w += gridDim.x) {
+      int t, kbb, kbe, tm, tn;
+      unit_range(w, p, t, kbb, kbe);
       tile_coords(t, p, tm, tn);
+      const int num_chunks = (kbe - kbb + p.chunk_kb - 1) / p.chunk_kb;
       for (int c = 0; c < num_chunks; ++c, ++u) {
         const int buf = u & 1;
         int got = 0;
@@ -472,7 +487,12 @@ __global__ void __launch_bounds__(tc_threads(FUSE), 1)
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            tma_store_2d(&tmC, stage_addr, tn * BN + col0 + g * 32, tm * kTcBM + quarter * 32);
+            // split K: every piece adds its partial sums into C (zeroed by the
+            // host); integer addition makes the order irrelevant
+            if (p.splits > 1)
+              tma_reduce_add_2d(&tmC, stage_addr, tn * BN + col0 + g * 32, tm * kTcBM + quarter * 32);
+            else
+              tma_store_2d(&tmC, stage_addr, tn * BN + col0 + g * 32, tm * kTcBM + quarter * 32);
             bulk_commit();
           }
         }

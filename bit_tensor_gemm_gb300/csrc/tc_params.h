@@ -14,6 +14,8 @@ struct TcParams {
   int num_kb;    // 128-byte K slices per tile row
   int chunk_kb;  // slices per exact fp32 accumulation chunk
   int tiles_m, tiles_n, num_tiles, group_m;
+  int splits;     // K splits per tile (> 1: partial tiles are added into a zeroed C)
+  int num_units;  // num_tiles * splits
   int vec_ok;    // rows of C/Y are 16-byte aligned: C goes out by TMA stores,
                  // Y by 16-byte vector stores
   int32_t* C;
