@@ -418,6 +418,12 @@ lbgemm_status run_tc_fused(DeviceState& d, int fuse, int tile_n, int64_t M, int6
   TcKernel k = lbg::tc_kernel_fused(fuse, tile_n, linear);
   if (!k.launch) return fail(LBGEMM_ERR_UNSUPPORTED, "no fused kernel (fuse %d, tile %d)", fuse, tile_n);
   const int64_t kp = enc_kp(8, K);  // == K when K % 16 == 0
+  const bool vec_ok = linear ? (N % 8 == 0) && aligned16(Y) : (N % 4 == 0) && aligned16(C);
+  const int splits = plan_splits(d, k, 8, M, N, K, linear, vec_ok);
+  if (splits > 1) {  // cleared before the encoder, so the GEMM can be its dependent
+    cudaError_t ez = cudaMemsetAsync(C, 0, (size_t)(M * N) * sizeof(int32_t), stream);
+    if (ez != cudaSuccess) return cuda_fail(ez, "cudaMemsetAsync (split K)");
+  }
   lbgemm_status st = fuse == 1 ? encode_operands(d, 8, A, M, ws, nullptr, 0, nullptr, K, stream)
                                : encode_operands(d, 8, B, N, ws, nullptr, 0, nullptr, K, stream);
   if (st != LBGEMM_OK) return st;
@@ -444,14 +450,14 @@ lbgemm_status run_tc_fused(DeviceState& d, int fuse, int tile_n, int64_t M, int6
   p.tiles_n = (int)((N + tile_n - 1) / tile_n);
   p.num_tiles = p.tiles_m * p.tiles_n;
   p.group_m = kGroupM;
-  p.splits = 1;
-  p.num_units = p.num_tiles;
+  p.splits = splits;
+  p.num_units = p.num_tiles * splits;
   p.C = C;
   p.sx = sx;
   p.sw = sw;
   p.Y = static_cast<__nv_bfloat16*>(Y);
   p.status = d.status;
-  p.vec_ok = linear ? (N % 8 == 0) && aligned16(Y) : (N % 4 == 0) && aligned16(C);
+  p.vec_ok = vec_ok;
   CUtensorMap mc;
   std::memset(&mc, 0, sizeof mc);
   if (!linear && p.vec_ok) {
