@@ -28,6 +28,10 @@
 #include "simt.h"
 #include "tc_params.h"
 
+namespace lbg {
+int mlp_pick(int bits, int64_t M, int64_t N, int64_t K, int sm_count);
+}
+
 // Device status word: kernels OR error bits into it (see lbgemm_device_status).
 __device__ int g_lbgemm_status_word;
 
@@ -232,9 +236,15 @@ std::mutex g_table_mu;
 std::map<Key, int> g_table;
 
 int table_select(int sm, int bits, int64_t M, int64_t N, int64_t K) {
+  {
+    std::lock_guard<std::mutex> lock(g_table_mu);
+    auto it = g_table.find(Key{sm, bits, M, N, K});
+    if (it != g_table.end()) return it->second;
+  }
+  // not swept: the learned selector when one is loaded for this bit width
+  const int v = lbg::mlp_pick(bits, M, N, K, sm);
+  if (v >= 0) return v;
   std::lock_guard<std::mutex> lock(g_table_mu);
-  auto it = g_table.find(Key{sm, bits, M, N, K});
-  if (it != g_table.end()) return it->second;
   int best = kDefaultVariant;
   double best_d = 0;
   bool have = false;

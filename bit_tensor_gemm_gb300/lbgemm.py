@@ -60,6 +60,9 @@ _SIGNATURES = {
     "lbgemm_table_load": (_i32, [ctypes.c_char_p]),
     "lbgemm_table_save": (_i32, [ctypes.c_char_p]),
     "lbgemm_choose": (_i32, [_vp, _i32, _f32]),
+    "lbgemm_mlp_load": (_i32, [ctypes.c_char_p]),
+    "lbgemm_mlp_clear": (_i32, []),
+    "lbgemm_mlp_predict": (_i32, [_i32, _i64, _i64, _i64, _i32, _vp]),
     "lbgemm_time_variants": (_i32, [_i32, _i64, _i64, _i64, _vp, _vp, _vp, _i32, _i32, _i32, _vp,
                                     _vp]),
     "lbgemm_run_host": (_i32, [_i32, _i64, _i64, _i64, _vp, _vp, _vp, _i32, _vp]),
@@ -234,6 +237,21 @@ def lbgemm_table_load(path: str) -> None:
 
 def lbgemm_table_save(path: str) -> None:
     _check(load().lbgemm_table_save(os.fsencode(path)))
+
+
+def lbgemm_mlp_load(path: str) -> None:
+    _check(load().lbgemm_mlp_load(os.fsencode(path)))
+
+
+def lbgemm_mlp_clear() -> None:
+    _check(load().lbgemm_mlp_clear())
+
+
+def lbgemm_mlp_predict(bits, M, N, K, sm_count) -> tuple[int, int]:
+    """(top class, second class) of the loaded network, (-1, -1) if none."""
+    second = ctypes.c_int(-1)
+    first = load().lbgemm_mlp_predict(bits, M, N, K, sm_count, ctypes.addressof(second))
+    return first, (second.value if first >= 0 else -1)
 
 
 def lbgemm_choose(times, default_variant: int = 7, keep_within: float = 0.02) -> int:

@@ -176,9 +176,10 @@ lbgemm_status lbgemm_linear_variant(int64_t M, int64_t N, int64_t K, const int8_
 
 /* ---- selection table: [LBG] sections 2-3 ------------------------------------
  * The table maps (bits, M, N, K) on this device's SM count to a variant.  A
- * shape with no entry takes the entry of the nearest one of the same bits and
- * SM count (distance: sum of |log2| differences of M, N, K; ties to the first
- * in (M, N, K) order); an empty table gives the default variant. */
+ * shape with no entry takes the learned selector's choice when a network is
+ * loaded for its bit width (below), else the entry of the nearest one of the
+ * same bits and SM count (distance: sum of |log2| differences of M, N, K;
+ * ties to the first in (M, N, K) order); an empty table gives the default. */
 int lbgemm_select(int bits, int64_t M, int64_t N, int64_t K);
 lbgemm_status lbgemm_table_set(int bits, int64_t M, int64_t N, int64_t K, int variant);
 /* The same two for an explicit SM count (no device needed). */
@@ -190,6 +191,21 @@ int64_t lbgemm_table_size(void);
 /* Text file, one entry per line: "sm_count bits M N K variant". */
 lbgemm_status lbgemm_table_load(const char* path);
 lbgemm_status lbgemm_table_save(const char* path);
+
+/* ---- learned selector: [LBG] section 3 ------------------------------------------
+ * A feed-forward network -- inputs log2(M), log2(N), log2(K) and the SM count,
+ * standardised; three hidden ReLU layers of 128; nine outputs -- trained
+ * offline on sweep timings (bit_tensor_gemm_gb300/selector_mlp.py writes the
+ * text file).  Once a nine-class network is loaded for a bit width,
+ * lbgemm_select answers shapes that have no table entry with the network's
+ * top class (before the nearest-entry rule).  The network runs on the host in
+ * float32.  lbgemm_mlp_load replaces the network of the file's bit width;
+ * LBGEMM_ERR_INVALID_ARG for a missing or malformed file. */
+lbgemm_status lbgemm_mlp_load(const char* path);
+lbgemm_status lbgemm_mlp_clear(void);
+/* Top class of the network loaded for `bits` (and the second one in *second
+ * when not NULL), or -1 when none is loaded or the arguments are bad. */
+int lbgemm_mlp_predict(int bits, int64_t M, int64_t N, int64_t K, int sm_count, int* second);
 
 /* The stored choice from nine measured times: the fastest variant (lowest
  * index on ties), unless times[default_variant] is within keep_within
