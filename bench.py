@@ -249,6 +249,28 @@ def run_ours(args):
         L.lbgemm_table_set(8, m, n, k, L.lbgemm_choose(t, L.lbgemm_default_variant(), 0.02))
     sweep_s = time.perf_counter() - t_sweep0
 
+    # -- the learned selector (trained offline on a separate random-shape GB300
+    #    sweep) judged on this run's own timings of the 729 grid shapes --------------------
+    mlp_eval = None
+    mlp_path = os.path.join(ROOT, "bit_tensor_gemm_gb300", "data", "mlp_gb300_s8.txt")
+    if os.path.exists(mlp_path):
+        L.lbgemm_mlp_load(mlp_path)
+        sm = torch.cuda.get_device_properties(dev).multi_processor_count
+        T = np.array(sweep_times)
+        pred = np.array([L.lbgemm_mlp_predict(8, m, n, k, sm) for (m, n, k) in shapes])
+        best = T.argmin(axis=1)
+        t_pred = T[np.arange(len(T)), pred[:, 0]]
+        mlp_eval = {
+            "network": "log2 M, log2 N, log2 K, SM count -> 3 x 128 ReLU -> 9 variants",
+            "trained_on": "bit_tensor_gemm_gb300/data/sweep_gb300_s8.csv (3000 random shapes)",
+            "top1_accuracy": float(np.mean(pred[:, 0] == best)),
+            "top2_accuracy": float(np.mean((pred[:, 0] == best) | (pred[:, 1] == best))),
+            "within_2pct_of_best": float(np.mean(t_pred <= T.min(axis=1) * 1.02)),
+            "time_pred_over_best": float(t_pred.sum() / T.min(axis=1).sum()),
+            "speedup_over_default": float(T[:, 7].sum() / t_pred.sum()),
+        }
+        L.lbgemm_mlp_clear()  # the timed steps use the measured table
+
     def timed_pass(run_one, shp_list=shapes):
         """One pass: flush L2, event, GEMM, event, per shape.  Returns per-shape ms."""
         evs = []
@@ -478,7 +500,8 @@ def run_ours(args):
                        "timing": "sum of per-GEMM CUDA-event times on the launching stream",
                        "parallelism": "replicas" if world > 1 else "single GPU"},
             "clocks": clk, "gpu_launches": launches, "e2e": e2e, "roofline": roofline,
-            "cpu_baseline": cpu, "selection": selection, "sweep_roofline": sweep_roofline,
+            "cpu_baseline": cpu, "selection": selection, "mlp_selector": mlp_eval,
+            "sweep_roofline": sweep_roofline,
             "per_config": per_config,
         }), flush=True)
         if args.dump:

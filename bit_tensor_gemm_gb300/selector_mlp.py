@@ -168,7 +168,48 @@ def labels_from_times(times: np.ndarray) -> np.ndarray:
     return np.argmin(times, axis=1)
 
 
+def within_accuracy(pred: np.ndarray, times: np.ndarray, tol: float = 0.02) -> float:
+    """Fraction of samples whose predicted variant is within tol of the fastest."""
+    t = times[np.arange(len(times)), pred]
+    return float(np.mean(t <= times.min(axis=1) * (1.0 + tol)))
+
+
+def load_dataset(path: str):
+    """(features, labels, times) of a CSV written by bit_tensor_gemm_gb300.sweep."""
+    D = np.loadtxt(path, delimiter=",", skiprows=1, ndmin=2)
+    return features(D[:, 0], D[:, 1], D[:, 2], D[:, 3]), labels_from_times(D[:, 4:13]), D[:, 4:13]
+
+
+def main(argv=None) -> int:
+    import argparse  # noqa: PLC0415
+    ap = argparse.ArgumentParser(description="train the variant selector on a sweep CSV")
+    ap.add_argument("--data", required=True)
+    ap.add_argument("--out", required=True)
+    ap.add_argument("--bits", type=int, default=8)
+    ap.add_argument("--epochs", type=int, default=100)
+    ap.add_argument("--seed", type=int, default=0)
+    a = ap.parse_args(argv)
+    X, y, T = load_dataset(a.data)
+    g = np.random.default_rng(a.seed)
+    perm = g.permutation(len(X))
+    ntr = int(0.8 * len(X))
+    tr, te = perm[:ntr], perm[ntr:]
+    probe = MLP(a.bits, seed=a.seed).fit(X[tr], y[tr], epochs=a.epochs)
+    p = probe.predict_top2(X[te])
+    t1, t2 = topk_accuracy(p, y[te])
+    w = within_accuracy(p[:, 0], T[te])
+    print(f"held-out 20 %: top-1 {t1:.3f}, top-2 {t2:.3f}, within 2 % of best {w:.3f}")
+    MLP(a.bits, seed=a.seed).fit(X, y, epochs=a.epochs).save(a.out)
+    print(f"trained on all {len(X)} samples -> {a.out}")
+    return 0
+
+
 def topk_accuracy(top2: np.ndarray, y: np.ndarray) -> tuple[float, float]:
     top1 = float(np.mean(top2[:, 0] == y))
     top2a = float(np.mean((top2[:, 0] == y) | (top2[:, 1] == y)))
     return top1, top2a
+
+
+if __name__ == "__main__":
+    import sys  # noqa: PLC0415
+    sys.exit(main())
