@@ -450,6 +450,19 @@ def run_ours(args):
         per_config[f"linear_M{M}_N11008_K4096"] = {
             "us": t * 1e3, "tops": 2 * M * 11008 * 4096 / t / 1e9, "gbs": byts / t / 1e6,
             "frac_of_hbm": byts / t / 1e6 / peaks["hbm_gbs"]}
+    # the linear layer on bf16 activations: per-token quantisation in front
+    for M in (1, 16, 128, 2048):
+        gq = np.random.default_rng(synth.config_seed(5) + 100 + M)
+        Xf = torch.from_numpy(gq.standard_normal((M, 4096), dtype=np.float32)).to(
+            dev).to(torch.bfloat16)
+        _, _, W, sw = synth.linear_operands(M, 11008, 4096, synth.config_seed(5) + M)
+        dW, dsw = torch.from_numpy(W).to(dev), torch.from_numpy(sw).to(dev)
+        Y = torch.empty((M, 11008), dtype=torch.bfloat16, device=dev)
+        t = median_ms(lambda: L.lbgemm_linear_quant(M, 11008, 4096, Xf, dW, dsw, Y), 20)
+        byts = 11008 * 4096 + 2 * M * 4096 + 4 * 11008 + 2 * M * 11008
+        per_config[f"linear_quant_M{M}_N11008_K4096"] = {
+            "us": t * 1e3, "tops": 2 * M * 11008 * 4096 / t / 1e9, "gbs": byts / t / 1e6,
+            "frac_of_hbm": byts / t / 1e6 / peaks["hbm_gbs"]}
     L.lbgemm_device_status()
 
     # -- end to end through the host-buffer entry point, on the balanced 81-shape ninth ----------

@@ -96,6 +96,7 @@ struct DeviceState {
   Scratch ws;           // operand re-encoding scratch
   Scratch host_stage;   // device staging for lbgemm_run_host
   Scratch flush;        // buffer written between timed runs to evict L2
+  Scratch quant;        // quantised activations of lbgemm_linear_quant
   std::map<const void*, int> occupancy;
 };
 
@@ -684,6 +685,53 @@ lbgemm_status lbgemm_run_ws(int bits, int64_t M, int64_t N, int64_t K, const voi
   try {
     return run_any(bits, M, N, K, A, B, C, variant, workspace, workspace_bytes, false,
                    as_stream(stream));
+  } catch (...) {
+    return fail(LBGEMM_ERR_CUDA, "internal error");
+  }
+}
+
+lbgemm_status lbgemm_quantize_rows(int64_t M, int64_t K, const void* X, int8_t* Q, float* S,
+                                   void* stream) {
+  try {
+    if (M < 0 || K < 1) return fail(LBGEMM_ERR_INVALID_ARG, "quantize: M >= 0 and K >= 1");
+    if (M == 0) return LBGEMM_OK;
+    if (!X || !Q || !S) return fail(LBGEMM_ERR_INVALID_ARG, "quantize: null pointer");
+    DeviceState* d = nullptr;
+    lbgemm_status st = device_state(&d);
+    if (st != LBGEMM_OK) return st;
+    cudaError_t e = lbg::launch_quant_rows_bf16(X, M, K, Q, S, as_stream(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "quantize launch");
+    g_launches += 1;
+    return LBGEMM_OK;
+  } catch (...) {
+    return fail(LBGEMM_ERR_CUDA, "internal error");
+  }
+}
+
+lbgemm_status lbgemm_linear_quant(int64_t M, int64_t N, int64_t K, const void* X, const int8_t* W,
+                                  const float* sw, void* Y, void* stream) {
+  try {
+    lbgemm_status st = check_gemm_args(8, M, N, K, X, W, Y);
+    if (st != LBGEMM_OK) return st;
+    if (M == 0 || N == 0) return LBGEMM_OK;
+    if (!sw) return fail(LBGEMM_ERR_INVALID_ARG, "null scale pointer");
+    DeviceState* d = nullptr;
+    st = device_state(&d);
+    if (st != LBGEMM_OK) return st;
+    cudaStream_t s = as_stream(stream);
+    static std::mutex quant_mu;
+    std::lock_guard<std::mutex> lock(quant_mu);
+    const size_t qbytes = (size_t)round_up(M * K, 256);
+    st = scratch_acquire(d->quant, qbytes + (size_t)M * sizeof(float), s);
+    if (st != LBGEMM_OK) return st;
+    int8_t* Q = static_cast<int8_t*>(d->quant.ptr);
+    float* S = reinterpret_cast<float*>(static_cast<uint8_t*>(d->quant.ptr) + qbytes);
+    cudaError_t e = lbg::launch_quant_rows_bf16(X, M, K, Q, S, s);
+    if (e != cudaSuccess) return cuda_fail(e, "quantize launch");
+    g_launches += 1;
+    st = run_linear(M, N, K, Q, S, W, sw, Y, -1, s);
+    lbgemm_status st2 = scratch_release(d->quant, s);
+    return st != LBGEMM_OK ? st : st2;
   } catch (...) {
     return fail(LBGEMM_ERR_CUDA, "internal error");
   }

@@ -149,6 +149,55 @@ __global__ void cvt_b1_e4m3_kernel(CvtJob ja, CvtJob jb, int64_t W) {
 }
 
 // ---------------------------------------------------------------------------
+// Per-row symmetric int8 quantisation of bf16 activations (the step before a
+// quantised linear layer): s = max(absmax(row), 1e-12) / 127 and
+// q = clamp(round_half_even(x / s), -127, 127), all in fp32 with IEEE
+// division.  One warp per row; two passes over the row (max, then codes).
+__global__ void quant_rows_bf16_kernel(const __nv_bfloat16* __restrict__ X, int64_t M, int64_t K,
+                                       int8_t* __restrict__ Q, float* __restrict__ S, int vec) {
+  const int lane = threadIdx.x & 31;
+  const int64_t row = (int64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+  if (row >= M) return;
+  const __nv_bfloat16* x = X + row * K;
+  int8_t* q = Q + row * K;
+  float amax = 0.0f;
+  if (vec) {
+    for (int64_t k = (int64_t)lane * 8; k < K; k += 32 * 8) {
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(x + k));
+      const __nv_bfloat16* h = reinterpret_cast<const __nv_bfloat16*>(&v);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(__bfloat162float(h[j])));
+    }
+  } else {
+    for (int64_t k = lane; k < K; k += 32) amax = fmaxf(amax, fabsf(__bfloat162float(x[k])));
+  }
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+  const float sc = __fdiv_rn(fmaxf(amax, 1e-12f), 127.0f);
+  if (lane == 0) S[row] = sc;
+  auto code = [&](float v) -> int8_t {
+    float r = rintf(__fdiv_rn(v, sc));
+    r = fminf(fmaxf(r, -127.0f), 127.0f);
+    return (int8_t)(int)r;
+  };
+  if (vec) {
+    for (int64_t k = (int64_t)lane * 8; k < K; k += 32 * 8) {
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(x + k));
+      const __nv_bfloat16* h = reinterpret_cast<const __nv_bfloat16*>(&v);
+      uint32_t lo = 0, hi = 0;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        lo |= (uint32_t)(uint8_t)code(__bfloat162float(h[j])) << (8 * j);
+        hi |= (uint32_t)(uint8_t)code(__bfloat162float(h[4 + j])) << (8 * j);
+      }
+      *reinterpret_cast<uint2*>(q + k) = make_uint2(lo, hi);
+    }
+  } else {
+    for (int64_t k = lane; k < K; k += 32) q[k] = code(__bfloat162float(x[k]));
+  }
+}
+
+// ---------------------------------------------------------------------------
 // Skinny 8-bit GEMM: M <= MT rows of A against all N rows of B, for M <= 16.
 // HBM-bound on B, which is streamed exactly once.  Persistent warps each own
 // groups of NR consecutive rows of B; a lane covers 16 bytes of K per step
@@ -491,6 +540,18 @@ static int grid_for(int64_t work, int threads, int sm_count) {
   const int64_t cap = (int64_t)sm_count * 16;
   if (blocks > cap) blocks = cap;
   return (int)(blocks < 1 ? 1 : blocks);
+}
+
+cudaError_t launch_quant_rows_bf16(const void* X, int64_t M, int64_t K, int8_t* Q, float* S,
+                                   cudaStream_t s) {
+  if (M == 0) return cudaSuccess;
+  const int vec = (K % 8 == 0) && ((reinterpret_cast<uintptr_t>(X) & 15) == 0) &&
+                  ((reinterpret_cast<uintptr_t>(Q) & 7) == 0);
+  const int rows_per_block = 8;
+  const unsigned grid = (unsigned)((M + rows_per_block - 1) / rows_per_block);
+  quant_rows_bf16_kernel<<<grid, 32 * rows_per_block, 0, s>>>(
+      static_cast<const __nv_bfloat16*>(X), M, K, Q, S, vec);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_encode_pair(int bits, const void* a, int64_t rows_a, void* enc_a,

@@ -18,6 +18,9 @@ cudaError_t launch_encode_pair(int bits, const void* a, int64_t rows_a, void* en
 cudaError_t launch_skinny_s8(const int8_t* A, const int8_t* B, int M, int N, int K, int32_t* C,
                              const float* sx, const float* sw, void* Y, int sm_count,
                              cudaStream_t s);
+// Per-row symmetric int8 quantisation of bf16 rows (Q: M x K int8, S: M fp32).
+cudaError_t launch_quant_rows_bf16(const void* X, int64_t M, int64_t K, int8_t* Q, float* S,
+                                   cudaStream_t s);
 // Small 8-bit GEMM on dp4a, one launch; K % 16 == 0, A and B 16-byte aligned.
 cudaError_t launch_small_s8(const int8_t* A, const int8_t* B, int64_t M, int64_t N, int64_t K,
                             int32_t* C, cudaStream_t s);

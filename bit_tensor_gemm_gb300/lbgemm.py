@@ -50,6 +50,8 @@ _SIGNATURES = {
     "lbgemm_encode": (_i32, [_i32, _i64, _i64, _vp, _vp, _vp]),
     "lbgemm_run_encoded": (_i32, [_i32, _i64, _i64, _i64, _vp, _vp, _vp, _i32, _vp]),
     "lbgemm_linear": (_i32, [_i64, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _vp]),
+    "lbgemm_quantize_rows": (_i32, [_i64, _i64, _vp, _vp, _vp, _vp]),
+    "lbgemm_linear_quant": (_i32, [_i64, _i64, _i64, _vp, _vp, _vp, _vp, _vp]),
     "lbgemm_linear_variant": (_i32, [_i64, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _i32, _vp]),
     "lbgemm_select": (_i32, [_i32, _i64, _i64, _i64]),
     "lbgemm_table_set": (_i32, [_i32, _i64, _i64, _i64, _i32]),
@@ -200,6 +202,15 @@ def lbgemm_run_encoded(bits, M, N, K, A_enc, B_enc, C, variant=-1, stream=None) 
 def lbgemm_linear(M, N, K, X, sx, W, sw, Y, stream=None) -> None:
     _check(load().lbgemm_linear(M, N, K, _addr(X), _addr(sx), _addr(W), _addr(sw), _addr(Y),
                                 _stream(stream)))
+
+
+def lbgemm_quantize_rows(M, K, X, Q, S, stream=None) -> None:
+    _check(load().lbgemm_quantize_rows(M, K, _addr(X), _addr(Q), _addr(S), _stream(stream)))
+
+
+def lbgemm_linear_quant(M, N, K, X, W, sw, Y, stream=None) -> None:
+    _check(load().lbgemm_linear_quant(M, N, K, _addr(X), _addr(W), _addr(sw), _addr(Y),
+                                      _stream(stream)))
 
 
 def lbgemm_linear_variant(M, N, K, X, sx, W, sw, Y, variant, stream=None) -> None:

@@ -174,6 +174,25 @@ lbgemm_status lbgemm_linear_variant(int64_t M, int64_t N, int64_t K, const int8_
                                     const float* sx, const int8_t* W, const float* sw, void* Y,
                                     int variant, void* stream);
 
+/* Per-token (per-row) symmetric int8 quantisation of activations, the step in
+ * front of a quantised linear layer ([LBG] section 4 and conclusion: low-bit
+ * layers of quantised networks; the page gives no quantiser, this is the
+ * plainest one): for each row of X (bf16, M x K row-major),
+ *   s[m] = max(max_k |X[m][k]|, 1e-12) / 127                (fp32)
+ *   Q[m][k] = clamp(round_half_even(X[m][k] / s[m]), -127, 127)
+ * with IEEE fp32 division, so the codes are reproducible bit for bit.
+ * Q: int8 M x K, S: fp32 [M]; device pointers owned by the caller. */
+lbgemm_status lbgemm_quantize_rows(int64_t M, int64_t K, const void* X, int8_t* Q, float* S,
+                                   void* stream);
+
+/* The linear layer on unquantised activations: lbgemm_quantize_rows of X
+ * (bf16 M x K) into library scratch, then lbgemm_linear with the resulting
+ * codes and per-token scales against W (int8 N x K, scales sw).  Y: bf16 M x N.
+ * The scratch (M*K + 4*M bytes) comes from a per-device buffer the library
+ * grows with cudaMalloc. */
+lbgemm_status lbgemm_linear_quant(int64_t M, int64_t N, int64_t K, const void* X, const int8_t* W,
+                                  const float* sw, void* Y, void* stream);
+
 /* ---- selection table: [LBG] sections 2-3 ------------------------------------
  * The table maps (bits, M, N, K) on this device's SM count to a variant.  A
  * shape with no entry takes the learned selector's choice when a network is

@@ -154,3 +154,24 @@ def linear(X: np.ndarray, sx: np.ndarray, W: np.ndarray, sw: np.ndarray,
                                threads or default_threads())
     _check(rc, "oracle linear")
     return ref
+
+
+def quantize_rows(x: np.ndarray):
+    """Per-row symmetric int8 quantisation, in float32 as the library states it:
+    s = max(max|x|, 1e-12) / 127 and q = clamp(round_half_even(x / s), -127, 127)
+    (the quantiser in front of a quantised linear layer, [LBG] section 4; the
+    page gives none, this is the plainest reading).  x: float32 [M, K]."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    amax = np.abs(x).max(axis=1) if x.shape[1] else np.zeros(x.shape[0], np.float32)
+    s = np.maximum(amax, np.float32(1e-12)).astype(np.float32) / np.float32(127.0)
+    q = np.rint(x / s[:, None].astype(np.float32))
+    q = np.clip(q, -127, 127).astype(np.int8)
+    return q, s.astype(np.float32)
+
+
+def linear_quant(x: np.ndarray, W: np.ndarray, sw: np.ndarray, threads: int | None = None,
+                 lib=None):
+    """fp64 reference of the linear layer on unquantised activations:
+    quantize_rows(x), then the quantised linear layer."""
+    q, s = quantize_rows(x)
+    return linear(q, s, W, sw, threads=threads, lib=lib)

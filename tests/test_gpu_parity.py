@@ -237,6 +237,44 @@ def test_linear_variants(variant):
     check_linear(G().linear(X, sx, W, sw, variant), ref, acc == 0, f"linear v{variant}")
 
 
+# ---- quantised activations ------------------------------------------------------
+
+def _bf16_rows(M, K, seed):
+    g = np.random.default_rng(seed)
+    x = (g.standard_normal((M, K)) * g.uniform(0.05, 20, (M, 1))).astype(np.float32)
+    x[min(1, M - 1)] = 0.0  # a zero row
+    xt = torch.from_numpy(x).to(torch.bfloat16)
+    return xt, xt.float().numpy()  # the exact values the GPU reads
+
+
+@pytest.mark.parametrize("M,K", [(37, 4096), (5, 100), (130, 1000), (1, 8)])
+def test_quantize_rows_bit_exact(M, K):
+    xt, xf = _bf16_rows(M, K, M + K)
+    Q = torch.empty((M, K), dtype=torch.int8, device=G().DEV)
+    S = torch.empty(M, dtype=torch.float32, device=G().DEV)
+    L.lbgemm_quantize_rows(M, K, xt.to(G().DEV), Q, S)
+    L.lbgemm_device_status()
+    q, s = oracle.quantize_rows(xf)
+    np.testing.assert_array_equal(S.cpu().numpy(), s)
+    assert_exact(Q.cpu().numpy(), q, f"quantize {M}x{K}")
+
+
+@pytest.mark.parametrize("M", [1, 16, 128, 300])
+def test_linear_quant(M):
+    N, K = 1024, 4096
+    xt, xf = _bf16_rows(M, K, 600 + M)
+    g = np.random.default_rng(M)
+    W = g.integers(-127, 128, (N, K)).astype(np.int8)
+    sw = (g.random(N) * 0.01).astype(np.float32)
+    Y = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device=G().DEV)
+    L.lbgemm_linear_quant(M, N, K, xt.to(G().DEV), G().to_dev(W), G().to_dev(sw), Y)
+    L.lbgemm_device_status()
+    ref = oracle.linear_quant(xf, W, sw)
+    q, s = oracle.quantize_rows(xf)
+    check_linear(Y.float().cpu().numpy().astype(np.float64), ref, oracle.gemm(8, q, W, K) == 0,
+                 f"linear_quant M={M}")
+
+
 # ---- status word ------------------------------------------------------------------
 
 def test_wait_timeout_is_reported_and_recovers():

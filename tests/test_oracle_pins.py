@@ -206,7 +206,30 @@ def pin_linear(lib=None):
     assert np.all(ref[1] == 0)
 
 
-PINS = [pin_golden, pin_s8_matches_numpy, pin_s4_bruteforce, pin_s4_matches_numpy,
+def pin_quantize(lib=None):
+    """Per-row quantiser: a hand-worked row, the zero row, and the bounds that
+    hold for any row (the row's absmax maps to +-127, |q| <= 127, and q*s is
+    within s/2 (plus fp32 rounding) of x)."""
+    q, s = oracle.quantize_rows(np.array([[1.0, -4.0, 0.5], [0.0, 0.0, 0.0]], np.float32))
+    # row 0: s = 4/127, x/s = (31.75, -127, 15.875) -> (32, -127, 16)
+    assert q[0].tolist() == [32, -127, 16] and s[0] == np.float32(4.0) / np.float32(127.0)
+    assert q[1].tolist() == [0, 0, 0] and s[1] == np.float32(1e-12) / np.float32(127.0)
+    g = np.random.default_rng(8)
+    x = (g.standard_normal((50, 333)) * g.uniform(0.01, 100, (50, 1))).astype(np.float32)
+    q, s = oracle.quantize_rows(x)
+    assert np.all(np.abs(q.astype(int)) <= 127)
+    am = np.argmax(np.abs(x), axis=1)
+    assert np.all(np.abs(q[np.arange(50), am].astype(int)) == 127)
+    err = np.abs(q.astype(np.float64) * s[:, None] - x)
+    assert np.all(err <= s[:, None] * (0.5 + 1e-5))
+    # the quantised linear reference is the linear reference of the codes
+    W = g.integers(-127, 128, (4, 333)).astype(np.int8)
+    sw = g.random(4).astype(np.float32)
+    np.testing.assert_array_equal(oracle.linear_quant(x[:3], W, sw, lib=lib),
+                                  oracle.linear(q[:3], s[:3], W, sw, lib=lib))
+
+
+PINS = [pin_golden, pin_quantize, pin_s8_matches_numpy, pin_s4_bruteforce, pin_s4_matches_numpy,
         pin_b1_bruteforce, pin_b1_matches_numpy, pin_identities, pin_overflow, pin_entries,
         pin_linear]
 
