@@ -74,6 +74,24 @@ def ops_of(shapes):
     return float(sum(2 * m * n * k for m, n, k in shapes))
 
 
+def max_over_ranks(x: float, device=None) -> float:
+    """The largest x over all ranks (replicas time the same workload; the
+    whole job takes as long as its slowest rank).  Identity without a
+    process group."""
+    import torch  # noqa: PLC0415
+    if not (torch.distributed.is_available() and torch.distributed.is_initialized()):
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(ops_per_step: float, steps: int, world: int, max_total_ms: float) -> float:
+    """Whole-job throughput in TOPS: every rank runs the full workload (weak
+    scaling), so the job does world x steps x ops in the slowest rank's time."""
+    return ops_per_step * steps * world / (max_total_ms / 1e3) / 1e12
+
+
 # ---- clocks during the timed region ------------------------------------------------
 
 class Clocks:
@@ -308,13 +326,9 @@ def run_ours(args):
     launches = L.lbgemm_launch_count() - launches0
     clk = clocks.stop()
     L.lbgemm_device_status()
-    total_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(step_ms), dev)
     ops_step = ops_of(shapes)
-    value = ops_step * args.steps * world / (total_ms / 1e3) / 1e12
+    value = job_value(ops_step, args.steps, world, total_ms)
 
     # -- selected vs default, on an independent re-time, interleaved --------------------------
     # The pages' comparison: the chosen tile x stage variant against the
