@@ -41,7 +41,7 @@ using lbg::TcKernel;
 using lbg::TcParams;
 
 constexpr int kNumVariants = 9;
-constexpr int kDefaultVariant = 7;  // large tile, 3 stages
+constexpr int kDefaultVariant = 7;  // large tile, middle stage level (5 stages)
 constexpr int kMaxDevices = 64;
 constexpr int kSkinnyMaxM = 16;
 constexpr int kGroupM = 16;
@@ -200,12 +200,20 @@ lbgemm_status check_gemm_args(int bits, int64_t M, int64_t N, int64_t K, const v
   return LBGEMM_OK;
 }
 
+// Pipeline stages of variant v: levels 0, 1, 2 of the stage dimension are
+// 2, 3, 4 stages for the single-CTA tiles and 4, 5, 6 for the CTA-pair large
+// tile, whose 256 x 256 tile needs at least 4 stages in flight to cover the
+// load latency (and stages cost it half as much shared memory per SM).
+int variant_stages(int variant) {
+  return variant / 3 == 2 ? variant % 3 + 4 : variant % 3 + 2;
+}
+
 TcKernel tc_kernel(int variant, bool f8, bool linear) {
-  const int tile = variant / 3, stages = variant % 3 + 2;
+  const int tile = variant / 3, stages = variant_stages(variant);
   switch (tile) {
     case 0: return lbg::tc_kernel_small(stages, f8, linear);
     case 1: return lbg::tc_kernel_medium(stages, f8, linear);
-    default: return lbg::tc_kernel_large(stages, f8, linear);
+    default: return lbg::tc_kernel_pair(stages, f8, linear);
   }
 }
 
@@ -283,18 +291,38 @@ lbgemm_status encode_kmajor(CUtensorMap* map, const void* base, int64_t rows, in
   return LBGEMM_OK;
 }
 
-int occupancy(DeviceState& d, const TcKernel& k) {
+// Work units a kernel can run at once on this device: resident CTAs per SM
+// times the SM count, or for a CTA-pair kernel the clusters of two that fit
+// at once (pairs must sit in one GPC, so this can be below half the SMs).
+int unit_slots(DeviceState& d, const TcKernel& k) {
   std::lock_guard<std::mutex> lock(g_mu);
   auto it = d.occupancy.find(k.func);
   if (it != d.occupancy.end()) return it->second;
   cudaFuncSetAttribute(k.func, cudaFuncAttributeMaxDynamicSharedMemorySize, k.smem);
-  int occ = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k.func, k.threads, k.smem) !=
-      cudaSuccess)
-    occ = 1;
-  occ = std::max(1, std::min(occ, 512 / k.tmem_cols));
-  d.occupancy[k.func] = occ;
-  return occ;
+  int slots = 0;
+  if (k.cluster > 1) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(d.sm_count / k.cluster * k.cluster);
+    cfg.blockDim = dim3(k.threads);
+    cfg.dynamicSmemBytes = k.smem;
+    int nc = 0;
+    if (cudaOccupancyMaxActiveClusters(&nc, k.func, &cfg) != cudaSuccess || nc < 1) {
+      cudaGetLastError();
+      nc = 1;
+    }
+    slots = std::min(nc, d.sm_count / k.cluster);
+  } else {
+    int occ = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k.func, k.threads, k.smem) !=
+        cudaSuccess) {
+      cudaGetLastError();
+      occ = 1;
+    }
+    occ = std::max(1, std::min(occ, 512 / k.tmem_cols));
+    slots = d.sm_count * occ;
+  }
+  d.occupancy[k.func] = slots;
+  return slots;
 }
 
 // ---- the tensor-core path (bits 8 and 4, and the linear layer) --------------------------------
@@ -320,8 +348,8 @@ int plan_splits(DeviceState& d, const TcKernel& k, int bits, int64_t M, int64_t 
   if (linear || !vec_ok) return 1;
   const int bk = bits == 8 ? 64 : 128;
   const int64_t num_kb = (enc_kp(bits, K) + bk - 1) / bk;
-  const int64_t tiles = ((M + 127) / 128) * ((N + k.tile_n - 1) / k.tile_n);
-  const int64_t slots = (int64_t)d.sm_count * occupancy(d, k);
+  const int64_t tiles = ((M + k.tile_m - 1) / k.tile_m) * ((N + k.tile_n - 1) / k.tile_n);
+  const int64_t slots = unit_slots(d, k);
   if (tiles * 2 > slots) return 1;
   const int64_t splits = std::min<int64_t>(std::min<int64_t>(slots / tiles, num_kb / 4), 64);
   return (int)std::max<int64_t>(splits, 1);
@@ -339,7 +367,7 @@ lbgemm_status run_tc_encoded(DeviceState& d, int bits, int64_t M, int64_t N, int
   CUtensorMap ma, mb;
   lbgemm_status st = encode_kmajor(&ma, encA, M, kp, !f8, 128);
   if (st != LBGEMM_OK) return st;
-  st = encode_kmajor(&mb, encB, N, kp, !f8, k.tile_n);
+  st = encode_kmajor(&mb, encB, N, kp, !f8, k.b_box_rows ? k.b_box_rows : k.tile_n);
   if (st != LBGEMM_OK) return st;
 
   TcParams p{};
@@ -351,7 +379,7 @@ lbgemm_status run_tc_encoded(DeviceState& d, int bits, int64_t M, int64_t N, int
   const int chunk_elems =
       bits == 8 ? g_chunk_s8.load() : bits == 4 ? g_chunk_s4.load() : g_chunk_b1.load();
   p.chunk_kb = std::max(1, chunk_elems / bk);
-  p.tiles_m = (int)((M + 127) / 128);
+  p.tiles_m = (int)((M + k.tile_m - 1) / k.tile_m);
   p.tiles_n = (int)((N + k.tile_n - 1) / k.tile_n);
   p.num_tiles = p.tiles_m * p.tiles_n;
   p.group_m = kGroupM;
@@ -386,7 +414,8 @@ lbgemm_status run_tc_encoded(DeviceState& d, int bits, int64_t M, int64_t N, int
     if (r != CUDA_SUCCESS)
       return fail(LBGEMM_ERR_CUDA, "cuTensorMapEncodeTiled (C) failed (%d)", (int)r);
   }
-  const int grid = (int)std::min<int64_t>(p.num_units, (int64_t)d.sm_count * occupancy(d, k));
+  const int grid =
+      (int)std::min<int64_t>(p.num_units, (int64_t)unit_slots(d, k)) * k.cluster;
   // Right after our own re-encoding launch, the GEMM is a programmatic
   // dependent launch: its prologue (barriers, TMEM, descriptor prefetch)
   // overlaps the encoder's tail and its producer waits for the encoder's
@@ -480,7 +509,7 @@ lbgemm_status run_tc_fused(DeviceState& d, int fuse, int tile_n, int64_t M, int6
                  CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(LBGEMM_ERR_CUDA, "cuTensorMapEncodeTiled (C) failed (%d)", (int)r);
   }
-  const int grid = (int)std::min<int64_t>(p.num_units, (int64_t)d.sm_count * occupancy(d, k));
+  const int grid = (int)std::min<int64_t>(p.num_units, (int64_t)unit_slots(d, k));
   cudaError_t e = k.launch(&ma, &mb, &mc, &p, grid, true, stream);
   if (e != cudaSuccess) return cuda_fail(e, "fused tensor-core GEMM launch");
   g_launches += 1;
@@ -625,11 +654,11 @@ lbgemm_status lbgemm_variant_info(int bits, int variant, int* tile_m, int* tile_
   if ((bits != 8 && bits != 4 && bits != 1) || variant < 0 || variant >= kNumVariants)
     return fail(LBGEMM_ERR_INVALID_ARG, "unknown bits/variant");
   const int tile = variant / 3;
-  const int bm = 128, bn = 64 << tile, bk = bits == 8 ? 64 : 128;
+  const int bm = tile == 2 ? 256 : 128, bn = 64 << tile, bk = bits == 8 ? 64 : 128;
   if (tile_m) *tile_m = bm;
   if (tile_n) *tile_n = bn;
   if (tile_k) *tile_k = bk;
-  if (stages) *stages = variant % 3 + 2;
+  if (stages) *stages = variant_stages(variant);
   return LBGEMM_OK;
 }
 

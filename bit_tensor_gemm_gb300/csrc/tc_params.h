@@ -34,7 +34,10 @@ struct TcKernel {
   const void* func = nullptr;
   int smem = 0;
   int tmem_cols = 0;
+  int tile_m = 128;     // output rows per tile (per CTA pair for cluster 2)
   int tile_n = 0;
+  int b_box_rows = 0;   // rows of B per TMA box (0: tile_n)
+  int cluster = 1;      // CTAs per tile: 2 for the cta_group::2 kernel
   int stages = 0;
   int threads = 320;
 };
@@ -48,10 +51,11 @@ inline constexpr int tc_smem_request(int used, int tmem_cols) {
   return used > min_req ? used : min_req;
 }
 
-// tile: 0 small (128 x 64), 1 medium (128 x 128), 2 large (128 x 256).
+// tile: 0 small (128 x 64), 1 medium (128 x 128), stages 2..4;
+// 2 large (256 x 256 on a pair of CTAs, cta_group::2 MMAs), stages 4..6.
 TcKernel tc_kernel_small(int stages, bool f8, bool linear);
 TcKernel tc_kernel_medium(int stages, bool f8, bool linear);
-TcKernel tc_kernel_large(int stages, bool f8, bool linear);
+TcKernel tc_kernel_pair(int stages, bool f8, bool linear);
 // Fused variants (8-bit only, 3 fp16 stages, 8 int8 staging stages): fuse 1 converts B in the kernel,
 // fuse 2 converts A; tile_n 64 or 128.
 TcKernel tc_kernel_fused(int fuse, int tile_n, bool linear);

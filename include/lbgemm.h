@@ -62,9 +62,12 @@ typedef enum {
 } lbgemm_status;
 
 /* Number of tile x stage variants (9) and the index of the default one.
- * Variant v has tile class v / 3 (0 small, 1 medium, 2 large) and v % 3 + 2
- * pipeline stages.  [LBG] section 2; the default (large, 3 stages = 7) is
- * this library's reading of the unnamed "default template" of section 4. */
+ * Variant v has tile class v / 3 (0 small, 1 medium, 2 large) and stage level
+ * v % 3.  [LBG] section 2 names three stage counts (2, 3, 4); here the levels
+ * are 2, 3, 4 stages for the small (128 x 64) and medium (128 x 128) tiles and
+ * 4, 5, 6 stages for the large tile (256 x 256, computed by a pair of CTAs).
+ * The default (large tile, middle level = 7) is this library's reading of
+ * the unnamed "default template" of section 4. */
 int lbgemm_num_variants(void);
 int lbgemm_default_variant(void);
 

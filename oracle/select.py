@@ -9,10 +9,14 @@ inputs are M, N, K and the SM count.  Section 4: the selected template is
 compared with a default template.
 
 Readings where the page is silent:
-  - variant index = 3 * tile + (stages - 2), tile 0 = small, 1 = medium,
-    2 = large; so index 0 is small/2 stages and index 8 is large/4 stages.
-  - the default template (not named on the page) is large tile, 3 stages,
-    index 7.
+  - variant index = 3 * tile + stage level, tile 0 = small, 1 = medium,
+    2 = large, stage level 0, 1, 2.  The page's three stage counts are 2, 3
+    and 4 (Ampere multistage templates); on GB300 the levels keep those counts
+    for the small and medium tiles and are 4, 5 and 6 for the large tile,
+    which is 256 x 256 on a pair of CTAs and halves the shared memory a stage
+    costs each SM.  Index 0 is small/2 stages, index 8 is large/6 stages.
+  - the default template (not named on the page) is the large tile at the
+    middle stage level, index 7.
   - label: the argmin of the measured times, the lowest index on exact ties.
   - the library's stored choice adds a no-regression guard: keep the default
     unless the label beats it by more than ``keep_within`` (2 %).
@@ -27,16 +31,17 @@ import math
 
 NUM_VARIANTS = 9
 TILES = ("small", "medium", "large")
-STAGES = (2, 3, 4)
-DEFAULT_VARIANT = 3 * 2 + (3 - 2)  # large tile, 3 stages
+STAGE_COUNTS = ((2, 3, 4), (2, 3, 4), (4, 5, 6))  # per tile class, levels 0..2
+DEFAULT_VARIANT = 3 * 2 + 1  # large tile, middle stage level
 
 
 def variant_index(tile: int, stages: int) -> int:
-    return 3 * tile + (stages - 2)
+    return 3 * tile + STAGE_COUNTS[tile].index(stages)
 
 
 def variant_of(index: int) -> tuple[int, int]:
-    return index // 3, index % 3 + 2
+    """(tile class, pipeline stages) of a variant index."""
+    return index // 3, STAGE_COUNTS[index // 3][index % 3]
 
 
 def label(times) -> int:

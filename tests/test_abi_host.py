@@ -45,10 +45,11 @@ def test_variant_space(lib):
         tile, stages = osel.variant_of(v)
         info = L.lbgemm_variant_info(8, v)
         assert info["stages"] == stages
-        assert info["tile_n"] == (64, 128, 256)[tile] and info["tile_m"] == 128
+        assert info["tile_n"] == (64, 128, 256)[tile]
+        assert info["tile_m"] == (128, 128, 256)[tile]
         assert L.lbgemm_variant_info(4, v)["tile_k"] == 128
         b1 = L.lbgemm_variant_info(1, v)
-        assert (b1["tile_m"], b1["tile_n"], b1["tile_k"]) == (128, (64, 128, 256)[tile], 128)
+        assert (b1["tile_m"], b1["tile_n"], b1["tile_k"]) == (info["tile_m"], info["tile_n"], 128)
     with pytest.raises(L.LbgemmError):
         L.lbgemm_variant_info(8, 9)
 

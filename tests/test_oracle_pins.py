@@ -288,7 +288,8 @@ def test_select_label_and_choice():
     assert osel.table_choice(t) == osel.DEFAULT_VARIANT  # default within 2 %
     t[7] = 4.5
     assert osel.table_choice(t) == 1
-    assert osel.DEFAULT_VARIANT == 7 and osel.variant_of(7) == (2, 3)
+    assert osel.DEFAULT_VARIANT == 7 and osel.variant_of(7) == (2, 5)
+    assert osel.variant_of(0) == (0, 2) and osel.variant_of(8) == (2, 6)
     assert [osel.variant_index(*osel.variant_of(i)) for i in range(9)] == list(range(9))
 
 
