@@ -201,7 +201,7 @@ def run_reference(args):
 def source_hash():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "bit_tensor_gemm_gb300", "csrc")
-    for name in ("tc_gemm.cuh", "ptx.cuh", "tc_params.h"):
+    for name in ("tc_gemm.cuh", "tc_pair.cuh", "ptx.cuh", "tc_params.h"):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -391,6 +391,7 @@ def run_ours(args):
     encA = torch.empty(L.lbgemm_encoded_size(8, MAXD, MAXD), dtype=torch.uint8, device=dev)
     encB = torch.empty(L.lbgemm_encoded_size(8, MAXD, MAXD), dtype=torch.uint8, device=dev)
     enc_ms = []
+    torch.cuda.nvtx.range_push("roofline")  # lets a profiler capture these launches alone
     for (m, n, k) in shapes:
         L.lbgemm_encode(8, m, k, A, encA)
         L.lbgemm_encode(8, n, k, B, encB)
@@ -402,11 +403,14 @@ def run_ours(args):
         e1.record(stream)
         e1.synchronize()
         enc_ms.append(e0.elapsed_time(e1))
+    torch.cuda.nvtx.range_pop()
     kernel_tflops = ops_step / (sum(enc_ms) / 1e3) / 1e12
     peak_tc = peaks["bf16_tflops_sustained"]
     roofline = {"bound": "tensor", "achieved": kernel_tflops, "peak": peak_tc, "unit": "TFLOP/s",
                 "frac": kernel_tflops / peak_tc, "traffic": profiled_traffic(),
-                "kernel": "tc_gemm_kernel (int8 encoded as fp16, tcgen05 kind::f16)",
+                "kernel": "tensor-core GEMM: tc_gemm_kernel (small and medium tiles) and "
+                          "tc_pair_kernel (large tile, CTA pairs); int8 encoded as fp16, "
+                          "tcgen05 kind::f16",
                 "per": "launch average over the sweep's 729 launches (selected variants)",
                 "peak_source": f"{peak_kind} bf16 dense, sustained",
                 "frac_of_burst": kernel_tflops / peaks["bf16_tflops"]}
