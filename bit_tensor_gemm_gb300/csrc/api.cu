@@ -51,11 +51,10 @@ constexpr double kPopcMaxWork = 1073741824.0;
 // 8-bit problems with K <= kSmallMaxK and at most kSmallMaxWork MACs go to the
 // one-launch dp4a kernel.
 constexpr int64_t kSmallMaxK = 512;
-// Skinny 8-bit problems on the fused-conversion kernel (see fused_route).
-constexpr int64_t kFusedMaxSide = 256;
-constexpr int64_t kFusedMinOther = 2048;
-constexpr int64_t kFusedMinK = 1024;
-constexpr int kFusedTileN = 128;
+// 8-bit problems on the in-kernel-conversion kernel (see fused_route).
+constexpr int64_t kFusedMaxSide = 512;
+constexpr int64_t kFusedMinOther = 1024;
+constexpr int64_t kFusedMinK = 2048;
 constexpr double kSmallMaxWork = 268435456.0;  // M-tiles per group of the tile order (L2 reuse)
 constexpr size_t kFlushBytes = size_t(256) << 20;  // twice the 129 MB L2
 
@@ -448,46 +447,56 @@ lbgemm_status run_tc(DeviceState& d, int bits, int64_t M, int64_t N, int64_t K, 
   return run_tc_encoded(d, bits, M, N, K, encA, encB, C, sx, sw, Y, variant, true, splits, stream);
 }
 
-// Skinny 8-bit problems: only the small operand is re-encoded ahead; the
-// kernel converts the large one from int8 itself (fuse 1: B large, fuse 2: A
-// large).  Requires K % 16 == 0 (16-byte int8 row strides for TMA).
-lbgemm_status run_tc_fused(DeviceState& d, int fuse, int tile_n, int64_t M, int64_t N, int64_t K,
-                           const void* A, const void* B, int32_t* C, const float* sx,
+// 8-bit problems with one operand converted in the kernel: only the other
+// operand is re-encoded ahead.  large_b: B is converted (the kernel computes
+// C transposed, rows of B on the tensor-memory A side); else A is converted.
+// Requires K % 16 == 0 (16-byte int8 row strides for TMA).
+lbgemm_status run_tc_fused(DeviceState& d, bool large_b, int tile_n, int64_t M, int64_t N,
+                           int64_t K, const void* A, const void* B, int32_t* C, const float* sx,
                            const float* sw, void* Y, void* ws, cudaStream_t stream) {
   const bool linear = Y != nullptr;
-  TcKernel k = lbg::tc_kernel_fused(fuse, tile_n, linear);
-  if (!k.launch) return fail(LBGEMM_ERR_UNSUPPORTED, "no fused kernel (fuse %d, tile %d)", fuse, tile_n);
+  TcKernel k = lbg::tc_kernel_ts(tile_n, large_b, linear);
+  if (!k.launch) return fail(LBGEMM_ERR_UNSUPPORTED, "no fused kernel (tile %d)", tile_n);
+  // rows of the converted (L) and of the re-encoded (S) operand
+  const int64_t rows_l = large_b ? N : M, rows_s = large_b ? M : N;
+  const void* opl = large_b ? B : A;
+  const void* ops = large_b ? A : B;
   const int64_t kp = enc_kp(8, K);  // == K when K % 16 == 0
-  const bool vec_ok = linear ? (N % 8 == 0) && aligned16(Y) : (N % 4 == 0) && aligned16(C);
-  const int splits = plan_splits(d, k, 8, M, N, K, linear, vec_ok);
+  // C goes out by TMA stores (untransposed, aligned) or by coalesced atomics
+  // (transposed); both can add split-K partial tiles.
+  const bool vec_ok = !large_b && (linear ? (N % 8 == 0) && aligned16(Y)
+                                          : (N % 4 == 0) && aligned16(C));
+  const int splits = plan_splits(d, k, 8, rows_l, rows_s, K, linear, vec_ok || large_b);
   if (splits > 1) {  // cleared before the encoder, so the GEMM can be its dependent
     cudaError_t ez = cudaMemsetAsync(C, 0, (size_t)(M * N) * sizeof(int32_t), stream);
     if (ez != cudaSuccess) return cuda_fail(ez, "cudaMemsetAsync (split K)");
   }
-  lbgemm_status st = fuse == 1 ? encode_operands(d, 8, A, M, ws, nullptr, 0, nullptr, K, stream)
-                               : encode_operands(d, 8, B, N, ws, nullptr, 0, nullptr, K, stream);
+  lbgemm_status st = encode_operands(d, 8, ops, rows_s, ws, nullptr, 0, nullptr, K, stream);
   if (st != LBGEMM_OK) return st;
-  CUtensorMap ma, mb;
-  cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)(fuse == 1 ? N : M)};
+  CUtensorMap ml, ms;
+  cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows_l};
   cuuint64_t strides[1] = {(cuuint64_t)K};
-  cuuint32_t box[2] = {64, (cuuint32_t)(fuse == 1 ? tile_n : 128)};
+  // the 256-wide kernel stages 128-element boxes (128-byte swizzle), the
+  // others 64-element boxes (64-byte swizzle)
+  const bool pairs = tile_n == 256;
+  cuuint32_t box[2] = {pairs ? 128u : 64u, 128};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = g_encode(fuse == 1 ? &mb : &ma, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
-                        const_cast<void*>(fuse == 1 ? B : A), dims, strides, box, estr,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+  CUresult r = g_encode(&ml, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(opl), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        pairs ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(LBGEMM_ERR_CUDA, "cuTensorMapEncodeTiled (int8) failed (%d)", (int)r);
-  st = fuse == 1 ? encode_kmajor(&ma, ws, M, kp, true, 128)
-                 : encode_kmajor(&mb, ws, N, kp, true, tile_n);
+  st = encode_kmajor(&ms, ws, rows_s, kp, true, tile_n);
   if (st != LBGEMM_OK) return st;
   TcParams p{};
-  p.M = (int)M;
-  p.N = (int)N;
+  p.M = (int)rows_l;
+  p.N = (int)rows_s;
   p.K = (int)K;
   p.num_kb = (int)((kp + 63) / 64);
   p.chunk_kb = std::max(1, g_chunk_s8.load() / 64);
-  p.tiles_m = (int)((M + 127) / 128);
-  p.tiles_n = (int)((N + tile_n - 1) / tile_n);
+  if (pairs) p.chunk_kb = std::max(4, p.chunk_kb & ~3);  // whole groups of 4 slices
+  p.tiles_m = (int)((rows_l + 127) / 128);
+  p.tiles_n = (int)((rows_s + tile_n - 1) / tile_n);
   p.num_tiles = p.tiles_m * p.tiles_n;
   p.group_m = kGroupM;
   p.splits = splits;
@@ -500,7 +509,7 @@ lbgemm_status run_tc_fused(DeviceState& d, int fuse, int tile_n, int64_t M, int6
   p.vec_ok = vec_ok;
   CUtensorMap mc;
   std::memset(&mc, 0, sizeof mc);
-  if (!linear && p.vec_ok) {
+  if (!linear && vec_ok) {
     cuuint64_t cd[2] = {(cuuint64_t)N, (cuuint64_t)M};
     cuuint64_t cs[1] = {(cuuint64_t)(N * 4)};
     cuuint32_t cb[2] = {32, 32};
@@ -510,21 +519,24 @@ lbgemm_status run_tc_fused(DeviceState& d, int fuse, int tile_n, int64_t M, int6
     if (r != CUDA_SUCCESS) return fail(LBGEMM_ERR_CUDA, "cuTensorMapEncodeTiled (C) failed (%d)", (int)r);
   }
   const int grid = (int)std::min<int64_t>(p.num_units, (int64_t)unit_slots(d, k));
-  cudaError_t e = k.launch(&ma, &mb, &mc, &p, grid, true, stream);
+  cudaError_t e = k.launch(&ml, &ms, &mc, &p, grid, true, stream);
   if (e != cudaSuccess) return cuda_fail(e, "fused tensor-core GEMM launch");
   g_launches += 1;
   return LBGEMM_OK;
 }
 
-// Route of the fused kernel for a skinny 8-bit problem (1: B is converted in
-// the kernel, 2: A is), or 0.  Measured on GB300: with one side <= 256, the
-// other >= 2048 and K >= 1024, skipping the large operand's re-encoding pass
-// is 1.1-2x faster (64 x 16384 x 16384: 294 -> 141 us); at 512 rows and up
-// the pre-pass route wins.
-int fused_route(int64_t M, int64_t N, int64_t K, const void* A, const void* B) {
+// Route of the in-kernel-conversion kernel for an 8-bit problem (1: B is
+// converted in the kernel, 2: A is; 0: re-encode both) and its tile width
+// along the re-encoded operand.  Measured on GB300 over the 729-shape grid:
+// with the small side <= 512, the large side >= 1024 and K >= 2048, skipping
+// the large operand's re-encoding pass wins (e.g. 512 x 8192 x 8192: 101 ->
+// 81 us; 256 x 16384 x 16384: 275 -> 146 us); the tile is the narrowest that
+// covers the small side (64, 128, else 256).
+int fused_route(int64_t M, int64_t N, int64_t K, const void* A, const void* B, int* tile_n) {
   if (K % 16 || !aligned16(A) || !aligned16(B)) return 0;
   const int64_t lo = std::min(M, N), hi = std::max(M, N);
   if (!(lo <= kFusedMaxSide && hi >= kFusedMinOther && K >= kFusedMinK)) return 0;
+  *tile_n = lo <= 64 ? 64 : lo <= 128 ? 128 : 256;
   return M <= N ? 1 : 2;
 }
 
@@ -565,21 +577,21 @@ lbgemm_status run_any(int bits, int64_t M, int64_t N, int64_t K, const void* A, 
     g_launches += 1;
     return LBGEMM_OK;
   }
-  const int fuse = (bits == 8 && auto_pick) ? fused_route(M, N, K, A, B) : 0;
-  const int fuse_tile = kFusedTileN;
+  int fuse_tile = 0;
+  const int fuse = (bits == 8 && auto_pick) ? fused_route(M, N, K, A, B, &fuse_tile) : 0;
   if (fuse) {
     const size_t need_f = enc_bytes(8, fuse == 1 ? M : N, K);
     if (!internal_ws) {
       if (!ws || ws_bytes < need_f)
         return fail(LBGEMM_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need_f,
                     ws_bytes);
-      return run_tc_fused(*d, fuse, fuse_tile, M, N, K, A, B, C, nullptr, nullptr, nullptr, ws,
+      return run_tc_fused(*d, fuse == 1, fuse_tile, M, N, K, A, B, C, nullptr, nullptr, nullptr, ws,
                           stream);
     }
     std::lock_guard<std::mutex> lock(g_ws_mu);
     st = scratch_acquire(d->ws, need_f, stream);
     if (st != LBGEMM_OK) return st;
-    st = run_tc_fused(*d, fuse, fuse_tile, M, N, K, A, B, C, nullptr, nullptr, nullptr, d->ws.ptr,
+    st = run_tc_fused(*d, fuse == 1, fuse_tile, M, N, K, A, B, C, nullptr, nullptr, nullptr, d->ws.ptr,
                       stream);
     lbgemm_status st2 = scratch_release(d->ws, stream);
     return st != LBGEMM_OK ? st : st2;
@@ -620,12 +632,13 @@ lbgemm_status run_linear(int64_t M, int64_t N, int64_t K, const int8_t* X, const
     g_launches += 1;
     return LBGEMM_OK;
   }
-  if (auto_pick && fused_route(M, N, K, X, W) == 1) {
+  int fuse_tile = 0;
+  if (auto_pick && fused_route(M, N, K, X, W, &fuse_tile) == 1) {
     // small token counts: only X is re-encoded; the kernel converts W itself
     std::lock_guard<std::mutex> lock(g_ws_mu);
     st = scratch_acquire(d->ws, enc_bytes(8, M, K), stream);
     if (st != LBGEMM_OK) return st;
-    st = run_tc_fused(*d, 1, kFusedTileN, M, N, K, X, W, nullptr, sx, sw, Y, d->ws.ptr, stream);
+    st = run_tc_fused(*d, true, fuse_tile, M, N, K, X, W, nullptr, sx, sw, Y, d->ws.ptr, stream);
     lbgemm_status st2 = scratch_release(d->ws, stream);
     return st != LBGEMM_OK ? st : st2;
   }
@@ -675,6 +688,31 @@ lbgemm_status lbgemm_run_variant(int bits, int64_t M, int64_t N, int64_t K, cons
                                  const void* B, int32_t* C, int variant, void* stream) {
   try {
     return run_any(bits, M, N, K, A, B, C, variant, nullptr, 0, true, as_stream(stream));
+  } catch (...) {
+    return fail(LBGEMM_ERR_CUDA, "internal error");
+  }
+}
+
+lbgemm_status lbgemm_run_fused(int64_t M, int64_t N, int64_t K, const int8_t* A, const int8_t* B,
+                               int32_t* C, int tile_n, void* stream) {
+  try {
+    lbgemm_status st = check_gemm_args(8, M, N, K, A, B, C);
+    if (st != LBGEMM_OK) return st;
+    if (tile_n != 64 && tile_n != 128 && tile_n != 256)
+      return fail(LBGEMM_ERR_INVALID_ARG, "tile_n must be 64, 128 or 256 (got %d)", tile_n);
+    if (K % 16) return fail(LBGEMM_ERR_ALIGNMENT, "the fused kernel needs K %% 16 == 0");
+    if (M == 0 || N == 0) return LBGEMM_OK;
+    DeviceState* d = nullptr;
+    st = device_state(&d);
+    if (st != LBGEMM_OK) return st;
+    const bool large_b = N >= M;
+    std::lock_guard<std::mutex> lock(g_ws_mu);
+    st = scratch_acquire(d->ws, enc_bytes(8, large_b ? M : N, K), as_stream(stream));
+    if (st != LBGEMM_OK) return st;
+    st = run_tc_fused(*d, large_b, tile_n, M, N, K, A, B, C, nullptr, nullptr, nullptr, d->ws.ptr,
+                      as_stream(stream));
+    lbgemm_status st2 = scratch_release(d->ws, as_stream(stream));
+    return st != LBGEMM_OK ? st : st2;
   } catch (...) {
     return fail(LBGEMM_ERR_CUDA, "internal error");
   }

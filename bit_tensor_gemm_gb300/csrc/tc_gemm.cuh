@@ -27,13 +27,6 @@
 //               shared memory (128-byte swizzle, conflict-free writes) and a
 //               TMA bulk store, so each store is whole 128-byte rows; bf16 Y
 //               of the linear layer is stored from registers.
-// Fused variant (FUSE = 1: B, FUSE = 2: A).  For skinny problems the big
-// operand's re-encoding pass would cost more than the GEMM, so that operand
-// stays int8 in memory: TMA copies its 64-byte K slices into a staging ring,
-// four converter warps (10..13) turn each into fp16 in the swizzled operand
-// layout (exact: v = (1024 + (v + 128)) - 1152 in fp16) and publish it with a
-// proxy fence and an mbarrier arrive; the MMA waits for both the TMA of the
-// other operand and the converters.
 // Every mbarrier wait is bounded; a wait that runs out raises the device
 // status word and winds the CTA down (waiting for its own copies in flight
 // and for its MMAs) before TMEM is freed.
@@ -51,11 +44,9 @@ namespace lbg {
 
 constexpr int kTcBM = 128;
 constexpr int kTcEpiWarps = 8;
-constexpr int kTcConvWarps = 4;
+constexpr int kTcThreads = 32 * (2 + kTcEpiWarps);  // 320
 
-__host__ __device__ constexpr int tc_threads(int fuse) { return fuse ? 448 : 320; }
-
-template <int BN, int STAGES, int FUSE = 0>
+template <int BN, int STAGES>
 struct TcLayout {
   static constexpr int kABytes = kTcBM * 128;
   static constexpr int kBBytes = BN * 128;
@@ -64,17 +55,9 @@ struct TcLayout {
   // epilogue staging: one 32-row x 128-byte tile per epilogue warp
   static constexpr int kEpiOffset = kRingBytes;
   static constexpr int kEpiBytes = kTcEpiWarps * 32 * 128;
-  // int8 staging ring of the fused operand: rows x 64 bytes per stage; deeper
-  // than the fp16 ring so that HBM latency hides behind the cheap staging
-  static constexpr int kConvRows = FUSE == 1 ? BN : kTcBM;
-  static constexpr int kStgStages = FUSE ? 8 : 0;
-  static constexpr int kStgStageBytes = FUSE ? kConvRows * 64 : 0;
-  static constexpr int kStgOffset = kEpiOffset + kEpiBytes;
-  static constexpr int kStgBytes = kStgStageBytes * kStgStages;
-  // barriers: full[S], empty[S], acc_full[2], acc_empty[2], mma_done,
-  // then (fused only) conv[S], stg_full[SS], stg_empty[SS]
-  static constexpr int kNumBars = 2 * STAGES + 5 + (FUSE ? STAGES + 2 * kStgStages : 0);
-  static constexpr int kBarOffset = kStgOffset + kStgBytes;
+  // barriers: full[S], empty[S], acc_full[2], acc_empty[2], mma_done
+  static constexpr int kNumBars = 2 * STAGES + 5;
+  static constexpr int kBarOffset = kEpiOffset + kEpiBytes;
   static constexpr int kTmemSlotOffset = kBarOffset + 8 * kNumBars;
   static constexpr int kAbortOffset = kTmemSlotOffset + 4;
   static constexpr int kUsedBytes = kAbortOffset + 4;
@@ -173,11 +156,11 @@ __device__ __forceinline__ void s8x16_to_f16(const int4 in, uint4& lo, uint4& hi
   hi = make_uint4(o[4], o[5], o[6], o[7]);
 }
 
-template <int BN, int STAGES, bool F8, bool LINEAR, int FUSE>
-__global__ void __launch_bounds__(tc_threads(FUSE), 1)
+template <int BN, int STAGES, bool F8, bool LINEAR>
+__global__ void __launch_bounds__(kTcThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const TcParams p) {
-  using L = TcLayout<BN, STAGES, FUSE>;
+  using L = TcLayout<BN, STAGES>;
   constexpr int kBkElems = F8 ? 128 : 64;  // elements per 128-byte K slice
   constexpr uint32_t kIdesc = instr_desc(kTcBM, BN);
   constexpr int kGroups = BN / 2 / 32;     // 32-column groups per epilogue thread
@@ -192,10 +175,6 @@ __global__ void __launch_bounds__(tc_threads(FUSE), 1)
   auto accf_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
   auto acce_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
   const uint32_t done_bar = bar0 + 8u * (2 * STAGES + 4);
-  constexpr int SS = L::kStgStages;
-  auto conv_bar = [&](int s) { return bar0 + 8u * (2 * STAGES + 5 + s); };
-  auto stgf_bar = [&](int s) { return bar0 + 8u * (3 * STAGES + 5 + s); };
-  auto stge_bar = [&](int s) { return bar0 + 8u * (3 * STAGES + 5 + SS + s); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kTmemSlotOffset);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kAbortOffset);
 
@@ -212,13 +191,6 @@ __global__ void __launch_bounds__(tc_threads(FUSE), 1)
       mbar_init(acce_bar(b), kTcEpiWarps);
     }
     mbar_init(done_bar, 1);
-    if (FUSE) {
-      for (int s = 0; s < STAGES; ++s) mbar_init(conv_bar(s), kTcConvWarps);
-      for (int s = 0; s < SS; ++s) {
-        mbar_init(stgf_bar(s), 1);
-        mbar_init(stge_bar(s), kTcConvWarps);
-      }
-    }
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -249,31 +221,16 @@ __global__ void __launch_bounds__(tc_threads(FUSE), 1)
         unit_range(w, p, t, kbb, kbe);
         tile_coords(t, p, tm, tn);
         for (int kb = kbb; kb < kbe; ++kb) {
-          if (FUSE == 0) {
-            if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.status)) {
-              ok = false;
-              break;
-            }
-            const uint32_t sa = sbase + stage * L::kStageBytes;
-            mbar_arrive_expect_tx(full_bar(stage), L::kStageBytes);
-            tma_load_2d(sa, &tmA, full_bar(stage), kb * kBkElems, tm * kTcBM);
-            tma_load_2d(sa + L::kABytes, &tmB, full_bar(stage), kb * kBkElems, tn * BN);
-          } else {
-            // fused: only the int8 operand's 64-byte K slices, into the deep
-            // staging ring (the converters fetch the other operand)
-            if (!mbar_wait(stge_bar(stage), phase ^ 1u, abort_flag, p.status)) {
-              ok = false;
-              break;
-            }
-            const uint32_t st = sbase + L::kStgOffset + stage * L::kStgStageBytes;
-            mbar_arrive_expect_tx(stgf_bar(stage), L::kStgStageBytes);
-            if (FUSE == 1)
-              tma_load_2d(st, &tmB, stgf_bar(stage), kb * 64, tn * BN);
-            else
-              tma_load_2d(st, &tmA, stgf_bar(stage), kb * 64, tm * kTcBM);
+          if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.status)) {
+            ok = false;
+            break;
           }
+          const uint32_t sa = sbase + stage * L::kStageBytes;
+          mbar_arrive_expect_tx(full_bar(stage), L::kStageBytes);
+          tma_load_2d(sa, &tmA, full_bar(stage), kb * kBkElems, tm * kTcBM);
+          tma_load_2d(sa + L::kABytes, &tmB, full_bar(stage), kb * kBkElems, tn * BN);
           ++issued;
-          if (++stage == (FUSE ? SS : STAGES)) {
+          if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
           }
@@ -281,16 +238,15 @@ __global__ void __launch_bounds__(tc_threads(FUSE), 1)
       }
       if (!ok) {
         // Wind-down: wait for this CTA's own copies still in flight.
-        constexpr int R = FUSE ? SS : STAGES;
-        int64_t back = issued < R ? issued : R;
+        int64_t back = issued < STAGES ? issued : STAGES;
         int s = stage;
         uint32_t ph = phase;
         for (int64_t i = 0; i < back; ++i) {
           if (--s < 0) {
-            s = R - 1;
+            s = STAGES - 1;
             ph ^= 1u;
           }
-          mbar_wait_drain(FUSE ? stgf_bar(s) : full_bar(s), ph);
+          mbar_wait_drain(full_bar(s), ph);
         }
       }
     }
@@ -316,8 +272,7 @@ __global__ void __launch_bounds__(tc_threads(FUSE), 1)
           const int kb0 = kbb + c * p.chunk_kb;
           const int kb1 = min(kb0 + p.chunk_kb, kbe);
           for (int kb = kb0; kb < kb1; ++kb) {
-            if (!mbar_wait(full_bar(stage), phase, abort_flag, p.status) ||
-                (FUSE && !mbar_wait(conv_bar(stage), phase, abort_flag, p.status))) {
+            if (!mbar_wait(full_bar(stage), phase, abort_flag, p.status)) {
               ok = false;
               break;
             }
@@ -344,90 +299,6 @@ __global__ void __launch_bounds__(tc_threads(FUSE), 1)
         }
       }
       mma_commit(done_bar);  // arrives once every MMA issued above has completed
-    }
-  } else if (FUSE && warp >= 2 + kTcEpiWarps) {
-    // ---------------- converters (fused variant) ----------------
-    const int ct = threadIdx.x - 32 * (2 + kTcEpiWarps);  // 0..127
-    constexpr int kChunks = L::kConvRows * 4;             // 16-byte int8 chunks per stage
-    const uint32_t dst_off = FUSE == 1 ? L::kABytes : 0;
-    const bool loader = threadIdx.x == 32 * (2 + kTcEpiWarps);  // issues the other operand's TMA
-    int os = 0, ss = 0;
-    uint32_t oph = 0, sph = 0;
-    int64_t issued = 0;
-    bool ok = true;
-    for (int w = blockIdx.x; ok && w < p.num_units; w += gridDim.x) {
-      int t, kbb, kbe, tm, tn;
-      unit_range(w, p, t, kbb, kbe);
-      tile_coords(t, p, tm, tn);
-      for (int kb = kbb; kb < kbe; ++kb) {
-        int got = 1;
-        if (lane == 0) {
-          got = mbar_wait(empty_bar(os), oph ^ 1u, abort_flag, p.status);
-          if (got && loader) {
-            const uint32_t sa = sbase + os * L::kStageBytes;
-            if (FUSE == 1) {
-              mbar_arrive_expect_tx(full_bar(os), L::kABytes);
-              tma_load_2d(sa, &tmA, full_bar(os), kb * kBkElems, tm * kTcBM);
-            } else {
-              mbar_arrive_expect_tx(full_bar(os), L::kBBytes);
-              tma_load_2d(sa + L::kABytes, &tmB, full_bar(os), kb * kBkElems, tn * BN);
-            }
-            ++issued;
-          }
-          got = got && mbar_wait(stgf_bar(ss), sph, abort_flag, p.status);
-        }
-        got = __shfl_sync(0xffffffffu, got, 0);
-        if (!got) {
-          ok = false;
-          break;
-        }
-        const uint8_t* stg = smem + L::kStgOffset + ss * L::kStgStageBytes;
-        const uint32_t dst = sbase + os * L::kStageBytes + dst_off;
-#pragma unroll
-        for (int c = ct; c < kChunks; c += 32 * kTcConvWarps) {
-          const int row = c >> 2, q = c & 3;
-          const int4 v = *reinterpret_cast<const int4*>(stg + row * 64 + q * 16);
-          uint4 lo, hi;
-          s8x16_to_f16(v, lo, hi);
-          const uint32_t rbase = dst + row * 128;
-          const int sw = row & 7;
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
-                           rbase + (((2 * q) ^ sw) << 4)),
-                       "r"(lo.x), "r"(lo.y), "r"(lo.z), "r"(lo.w)
-                       : "memory");
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
-                           rbase + (((2 * q + 1) ^ sw) << 4)),
-                       "r"(hi.x), "r"(hi.y), "r"(hi.z), "r"(hi.w)
-                       : "memory");
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(conv_bar(os));
-          mbar_arrive(stge_bar(ss));
-        }
-        if (++os == STAGES) {
-          os = 0;
-          oph ^= 1u;
-        }
-        if (++ss == SS) {
-          ss = 0;
-          sph ^= 1u;
-        }
-      }
-    }
-    if (!ok && loader) {
-      // Wind-down: wait for the operand copies this thread still has in flight.
-      int64_t back = issued < STAGES ? issued : STAGES;
-      int s2 = os;
-      uint32_t ph = oph;
-      for (int64_t i = 0; i < back; ++i) {
-        if (--s2 < 0) {
-          s2 = STAGES - 1;
-          ph ^= 1u;
-        }
-        mbar_wait_drain(full_bar(s2), ph);
-      }
     }
   } else {
     // ---------------- epilogue ----------------
@@ -517,14 +388,14 @@ __global__ void __launch_bounds__(tc_threads(FUSE), 1)
   }
 }
 
-template <int BN, int STAGES, bool F8, bool LINEAR, int FUSE>
+template <int BN, int STAGES, bool F8, bool LINEAR>
 cudaError_t tc_launch(const CUtensorMap* a, const CUtensorMap* b, const CUtensorMap* c,
                       const TcParams* p, int grid, bool pdl, cudaStream_t stream) {
-  using L = TcLayout<BN, STAGES, FUSE>;
+  using L = TcLayout<BN, STAGES>;
   // The dynamic shared memory limit was raised once per device by the caller.
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(tc_threads(FUSE));
+  cfg.blockDim = dim3(kTcThreads);
   cfg.dynamicSmemBytes = tc_smem_request(L::kDynSmem, L::kTmemCols);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -532,16 +403,16 @@ cudaError_t tc_launch(const CUtensorMap* a, const CUtensorMap* b, const CUtensor
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<BN, STAGES, F8, LINEAR, FUSE>, *a, *b, *c, *p);
+  return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<BN, STAGES, F8, LINEAR>, *a, *b, *c, *p);
 }
 
-template <int BN, int STAGES, bool F8, bool LINEAR, int FUSE = 0>
+template <int BN, int STAGES, bool F8, bool LINEAR>
 TcKernel tc_kernel_entry() {
-  using L = TcLayout<BN, STAGES, FUSE>;
+  using L = TcLayout<BN, STAGES>;
   TcKernel k;
-  k.launch = &tc_launch<BN, STAGES, F8, LINEAR, FUSE>;
-  k.func = reinterpret_cast<const void*>(&tc_gemm_kernel<BN, STAGES, F8, LINEAR, FUSE>);
-  k.threads = tc_threads(FUSE);
+  k.launch = &tc_launch<BN, STAGES, F8, LINEAR>;
+  k.func = reinterpret_cast<const void*>(&tc_gemm_kernel<BN, STAGES, F8, LINEAR>);
+  k.threads = kTcThreads;
   k.smem = tc_smem_request(L::kDynSmem, L::kTmemCols);
   k.tmem_cols = L::kTmemCols;
   k.tile_n = BN;

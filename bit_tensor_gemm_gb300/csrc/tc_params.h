@@ -56,8 +56,9 @@ inline constexpr int tc_smem_request(int used, int tmem_cols) {
 TcKernel tc_kernel_small(int stages, bool f8, bool linear);
 TcKernel tc_kernel_medium(int stages, bool f8, bool linear);
 TcKernel tc_kernel_pair(int stages, bool f8, bool linear);
-// Fused variants (8-bit only, 3 fp16 stages, 8 int8 staging stages): fuse 1 converts B in the kernel,
-// fuse 2 converts A; tile_n 64 or 128.
-TcKernel tc_kernel_fused(int fuse, int tile_n, bool linear);
+// One operand converted from int8 in the kernel and fed to the MMA from tensor
+// memory (8-bit only, 6 stages): trans = false converts A, trans = true
+// converts B (C is written transposed from the accumulator); tile_n 64, 128 or 256.
+TcKernel tc_kernel_ts(int tile_n, bool trans, bool linear);
 
 }  // namespace lbg

@@ -9,8 +9,9 @@ against a reference here; the tests do that.
         [--variant 7] [--encoded] [--linear] [--reps 2]
 
 --variant forces a tile x stage variant of the tensor-core kernel
-(lbgemm_run_variant); without it the library's own dispatch runs
-(lbgemm_run).  --encoded re-encodes A and B once and times only the GEMM
+(lbgemm_run_variant); --fused forces the kernel that converts the larger
+operand itself (lbgemm_run_fused); without either the library's own
+dispatch runs (lbgemm_run).  --encoded re-encodes A and B once and times only the GEMM
 kernel (lbgemm_run_encoded).  --linear runs lbgemm_linear (bits 8).
 """
 from __future__ import annotations
@@ -27,6 +28,8 @@ def main(argv=None) -> int:
     ap.add_argument("-K", type=int, required=True)
     ap.add_argument("--variant", type=int, default=-1)
     ap.add_argument("--encoded", action="store_true")
+    ap.add_argument("--fused", type=int, default=0, metavar="TILE_N",
+                    help="run lbgemm_run_fused with this tile width (64, 128 or 256)")
     ap.add_argument("--linear", action="store_true")
     ap.add_argument("--reps", type=int, default=2)
     ap.add_argument("--seed", type=int, default=1)
@@ -65,6 +68,9 @@ def main(argv=None) -> int:
 
             def call():
                 L.lbgemm_run_encoded(a.bits, M, N, K, eA, eB, C, a.variant)
+        elif a.fused:
+            def call():
+                L.lbgemm_run_fused(M, N, K, dA, dB, C, a.fused)
         elif a.variant >= 0:
             def call():
                 L.lbgemm_run_variant(a.bits, M, N, K, dA, dB, C, a.variant)

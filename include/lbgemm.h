@@ -100,6 +100,19 @@ lbgemm_status lbgemm_run(int bits, int64_t M, int64_t N, int64_t K, const void* 
 lbgemm_status lbgemm_run_variant(int bits, int64_t M, int64_t N, int64_t K, const void* A,
                                  const void* B, int32_t* C, int variant, void* stream);
 
+/* 8-bit C = A . B^T forced onto the kernel that converts one operand from
+ * int8 itself and feeds it to the tensor cores from tensor memory; only the
+ * other operand is re-encoded ahead (scratch: its fp16 copy, from the same
+ * per-device buffer as lbgemm_run).  The larger operand is the converted one
+ * (B when N >= M; C is then produced transposed from the accumulator).
+ * tile_n (64, 128 or 256) is the tile width along the re-encoded operand.
+ * Requires K % 16 == 0 and 16-byte-aligned A and B (LBGEMM_ERR_ALIGNMENT
+ * otherwise).  lbgemm_run takes this route by itself for the shapes where it
+ * is measured faster; this entry exists for tests and timing.  [LBG]
+ * section 1 (tiled GEMM with a multi-stage pipeline). */
+lbgemm_status lbgemm_run_fused(int64_t M, int64_t N, int64_t K, const int8_t* A, const int8_t* B,
+                               int32_t* C, int tile_n, void* stream);
+
 /* Bytes of scratch that lbgemm_run_ws needs for this problem on the
  * tensor-core route (0 for bad arguments): the re-encoded A and B. */
 size_t lbgemm_workspace_size(int bits, int64_t M, int64_t N, int64_t K);

@@ -27,6 +27,16 @@ def gemm(bits, A, B, K, variant=-1, stream=None):
     return dC.cpu().numpy()
 
 
+def fused(A, B, K, tile_n):
+    """lbgemm_run_fused: the larger operand converted from int8 in the kernel."""
+    M, N = A.shape[0], B.shape[0]
+    dA, dB = to_dev(A), to_dev(B)
+    dC = torch.full((M, N), -7, dtype=torch.int32, device=DEV)
+    L.lbgemm_run_fused(M, N, K, dA, dB, dC, tile_n)
+    L.lbgemm_device_status()
+    return dC.cpu().numpy()
+
+
 def linear(X, sx, W, sw, variant=-1):
     M, K = X.shape
     N = W.shape[0]

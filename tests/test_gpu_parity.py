@@ -76,13 +76,67 @@ def test_int8_small_dp4a_path():
     assert np.all(G().gemm(8, A, A, 512) == 16384 * 512)
 
 
-@pytest.mark.parametrize("M,N,K", [(64, 4096, 2048), (200, 2500, 1040), (4096, 100, 1024),
-                                   (3000, 256, 2064), (17, 2048, 4096)])
+@pytest.mark.parametrize("M,N,K", [(64, 4096, 2048), (200, 2500, 2064), (4096, 100, 4096),
+                                   (3000, 256, 2064), (17, 2048, 4096), (500, 1100, 2048),
+                                   (1030, 512, 3008)])
 def test_int8_fused_conversion_path(M, N, K):
-    """Skinny problems (one side <= 256, the other >= 2048, K >= 1024): the
-    kernel converts the large int8 operand itself; ragged tiles included."""
+    """Default dispatch of problems with one side <= 512, the other >= 1024 and
+    K >= 2048: the kernel converts the large int8 operand itself (B when
+    N >= M, giving C transposed from the accumulator); ragged tiles and K
+    tails included."""
     A, B = synth.operands(8, M, N, K, 7 * M + N + K)
     assert_exact(G().gemm(8, A, B, K), oracle.gemm(8, A, B, K), f"int8 fused {M}x{N}x{K}")
+
+
+# (M, N, K): both orientations, ragged rows and columns, K that ends inside a
+# 64-element slice, odd slice counts, a last group of 1-3 slices, chunk
+# boundaries (1024), few tiles (split K), one tile
+FUSED_SHAPES = [(300, 520, 1040), (520, 300, 1040), (129, 4100, 2048), (4100, 129, 2112),
+                (130, 70, 48), (16, 300, 4160), (257, 513, 1024), (700, 900, 4096),
+                (100, 1100, 16384), (1, 1, 16), (256, 256, 3008)]
+
+
+@pytest.mark.parametrize("tile_n", [64, 128, 256])
+def test_int8_fused_every_tile(tile_n):
+    """lbgemm_run_fused with each tile width (64 and 128: double-buffered
+    accumulators; 256: one accumulator, K in groups of 4 slices)."""
+    for i, (M, N, K) in enumerate(FUSED_SHAPES):
+        A, B = synth.operands(8, M, N, K, 900 + 17 * i + tile_n)
+        assert_exact(G().fused(A, B, K, tile_n), oracle.gemm(8, A, B, K),
+                     f"fused tile {tile_n} {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("tile_n", [64, 128, 256])
+def test_int8_fused_extremes(tile_n):
+    """Every value -128 (chunk sums exactly 2^24) and the adversarial order
+    of large then +-1 products, on the in-kernel conversion."""
+    K = 4096
+    A = np.full((200, K), -128, np.int8)
+    B = np.full((300, K), -128, np.int8)
+    assert np.all(G().fused(A, B, K, tile_n) == 16384 * K)
+    A = np.ones((128, K), np.int8)
+    B = np.ones((64, K), np.int8)
+    A[:, :511] = -128
+    B[:, :511] = -128
+    A[:, 1024:2047] = -128
+    B[:, 1024:2047] = -128
+    B[1::2, 600:1000] = -1
+    assert_exact(G().fused(A, B, K, tile_n), oracle.gemm(8, A, B, K), "fused adversarial")
+    assert_exact(G().fused(B, A, K, tile_n), oracle.gemm(8, B, A, K), "fused adversarial (T)")
+
+
+def test_int8_fused_short_chunks():
+    """A shorter exact chunk (512 elements) changes where the accumulator is
+    read out; the result must not change."""
+    M, N, K = 200, 1500, 5120
+    A, B = synth.operands(8, M, N, K, 31)
+    want = oracle.gemm(8, A, B, K)
+    try:
+        L.lbgemm_set_exact_chunk(8, 512)
+        for tile_n in (64, 256):
+            assert_exact(G().fused(A, B, K, tile_n), want, f"fused chunk 512 tile {tile_n}")
+    finally:
+        L.lbgemm_set_exact_chunk(8, 1024)
 
 
 def test_int8_full_range_and_extremes():
@@ -226,6 +280,18 @@ def test_linear_small(M):
     ref = oracle.linear(X, sx, W, sw)
     acc = oracle.gemm(8, X, W, K)
     check_linear(G().linear(X, sx, W, sw), ref, acc == 0, f"linear M={M}")
+
+
+@pytest.mark.parametrize("M", [17, 128, 300])
+def test_linear_fused_route(M):
+    """Token counts 17..512 with N >= 1024 and K >= 2048: the weights are
+    converted in the kernel and Y is written transposed from the accumulator."""
+    N, K = 2100, 4096
+    X, sx, W, sw = synth.linear_operands(M, N, K, 600 + M)
+    X[1, :] = 0
+    ref = oracle.linear(X, sx, W, sw)
+    acc = oracle.gemm(8, X, W, K)
+    check_linear(G().linear(X, sx, W, sw), ref, acc == 0, f"linear fused M={M}")
 
 
 @pytest.mark.parametrize("variant", [0, 4, 8])
