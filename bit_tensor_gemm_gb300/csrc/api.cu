@@ -43,7 +43,9 @@ using lbg::TcParams;
 constexpr int kNumVariants = 9;
 constexpr int kDefaultVariant = 7;  // large tile, middle stage level (5 stages)
 constexpr int kMaxDevices = 64;
-constexpr int kSkinnyMaxM = 16;
+// M <= 4 runs on the dp4a kernel that streams B once (measured on GB300: at
+// one to four rows it beats the warp-MMA kernel, which pays for 16-row MMAs)
+constexpr int kSkinnyMaxM = 4;
 constexpr int kGroupM = 16;
 // 1-bit problems below this many bit-MACs go to the popcount kernel: there
 // the expansion pass and the second launch cost more than they save.
@@ -55,6 +57,8 @@ constexpr int64_t kSmallMaxK = 512;
 constexpr int64_t kFusedMaxSide = 512;
 constexpr int64_t kFusedMinOther = 1024;
 constexpr int64_t kFusedMinK = 2048;
+// Small side of the warp-level fp16 MMA kernel (hmma_skinny.cu).
+constexpr int64_t kWarpMmaMaxSide = 32;
 constexpr double kSmallMaxWork = 268435456.0;  // M-tiles per group of the tile order (L2 reuse)
 constexpr size_t kFlushBytes = size_t(256) << 20;  // twice the 129 MB L2
 
@@ -525,6 +529,31 @@ lbgemm_status run_tc_fused(DeviceState& d, bool large_b, int tile_n, int64_t M, 
   return LBGEMM_OK;
 }
 
+// The warp-level fp16 MMA kernel for a small side (<= kWarpMmaMaxSide rows):
+// X is the small operand, W the large one; C (or Y) is written transposed
+// from the kernel's point of view when the small side is B.
+lbgemm_status run_warpmma(DeviceState& d, int64_t M, int64_t N, int64_t K, const int8_t* A,
+                          const int8_t* B, int32_t* C, const float* sx, const float* sw, void* Y,
+                          cudaStream_t stream) {
+  const bool small_a = M <= N;
+  cudaError_t e =
+      small_a ? lbg::launch_hmma_skinny(A, B, (int)M, (int)N, (int)K, false, C, sx, sw, Y,
+                                        g_chunk_s8.load(), d.sm_count, stream)
+              : lbg::launch_hmma_skinny(B, A, (int)N, (int)M, (int)K, true, C, sw, sx, Y,
+                                        g_chunk_s8.load(), d.sm_count, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "warp-MMA GEMM launch");
+  g_launches += 1;
+  return LBGEMM_OK;
+}
+
+// The warp-MMA kernel takes the problem: small side <= kWarpMmaMaxSide rows,
+// X fits its shared memory, K % 16 == 0, aligned operands.
+bool warpmma_ok(int64_t M, int64_t N, int64_t K, const void* A, const void* B) {
+  const int64_t lo = std::min(M, N);
+  return lo <= kWarpMmaMaxSide && K % 16 == 0 && K <= lbg::hmma_skinny_max_k((int)lo) &&
+         aligned16(A) && aligned16(B);
+}
+
 // Route of the in-kernel-conversion kernel for an 8-bit problem (1: B is
 // converted in the kernel, 2: A is; 0: re-encode both) and its tile width
 // along the re-encoded operand.  Measured on GB300 over the 729-shape grid:
@@ -570,6 +599,9 @@ lbgemm_status run_any(int bits, int64_t M, int64_t N, int64_t K, const void* A, 
     g_launches += 1;
     return LBGEMM_OK;
   }
+  if (bits == 8 && auto_pick && warpmma_ok(M, N, K, A, B))
+    return run_warpmma(*d, M, N, K, static_cast<const int8_t*>(A), static_cast<const int8_t*>(B),
+                       C, nullptr, nullptr, nullptr, stream);
   if (bits == 8 && auto_pick && small_ok(M, N, K, A, B)) {
     e = lbg::launch_small_s8(static_cast<const int8_t*>(A), static_cast<const int8_t*>(B), M, N, K,
                              C, stream);
@@ -632,6 +664,8 @@ lbgemm_status run_linear(int64_t M, int64_t N, int64_t K, const int8_t* X, const
     g_launches += 1;
     return LBGEMM_OK;
   }
+  if (auto_pick && warpmma_ok(M, N, K, X, W))
+    return run_warpmma(*d, M, N, K, X, W, nullptr, sx, sw, Y, stream);
   int fuse_tile = 0;
   if (auto_pick && fused_route(M, N, K, X, W, &fuse_tile) == 1) {
     // small token counts: only X is re-encoded; the kernel converts W itself
@@ -713,6 +747,28 @@ lbgemm_status lbgemm_run_fused(int64_t M, int64_t N, int64_t K, const int8_t* A,
                       as_stream(stream));
     lbgemm_status st2 = scratch_release(d->ws, as_stream(stream));
     return st != LBGEMM_OK ? st : st2;
+  } catch (...) {
+    return fail(LBGEMM_ERR_CUDA, "internal error");
+  }
+}
+
+lbgemm_status lbgemm_run_warpmma(int64_t M, int64_t N, int64_t K, const int8_t* A,
+                                 const int8_t* B, int32_t* C, void* stream) {
+  try {
+    lbgemm_status st = check_gemm_args(8, M, N, K, A, B, C);
+    if (st != LBGEMM_OK) return st;
+    if (std::min(M, N) > kWarpMmaMaxSide)
+      return fail(LBGEMM_ERR_INVALID_ARG, "the warp-MMA kernel needs min(M, N) <= %d",
+                  (int)kWarpMmaMaxSide);
+    if (K % 16) return fail(LBGEMM_ERR_ALIGNMENT, "the warp-MMA kernel needs K %% 16 == 0");
+    if (M == 0 || N == 0) return LBGEMM_OK;
+    if (K > lbg::hmma_skinny_max_k((int)std::min(M, N)))
+      return fail(LBGEMM_ERR_INVALID_ARG, "the warp-MMA kernel takes K <= %lld here",
+                  (long long)lbg::hmma_skinny_max_k((int)std::min(M, N)));
+    DeviceState* d = nullptr;
+    st = device_state(&d);
+    if (st != LBGEMM_OK) return st;
+    return run_warpmma(*d, M, N, K, A, B, C, nullptr, nullptr, nullptr, as_stream(stream));
   } catch (...) {
     return fail(LBGEMM_ERR_CUDA, "internal error");
   }

@@ -19,6 +19,14 @@ cudaError_t launch_skinny_s8(const int8_t* A, const int8_t* B, int M, int N, int
                              const float* sx, const float* sw, void* Y, int sm_count,
                              cudaStream_t s);
 // Per-row symmetric int8 quantisation of bf16 rows (Q: M x K int8, S: M fp32).
+// 8-bit GEMM with a small side X (MX <= 32 rows, K <= hmma_skinny_max_k(MX))
+// against W (NW rows) on the warp-level fp16 MMA; out[x][w] (or out[w][x]
+// when trans); K % 16 == 0 and 16-byte-aligned rows.  Linear layer when Y is
+// given.  hmma_skinny.cu.
+int64_t hmma_skinny_max_k(int MX);
+cudaError_t launch_hmma_skinny(const int8_t* X, const int8_t* W, int MX, int NW, int K,
+                               bool trans, int32_t* C, const float* sx, const float* sw, void* Y,
+                               int chunk_elems, int sm_count, cudaStream_t s);
 cudaError_t launch_quant_rows_bf16(const void* X, int64_t M, int64_t K, int8_t* Q, float* S,
                                    cudaStream_t s);
 // Small 8-bit GEMM on dp4a, one launch; K % 16 == 0, A and B 16-byte aligned.

@@ -10,7 +10,8 @@ against a reference here; the tests do that.
 
 --variant forces a tile x stage variant of the tensor-core kernel
 (lbgemm_run_variant); --fused forces the kernel that converts the larger
-operand itself (lbgemm_run_fused); without either the library's own
+operand itself (lbgemm_run_fused); --warpmma the warp-level fp16 MMA kernel
+for a small side (lbgemm_run_warpmma); without these the library's own
 dispatch runs (lbgemm_run).  --encoded re-encodes A and B once and times only the GEMM
 kernel (lbgemm_run_encoded).  --linear runs lbgemm_linear (bits 8).
 """
@@ -30,6 +31,8 @@ def main(argv=None) -> int:
     ap.add_argument("--encoded", action="store_true")
     ap.add_argument("--fused", type=int, default=0, metavar="TILE_N",
                     help="run lbgemm_run_fused with this tile width (64, 128 or 256)")
+    ap.add_argument("--warpmma", action="store_true",
+                    help="run lbgemm_run_warpmma (small side <= 32 rows)")
     ap.add_argument("--linear", action="store_true")
     ap.add_argument("--reps", type=int, default=2)
     ap.add_argument("--seed", type=int, default=1)
@@ -68,6 +71,9 @@ def main(argv=None) -> int:
 
             def call():
                 L.lbgemm_run_encoded(a.bits, M, N, K, eA, eB, C, a.variant)
+        elif a.warpmma:
+            def call():
+                L.lbgemm_run_warpmma(M, N, K, dA, dB, C)
         elif a.fused:
             def call():
                 L.lbgemm_run_fused(M, N, K, dA, dB, C, a.fused)

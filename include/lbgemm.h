@@ -81,13 +81,17 @@ lbgemm_status lbgemm_variant_info(int bits, int variant, int* tile_m, int* tile_
 /* C = A . B^T with the variant the selection table picks for
  * (bits, M, N, K, SM count).  [LBG] intro, sections 1-2.  Every bit width
  * runs on the tensor cores through an exact re-encoding of its operands
- * (int8 -> fp16, int4 -> e4m3, +-1 -> e4m3), except four shape rules:
- * 8-bit problems with M <= 16 run on a kernel that streams B once; 8-bit
- * problems with K <= 512 and M*N*K <= 2^28 on a one-launch dp4a kernel;
- * skinny 8-bit problems (min(M, N) <= 256, max(M, N) >= 2048, K >= 1024) on
- * a tensor-core kernel that converts the large operand itself, with only the
- * small one re-encoded ahead (these three need K % 16 == 0); and 1-bit
- * problems with M*N*K < 2^30 on the XOR-popcount kernel of lbgemm_run_popc.  Scratch memory for the re-encoding is
+ * (int8 -> fp16, int4 -> e4m3, +-1 -> e4m3), except these shape rules, in
+ * order (the 8-bit ones need K % 16 == 0 and 16-byte-aligned operands):
+ * 8-bit problems with M <= 4 run on a dp4a kernel that streams B once;
+ * 8-bit problems with min(M, N) <= 32 (and K within the limit of
+ * lbgemm_run_warpmma) on the warp-level fp16 MMA kernel, which streams the
+ * large operand once; 8-bit problems with K <= 512 and M*N*K <= 2^28 on a
+ * one-launch dp4a kernel; 8-bit problems with min(M, N) <= 512,
+ * max(M, N) >= 1024 and K >= 2048 on a tensor-core kernel that converts the
+ * large operand itself (lbgemm_run_fused), with only the small one
+ * re-encoded ahead; and 1-bit problems with M*N*K < 2^30 on the
+ * XOR-popcount kernel of lbgemm_run_popc.  Scratch memory for the re-encoding is
  * taken from a per-device buffer the library grows with cudaMalloc on demand;
  * calls from different streams are ordered on it with events.  A call that
  * grows the buffer synchronises the device, so make the first call of the
@@ -112,6 +116,19 @@ lbgemm_status lbgemm_run_variant(int bits, int64_t M, int64_t N, int64_t K, cons
  * section 1 (tiled GEMM with a multi-stage pipeline). */
 lbgemm_status lbgemm_run_fused(int64_t M, int64_t N, int64_t K, const int8_t* A, const int8_t* B,
                                int32_t* C, int tile_n, void* stream);
+
+/* 8-bit C = A . B^T forced onto the warp-level fp16 MMA kernel for problems
+ * with a small side: min(M, N) <= 32 rows, and K at most 4224 (small side
+ * <= 16) or 2048 (<= 32) so that the small operand fits the kernel's shared
+ * memory (LBGEMM_ERR_INVALID_ARG otherwise).
+ * Both operands stay int8 in memory and are converted to fp16 in registers;
+ * the large side is streamed from HBM once.  No scratch, one launch.
+ * Requires K % 16 == 0 and 16-byte-aligned A and B (LBGEMM_ERR_ALIGNMENT).
+ * lbgemm_run takes this route by itself for the shapes where it is measured
+ * faster; this entry exists for tests and timing.  [LBG] intro (8-bit GEMM),
+ * section 4 (linear layers with few tokens). */
+lbgemm_status lbgemm_run_warpmma(int64_t M, int64_t N, int64_t K, const int8_t* A,
+                                 const int8_t* B, int32_t* C, void* stream);
 
 /* Bytes of scratch that lbgemm_run_ws needs for this problem on the
  * tensor-core route (0 for bad arguments): the re-encoded A and B. */
@@ -179,9 +196,10 @@ lbgemm_status lbgemm_run_popc(int64_t M, int64_t N, int64_t K, const uint32_t* A
  * with acc = X . W^T exact in int32.  X: int8 M x K (per-token scale sx, fp32
  * [M]); W: int8 N x K (per-output-channel scale sw, fp32 [N]); Y: bf16 M x N
  * row-major, passed as void* (2 bytes per element).  The scale product is
- * formed in fp32, left to right.  K <= 131071.  M <= 16 runs on the kernel
- * that streams W once, 16 < M <= 256 (N >= 2048, K >= 1024) on the fused
- * conversion kernel, larger M on the tensor-core variant table. */
+ * formed in fp32, left to right.  K <= 131071.  The shape rules of
+ * lbgemm_run apply: M <= 4 on the dp4a kernel that streams W once, M <= 32
+ * on the warp-level fp16 MMA kernel, M <= 512 (N >= 1024, K >= 2048) on the
+ * kernel that converts W itself, larger M on the tensor-core variant table. */
 lbgemm_status lbgemm_linear(int64_t M, int64_t N, int64_t K, const int8_t* X, const float* sx,
                             const int8_t* W, const float* sw, void* Y, void* stream);
 

@@ -37,6 +37,16 @@ def fused(A, B, K, tile_n):
     return dC.cpu().numpy()
 
 
+def warpmma(A, B, K):
+    """lbgemm_run_warpmma: the warp-level fp16 MMA kernel (small side <= 32)."""
+    M, N = A.shape[0], B.shape[0]
+    dA, dB = to_dev(A), to_dev(B)
+    dC = torch.full((M, N), -7, dtype=torch.int32, device=DEV)
+    L.lbgemm_run_warpmma(M, N, K, dA, dB, dC)
+    L.lbgemm_device_status()
+    return dC.cpu().numpy()
+
+
 def linear(X, sx, W, sw, variant=-1):
     M, K = X.shape
     N = W.shape[0]

@@ -138,6 +138,23 @@ def test_argument_errors_need_no_device(lib, args, status):
     assert L.lbgemm_last_error()
 
 
+@pytest.mark.parametrize("M,N,K,tile,status", [
+    (64, 100, 64, 0, L.ERR_INVALID_ARG),     # warp-MMA: small side above 32
+    (16, 100, 4240, 0, L.ERR_INVALID_ARG),   # warp-MMA: K above its limit at 16 rows
+    (32, 100, 2064, 0, L.ERR_INVALID_ARG),   # warp-MMA: K above its limit at 32 rows
+    (16, 100, 40, 0, L.ERR_ALIGNMENT),       # warp-MMA: K % 16
+    (16, 100, 64, 96, L.ERR_INVALID_ARG),    # fused: tile width
+    (16, 100, 40, 128, L.ERR_ALIGNMENT),     # fused: K % 16
+])
+def test_forced_route_errors_need_no_device(lib, M, N, K, tile, status):
+    with pytest.raises(L.LbgemmError) as e:
+        if tile:
+            L.lbgemm_run_fused(M, N, K, 16, 16, 16, tile, 0)
+        else:
+            L.lbgemm_run_warpmma(M, N, K, 16, 16, 16, 0)
+    assert e.value.status == status
+
+
 def test_empty_problem_is_a_noop(lib):
     L.lbgemm_run(8, 0, 5, 16, 16, 16, 16, 0)
     L.lbgemm_run(1, 7, 0, 32, None, None, None, 0)

@@ -139,6 +139,53 @@ def test_int8_fused_short_chunks():
         L.lbgemm_set_exact_chunk(8, 1024)
 
 
+# (M, N, K): small side 1..32 on either operand, ragged W tiles (N % 16 != 0),
+# K of one 16-byte piece, K ending inside a 256-element step, the K limits
+WARPMMA_SHAPES = [(1, 1000, 4096), (5, 77, 16), (16, 300, 1040), (32, 4100, 2048),
+                  (20, 1000, 2048), (300, 16, 1040), (4100, 30, 2000), (32, 32, 128),
+                  (17, 11008, 576), (16, 9, 4224), (3, 5000, 4224), (30, 700, 2048),
+                  (7, 300, 4160), (9, 1000, 272), (1, 1, 16)]
+
+
+def test_int8_warpmma_forced():
+    """lbgemm_run_warpmma on every shape class it takes."""
+    for i, (M, N, K) in enumerate(WARPMMA_SHAPES):
+        A, B = synth.operands(8, M, N, K, 1300 + i)
+        assert_exact(G().warpmma(A, B, K), oracle.gemm(8, A, B, K), f"warp-MMA {M}x{N}x{K}")
+
+
+def test_int8_warpmma_extremes():
+    """Every value -128 (int32 sums at 16384 K), the adversarial order of
+    large then +-1 products, and a shorter exact chunk."""
+    for K in (1024, 4096):
+        A = np.full((16, K), -128, np.int8)
+        B = np.full((100, K), -128, np.int8)
+        assert np.all(G().warpmma(A, B, K) == 16384 * K)
+        assert np.all(G().warpmma(B[:20], A, K) == 16384 * K)
+    K = 4096
+    A = np.ones((16, K), np.int8)
+    B = np.ones((64, K), np.int8)
+    A[:, :511] = -128
+    B[:, :511] = -128
+    A[:, 1024:2047] = -128
+    B[:, 1024:2047] = -128
+    B[1::2, 600:1000] = -1
+    assert_exact(G().warpmma(A, B, K), oracle.gemm(8, A, B, K), "warp-MMA adversarial")
+    try:
+        L.lbgemm_set_exact_chunk(8, 512)
+        assert_exact(G().warpmma(A, B, K), oracle.gemm(8, A, B, K), "warp-MMA chunk 512")
+    finally:
+        L.lbgemm_set_exact_chunk(8, 1024)
+
+
+@pytest.mark.parametrize("M,N,K", [(8, 2000, 1024), (32, 700, 2048), (2000, 24, 512),
+                                   (3000, 5, 64)])
+def test_int8_warpmma_dispatch(M, N, K):
+    """Default dispatch of problems with a side of 5..32 rows."""
+    A, B = synth.operands(8, M, N, K, 11 * M + N)
+    assert_exact(G().gemm(8, A, B, K), oracle.gemm(8, A, B, K), f"int8 warp-MMA {M}x{N}x{K}")
+
+
 def test_int8_full_range_and_extremes():
     g = np.random.default_rng(5)
     M, N, K = 130, 70, 3000
@@ -282,7 +329,19 @@ def test_linear_small(M):
     check_linear(G().linear(X, sx, W, sw), ref, acc == 0, f"linear M={M}")
 
 
-@pytest.mark.parametrize("M", [17, 128, 300])
+@pytest.mark.parametrize("M", [5, 16, 32])
+def test_linear_warpmma_route(M):
+    """Token counts 5..32: the warp-level fp16 MMA kernel, Y scaled in its
+    final reduction."""
+    N, K = 2100, 4096 if M <= 16 else 2048
+    X, sx, W, sw = synth.linear_operands(M, N, K, 700 + M)
+    X[1, :] = 0
+    ref = oracle.linear(X, sx, W, sw)
+    acc = oracle.gemm(8, X, W, K)
+    check_linear(G().linear(X, sx, W, sw), ref, acc == 0, f"linear warp-MMA M={M}")
+
+
+@pytest.mark.parametrize("M", [33, 128, 300])
 def test_linear_fused_route(M):
     """Token counts 17..512 with N >= 1024 and K >= 2048: the weights are
     converted in the kernel and Y is written transposed from the accumulator."""
