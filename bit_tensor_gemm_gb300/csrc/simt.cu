@@ -70,6 +70,61 @@ __global__ void cvt_s8_f16_kernel(CvtJob ja, CvtJob jb, int64_t K, int64_t Kp) {
   }
 }
 
+// int8 -> fp16 for K % 16 == 0 and 16-byte-aligned rows (then Kp == K): each
+// thread converts two 16-byte chunks per iteration (both loads in flight),
+// four bytes at a time with integer and half2 arithmetic: the fp16 with bits
+// 0x6400 | u is 1024 + u, so (v ^ 0x80) as u, minus 1152, is v exactly.
+__device__ __forceinline__ void s8x4_f16x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  const uint32_t u = w ^ 0x80808080u;
+  const uint32_t a = __byte_perm(u, 0x64646464u, 0x5140);
+  const uint32_t b = __byte_perm(u, 0x64646464u, 0x7362);
+  const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));
+  const __half2 ha = __hsub2(*reinterpret_cast<const __half2*>(&a), bias);
+  const __half2 hb = __hsub2(*reinterpret_cast<const __half2*>(&b), bias);
+  lo = *reinterpret_cast<const uint32_t*>(&ha);
+  hi = *reinterpret_cast<const uint32_t*>(&hb);
+}
+
+template <bool SMALL>  // SMALL: chunk indices fit 32 bits
+__global__ void cvt_s8_f16_fast_kernel(CvtJob ja, CvtJob jb, int64_t K) {
+  allow_dependent_launch();
+  const int64_t cpr = K / 16;  // 16-byte chunks per row
+  const int64_t total_a = ja.rows * cpr;
+  const int64_t total = total_a + jb.rows * cpr;
+  const int64_t stride = 2 * (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i0 = 2 * ((int64_t)blockIdx.x * blockDim.x + threadIdx.x); i0 < total;
+       i0 += stride) {
+    int4 v[2];
+    uint4* dst[2];
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const int64_t i = i0 + q;
+      dst[q] = nullptr;
+      v[q] = make_int4(0, 0, 0, 0);
+      if (i < total) {
+        const bool in_a = i < total_a;
+        const int64_t ii = in_a ? i : i - total_a;
+        const CvtJob& j = in_a ? ja : jb;
+        const int64_t r = SMALL ? (int64_t)((uint32_t)ii / (uint32_t)cpr) : ii / cpr;
+        const int64_t c = ii - r * cpr;
+        v[q] = __ldg(reinterpret_cast<const int4*>(static_cast<const int8_t*>(j.src) + r * K) + c);
+        dst[q] = reinterpret_cast<uint4*>(static_cast<__half*>(j.dst) + r * K) + 2 * c;
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      if (dst[q] == nullptr) continue;
+      uint32_t o[8];
+      s8x4_f16x2((uint32_t)v[q].x, o[0], o[1]);
+      s8x4_f16x2((uint32_t)v[q].y, o[2], o[3]);
+      s8x4_f16x2((uint32_t)v[q].z, o[4], o[5]);
+      s8x4_f16x2((uint32_t)v[q].w, o[6], o[7]);
+      dst[q][0] = make_uint4(o[0], o[1], o[2], o[3]);
+      dst[q][1] = make_uint4(o[4], o[5], o[6], o[7]);
+    }
+  }
+}
+
 // packed int4 (two per byte, low nibble first) -> e4m3 bytes; K is even.
 // Each thread writes 16 output bytes from 8 input bytes through a 256-entry
 // table (byte -> two e4m3 codes) built per block with CUDA's fp8 conversion.
@@ -567,6 +622,18 @@ cudaError_t launch_encode_pair(int bits, const void* a, int64_t rows_a, void* en
   if (bits == 1) {  // K % 32 == 0 and Kp == K: rows are contiguous words
     const int64_t W = K / 32;
     cvt_b1_e4m3_kernel<<<grid_for((rows_a + rows_b) * W, 256, sm_count), 256, 0, s>>>(ja, jb, W);
+    return cudaGetLastError();
+  }
+  auto aligned16 = [&](const void* p) {
+    return p == nullptr || (reinterpret_cast<uintptr_t>(p) & 15) == 0;
+  };
+  if (bits == 8 && K % 16 == 0 && aligned16(a) && aligned16(b)) {
+    const int64_t chunks = (rows_a + rows_b) * (K / 16);
+    const int grid = grid_for((chunks + 1) / 2, 256, sm_count);
+    if (chunks < ((int64_t)1 << 32))
+      cvt_s8_f16_fast_kernel<true><<<grid, 256, 0, s>>>(ja, jb, K);
+    else
+      cvt_s8_f16_fast_kernel<false><<<grid, 256, 0, s>>>(ja, jb, K);
     return cudaGetLastError();
   }
   const int64_t vec = bits == 8 ? Kp / 8 : Kp / 16;
