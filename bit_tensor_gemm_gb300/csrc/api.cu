@@ -46,7 +46,7 @@ constexpr int kMaxDevices = 64;
 // M <= 4 runs on the dp4a kernel that streams B once (measured on GB300: at
 // one to four rows it beats the warp-MMA kernel, which pays for 16-row MMAs)
 constexpr int kSkinnyMaxM = 4;
-constexpr int kGroupM = 16;
+constexpr int kGroupM = 16;  // M-tiles per group of the tile order (L2 reuse)
 // 1-bit problems below this many bit-MACs go to the popcount kernel: there
 // the expansion pass and the second launch cost more than they save.
 constexpr double kPopcMaxWork = 1073741824.0;
@@ -59,7 +59,7 @@ constexpr int64_t kFusedMinOther = 1024;
 constexpr int64_t kFusedMinK = 2048;
 // Small side of the warp-level fp16 MMA kernel (hmma_skinny.cu).
 constexpr int64_t kWarpMmaMaxSide = 32;
-constexpr double kSmallMaxWork = 268435456.0;  // M-tiles per group of the tile order (L2 reuse)
+constexpr double kSmallMaxWork = 268435456.0;
 constexpr size_t kFlushBytes = size_t(256) << 20;  // twice the 129 MB L2
 
 thread_local std::string t_last_error;
@@ -67,6 +67,7 @@ std::atomic<int64_t> g_launches{0};
 std::atomic<int> g_chunk_s8{1024};
 std::atomic<int> g_chunk_s4{131072};
 std::atomic<int> g_chunk_b1{1 << 23};
+std::atomic<int> g_tail_split{1};  // 0 whole-problem splits only, 1 also a last partial wave, 2 forced
 
 lbgemm_status fail(lbgemm_status st, const char* fmt, ...) {
   char buf[512];
@@ -341,27 +342,91 @@ lbgemm_status encode_operands(DeviceState& d, int bits, const void* a, int64_t r
   return LBGEMM_OK;
 }
 
-// The GEMM kernel alone, on encoded operands.
-// K splits for a problem with few output tiles: when at most half of the
-// CTA slots would get a tile, each tile's K range is cut into pieces (at
-// least 4 K slices each) whose int32 partial sums are added into a zeroed C.
-// Only for int32 C stored by TMA (the linear layer scales the whole sum).
-int plan_splits(DeviceState& d, const TcKernel& k, int bits, int64_t M, int64_t N, int64_t K,
-                bool linear, bool vec_ok) {
-  if (linear || !vec_ok) return 1;
+// How the K dimension is shared out among CTAs.  Whole output tiles, one
+// per unit, fill the complete waves of the device's CTA slots.  The tiles of
+// a last, partial wave that would keep at most half of the slots busy are
+// cut along K into `splits` pieces (at least 4 K slices each), so that the
+// wave's pieces keep more slots busy and end sooner; so is the whole problem
+// when it has at most half a wave of tiles.  Pieces add their int32 partial
+// tiles into C, cleared beforehand: only for int32 C stored by TMA (the
+// linear layer scales the whole sum).
+struct KPlan {
+  int dp_tiles = 0;  // TcParams::dp_tiles
+  int splits = 1;    // TcParams::splits
+  bool adds() const { return splits > 1; }
+};
+
+KPlan plan_k(DeviceState& d, const TcKernel& k, int bits, int64_t M, int64_t N, int64_t K,
+             bool linear, bool vec_ok) {
+  KPlan kp;
+  if (linear || !vec_ok) return kp;
   const int bk = bits == 8 ? 64 : 128;
   const int64_t num_kb = (enc_kp(bits, K) + bk - 1) / bk;
   const int64_t tiles = ((M + k.tile_m - 1) / k.tile_m) * ((N + k.tile_n - 1) / k.tile_n);
   const int64_t slots = unit_slots(d, k);
-  if (tiles * 2 > slots) return 1;
-  const int64_t splits = std::min<int64_t>(std::min<int64_t>(slots / tiles, num_kb / 4), 64);
-  return (int)std::max<int64_t>(splits, 1);
+  const int mode = g_tail_split.load();
+  int64_t full = tiles / slots, rem = tiles - full * slots;
+  if (full > 0 && mode == 0) return kp;
+  if (mode == 2 && rem == 0) {  // forced: the last full wave is the tail
+    --full;
+    rem = slots;
+  }
+  if (rem == 0) return kp;
+  const int64_t fit = slots / rem;  // pieces per tail tile that still fit the wave
+  int64_t splits = std::min<int64_t>(std::min<int64_t>(fit, num_kb / 4), 64);
+  if (mode == 2) splits = std::max<int64_t>(splits, std::min<int64_t>(num_kb, 2));
+  if (splits < 2) return kp;
+  kp.dp_tiles = (int)(full * slots);
+  kp.splits = (int)splits;
+  return kp;
+}
+
+// The rectangle of C that holds the split tiles (those from dp_tiles on, in
+// the kernels' tile order), as rows [r0, r1) and columns [c0, c1), clipped to
+// M x N.
+void split_tiles_box(const TcKernel& k, int64_t M, int64_t N, int dp_tiles, int64_t* r0,
+                     int64_t* r1, int64_t* c0, int64_t* c1) {
+  const int64_t tiles_m = (M + k.tile_m - 1) / k.tile_m, tiles_n = (N + k.tile_n - 1) / k.tile_n;
+  const int64_t tiles = tiles_m * tiles_n;
+  int64_t tm_lo = tiles_m, tm_hi = -1, tn_lo = tiles_n, tn_hi = -1;
+  for (int64_t t = dp_tiles; t < tiles; ++t) {
+    // the tile order of the kernels: groups of kGroupM tile rows, column-major inside
+    const int64_t per_group = (int64_t)kGroupM * tiles_n;
+    const int64_t g = t / per_group, first = g * kGroupM;
+    const int64_t gs = std::min<int64_t>(tiles_m - first, kGroupM);
+    const int64_t r = t - g * per_group;
+    const int64_t tm = first + r % gs, tn = r / gs;
+    tm_lo = std::min(tm_lo, tm);
+    tm_hi = std::max(tm_hi, tm);
+    tn_lo = std::min(tn_lo, tn);
+    tn_hi = std::max(tn_hi, tn);
+  }
+  *r0 = tm_lo * k.tile_m;
+  *r1 = std::min<int64_t>((tm_hi + 1) * k.tile_m, M);
+  *c0 = tn_lo * k.tile_n;
+  *c1 = std::min<int64_t>((tn_hi + 1) * k.tile_n, N);
+}
+
+// Clears the part of C that split tiles add into.
+lbgemm_status clear_split_tiles(const TcKernel& k, const KPlan& kp, int64_t M, int64_t N,
+                                int32_t* C, cudaStream_t stream) {
+  if (!kp.adds()) return LBGEMM_OK;
+  cudaError_t e;
+  if (kp.dp_tiles == 0) {
+    e = cudaMemsetAsync(C, 0, (size_t)(M * N) * sizeof(int32_t), stream);
+  } else {
+    int64_t r0, r1, c0, c1;
+    split_tiles_box(k, M, N, kp.dp_tiles, &r0, &r1, &c0, &c1);
+    e = cudaMemset2DAsync(C + r0 * N + c0, (size_t)N * sizeof(int32_t), 0,
+                          (size_t)(c1 - c0) * sizeof(int32_t), (size_t)(r1 - r0), stream);
+  }
+  return e == cudaSuccess ? LBGEMM_OK : cuda_fail(e, "clearing C for split tiles");
 }
 
 lbgemm_status run_tc_encoded(DeviceState& d, int bits, int64_t M, int64_t N, int64_t K,
                              const void* encA, const void* encB, int32_t* C, const float* sx,
                              const float* sw, void* Y, int variant, bool after_encode,
-                             int splits, cudaStream_t stream) {
+                             const KPlan* planned, cudaStream_t stream) {
   const bool f8 = bits != 8;  // 4-bit and 1-bit operands are e4m3-encoded
   const bool linear = Y != nullptr;
   TcKernel k = tc_kernel(variant, f8, linear);
@@ -395,15 +460,17 @@ lbgemm_status run_tc_encoded(DeviceState& d, int bits, int64_t M, int64_t N, int
     p.vec_ok = (N % 8 == 0) && aligned16(Y);
   else
     p.vec_ok = (N % 4 == 0) && aligned16(C);
-  if (splits < 0) {  // not planned by the caller: plan here and clear C now
-    splits = plan_splits(d, k, bits, M, N, K, linear, p.vec_ok);
-    if (splits > 1) {
-      cudaError_t ez = cudaMemsetAsync(C, 0, (size_t)(M * N) * sizeof(int32_t), stream);
-      if (ez != cudaSuccess) return cuda_fail(ez, "cudaMemsetAsync (split K)");
-    }
+  KPlan plan;
+  if (planned) {
+    plan = *planned;
+  } else {  // not planned by the caller: plan here and clear C now
+    plan = plan_k(d, k, bits, M, N, K, linear, p.vec_ok);
+    st = clear_split_tiles(k, plan, M, N, C, stream);
+    if (st != LBGEMM_OK) return st;
   }
-  p.splits = splits;
-  p.num_units = p.num_tiles * splits;
+  p.dp_tiles = plan.dp_tiles;
+  p.splits = plan.splits;
+  p.num_units = plan.dp_tiles + (p.num_tiles - plan.dp_tiles) * plan.splits;
   CUtensorMap mc;
   std::memset(&mc, 0, sizeof mc);
   if (!linear && p.vec_ok) {
@@ -417,6 +484,8 @@ lbgemm_status run_tc_encoded(DeviceState& d, int bits, int64_t M, int64_t N, int
     if (r != CUDA_SUCCESS)
       return fail(LBGEMM_ERR_CUDA, "cuTensorMapEncodeTiled (C) failed (%d)", (int)r);
   }
+  // whole waves: dp_tiles is a multiple of the slots, so each CTA (pair) takes
+  // the same number of whole tiles before the pieces of the last wave
   const int grid =
       (int)std::min<int64_t>(p.num_units, (int64_t)unit_slots(d, k)) * k.cluster;
   // Right after our own re-encoding launch, the GEMM is a programmatic
@@ -436,19 +505,17 @@ lbgemm_status run_tc(DeviceState& d, int bits, int64_t M, int64_t N, int64_t K, 
   uint8_t* encB = encA + enc_bytes(bits, M, K);
   // Plan K splits first: C must be cleared before the encoder, so that the
   // GEMM can still be launched as the encoder's dependent.
-  int splits = 1;
+  KPlan plan;
   const bool linear = Y != nullptr;
   TcKernel k = tc_kernel(variant, bits != 8, linear);
   if (k.launch) {
-    splits = plan_splits(d, k, bits, M, N, K, linear, (N % 4 == 0) && aligned16(C));
-    if (splits > 1) {
-      cudaError_t ez = cudaMemsetAsync(C, 0, (size_t)(M * N) * sizeof(int32_t), stream);
-      if (ez != cudaSuccess) return cuda_fail(ez, "cudaMemsetAsync (split K)");
-    }
+    plan = plan_k(d, k, bits, M, N, K, linear, (N % 4 == 0) && aligned16(C));
+    lbgemm_status sc = clear_split_tiles(k, plan, M, N, C, stream);
+    if (sc != LBGEMM_OK) return sc;
   }
   lbgemm_status st = encode_operands(d, bits, A, M, encA, B, N, encB, K, stream);
   if (st != LBGEMM_OK) return st;
-  return run_tc_encoded(d, bits, M, N, K, encA, encB, C, sx, sw, Y, variant, true, splits, stream);
+  return run_tc_encoded(d, bits, M, N, K, encA, encB, C, sx, sw, Y, variant, true, &plan, stream);
 }
 
 // 8-bit problems with one operand converted in the kernel: only the other
@@ -470,7 +537,9 @@ lbgemm_status run_tc_fused(DeviceState& d, bool large_b, int tile_n, int64_t M, 
   // (transposed); both can add split-K partial tiles.
   const bool vec_ok = !large_b && (linear ? (N % 8 == 0) && aligned16(Y)
                                           : (N % 4 == 0) && aligned16(C));
-  const int splits = plan_splits(d, k, 8, rows_l, rows_s, K, linear, vec_ok || large_b);
+  // (the tiles of a partial last wave stay whole here: whole-problem splits only)
+  KPlan kpl = plan_k(d, k, 8, rows_l, rows_s, K, linear, vec_ok || large_b);
+  const int splits = kpl.dp_tiles == 0 ? kpl.splits : 1;
   if (splits > 1) {  // cleared before the encoder, so the GEMM can be its dependent
     cudaError_t ez = cudaMemsetAsync(C, 0, (size_t)(M * N) * sizeof(int32_t), stream);
     if (ez != cudaSuccess) return cuda_fail(ez, "cudaMemsetAsync (split K)");
@@ -896,7 +965,7 @@ lbgemm_status lbgemm_run_encoded(int bits, int64_t M, int64_t N, int64_t K, cons
     if (st != LBGEMM_OK) return st;
     if (variant < 0) variant = table_select(d->sm_count, bits, M, N, K);
     return run_tc_encoded(*d, bits, M, N, K, A_enc, B_enc, C, nullptr, nullptr, nullptr, variant,
-                          false, -1, as_stream(stream));
+                          false, nullptr, as_stream(stream));
   } catch (...) {
     return fail(LBGEMM_ERR_CUDA, "internal error");
   }
@@ -1120,6 +1189,14 @@ lbgemm_status lbgemm_set_exact_chunk(int bits, int k_elems) {
   }
   return fail(LBGEMM_ERR_INVALID_ARG, "bits must be 8, 4 or 1");
 }
+
+lbgemm_status lbgemm_set_tail_split(int mode) {
+  if (mode < 0 || mode > 2) return fail(LBGEMM_ERR_INVALID_ARG, "tail split mode must be 0, 1 or 2");
+  g_tail_split = mode;
+  return LBGEMM_OK;
+}
+
+int lbgemm_get_tail_split(void) { return g_tail_split.load(); }
 
 int lbgemm_get_exact_chunk(int bits) {
   return bits == 8 ? g_chunk_s8.load()

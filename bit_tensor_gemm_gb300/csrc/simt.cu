@@ -14,6 +14,7 @@
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdint>
 
 #include "ptx.cuh"
@@ -70,10 +71,12 @@ __global__ void cvt_s8_f16_kernel(CvtJob ja, CvtJob jb, int64_t K, int64_t Kp) {
   }
 }
 
-// int8 -> fp16 for K % 16 == 0 and 16-byte-aligned rows (then Kp == K): each
-// thread converts two 16-byte chunks per iteration (both loads in flight),
-// four bytes at a time with integer and half2 arithmetic: the fp16 with bits
-// 0x6400 | u is 1024 + u, so (v ^ 0x80) as u, minus 1152, is v exactly.
+// int8 -> fp16 for K % 16 == 0 and 16-byte-aligned rows.  Then Kp == K, so
+// both operands are flat arrays and the fp16 of input byte x sits at output
+// byte 2x: the kernel streams 8-byte units (a warp loads 256 contiguous bytes
+// and stores 512), four units in flight per thread, converting four bytes at
+// a time with integer and half2 arithmetic: the fp16 with bits 0x6400 | u is
+// 1024 + u, so (v ^ 0x80) as u, minus 1152, is v exactly.
 __device__ __forceinline__ void s8x4_f16x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
   const uint32_t u = w ^ 0x80808080u;
   const uint32_t a = __byte_perm(u, 0x64646464u, 0x5140);
@@ -85,43 +88,42 @@ __device__ __forceinline__ void s8x4_f16x2(uint32_t w, uint32_t& lo, uint32_t& h
   hi = *reinterpret_cast<const uint32_t*>(&hb);
 }
 
-template <bool SMALL>  // SMALL: chunk indices fit 32 bits
-__global__ void cvt_s8_f16_fast_kernel(CvtJob ja, CvtJob jb, int64_t K) {
+__device__ __forceinline__ uint4 s8x8_f16x8(int2 v) {
+  uint4 o;
+  s8x4_f16x2((uint32_t)v.x, o.x, o.y);
+  s8x4_f16x2((uint32_t)v.y, o.z, o.w);
+  return o;
+}
+
+// units: 8-byte groups; na of operand a, then nb of operand b
+__global__ void cvt_s8_f16_flat_kernel(const int2* __restrict__ a, int64_t na, uint4* ea,
+                                       const int2* __restrict__ b, int64_t nb, uint4* eb) {
   allow_dependent_launch();
-  const int64_t cpr = K / 16;  // 16-byte chunks per row
-  const int64_t total_a = ja.rows * cpr;
-  const int64_t total = total_a + jb.rows * cpr;
-  const int64_t stride = 2 * (int64_t)gridDim.x * blockDim.x;
-  for (int64_t i0 = 2 * ((int64_t)blockIdx.x * blockDim.x + threadIdx.x); i0 < total;
-       i0 += stride) {
-    int4 v[2];
-    uint4* dst[2];
+  const int64_t total = na + nb;
+  const int64_t nt = (int64_t)gridDim.x * blockDim.x;
+  int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  for (; i + 3 * nt < total; i += 4 * nt) {
+    int2 v[4];
 #pragma unroll
-    for (int q = 0; q < 2; ++q) {
-      const int64_t i = i0 + q;
-      dst[q] = nullptr;
-      v[q] = make_int4(0, 0, 0, 0);
-      if (i < total) {
-        const bool in_a = i < total_a;
-        const int64_t ii = in_a ? i : i - total_a;
-        const CvtJob& j = in_a ? ja : jb;
-        const int64_t r = SMALL ? (int64_t)((uint32_t)ii / (uint32_t)cpr) : ii / cpr;
-        const int64_t c = ii - r * cpr;
-        v[q] = __ldg(reinterpret_cast<const int4*>(static_cast<const int8_t*>(j.src) + r * K) + c);
-        dst[q] = reinterpret_cast<uint4*>(static_cast<__half*>(j.dst) + r * K) + 2 * c;
-      }
+    for (int q = 0; q < 4; ++q) {
+      const int64_t u = i + q * nt;
+      v[q] = u < na ? __ldg(a + u) : __ldg(b + (u - na));
     }
 #pragma unroll
-    for (int q = 0; q < 2; ++q) {
-      if (dst[q] == nullptr) continue;
-      uint32_t o[8];
-      s8x4_f16x2((uint32_t)v[q].x, o[0], o[1]);
-      s8x4_f16x2((uint32_t)v[q].y, o[2], o[3]);
-      s8x4_f16x2((uint32_t)v[q].z, o[4], o[5]);
-      s8x4_f16x2((uint32_t)v[q].w, o[6], o[7]);
-      dst[q][0] = make_uint4(o[0], o[1], o[2], o[3]);
-      dst[q][1] = make_uint4(o[4], o[5], o[6], o[7]);
+    for (int q = 0; q < 4; ++q) {
+      const int64_t u = i + q * nt;
+      const uint4 o = s8x8_f16x8(v[q]);
+      if (u < na)
+        ea[u] = o;
+      else
+        eb[u - na] = o;
     }
+  }
+  for (; i < total; i += nt) {
+    if (i < na)
+      ea[i] = s8x8_f16x8(__ldg(a + i));
+    else
+      eb[i - na] = s8x8_f16x8(__ldg(b + (i - na)));
   }
 }
 
@@ -627,13 +629,14 @@ cudaError_t launch_encode_pair(int bits, const void* a, int64_t rows_a, void* en
   auto aligned16 = [&](const void* p) {
     return p == nullptr || (reinterpret_cast<uintptr_t>(p) & 15) == 0;
   };
-  if (bits == 8 && K % 16 == 0 && aligned16(a) && aligned16(b)) {
-    const int64_t chunks = (rows_a + rows_b) * (K / 16);
-    const int grid = grid_for((chunks + 1) / 2, 256, sm_count);
-    if (chunks < ((int64_t)1 << 32))
-      cvt_s8_f16_fast_kernel<true><<<grid, 256, 0, s>>>(ja, jb, K);
-    else
-      cvt_s8_f16_fast_kernel<false><<<grid, 256, 0, s>>>(ja, jb, K);
+  if (bits == 8 && K % 16 == 0 && aligned16(a) && aligned16(b) && aligned16(enc_a) &&
+      aligned16(enc_b)) {
+    const int64_t na = a ? rows_a * (K / 8) : 0, nb = b ? rows_b * (K / 8) : 0;
+    int64_t blocks = (na + nb + 4 * 256 - 1) / (4 * 256);
+    blocks = std::min<int64_t>(std::max<int64_t>(blocks, 1), (int64_t)sm_count * 8);
+    cvt_s8_f16_flat_kernel<<<(int)blocks, 256, 0, s>>>(
+        static_cast<const int2*>(a), na, static_cast<uint4*>(enc_a), static_cast<const int2*>(b),
+        nb, static_cast<uint4*>(enc_b));
     return cudaGetLastError();
   }
   const int64_t vec = bits == 8 ? Kp / 8 : Kp / 16;

@@ -67,11 +67,26 @@ struct TcLayout {
 
 // Work unit u = (output tile, K split): split sp of tile t covers the
 // 128-byte K slices [kb0, kb1).  With one split per tile a unit is a tile.
-__device__ __forceinline__ void unit_range(int u, const TcParams& p, int& t, int& kb0, int& kb1) {
-  t = u / p.splits;
-  const int sp = u - t * p.splits;
+// Unit u -> tile t and its K slices [kb0, kb1); returns whether the unit's
+// partial tile is added into C (else stored).  Units below dp_tiles are whole
+// tiles; the rest cut each of the remaining tiles into `splits` K pieces, in
+// tile-major order.  With a grid of G CTAs stepping through the units, the
+// whole tiles fill complete waves when dp_tiles is a multiple of G and the
+// pieces share out the last, partial wave.
+__device__ __forceinline__ bool unit_range(int u, const TcParams& p, int& t, int& kb0, int& kb1) {
+  if (u < p.dp_tiles) {
+    t = u;
+    kb0 = 0;
+    kb1 = p.num_kb;
+    return false;
+  }
+  const int v = u - p.dp_tiles;
+  const int q = v / p.splits;
+  const int sp = v - q * p.splits;
+  t = p.dp_tiles + q;
   kb0 = (int)((int64_t)sp * p.num_kb / p.splits);
   kb1 = (int)((int64_t)(sp + 1) * p.num_kb / p.splits);
+  return p.splits > 1;
 }
 
 __device__ __forceinline__ void tile_coords(int t, const TcParams& p, int& tm, int& tn) {
@@ -313,7 +328,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     bool ok = true;
     for (int w = blockIdx.x; ok && w < p.num_units; w += gridDim.x) {
       int t, kbb, kbe, tm, tn;
-      unit_range(w, p, t, kbb, kbe);
+      const bool adds = unit_range(w, p, t, kbb, kbe);
       tile_coords(t, p, tm, tn);
       const int num_chunks = (kbe - kbb + p.chunk_kb - 1) / p.chunk_kb;
       for (int c = 0; c < num_chunks; ++c, ++u) {
@@ -360,7 +375,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           if (lane == 0) {
             // split K: every piece adds its partial sums into C (zeroed by the
             // host); integer addition makes the order irrelevant
-            if (p.splits > 1)
+            if (adds)
               tma_reduce_add_2d(&tmC, stage_addr, tn * BN + col0 + g * 32, tm * kTcBM + quarter * 32);
             else
               tma_store_2d(&tmC, stage_addr, tn * BN + col0 + g * 32, tm * kTcBM + quarter * 32);

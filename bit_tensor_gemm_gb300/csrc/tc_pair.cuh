@@ -349,7 +349,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
     bool ok = true;
     for (int w = cid; ok && w < p.num_units; w += ncl) {
       int t, kbb, kbe, tm, tn;
-      unit_range(w, p, t, kbb, kbe);
+      const bool adds = unit_range(w, p, t, kbb, kbe);
       tile_coords(t, p, tm, tn);
       const int num_chunks = (kbe - kbb + p.chunk_kb - 1) / p.chunk_kb;
       for (int c = 0; c < num_chunks; ++c, ++u) {
@@ -397,7 +397,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
           __syncwarp();
           if (lane == 0) {
             const int x = tn * kPairTile + col0 + g * 32, y = m0 + quarter * 32;
-            if (p.splits > 1)
+            if (adds)
               tma_reduce_add_2d(&tmC, stage_addr, x, y);
             else
               tma_store_2d(&tmC, stage_addr, x, y);

@@ -14,8 +14,10 @@ struct TcParams {
   int num_kb;    // 128-byte K slices per tile row
   int chunk_kb;  // slices per exact fp32 accumulation chunk
   int tiles_m, tiles_n, num_tiles, group_m;
-  int splits;     // K splits per tile (> 1: partial tiles are added into a zeroed C)
-  int num_units;  // num_tiles * splits
+  int dp_tiles;   // leading tiles (in tile order) computed whole, one unit each
+  int splits;     // K pieces of each remaining tile (> 1: its partial tiles are
+                  // added into C, zeroed there beforehand)
+  int num_units;  // dp_tiles + (num_tiles - dp_tiles) * splits
   int vec_ok;    // rows of C/Y are 16-byte aligned: C goes out by TMA stores,
                  // Y by 16-byte vector stores
   int32_t* C;

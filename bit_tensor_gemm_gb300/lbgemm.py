@@ -72,6 +72,8 @@ _SIGNATURES = {
     "lbgemm_run_host": (_i32, [_i32, _i64, _i64, _i64, _vp, _vp, _vp, _i32, _vp]),
     "lbgemm_set_exact_chunk": (_i32, [_i32, _i32]),
     "lbgemm_get_exact_chunk": (_i32, [_i32]),
+    "lbgemm_set_tail_split": (_i32, [_i32]),
+    "lbgemm_get_tail_split": (_i32, []),
     "lbgemm_device_status": (_i32, [_vp]),
     "lbgemm_selftest_timeout": (_i32, [_vp]),
     "lbgemm_last_error": (ctypes.c_char_p, []),
@@ -300,6 +302,15 @@ def lbgemm_set_exact_chunk(bits: int, k_elems: int) -> None:
 
 def lbgemm_get_exact_chunk(bits: int) -> int:
     return load().lbgemm_get_exact_chunk(bits)
+
+
+def lbgemm_set_tail_split(mode: int) -> None:
+    """0 whole-problem splits only, 1 also a partial last wave (default), 2 forced."""
+    _check(load().lbgemm_set_tail_split(mode))
+
+
+def lbgemm_get_tail_split() -> int:
+    return load().lbgemm_get_tail_split()
 
 
 def lbgemm_device_status(stream=None) -> None:

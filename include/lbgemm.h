@@ -295,6 +295,24 @@ lbgemm_status lbgemm_run_host(int bits, int64_t M, int64_t N, int64_t K, const v
 lbgemm_status lbgemm_set_exact_chunk(int bits, int k_elems);
 int lbgemm_get_exact_chunk(int bits);
 
+/* ---- K splits of a partial last wave -------------------------------------------
+ * The tensor-core GEMM kernels run whole output tiles in waves of the
+ * device's CTA slots.  When the tiles of the last wave would fill at most half
+ * of the slots, each of them is cut along K into pieces (at least 4 K slices
+ * each, as many as fit the wave) whose int32 partial tiles are added into C by
+ * TMA reduce-add, after the part of C they cover is cleared; a problem with at
+ * most half a wave of tiles is split the same way.  A scheduling choice only:
+ * C is the same exact int32 result in every mode.
+ * mode 0: split only problems of at most half a wave; 1 (default): also the
+ * last partial wave; 2: always cut the last wave's tiles (at least 2 pieces,
+ * or 1 K slice each) -- for tests.  Splits need int32 C with N % 4 == 0 and a
+ * 16-byte-aligned C; never for the linear layer.  Applies to the re-encoding
+ * route (lbgemm_run, lbgemm_run_variant, lbgemm_run_encoded); process-wide;
+ * affects calls launched afterwards.  Returns LBGEMM_ERR_INVALID_ARG for a
+ * mode outside 0..2. */
+lbgemm_status lbgemm_set_tail_split(int mode);
+int lbgemm_get_tail_split(void);
+
 /* ---- status ------------------------------------------------------------------ */
 
 /* Synchronises `stream`, then returns LBGEMM_ERR_TIMEOUT if any kernel of this

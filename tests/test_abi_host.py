@@ -120,6 +120,17 @@ def test_exact_chunk_settings(lib):
     L.lbgemm_set_exact_chunk(8, 1024)
 
 
+def test_tail_split_settings(lib):
+    assert L.lbgemm_get_tail_split() == 1
+    for bad in (-1, 3):
+        with pytest.raises(L.LbgemmError):
+            L.lbgemm_set_tail_split(bad)
+    assert L.lbgemm_get_tail_split() == 1
+    for mode in (0, 2, 1):
+        L.lbgemm_set_tail_split(mode)
+        assert L.lbgemm_get_tail_split() == mode
+
+
 @pytest.mark.parametrize("args,status", [
     ((3, 4, 4, 4, 16, 16, 16), L.ERR_INVALID_ARG),           # bits
     ((8, -1, 4, 4, 16, 16, 16), L.ERR_INVALID_ARG),          # negative M

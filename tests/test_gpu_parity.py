@@ -186,6 +186,66 @@ def test_int8_warpmma_dispatch(M, N, K):
     assert_exact(G().gemm(8, A, B, K), oracle.gemm(8, A, B, K), f"int8 warp-MMA {M}x{N}x{K}")
 
 
+# (M, N, K): one tile, ragged tiles, K tails, a single K slice per tile, more
+# pieces than K slices allow, N % 4 != 0 (no splits), and more than one wave
+# of tiles on every tile class (2500 x 2000: 80 large, 320 medium, 640 small)
+TAIL_SHAPES = [(256, 256, 256), (300, 200, 136), (1000, 1000, 2064), (129, 65, 4104),
+               (2048, 520, 1024), (700, 900, 8192), (64, 64, 64), (100, 203, 1000),
+               (2500, 2000, 1040)]
+
+
+@pytest.mark.parametrize("variant", range(9))
+def test_int8_tail_split_forced(variant):
+    """Mode 2 on every tile x stage variant: the tiles of the last wave cut
+    into K pieces added into C, the tiles before them stored whole (C starts
+    filled with -7, so a piece outside the cleared part shows)."""
+    try:
+        L.lbgemm_set_tail_split(2)
+        for i, (M, N, K) in enumerate(TAIL_SHAPES):
+            A, B = synth.operands(8, M, N, K, 1700 + 13 * i + variant)
+            assert_exact(G().gemm(8, A, B, K, variant), oracle.gemm(8, A, B, K),
+                         f"tail split variant {variant} {M}x{N}x{K}")
+    finally:
+        L.lbgemm_set_tail_split(1)
+
+
+def test_tail_split_modes_widths_and_chunks():
+    """The default mode on shapes with one or more whole waves and a small
+    last wave (2560 x 2048 and a ragged 2500 x 2000, every variant), mode 0
+    on the same, mode 2 on the 4-bit and 1-bit (e4m3) kernels and with a
+    shorter exact chunk."""
+    for M, N, K in [(2560, 2048, 1024), (2500, 2000, 1040)]:
+        A, B = synth.operands(8, M, N, K, 1960 + M)
+        want = oracle.gemm(8, A, B, K)
+        for variant in range(9):
+            assert_exact(G().gemm(8, A, B, K, variant), want,
+                         f"tail split (default mode) v{variant} {M}x{N}x{K}")
+        try:
+            L.lbgemm_set_tail_split(0)
+            for variant in (1, 7):
+                assert_exact(G().gemm(8, A, B, K, variant), want, f"mode 0 v{variant}")
+        finally:
+            L.lbgemm_set_tail_split(1)
+    try:
+        L.lbgemm_set_tail_split(2)
+        for bits, M, N, K in [(4, 700, 900, 8192), (4, 129, 300, 1000), (1, 500, 260, 20000),
+                              (1, 129, 65, 4000), (4, 2500, 2000, 1024)]:
+            A, B = synth.operands(bits, M, N, K, 1900 + M)
+            want = oracle.gemm(bits, A, B, K)
+            for variant in (1, 4, 7):
+                assert_exact(G().gemm(bits, A, B, K, variant), want,
+                             f"tail split bits {bits} variant {variant} {M}x{N}x{K}")
+        L.lbgemm_set_exact_chunk(8, 512)
+        M, N, K = 2500, 2000, 3008
+        A, B = synth.operands(8, M, N, K, 1950)
+        want = oracle.gemm(8, A, B, K)
+        for variant in (2, 5, 8):
+            assert_exact(G().gemm(8, A, B, K, variant), want, f"tail split chunk 512 v{variant}")
+    finally:
+        L.lbgemm_set_exact_chunk(8, 1024)
+        L.lbgemm_set_tail_split(1)
+
+
 def test_int8_full_range_and_extremes():
     g = np.random.default_rng(5)
     M, N, K = 130, 70, 3000
