@@ -52,21 +52,34 @@ struct TcLayout {
   static constexpr int kBBytes = BN * 128;
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kRingBytes = kStageBytes * STAGES;
-  // epilogue staging: one 32-row x 128-byte tile per epilogue warp
-  static constexpr int kEpiOffset = kRingBytes;
-  static constexpr int kEpiBytes = kTcEpiWarps * 32 * 128;
   // barriers: full[S], empty[S], acc_full[2], acc_empty[2], mma_done
   static constexpr int kNumBars = 2 * STAGES + 5;
+  static constexpr int kTmemCols = 2 * BN;
+  // epilogue staging: per epilogue warp, one or two 32-row x 128-byte tiles
+  // (two where that keeps as many CTAs per SM: a warp then fills one while
+  // the other is stored)
+  static constexpr int kOneBuf = kTcEpiWarps * 32 * 128;
+  static constexpr int kFixed = kRingBytes + 8 * kNumBars + 8 + 1024;
+  static constexpr int ctas_per_sm(int used) {
+    return (512 / kTmemCols) < 233472 / (tc_smem_request(used, kTmemCols) + 1024)
+               ? 512 / kTmemCols
+               : 233472 / (tc_smem_request(used, kTmemCols) + 1024);
+  }
+  static constexpr int kEpiBufs = kFixed + 2 * kOneBuf <= 232448 &&
+                                          ctas_per_sm(kFixed + 2 * kOneBuf) ==
+                                              ctas_per_sm(kFixed + kOneBuf)
+                                      ? 2
+                                      : 1;
+  static constexpr int kEpiOffset = kRingBytes;
+  static constexpr int kEpiBytes = kEpiBufs * kOneBuf;
   static constexpr int kBarOffset = kEpiOffset + kEpiBytes;
   static constexpr int kTmemSlotOffset = kBarOffset + 8 * kNumBars;
   static constexpr int kAbortOffset = kTmemSlotOffset + 4;
   static constexpr int kUsedBytes = kAbortOffset + 4;
   static constexpr int kDynSmem = kUsedBytes + 1024;  // slack to align the ring to 1024
-  static constexpr int kTmemCols = 2 * BN;
+  static_assert(kDynSmem <= 232448, "shared memory of one CTA");
 };
 
-// Work unit u = (output tile, K split): split sp of tile t covers the
-// 128-byte K slices [kb0, kb1).  With one split per tile a unit is a tile.
 // Unit u -> tile t and its K slices [kb0, kb1); returns whether the unit's
 // partial tile is added into C (else stored).  Units below dp_tiles are whole
 // tiles; the rest cut each of the remaining tiles into `splits` K pieces, in
@@ -322,7 +335,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int row = quarter * 32 + lane;
     const int col0 = (e >> 2) * (BN / 2);
     const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
-    const uint32_t stage_addr = sbase + L::kEpiOffset + e * (32 * 128);
+    const uint32_t stage_addr = sbase + L::kEpiOffset + e * (L::kEpiBufs * 32 * 128);
+    uint32_t stores = 0;  // TMA stores issued by this warp (staging buffer = stores % kEpiBufs)
     uint32_t u = 0;
     int32_t acc[kGroups][32];
     bool ok = true;
@@ -363,22 +377,24 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // 128-byte-swizzled TMA box has.  The TMA store clips rows >= M and
         // columns >= N.
 #pragma unroll
-        for (int g = 0; g < kGroups; ++g) {
-          if (lane == 0) bulk_wait_read_all();  // the previous store has read the tile
+        for (int g = 0; g < kGroups; ++g, ++stores) {
+          // the store that last used this buffer has read it
+          if (lane == 0) bulk_wait_read<L::kEpiBufs - 1>();
           __syncwarp();
+          const uint32_t buf = stage_addr + (stores % L::kEpiBufs) * (32 * 128);
 #pragma unroll
           for (int q = 0; q < 8; ++q)
-            st_shared_v4(stage_addr + lane * 128 + ((q ^ (lane & 7)) << 4), acc[g][4 * q],
+            st_shared_v4(buf + lane * 128 + ((q ^ (lane & 7)) << 4), acc[g][4 * q],
                          acc[g][4 * q + 1], acc[g][4 * q + 2], acc[g][4 * q + 3]);
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            // split K: every piece adds its partial sums into C (zeroed by the
-            // host); integer addition makes the order irrelevant
+            // split K: every piece adds its partial sums into C (cleared by
+            // the host); integer addition makes the order irrelevant
             if (adds)
-              tma_reduce_add_2d(&tmC, stage_addr, tn * BN + col0 + g * 32, tm * kTcBM + quarter * 32);
+              tma_reduce_add_2d(&tmC, buf, tn * BN + col0 + g * 32, tm * kTcBM + quarter * 32);
             else
-              tma_store_2d(&tmC, stage_addr, tn * BN + col0 + g * 32, tm * kTcBM + quarter * 32);
+              tma_store_2d(&tmC, buf, tn * BN + col0 + g * 32, tm * kTcBM + quarter * 32);
             bulk_commit();
           }
         }

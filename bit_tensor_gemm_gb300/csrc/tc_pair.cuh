@@ -46,7 +46,12 @@ struct PairLayout {
   static constexpr int kBBytes = 128 * 128;  // this CTA's 128 rows of B
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kEpiOffset = kStageBytes * STAGES;
-  static constexpr int kEpiBytes = kTcEpiWarps * 32 * 128;
+  // epilogue staging: per epilogue warp, one or two 32-row x 128-byte tiles
+  // (two, where they fit: a warp then fills one while the other is stored)
+  static constexpr int kEpiBufs =
+      kEpiOffset + 2 * kTcEpiWarps * 32 * 128 + 8 * (2 * STAGES + 5) + 24 + 1024 <= 232448 ? 2
+                                                                                          : 1;
+  static constexpr int kEpiBytes = kEpiBufs * kTcEpiWarps * 32 * 128;
   // barriers: full[S], empty[S], acc_full[2], acc_empty[2], mma_done
   static constexpr int kNumBars = 2 * STAGES + 5;
   static constexpr int kBarOffset = kEpiOffset + kEpiBytes;
@@ -56,6 +61,7 @@ struct PairLayout {
   static constexpr int kUsedBytes = kAbortOffset + 4;
   static constexpr int kDynSmem = kUsedBytes + 1024;  // slack to align the ring to 1024
   static constexpr int kTmemCols = 512;              // two 256-column fp32 accumulators
+  static_assert(kDynSmem <= 232448, "shared memory of one CTA");
 };
 
 // ---- cluster and cta_group::2 forms ------------------------------------------------------
@@ -342,9 +348,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
     const int row = quarter * 32 + lane;
     const int col0 = (e >> 2) * (kPairTile / 2);
     const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
-    const uint32_t stage_addr = sbase + L::kEpiOffset + e * (32 * 128);
+    const uint32_t stage_addr = sbase + L::kEpiOffset + e * (L::kEpiBufs * 32 * 128);
     const int row_off = (int)rank * 128;
     uint32_t u = 0;
+    uint32_t stores = 0;  // TMA stores issued by this warp (staging buffer = stores % kEpiBufs)
     int32_t acc[kGroups][32];
     bool ok = true;
     for (int w = cid; ok && w < p.num_units; w += ncl) {
@@ -386,21 +393,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
       const int m0 = tm * kPairTile + row_off;
       if (!LINEAR && p.vec_ok) {
 #pragma unroll
-        for (int g = 0; g < kGroups; ++g) {
-          if (lane == 0) bulk_wait_read_all();
+        for (int g = 0; g < kGroups; ++g, ++stores) {
+          // the store that last used this buffer has read it
+          if (lane == 0) bulk_wait_read<L::kEpiBufs - 1>();
           __syncwarp();
+          const uint32_t buf = stage_addr + (stores % L::kEpiBufs) * (32 * 128);
 #pragma unroll
           for (int q = 0; q < 8; ++q)
-            st_shared_v4(stage_addr + lane * 128 + ((q ^ (lane & 7)) << 4), acc[g][4 * q],
+            st_shared_v4(buf + lane * 128 + ((q ^ (lane & 7)) << 4), acc[g][4 * q],
                          acc[g][4 * q + 1], acc[g][4 * q + 2], acc[g][4 * q + 3]);
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
             const int x = tn * kPairTile + col0 + g * 32, y = m0 + quarter * 32;
             if (adds)
-              tma_reduce_add_2d(&tmC, stage_addr, x, y);
+              tma_reduce_add_2d(&tmC, buf, x, y);
             else
-              tma_store_2d(&tmC, stage_addr, x, y);
+              tma_store_2d(&tmC, buf, x, y);
             bulk_commit();
           }
         }
