@@ -332,13 +332,15 @@ int unit_slots(DeviceState& d, const TcKernel& k) {
 // ---- the tensor-core path (bits 8 and 4, and the linear layer) --------------------------------
 
 // Re-encodes operand a (and b, when rows_b > 0) in one launch.
+// The same launch clears `zero` (the part of C that the GEMM launched after
+// it adds partial tiles into), when given.
 lbgemm_status encode_operands(DeviceState& d, int bits, const void* a, int64_t rows_a, void* enc_a,
                               const void* b, int64_t rows_b, void* enc_b, int64_t K,
-                              cudaStream_t stream) {
+                              cudaStream_t stream, const lbg::ZeroRect& zero = lbg::ZeroRect{}) {
   cudaError_t e = lbg::launch_encode_pair(bits, a, rows_a, enc_a, b, rows_b, enc_b, K,
-                                          enc_kp(bits, K), d.sm_count, stream);
+                                          enc_kp(bits, K), d.sm_count, stream, zero);
   if (e != cudaSuccess) return cuda_fail(e, "operand re-encoding launch");
-  g_launches += (rows_a + rows_b) > 0 ? 1 : 0;
+  g_launches += (rows_a + rows_b) > 0 || zero.C ? 1 : 0;
   return LBGEMM_OK;
 }
 
@@ -407,7 +409,24 @@ void split_tiles_box(const TcKernel& k, int64_t M, int64_t N, int dp_tiles, int6
   *c1 = std::min<int64_t>((tn_hi + 1) * k.tile_n, N);
 }
 
-// Clears the part of C that split tiles add into.
+// The part of C that split tiles add into, as a rectangle for the encoder
+// launch to clear (nothing when no tile is split).
+lbg::ZeroRect split_rect(const TcKernel& k, const KPlan& kp, int64_t M, int64_t N, int32_t* C) {
+  lbg::ZeroRect z;
+  if (!kp.adds()) return z;
+  z.C = C;
+  z.ld = N;
+  if (kp.dp_tiles == 0) {
+    z.r1 = M;
+    z.c1 = N;
+  } else {
+    split_tiles_box(k, M, N, kp.dp_tiles, &z.r0, &z.r1, &z.c0, &z.c1);
+  }
+  return z;
+}
+
+// Clears the part of C that split tiles add into (when no encoder launch
+// precedes the GEMM).
 lbgemm_status clear_split_tiles(const TcKernel& k, const KPlan& kp, int64_t M, int64_t N,
                                 int32_t* C, cudaStream_t stream) {
   if (!kp.adds()) return LBGEMM_OK;
@@ -503,17 +522,17 @@ lbgemm_status run_tc(DeviceState& d, int bits, int64_t M, int64_t N, int64_t K, 
                      int variant, void* ws, cudaStream_t stream) {
   uint8_t* encA = static_cast<uint8_t*>(ws);
   uint8_t* encB = encA + enc_bytes(bits, M, K);
-  // Plan K splits first: C must be cleared before the encoder, so that the
-  // GEMM can still be launched as the encoder's dependent.
+  // Plan K splits first: the encoder launch clears the part of C that split
+  // tiles add into, and the GEMM is launched as its dependent.
   KPlan plan;
   const bool linear = Y != nullptr;
   TcKernel k = tc_kernel(variant, bits != 8, linear);
   if (k.launch) {
     plan = plan_k(d, k, bits, M, N, K, linear, (N % 4 == 0) && aligned16(C));
-    lbgemm_status sc = clear_split_tiles(k, plan, M, N, C, stream);
-    if (sc != LBGEMM_OK) return sc;
   }
-  lbgemm_status st = encode_operands(d, bits, A, M, encA, B, N, encB, K, stream);
+  // the encoder also clears the part of C that split tiles add into
+  lbgemm_status st = encode_operands(d, bits, A, M, encA, B, N, encB, K, stream,
+                                     split_rect(k, plan, M, N, C));
   if (st != LBGEMM_OK) return st;
   return run_tc_encoded(d, bits, M, N, K, encA, encB, C, sx, sw, Y, variant, true, &plan, stream);
 }
@@ -540,11 +559,15 @@ lbgemm_status run_tc_fused(DeviceState& d, bool large_b, int tile_n, int64_t M, 
   // (the tiles of a partial last wave stay whole here: whole-problem splits only)
   KPlan kpl = plan_k(d, k, 8, rows_l, rows_s, K, linear, vec_ok || large_b);
   const int splits = kpl.dp_tiles == 0 ? kpl.splits : 1;
-  if (splits > 1) {  // cleared before the encoder, so the GEMM can be its dependent
-    cudaError_t ez = cudaMemsetAsync(C, 0, (size_t)(M * N) * sizeof(int32_t), stream);
-    if (ez != cudaSuccess) return cuda_fail(ez, "cudaMemsetAsync (split K)");
+  // the encoder also clears C when K is split (partial tiles are added into it)
+  lbg::ZeroRect zero;
+  if (splits > 1) {
+    zero.C = C;
+    zero.ld = N;
+    zero.r1 = M;
+    zero.c1 = N;
   }
-  lbgemm_status st = encode_operands(d, 8, ops, rows_s, ws, nullptr, 0, nullptr, K, stream);
+  lbgemm_status st = encode_operands(d, 8, ops, rows_s, ws, nullptr, 0, nullptr, K, stream, zero);
   if (st != LBGEMM_OK) return st;
   CUtensorMap ml, ms;
   cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows_l};

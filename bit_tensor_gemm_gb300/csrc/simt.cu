@@ -39,9 +39,33 @@ __device__ __forceinline__ void allow_dependent_launch() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// Clears the rectangle z of an int32 matrix, grid-stride over the whole grid;
+// 16-byte stores when the rows and columns allow.
+__device__ __forceinline__ void zero_rect(const ZeroRect& z) {
+  if (z.C == nullptr) return;
+  const int64_t w = z.c1 - z.c0, h = z.r1 - z.r0;
+  const int64_t nt = (int64_t)gridDim.x * blockDim.x;
+  const int64_t t0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const bool vec = w % 4 == 0 && z.c0 % 4 == 0 && z.ld % 4 == 0 &&
+                   (reinterpret_cast<uintptr_t>(z.C) & 15) == 0;
+  if (vec) {
+    const int64_t wq = w / 4;
+    for (int64_t i = t0; i < h * wq; i += nt) {
+      const int64_t r = i / wq, c = i - r * wq;
+      *reinterpret_cast<int4*>(z.C + (z.r0 + r) * z.ld + z.c0 + 4 * c) = make_int4(0, 0, 0, 0);
+    }
+  } else {
+    for (int64_t i = t0; i < h * w; i += nt) {
+      const int64_t r = i / w, c = i - r * w;
+      z.C[(z.r0 + r) * z.ld + z.c0 + c] = 0;
+    }
+  }
+}
+
 // int8 -> fp16; each thread writes 8 halves (16 bytes).
-__global__ void cvt_s8_f16_kernel(CvtJob ja, CvtJob jb, int64_t K, int64_t Kp) {
+__global__ void cvt_s8_f16_kernel(CvtJob ja, CvtJob jb, int64_t K, int64_t Kp, ZeroRect z) {
   allow_dependent_launch();
+  zero_rect(z);
   const int64_t vec_per_row = Kp / 8;
   const int64_t total_a = ja.rows * vec_per_row;
   const int64_t total = total_a + jb.rows * vec_per_row;
@@ -97,8 +121,10 @@ __device__ __forceinline__ uint4 s8x8_f16x8(int2 v) {
 
 // units: 8-byte groups; na of operand a, then nb of operand b
 __global__ void cvt_s8_f16_flat_kernel(const int2* __restrict__ a, int64_t na, uint4* ea,
-                                       const int2* __restrict__ b, int64_t nb, uint4* eb) {
+                                       const int2* __restrict__ b, int64_t nb, uint4* eb,
+                                       ZeroRect z) {
   allow_dependent_launch();
+  zero_rect(z);
   const int64_t total = na + nb;
   const int64_t nt = (int64_t)gridDim.x * blockDim.x;
   int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -130,8 +156,9 @@ __global__ void cvt_s8_f16_flat_kernel(const int2* __restrict__ a, int64_t na, u
 // packed int4 (two per byte, low nibble first) -> e4m3 bytes; K is even.
 // Each thread writes 16 output bytes from 8 input bytes through a 256-entry
 // table (byte -> two e4m3 codes) built per block with CUDA's fp8 conversion.
-__global__ void cvt_s4_e4m3_kernel(CvtJob ja, CvtJob jb, int64_t K, int64_t Kp) {
+__global__ void cvt_s4_e4m3_kernel(CvtJob ja, CvtJob jb, int64_t K, int64_t Kp, ZeroRect z) {
   allow_dependent_launch();
+  zero_rect(z);
   __shared__ uint16_t table[256];
   for (int b = threadIdx.x; b < 256; b += blockDim.x) {
     const int lo = (b & 15) >= 8 ? (b & 15) - 16 : (b & 15);
@@ -177,8 +204,9 @@ __global__ void cvt_s4_e4m3_kernel(CvtJob ja, CvtJob jb, int64_t K, int64_t Kp) 
 // words become rows of 32 W bytes.  Each thread expands one word through a
 // 16-entry table (four bits -> four codes) built per block with CUDA's fp8
 // conversion of +1 and -1.
-__global__ void cvt_b1_e4m3_kernel(CvtJob ja, CvtJob jb, int64_t W) {
+__global__ void cvt_b1_e4m3_kernel(CvtJob ja, CvtJob jb, int64_t W, ZeroRect z) {
   allow_dependent_launch();
+  zero_rect(z);
   __shared__ uint32_t nib[16];
   if (threadIdx.x < 16) {
     const uint32_t pos = __nv_cvt_float_to_fp8(1.0f, __NV_SATFINITE, __NV_E4M3);
@@ -613,17 +641,25 @@ cudaError_t launch_quant_rows_bf16(const void* X, int64_t M, int64_t K, int8_t* 
 
 cudaError_t launch_encode_pair(int bits, const void* a, int64_t rows_a, void* enc_a,
                                const void* b, int64_t rows_b, void* enc_b, int64_t K, int64_t Kp,
-                               int sm_count, cudaStream_t s) {
-  if (rows_a + rows_b == 0) return cudaSuccess;
+                               int sm_count, cudaStream_t s, const ZeroRect& zero) {
+  if (rows_a + rows_b == 0 && zero.C == nullptr) return cudaSuccess;
   const int64_t row_bytes = bits == 8 ? K : bits == 4 ? K / 2 : K / 8;
   auto fast = [&](const void* p) {
     return (int)(row_bytes % 8 == 0 && (reinterpret_cast<uintptr_t>(p) & 7) == 0);
   };
   CvtJob ja{a, rows_a, enc_a, a ? fast(a) : 0};
   CvtJob jb{b, rows_b, enc_b, b ? fast(b) : 0};
+  // threads enough for the clearing too (about four 16-byte stores each)
+  const int64_t zero_threads =
+      zero.C ? ((zero.r1 - zero.r0) * (zero.c1 - zero.c0) + 15) / 16 : 0;
+  auto with_zero = [&](int grid) {
+    const int64_t zb = std::min<int64_t>((zero_threads + 255) / 256, (int64_t)sm_count * 16);
+    return (int)std::max<int64_t>(grid, zb);
+  };
   if (bits == 1) {  // K % 32 == 0 and Kp == K: rows are contiguous words
     const int64_t W = K / 32;
-    cvt_b1_e4m3_kernel<<<grid_for((rows_a + rows_b) * W, 256, sm_count), 256, 0, s>>>(ja, jb, W);
+    cvt_b1_e4m3_kernel<<<with_zero(grid_for((rows_a + rows_b) * W, 256, sm_count)), 256, 0, s>>>(
+        ja, jb, W, zero);
     return cudaGetLastError();
   }
   auto aligned16 = [&](const void* p) {
@@ -634,17 +670,17 @@ cudaError_t launch_encode_pair(int bits, const void* a, int64_t rows_a, void* en
     const int64_t na = a ? rows_a * (K / 8) : 0, nb = b ? rows_b * (K / 8) : 0;
     int64_t blocks = (na + nb + 4 * 256 - 1) / (4 * 256);
     blocks = std::min<int64_t>(std::max<int64_t>(blocks, 1), (int64_t)sm_count * 8);
-    cvt_s8_f16_flat_kernel<<<(int)blocks, 256, 0, s>>>(
+    cvt_s8_f16_flat_kernel<<<with_zero((int)blocks), 256, 0, s>>>(
         static_cast<const int2*>(a), na, static_cast<uint4*>(enc_a), static_cast<const int2*>(b),
-        nb, static_cast<uint4*>(enc_b));
+        nb, static_cast<uint4*>(enc_b), zero);
     return cudaGetLastError();
   }
   const int64_t vec = bits == 8 ? Kp / 8 : Kp / 16;
-  const int grid = grid_for((rows_a + rows_b) * vec, 256, sm_count);
+  const int grid = with_zero(grid_for((rows_a + rows_b) * vec, 256, sm_count));
   if (bits == 8)
-    cvt_s8_f16_kernel<<<grid, 256, 0, s>>>(ja, jb, K, Kp);
+    cvt_s8_f16_kernel<<<grid, 256, 0, s>>>(ja, jb, K, Kp, zero);
   else
-    cvt_s4_e4m3_kernel<<<grid, 256, 0, s>>>(ja, jb, K, Kp);
+    cvt_s4_e4m3_kernel<<<grid, 256, 0, s>>>(ja, jb, K, Kp, zero);
   return cudaGetLastError();
 }
 

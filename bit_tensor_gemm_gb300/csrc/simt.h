@@ -10,9 +10,16 @@ namespace lbg {
 // Kp % 8 == 0; bits 4: packed int4 -> e4m3 rows of Kp bytes, Kp % 16 == 0;
 // bits 1: +-1 bits -> e4m3 rows of Kp == K bytes), zero padded, for up to two
 // operands in one launch (rows_b may be 0).
+// The same launch can also clear a rectangle of an int32 matrix (rows
+// [r0, r1), columns [c0, c1), row stride ld elements) that the GEMM launched
+// after it adds partial tiles into; C == nullptr clears nothing.
+struct ZeroRect {
+  int32_t* C = nullptr;
+  int64_t ld = 0, r0 = 0, r1 = 0, c0 = 0, c1 = 0;
+};
 cudaError_t launch_encode_pair(int bits, const void* a, int64_t rows_a, void* enc_a,
                                const void* b, int64_t rows_b, void* enc_b, int64_t K, int64_t Kp,
-                               int sm_count, cudaStream_t s);
+                               int sm_count, cudaStream_t s, const ZeroRect& zero = ZeroRect{});
 // M <= 16, K % 16 == 0, A and B 16-byte aligned.  Y != nullptr selects the
 // linear epilogue (bf16 Y with scales sx, sw) instead of int32 C.
 cudaError_t launch_skinny_s8(const int8_t* A, const int8_t* B, int M, int N, int K, int32_t* C,

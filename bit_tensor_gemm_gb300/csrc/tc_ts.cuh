@@ -351,6 +351,9 @@ __global__ void __launch_bounds__(kTsThreads, 1)
     }
   } else {
     // ---------------- epilogue ----------------
+    // C may have been cleared by the grid this kernel was launched as a
+    // dependent of: wait for that grid before the first store into C.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int e = warp - 2;
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;

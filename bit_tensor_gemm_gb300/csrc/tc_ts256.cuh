@@ -430,6 +430,9 @@ __global__ void __launch_bounds__(kT2Threads, 1)
         dq += n_in_chunk;
         if (dq >= dnq) {
           // ---- the unit's tile is complete: store it ----
+          // (C may have been cleared by the grid this kernel was launched as
+          // a dependent of: that grid is complete before the first store)
+          asm volatile("griddepcontrol.wait;" ::: "memory");
           int t, kb_a, kb_b, tm, tn;
           unit_range(dw, p, t, kb_a, kb_b);
           tile_coords(t, p, tm, tn);
