@@ -57,8 +57,16 @@ constexpr int64_t kSmallMaxK = 512;
 constexpr int64_t kFusedMaxSide = 512;
 constexpr int64_t kFusedMinOther = 1024;
 constexpr int64_t kFusedMinK = 2048;
-// Small side of the warp-level fp16 MMA kernel (hmma_skinny.cu).
+// Small side of the warp-level fp16 MMA kernel (hmma_skinny.cu): any problem
+// up to kWarpMmaMaxSide rows; with more rows (up to kWarpMmaMaxSideSmall,
+// each 32 rows re-reading the large operand) only small problems, where the
+// re-encoding route's two launches cost more (measured on GB300: 64-256 x
+// 1024-4096 x 1024-2048, 3-7 us faster; with a side of 16384, or K of 4096,
+// slower).
 constexpr int64_t kWarpMmaMaxSide = 32;
+constexpr int64_t kWarpMmaMaxSideSmall = 256;
+constexpr int64_t kWarpMmaMaxArea = int64_t(1) << 19;  // min(M, N) * max(M, N)
+constexpr int64_t kWarpMmaMaxKSmall = 2048;
 constexpr double kSmallMaxWork = 268435456.0;
 constexpr size_t kFlushBytes = size_t(256) << 20;  // twice the 129 MB L2
 
@@ -646,6 +654,14 @@ bool warpmma_ok(int64_t M, int64_t N, int64_t K, const void* A, const void* B) {
          aligned16(A) && aligned16(B);
 }
 
+// The same kernel for a small problem with a side of up to
+// kWarpMmaMaxSideSmall rows (taken after the one-launch dp4a route).
+bool warpmma_small_ok(int64_t M, int64_t N, int64_t K, const void* A, const void* B) {
+  const int64_t lo = std::min(M, N), hi = std::max(M, N);
+  return lo <= kWarpMmaMaxSideSmall && lo * hi <= kWarpMmaMaxArea && K <= kWarpMmaMaxKSmall &&
+         K % 16 == 0 && K <= lbg::hmma_skinny_max_k((int)lo) && aligned16(A) && aligned16(B);
+}
+
 // Route of the in-kernel-conversion kernel for an 8-bit problem (1: B is
 // converted in the kernel, 2: A is; 0: re-encode both) and its tile width
 // along the re-encoded operand.  Measured on GB300 over the 729-shape grid:
@@ -701,6 +717,9 @@ lbgemm_status run_any(int bits, int64_t M, int64_t N, int64_t K, const void* A, 
     g_launches += 1;
     return LBGEMM_OK;
   }
+  if (bits == 8 && auto_pick && warpmma_small_ok(M, N, K, A, B))
+    return run_warpmma(*d, M, N, K, static_cast<const int8_t*>(A), static_cast<const int8_t*>(B),
+                       C, nullptr, nullptr, nullptr, stream);
   int fuse_tile = 0;
   const int fuse = (bits == 8 && auto_pick) ? fused_route(M, N, K, A, B, &fuse_tile) : 0;
   if (fuse) {
@@ -849,9 +868,9 @@ lbgemm_status lbgemm_run_warpmma(int64_t M, int64_t N, int64_t K, const int8_t* 
   try {
     lbgemm_status st = check_gemm_args(8, M, N, K, A, B, C);
     if (st != LBGEMM_OK) return st;
-    if (std::min(M, N) > kWarpMmaMaxSide)
+    if (std::min(M, N) > kWarpMmaMaxSideSmall)
       return fail(LBGEMM_ERR_INVALID_ARG, "the warp-MMA kernel needs min(M, N) <= %d",
-                  (int)kWarpMmaMaxSide);
+                  (int)kWarpMmaMaxSideSmall);
     if (K % 16) return fail(LBGEMM_ERR_ALIGNMENT, "the warp-MMA kernel needs K %% 16 == 0");
     if (M == 0 || N == 0) return LBGEMM_OK;
     if (K > lbg::hmma_skinny_max_k((int)std::min(M, N)))

@@ -87,7 +87,9 @@ lbgemm_status lbgemm_variant_info(int bits, int variant, int* tile_m, int* tile_
  * 8-bit problems with min(M, N) <= 32 (and K within the limit of
  * lbgemm_run_warpmma) on the warp-level fp16 MMA kernel, which streams the
  * large operand once; 8-bit problems with K <= 512 and M*N*K <= 2^28 on a
- * one-launch dp4a kernel; 8-bit problems with min(M, N) <= 512,
+ * one-launch dp4a kernel; small 8-bit problems with min(M, N) <= 256,
+ * M*N <= 2^19 and K <= 2048 on the warp-level fp16 MMA kernel too (each 32
+ * rows of the small side re-read the large one); 8-bit problems with min(M, N) <= 512,
  * max(M, N) >= 1024 and K >= 2048 on a tensor-core kernel that converts the
  * large operand itself (lbgemm_run_fused), with only the small one
  * re-encoded ahead; and 1-bit problems with M*N*K < 2^30 on the
@@ -118,11 +120,12 @@ lbgemm_status lbgemm_run_fused(int64_t M, int64_t N, int64_t K, const int8_t* A,
                                int32_t* C, int tile_n, void* stream);
 
 /* 8-bit C = A . B^T forced onto the warp-level fp16 MMA kernel for problems
- * with a small side: min(M, N) <= 32 rows, and K at most 4224 (small side
- * <= 16) or 2048 (<= 32) so that the small operand fits the kernel's shared
- * memory (LBGEMM_ERR_INVALID_ARG otherwise).
+ * with a small side: min(M, N) <= 256 rows, and K at most 4224 (small side
+ * <= 16) or 2048 (> 16) so that 16 or 32 rows of the small operand fit the
+ * kernel's shared memory (LBGEMM_ERR_INVALID_ARG otherwise).
  * Both operands stay int8 in memory and are converted to fp16 in registers;
- * the large side is streamed from HBM once.  No scratch, one launch.
+ * the large side is streamed from HBM once per 32 rows of the small side.
+ * No scratch, one launch.
  * Requires K % 16 == 0 and 16-byte-aligned A and B (LBGEMM_ERR_ALIGNMENT).
  * lbgemm_run takes this route by itself for the shapes where it is measured
  * faster; this entry exists for tests and timing.  [LBG] intro (8-bit GEMM),

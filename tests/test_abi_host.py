@@ -150,9 +150,10 @@ def test_argument_errors_need_no_device(lib, args, status):
 
 
 @pytest.mark.parametrize("M,N,K,tile,status", [
-    (64, 100, 64, 0, L.ERR_INVALID_ARG),     # warp-MMA: small side above 32
     (16, 100, 4240, 0, L.ERR_INVALID_ARG),   # warp-MMA: K above its limit at 16 rows
     (32, 100, 2064, 0, L.ERR_INVALID_ARG),   # warp-MMA: K above its limit at 32 rows
+    (257, 300, 64, 0, L.ERR_INVALID_ARG),    # warp-MMA: small side above 256 rows
+    (200, 300, 2064, 0, L.ERR_INVALID_ARG),  # warp-MMA: K above its limit past 16 rows
     (16, 100, 40, 0, L.ERR_ALIGNMENT),       # warp-MMA: K % 16
     (16, 100, 64, 96, L.ERR_INVALID_ARG),    # fused: tile width
     (16, 100, 40, 128, L.ERR_ALIGNMENT),     # fused: K % 16

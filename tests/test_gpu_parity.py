@@ -144,7 +144,10 @@ def test_int8_fused_short_chunks():
 WARPMMA_SHAPES = [(1, 1000, 4096), (5, 77, 16), (16, 300, 1040), (32, 4100, 2048),
                   (20, 1000, 2048), (300, 16, 1040), (4100, 30, 2000), (32, 32, 128),
                   (17, 11008, 576), (16, 9, 4224), (3, 5000, 4224), (30, 700, 2048),
-                  (7, 300, 4160), (9, 1000, 272), (1, 1, 16)]
+                  (7, 300, 4160), (9, 1000, 272), (1, 1, 16),
+                  # more than 32 rows on the small side: several row blocks of 32
+                  (33, 1000, 512), (64, 1024, 1024), (100, 700, 2048), (1500, 128, 1040),
+                  (256, 256, 64), (200, 3000, 16)]
 
 
 def test_int8_warpmma_forced():
@@ -179,9 +182,11 @@ def test_int8_warpmma_extremes():
 
 
 @pytest.mark.parametrize("M,N,K", [(8, 2000, 1024), (32, 700, 2048), (2000, 24, 512),
-                                   (3000, 5, 64)])
+                                   (3000, 5, 64), (64, 1024, 1024), (4096, 128, 2048),
+                                   (250, 2000, 1040)])
 def test_int8_warpmma_dispatch(M, N, K):
-    """Default dispatch of problems with a side of 5..32 rows."""
+    """Default dispatch of problems with a side of 5..32 rows, and of small
+    problems with a side of up to 256 rows (M*N <= 2^19, K <= 2048)."""
     A, B = synth.operands(8, M, N, K, 11 * M + N)
     assert_exact(G().gemm(8, A, B, K), oracle.gemm(8, A, B, K), f"int8 warp-MMA {M}x{N}x{K}")
 
