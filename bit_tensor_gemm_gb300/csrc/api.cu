@@ -110,6 +110,9 @@ struct DeviceState {
   Scratch flush;        // buffer written between timed runs to evict L2
   Scratch quant;        // quantised activations of lbgemm_linear_quant
   std::map<const void*, int> occupancy;
+  // lbgemm_run_host's copy streams (host-to-device, device-to-host) and events
+  cudaStream_t copy_in = nullptr, copy_out = nullptr;
+  std::vector<cudaEvent_t> host_events;
 };
 
 std::mutex g_mu;     // device state
@@ -1171,6 +1174,24 @@ lbgemm_status lbgemm_time_variants(int bits, int64_t M, int64_t N, int64_t K, co
   return st;
 }
 
+// Row blocks of a host-buffer call: the copies of block i's rows of A in and
+// of block i - 1's rows of C out (each direction on a copy stream of its own)
+// overlap block i's GEMM.  One block below kHostBlockBytes of A or C per block.
+constexpr int64_t kHostBlockBytes = int64_t(64) << 20;
+constexpr int kHostMaxBlocks = 8;
+
+lbgemm_status host_streams(DeviceState& d) {
+  if (d.copy_in) return LBGEMM_OK;
+  cudaError_t e = cudaStreamCreateWithFlags(&d.copy_in, cudaStreamNonBlocking);
+  if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&d.copy_out, cudaStreamNonBlocking);
+  for (int i = 0; e == cudaSuccess && i < 2 * kHostMaxBlocks + 3; ++i) {
+    cudaEvent_t ev = nullptr;
+    e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
+    if (e == cudaSuccess) d.host_events.push_back(ev);
+  }
+  return e == cudaSuccess ? LBGEMM_OK : cuda_fail(e, "copy streams for lbgemm_run_host");
+}
+
 lbgemm_status lbgemm_run_host(int bits, int64_t M, int64_t N, int64_t K, const void* A_host,
                               const void* B_host, int32_t* C_host, int variant, void* stream) {
   try {
@@ -1187,19 +1208,67 @@ lbgemm_status lbgemm_run_host(int bits, int64_t M, int64_t N, int64_t K, const v
     const size_t c_bytes = (size_t)(M * N * 4);
     static std::mutex host_mu;
     std::lock_guard<std::mutex> lock(host_mu);
+    st = host_streams(*d);
+    if (st != LBGEMM_OK) return st;
     st = scratch_acquire(d->host_stage, a_bytes + b_bytes + round_up(c_bytes, 256), s);
     if (st != LBGEMM_OK) return st;
     uint8_t* dA = static_cast<uint8_t*>(d->host_stage.ptr);
     uint8_t* dB = dA + a_bytes;
     int32_t* dC = reinterpret_cast<int32_t*>(dB + b_bytes);
-    cudaError_t e = cudaMemcpyAsync(dA, A_host, (size_t)(M * row_bytes), cudaMemcpyHostToDevice, s);
+    // blocks of whole 256-row tiles, as many as the larger of A and C asks for
+    const int64_t big = std::max<int64_t>(M * row_bytes, (int64_t)c_bytes);
+    int64_t nb = std::min<int64_t>((big + kHostBlockBytes - 1) / kHostBlockBytes, kHostMaxBlocks);
+    const int64_t rows = round_up((M + nb - 1) / nb, 256);
+    nb = (M + rows - 1) / rows;
+    if (nb == 1) {  // small: everything in order on the caller's stream
+      cudaError_t e =
+          cudaMemcpyAsync(dA, A_host, (size_t)(M * row_bytes), cudaMemcpyHostToDevice, s);
+      if (e == cudaSuccess)
+        e = cudaMemcpyAsync(dB, B_host, (size_t)(N * row_bytes), cudaMemcpyHostToDevice, s);
+      if (e != cudaSuccess) return cuda_fail(e, "host-to-device copy");
+      st = run_any(bits, M, N, K, dA, dB, dC, variant, nullptr, 0, true, s);
+      if (st != LBGEMM_OK) return st;
+      e = cudaMemcpyAsync(C_host, dC, c_bytes, cudaMemcpyDeviceToHost, s);
+      if (e != cudaSuccess) return cuda_fail(e, "device-to-host copy");
+      st = scratch_release(d->host_stage, s);
+      if (st != LBGEMM_OK) return st;
+      e = cudaStreamSynchronize(s);
+      return e == cudaSuccess ? LBGEMM_OK : cuda_fail(e, "cudaStreamSynchronize");
+    }
+    cudaEvent_t* ev = d->host_events.data();  // [0] start, [1] B in, A in[i], C done[i], [last] out
+    cudaEvent_t ev_start = ev[0], ev_b = ev[1], ev_out = ev[2 + 2 * kHostMaxBlocks];
+    // the copies start after the caller's earlier work on `s` (the staging
+    // buffer's previous user included)
+    cudaError_t e = cudaEventRecord(ev_start, s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(d->copy_in, ev_start, 0);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(d->copy_out, ev_start, 0);
     if (e == cudaSuccess)
-      e = cudaMemcpyAsync(dB, B_host, (size_t)(N * row_bytes), cudaMemcpyHostToDevice, s);
+      e = cudaMemcpyAsync(dB, B_host, (size_t)(N * row_bytes), cudaMemcpyHostToDevice, d->copy_in);
+    if (e == cudaSuccess) e = cudaEventRecord(ev_b, d->copy_in);
+    for (int64_t i = 0; e == cudaSuccess && i < nb; ++i) {
+      const int64_t r0 = i * rows, r = std::min(rows, M - r0);
+      e = cudaMemcpyAsync(dA + r0 * row_bytes, static_cast<const uint8_t*>(A_host) + r0 * row_bytes,
+                          (size_t)(r * row_bytes), cudaMemcpyHostToDevice, d->copy_in);
+      if (e == cudaSuccess) e = cudaEventRecord(ev[2 + i], d->copy_in);
+    }
     if (e != cudaSuccess) return cuda_fail(e, "host-to-device copy");
-    st = run_any(bits, M, N, K, dA, dB, dC, variant, nullptr, 0, true, s);
-    if (st != LBGEMM_OK) return st;
-    e = cudaMemcpyAsync(C_host, dC, c_bytes, cudaMemcpyDeviceToHost, s);
-    if (e != cudaSuccess) return cuda_fail(e, "device-to-host copy");
+    e = cudaStreamWaitEvent(s, ev_b, 0);
+    for (int64_t i = 0; e == cudaSuccess && i < nb; ++i) {
+      const int64_t r0 = i * rows, r = std::min(rows, M - r0);
+      e = cudaStreamWaitEvent(s, ev[2 + i], 0);
+      if (e != cudaSuccess) break;
+      st = run_any(bits, r, N, K, dA + r0 * row_bytes, dB, dC + r0 * N, variant, nullptr, 0, true,
+                   s);
+      if (st != LBGEMM_OK) return st;
+      e = cudaEventRecord(ev[2 + kHostMaxBlocks + i], s);
+      if (e == cudaSuccess) e = cudaStreamWaitEvent(d->copy_out, ev[2 + kHostMaxBlocks + i], 0);
+      if (e == cudaSuccess)
+        e = cudaMemcpyAsync(C_host + r0 * N, dC + r0 * N, (size_t)(r * N * 4),
+                            cudaMemcpyDeviceToHost, d->copy_out);
+    }
+    if (e == cudaSuccess) e = cudaEventRecord(ev_out, d->copy_out);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(s, ev_out, 0);
+    if (e != cudaSuccess) return cuda_fail(e, "pipelined host copies");
     st = scratch_release(d->host_stage, s);
     if (st != LBGEMM_OK) return st;
     e = cudaStreamSynchronize(s);

@@ -310,6 +310,18 @@ def test_int8_host_buffers():
     assert_exact(C, oracle.gemm(8, A, B, K), "int8 host buffers")
 
 
+@pytest.mark.parametrize("bits,M,N,K", [(8, 4500, 4000, 256), (8, 20000, 64, 4096),
+                                        (4, 4500, 4000, 128), (1, 5000, 4000, 64)])
+def test_host_buffers_in_row_blocks(bits, M, N, K):
+    """Problems whose A or C passes 64 MB run in row blocks (copies in and
+    out on their own streams, overlapping the blocks' GEMMs): ragged last
+    block, a large A with a small C, and every bit width."""
+    A, B = synth.operands(bits, M, N, K, 80 + bits)
+    C = np.zeros((M, N), np.int32)
+    L.lbgemm_run_host(bits, M, N, K, A, B, C, -1, 0)
+    assert_exact(C, oracle.gemm(bits, A, B, K), f"host buffers bits {bits} {M}x{N}x{K}")
+
+
 # ---- 4-bit ---------------------------------------------------------------------
 
 SHAPES_4 = [(256, 256, 256), (300, 200, 138), (129, 65, 1000), (128, 512, 4096), (3, 5, 2)]
