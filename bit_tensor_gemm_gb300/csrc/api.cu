@@ -59,10 +59,12 @@ constexpr int64_t kFusedMinOther = 1024;
 constexpr int64_t kFusedMinK = 2048;
 // Small side of the warp-level fp16 MMA kernel (hmma_skinny.cu): any problem
 // up to kWarpMmaMaxSide rows; with more rows (up to kWarpMmaMaxSideSmall,
-// each 32 rows re-reading the large operand) only small problems, where the
-// re-encoding route's two launches cost more (measured on GB300: 64-256 x
-// 1024-4096 x 1024-2048, 3-7 us faster; with a side of 16384, or K of 4096,
-// slower).
+// each 32 rows re-reading the large operand) only small problems with
+// 256 < K <= 2048, where the re-encoding route's two launches cost more
+// (measured on GB300: 64-256 x 1024-4096 x 1024-2048, 3-7 us faster; with a
+// side of 16384, or K of 4096, slower), and where the one-launch dp4a kernel
+// does (K of 272-512: 8.8-10.9 us against 12.9 us; at K <= 256 the dp4a
+// kernel is as fast or faster).
 constexpr int64_t kWarpMmaMaxSide = 32;
 constexpr int64_t kWarpMmaMaxSideSmall = 256;
 constexpr int64_t kWarpMmaMaxArea = int64_t(1) << 19;  // min(M, N) * max(M, N)
@@ -658,10 +660,13 @@ bool warpmma_ok(int64_t M, int64_t N, int64_t K, const void* A, const void* B) {
 }
 
 // The same kernel for a small problem with a side of up to
-// kWarpMmaMaxSideSmall rows (taken after the one-launch dp4a route).
+// kWarpMmaMaxSideSmall rows and 256 < K <= 2048: M*N <= 2^19, or the
+// one-launch dp4a kernel's problems (K <= 512, M*N*K <= 2^28).
 bool warpmma_small_ok(int64_t M, int64_t N, int64_t K, const void* A, const void* B) {
   const int64_t lo = std::min(M, N), hi = std::max(M, N);
-  return lo <= kWarpMmaMaxSideSmall && lo * hi <= kWarpMmaMaxArea && K <= kWarpMmaMaxKSmall &&
+  const bool area = lo * hi <= kWarpMmaMaxArea ||
+                    (K <= kSmallMaxK && (double)M * (double)N * (double)K <= kSmallMaxWork);
+  return lo <= kWarpMmaMaxSideSmall && K > 256 && K <= kWarpMmaMaxKSmall && area &&
          K % 16 == 0 && K <= lbg::hmma_skinny_max_k((int)lo) && aligned16(A) && aligned16(B);
 }
 
@@ -713,6 +718,9 @@ lbgemm_status run_any(int bits, int64_t M, int64_t N, int64_t K, const void* A, 
   if (bits == 8 && auto_pick && warpmma_ok(M, N, K, A, B))
     return run_warpmma(*d, M, N, K, static_cast<const int8_t*>(A), static_cast<const int8_t*>(B),
                        C, nullptr, nullptr, nullptr, stream);
+  if (bits == 8 && auto_pick && warpmma_small_ok(M, N, K, A, B))
+    return run_warpmma(*d, M, N, K, static_cast<const int8_t*>(A), static_cast<const int8_t*>(B),
+                       C, nullptr, nullptr, nullptr, stream);
   if (bits == 8 && auto_pick && small_ok(M, N, K, A, B)) {
     e = lbg::launch_small_s8(static_cast<const int8_t*>(A), static_cast<const int8_t*>(B), M, N, K,
                              C, stream);
@@ -720,9 +728,6 @@ lbgemm_status run_any(int bits, int64_t M, int64_t N, int64_t K, const void* A, 
     g_launches += 1;
     return LBGEMM_OK;
   }
-  if (bits == 8 && auto_pick && warpmma_small_ok(M, N, K, A, B))
-    return run_warpmma(*d, M, N, K, static_cast<const int8_t*>(A), static_cast<const int8_t*>(B),
-                       C, nullptr, nullptr, nullptr, stream);
   int fuse_tile = 0;
   const int fuse = (bits == 8 && auto_pick) ? fused_route(M, N, K, A, B, &fuse_tile) : 0;
   if (fuse) {

@@ -86,10 +86,11 @@ lbgemm_status lbgemm_variant_info(int bits, int variant, int* tile_m, int* tile_
  * 8-bit problems with M <= 4 run on a dp4a kernel that streams B once;
  * 8-bit problems with min(M, N) <= 32 (and K within the limit of
  * lbgemm_run_warpmma) on the warp-level fp16 MMA kernel, which streams the
- * large operand once; 8-bit problems with K <= 512 and M*N*K <= 2^28 on a
- * one-launch dp4a kernel; small 8-bit problems with min(M, N) <= 256,
- * M*N <= 2^19 and K <= 2048 on the warp-level fp16 MMA kernel too (each 32
- * rows of the small side re-read the large one); 8-bit problems with min(M, N) <= 512,
+ * large operand once; small 8-bit problems with min(M, N) <= 256,
+ * 256 < K <= 2048 and either M*N <= 2^19 or (K <= 512 and M*N*K <= 2^28) on
+ * the warp-level fp16 MMA kernel too (each 32 rows of the small side re-read
+ * the large one); 8-bit problems with K <= 512 and M*N*K <= 2^28 on a
+ * one-launch dp4a kernel; 8-bit problems with min(M, N) <= 512,
  * max(M, N) >= 1024 and K >= 2048 on a tensor-core kernel that converts the
  * large operand itself (lbgemm_run_fused), with only the small one
  * re-encoded ahead; and 1-bit problems with M*N*K < 2^30 on the

@@ -68,12 +68,16 @@ def test_int8_skinny_path(M):
 
 def test_int8_small_dp4a_path():
     """Default dispatch of small problems (K <= 512, M*N*K <= 2^28): the
-    one-launch dp4a kernel, with ragged M, N and K tails."""
-    for M, N, K in [(17, 19, 16), (64, 64, 64), (100, 300, 144), (1000, 250, 512), (65, 4000, 32)]:
+    one-launch dp4a kernel (K <= 256, or both sides above 256 rows), with
+    ragged M, N and K tails; with a side of at most 256 rows and K > 256 the
+    warp-MMA kernel."""
+    for M, N, K in [(17, 19, 16), (64, 64, 64), (100, 300, 144), (1000, 250, 512), (65, 4000, 32),
+                    (300, 1000, 512), (257, 260, 272)]:
         A, B = synth.operands(8, M, N, K, 13 * M + K)
         assert_exact(G().gemm(8, A, B, K), oracle.gemm(8, A, B, K), f"int8 small {M}x{N}x{K}")
-    A = np.full((40, 512), -128, np.int8)
-    assert np.all(G().gemm(8, A, A, 512) == 16384 * 512)
+    for rows in (40, 300):
+        A = np.full((rows, 512), -128, np.int8)
+        assert np.all(G().gemm(8, A, A, 512) == 16384 * 512)
 
 
 @pytest.mark.parametrize("M,N,K", [(64, 4096, 2048), (200, 2500, 2064), (4096, 100, 4096),
