@@ -660,11 +660,14 @@ bool warpmma_ok(int64_t M, int64_t N, int64_t K, const void* A, const void* B) {
 }
 
 // The same kernel for a small problem with a side of up to
-// kWarpMmaMaxSideSmall rows and 256 < K <= 2048: M*N <= 2^19, or the
-// one-launch dp4a kernel's problems (K <= 512, M*N*K <= 2^28).
+// kWarpMmaMaxSideSmall rows and 256 < K <= 2048: M*N <= 2^19 (2^20 with a
+// side of at most 64 rows and K <= 1024: 64 x 16384 x 512-1024 measured 2-4
+// us faster), or the one-launch dp4a kernel's problems (K <= 512,
+// M*N*K <= 2^28).
 bool warpmma_small_ok(int64_t M, int64_t N, int64_t K, const void* A, const void* B) {
   const int64_t lo = std::min(M, N), hi = std::max(M, N);
-  const bool area = lo * hi <= kWarpMmaMaxArea ||
+  const int64_t max_area = lo <= 64 && K <= 1024 ? 2 * kWarpMmaMaxArea : kWarpMmaMaxArea;
+  const bool area = lo * hi <= max_area ||
                     (K <= kSmallMaxK && (double)M * (double)N * (double)K <= kSmallMaxWork);
   return lo <= kWarpMmaMaxSideSmall && K > 256 && K <= kWarpMmaMaxKSmall && area &&
          K % 16 == 0 && K <= lbg::hmma_skinny_max_k((int)lo) && aligned16(A) && aligned16(B);

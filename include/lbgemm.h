@@ -87,7 +87,8 @@ lbgemm_status lbgemm_variant_info(int bits, int variant, int* tile_m, int* tile_
  * 8-bit problems with min(M, N) <= 32 (and K within the limit of
  * lbgemm_run_warpmma) on the warp-level fp16 MMA kernel, which streams the
  * large operand once; small 8-bit problems with min(M, N) <= 256,
- * 256 < K <= 2048 and either M*N <= 2^19 or (K <= 512 and M*N*K <= 2^28) on
+ * 256 < K <= 2048 and either M*N <= 2^19 (2^20 with min(M, N) <= 64 and
+ * K <= 1024) or (K <= 512 and M*N*K <= 2^28) on
  * the warp-level fp16 MMA kernel too (each 32 rows of the small side re-read
  * the large one); 8-bit problems with K <= 512 and M*N*K <= 2^28 on a
  * one-launch dp4a kernel; 8-bit problems with min(M, N) <= 512,

@@ -187,7 +187,7 @@ def test_int8_warpmma_extremes():
 
 @pytest.mark.parametrize("M,N,K", [(8, 2000, 1024), (32, 700, 2048), (2000, 24, 512),
                                    (3000, 5, 64), (64, 1024, 1024), (4096, 128, 2048),
-                                   (250, 2000, 1040)])
+                                   (250, 2000, 1040), (16000, 64, 1024)])
 def test_int8_warpmma_dispatch(M, N, K):
     """Default dispatch of problems with a side of 5..32 rows, and of small
     problems with a side of up to 256 rows (M*N <= 2^19, K <= 2048)."""
