@@ -661,12 +661,12 @@ bool warpmma_ok(int64_t M, int64_t N, int64_t K, const void* A, const void* B) {
 
 // The same kernel for a small problem with a side of up to
 // kWarpMmaMaxSideSmall rows and 256 < K <= 2048: M*N <= 2^19 (2^20 with a
-// side of at most 64 rows and K <= 1024: 64 x 16384 x 512-1024 measured 2-4
-// us faster), or the one-launch dp4a kernel's problems (K <= 512,
+// side of at most 64 rows and K <= 512: 64 x 16384 x 512 measured 4 us
+// faster), or the one-launch dp4a kernel's problems (K <= 512,
 // M*N*K <= 2^28).
 bool warpmma_small_ok(int64_t M, int64_t N, int64_t K, const void* A, const void* B) {
   const int64_t lo = std::min(M, N), hi = std::max(M, N);
-  const int64_t max_area = lo <= 64 && K <= 1024 ? 2 * kWarpMmaMaxArea : kWarpMmaMaxArea;
+  const int64_t max_area = lo <= 64 && K <= 512 ? 2 * kWarpMmaMaxArea : kWarpMmaMaxArea;
   const bool area = lo * hi <= max_area ||
                     (K <= kSmallMaxK && (double)M * (double)N * (double)K <= kSmallMaxWork);
   return lo <= kWarpMmaMaxSideSmall && K > 256 && K <= kWarpMmaMaxKSmall && area &&
@@ -683,7 +683,18 @@ bool warpmma_small_ok(int64_t M, int64_t N, int64_t K, const void* A, const void
 int fused_route(int64_t M, int64_t N, int64_t K, const void* A, const void* B, int* tile_n) {
   if (K % 16 || !aligned16(A) || !aligned16(B)) return 0;
   const int64_t lo = std::min(M, N), hi = std::max(M, N);
-  if (!(lo <= kFusedMaxSide && hi >= kFusedMinOther && K >= kFusedMinK)) return 0;
+  if (!(lo <= kFusedMaxSide && hi >= kFusedMinOther)) return 0;
+  // Re-measured on GB300 after the re-encoder got faster: with more than 256
+  // rows on the small side and a large side under 4096, K < 4096 runs faster
+  // re-encoded; with K of 1024-2047 the conversion pays once the large side
+  // reaches 8192 rows (16384 with 129-256 on the small side).
+  if (K >= kFusedMinK) {
+    if (lo > 256 && hi < 4096 && K < 4096) return 0;
+  } else if (K >= 1024) {
+    if (hi < 8192 || (lo > 128 && lo <= 256 && hi < 16384)) return 0;
+  } else {
+    return 0;
+  }
   *tile_n = lo <= 64 ? 64 : lo <= 128 ? 128 : 256;
   return M <= N ? 1 : 2;
 }

@@ -88,11 +88,13 @@ lbgemm_status lbgemm_variant_info(int bits, int variant, int* tile_m, int* tile_
  * lbgemm_run_warpmma) on the warp-level fp16 MMA kernel, which streams the
  * large operand once; small 8-bit problems with min(M, N) <= 256,
  * 256 < K <= 2048 and either M*N <= 2^19 (2^20 with min(M, N) <= 64 and
- * K <= 1024) or (K <= 512 and M*N*K <= 2^28) on
+ * K <= 512) or (K <= 512 and M*N*K <= 2^28) on
  * the warp-level fp16 MMA kernel too (each 32 rows of the small side re-read
  * the large one); 8-bit problems with K <= 512 and M*N*K <= 2^28 on a
  * one-launch dp4a kernel; 8-bit problems with min(M, N) <= 512,
- * max(M, N) >= 1024 and K >= 2048 on a tensor-core kernel that converts the
+ * max(M, N) >= 1024 and K >= 2048 (but not min(M, N) > 256 with
+ * max(M, N) < 4096 and K < 4096), or K >= 1024 with max(M, N) >= 8192 (16384
+ * when 128 < min(M, N) <= 256), on a tensor-core kernel that converts the
  * large operand itself (lbgemm_run_fused), with only the small one
  * re-encoded ahead; and 1-bit problems with M*N*K < 2^30 on the
  * XOR-popcount kernel of lbgemm_run_popc.  Scratch memory for the re-encoding is

@@ -81,13 +81,13 @@ def test_int8_small_dp4a_path():
 
 
 @pytest.mark.parametrize("M,N,K", [(64, 4096, 2048), (200, 2500, 2064), (4096, 100, 4096),
-                                   (3000, 256, 2064), (17, 2048, 4096), (500, 1100, 2048),
-                                   (1030, 512, 3008)])
+                                   (3000, 256, 2064), (17, 2048, 4096), (500, 1100, 4096),
+                                   (1030, 512, 3008), (100, 9000, 1040), (8200, 400, 1024)])
 def test_int8_fused_conversion_path(M, N, K):
     """Default dispatch of problems with one side <= 512, the other >= 1024 and
-    K >= 2048: the kernel converts the large int8 operand itself (B when
-    N >= M, giving C transposed from the accumulator); ragged tiles and K
-    tails included."""
+    K >= 2048 (or K >= 1024 with the large side >= 8192): the kernel converts
+    the large int8 operand itself (B when N >= M, giving C transposed from the
+    accumulator); ragged tiles and K tails included."""
     A, B = synth.operands(8, M, N, K, 7 * M + N + K)
     assert_exact(G().gemm(8, A, B, K), oracle.gemm(8, A, B, K), f"int8 fused {M}x{N}x{K}")
 
@@ -187,7 +187,7 @@ def test_int8_warpmma_extremes():
 
 @pytest.mark.parametrize("M,N,K", [(8, 2000, 1024), (32, 700, 2048), (2000, 24, 512),
                                    (3000, 5, 64), (64, 1024, 1024), (4096, 128, 2048),
-                                   (250, 2000, 1040), (16000, 64, 1024)])
+                                   (250, 2000, 1040), (16000, 64, 512)])
 def test_int8_warpmma_dispatch(M, N, K):
     """Default dispatch of problems with a side of 5..32 rows, and of small
     problems with a side of up to 256 rows (M*N <= 2^19, K <= 2048)."""
