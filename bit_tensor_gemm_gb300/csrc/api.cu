@@ -569,9 +569,37 @@ lbgemm_status run_tc_fused(DeviceState& d, bool large_b, int tile_n, int64_t M, 
   // (transposed); both can add split-K partial tiles.
   const bool vec_ok = !large_b && (linear ? (N % 8 == 0) && aligned16(Y)
                                           : (N % 4 == 0) && aligned16(C));
-  // (the tiles of a partial last wave stay whole here: whole-problem splits only)
-  KPlan kpl = plan_k(d, k, 8, rows_l, rows_s, K, linear, vec_ok || large_b);
-  const int splits = kpl.dp_tiles == 0 ? kpl.splits : 1;
+  // K pieces per tile.  The 128 x 256 kernel (compute-bound, one
+  // accumulator): split only a problem of at most half a wave of tiles.  The
+  // 64- and 128-wide kernels stream the int8 operand: as many pieces (up to
+  // 16, at least 4 K slices each) as make the waves of units over the CTA
+  // slots shortest, a unit costing its share of the tile's int8 rows plus
+  // its partial tile of C (4 tile_n bytes per row against K) -- e.g. 128
+  // tiles on 152 slots at K = 16384: 7 pieces (896 units in 6 waves, 6/7 of a
+  // tile each) instead of one wave with 128 of the 152 slots busy (measured
+  // on GB300: 64 x 16384 x 16384, 114 -> 106 us).
+  int splits = 1;
+  if (!linear && (vec_ok || large_b)) {
+    if (tile_n == 256) {
+      KPlan kpl = plan_k(d, k, 8, rows_l, rows_s, K, linear, true);
+      splits = kpl.dp_tiles == 0 ? kpl.splits : 1;
+    } else {
+      const int64_t tiles =
+          ((rows_l + k.tile_m - 1) / k.tile_m) * ((rows_s + tile_n - 1) / tile_n);
+      const int64_t slots = unit_slots(d, k);
+      const int64_t num_kb = (enc_kp(8, K) + 63) / 64;
+      const double c_share = 4.0 * tile_n / (double)K;
+      double best = 1e30;
+      for (int sp = 1; sp <= 16 && (sp == 1 || num_kb / sp >= 4); ++sp) {
+        const int64_t waves = (tiles * sp + slots - 1) / slots;
+        const double cost = (double)waves * (1.0 / sp + (sp > 1 ? c_share : 0.0));
+        if (cost < best - 1e-9) {
+          best = cost;
+          splits = sp;
+        }
+      }
+    }
+  }
   // the encoder also clears C when K is split (partial tiles are added into it)
   lbg::ZeroRect zero;
   if (splits > 1) {
