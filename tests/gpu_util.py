@@ -65,3 +65,18 @@ def sample_positions(M, N, count, seed):
     rows = np.concatenate([g.integers(0, M, count), [0, M - 1, M - 1, 0]])
     cols = np.concatenate([g.integers(0, N, count), [0, N - 1, 0, N - 1]])
     return rows, cols
+
+
+def encoded(bits, A, B, K, variant=-1):
+    """lbgemm_encode of both operands, then lbgemm_run_encoded (the GEMM
+    kernel alone on the re-encoded operands)."""
+    M, N = A.shape[0], B.shape[0]
+    dA, dB = to_dev(A), to_dev(B)
+    eA = torch.empty(L.lbgemm_encoded_size(bits, M, K), dtype=torch.uint8, device=DEV)
+    eB = torch.empty(L.lbgemm_encoded_size(bits, N, K), dtype=torch.uint8, device=DEV)
+    L.lbgemm_encode(bits, M, K, dA, eA)
+    L.lbgemm_encode(bits, N, K, dB, eB)
+    dC = torch.full((M, N), -7, dtype=torch.int32, device=DEV)
+    L.lbgemm_run_encoded(bits, M, N, K, eA, eB, dC, variant)
+    L.lbgemm_device_status()
+    return dC.cpu().numpy()

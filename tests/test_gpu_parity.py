@@ -306,6 +306,32 @@ def test_int8_workspace_entry_matches():
     assert e.value.status == L.ERR_WORKSPACE
 
 
+@pytest.mark.parametrize("bits", [8, 4, 1])
+def test_encode_then_run_encoded(bits):
+    """lbgemm_encode + lbgemm_run_encoded (operands kept re-encoded, e.g.
+    weights): the table's variant and forced ones, few tiles (split K: C is
+    cleared by a memset here, there being no encoder launch), ragged shapes,
+    and a forced split of the last wave."""
+    Ks = {8: (1000, 4104), 4: (1002, 4096), 1: (1024, 8192)}[bits]
+    for i, (M, N) in enumerate([(300, 200), (129, 65), (2500, 2000)]):
+        K = Ks[i % 2]
+        A, B = synth.operands(bits, M, N, K, 60 + 7 * i + bits)
+        want = oracle.gemm(bits, A, B, K)
+        for variant in (-1, 1, 7):
+            assert_exact(G().encoded(bits, A, B, K, variant), want,
+                         f"encoded bits {bits} v{variant} {M}x{N}x{K}")
+    try:
+        L.lbgemm_set_tail_split(2)
+        M, N, K = 2500, 2000, Ks[0]
+        A, B = synth.operands(bits, M, N, K, 90 + bits)
+        want = oracle.gemm(bits, A, B, K)
+        for variant in (2, 5, 8):
+            assert_exact(G().encoded(bits, A, B, K, variant), want,
+                         f"encoded tail split bits {bits} v{variant}")
+    finally:
+        L.lbgemm_set_tail_split(1)
+
+
 def test_int8_host_buffers():
     M, N, K = 96, 160, 640
     A, B = synth.operands(8, M, N, K, 78)
