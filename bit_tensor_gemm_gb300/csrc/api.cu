@@ -1221,11 +1221,14 @@ lbgemm_status lbgemm_time_variants(int bits, int64_t M, int64_t N, int64_t K, co
   return st;
 }
 
-// Row blocks of a host-buffer call: the copies of block i's rows of A in and
-// of block i - 1's rows of C out (each direction on a copy stream of its own)
-// overlap block i's GEMM.  One block below kHostBlockBytes of A or C per block.
-constexpr int64_t kHostBlockBytes = int64_t(64) << 20;
-constexpr int kHostMaxBlocks = 8;
+// Blocks of a host-buffer call: the larger of M and N is cut into blocks of
+// whole 256-row (or 256-column) pieces; the other operand goes in whole
+// first, then each block's slice of the cut operand is copied in, its GEMM
+// runs, and its part of C is copied out, the copies in and out on copy
+// streams of their own so that they overlap each other and the GEMMs.  A
+// block carries about kHostBlockBytes of copies; small problems run as one.
+constexpr int64_t kHostBlockBytes = int64_t(8) << 20;
+constexpr int kHostMaxBlocks = 16;
 
 lbgemm_status host_streams(DeviceState& d) {
   if (d.copy_in) return LBGEMM_OK;
@@ -1262,11 +1265,23 @@ lbgemm_status lbgemm_run_host(int bits, int64_t M, int64_t N, int64_t K, const v
     uint8_t* dA = static_cast<uint8_t*>(d->host_stage.ptr);
     uint8_t* dB = dA + a_bytes;
     int32_t* dC = reinterpret_cast<int32_t*>(dB + b_bytes);
-    // blocks of whole 256-row tiles, as many as the larger of A and C asks for
-    const int64_t big = std::max<int64_t>(M * row_bytes, (int64_t)c_bytes);
-    int64_t nb = std::min<int64_t>((big + kHostBlockBytes - 1) / kHostBlockBytes, kHostMaxBlocks);
-    const int64_t rows = round_up((M + nb - 1) / nb, 256);
-    nb = (M + rows - 1) / rows;
+    // Cut M (rows of A and C) or N (rows of B, columns of C): the operand
+    // copied in whole waits for nothing to overlap it, the copies out overlap
+    // the blocks' copies in.  Column blocks of C leave by 2-D copies, which
+    // keep near full speed while C spans at most 256 MB of host memory and
+    // drop to ~0.6 of it beyond (measured); so columns only where that fits
+    // and the estimate of copy time favours them, or ties with N > M (the
+    // blocks' GEMMs then overlap the copy of the larger operand).
+    const double c_out = 4.0 * (double)M * (double)N;
+    const double t_rows = (double)(N * row_bytes) + std::max((double)(M * row_bytes), c_out);
+    const double t_cols = (double)(M * row_bytes) + std::max((double)(N * row_bytes), 1.15 * c_out);
+    const bool by_rows =
+        c_out > double(int64_t(256) << 20) || t_cols > t_rows || (t_cols == t_rows && M >= N);
+    const int64_t cut = by_rows ? M : N, other = by_rows ? N : M;
+    const int64_t piped = cut * (row_bytes + 4 * other);  // bytes the blocks copy
+    int64_t nb = std::min<int64_t>((piped + kHostBlockBytes - 1) / kHostBlockBytes, kHostMaxBlocks);
+    const int64_t rows = round_up((cut + nb - 1) / nb, 256);
+    nb = (cut + rows - 1) / rows;
     if (nb == 1) {  // small: everything in order on the caller's stream
       cudaError_t e =
           cudaMemcpyAsync(dA, A_host, (size_t)(M * row_bytes), cudaMemcpyHostToDevice, s);
@@ -1282,36 +1297,48 @@ lbgemm_status lbgemm_run_host(int bits, int64_t M, int64_t N, int64_t K, const v
       e = cudaStreamSynchronize(s);
       return e == cudaSuccess ? LBGEMM_OK : cuda_fail(e, "cudaStreamSynchronize");
     }
-    cudaEvent_t* ev = d->host_events.data();  // [0] start, [1] B in, A in[i], C done[i], [last] out
-    cudaEvent_t ev_start = ev[0], ev_b = ev[1], ev_out = ev[2 + 2 * kHostMaxBlocks];
+    cudaEvent_t* ev = d->host_events.data();  // [0] start, [1] whole operand in,
+    // block i in at [2 + i], its GEMM done at [2 + kHostMaxBlocks + i], [last] all out
+    cudaEvent_t ev_start = ev[0], ev_whole = ev[1], ev_out = ev[2 + 2 * kHostMaxBlocks];
+    const uint8_t* cut_host = static_cast<const uint8_t*>(by_rows ? A_host : B_host);
+    uint8_t* cut_dev = by_rows ? dA : dB;
     // the copies start after the caller's earlier work on `s` (the staging
     // buffer's previous user included)
     cudaError_t e = cudaEventRecord(ev_start, s);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(d->copy_in, ev_start, 0);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(d->copy_out, ev_start, 0);
     if (e == cudaSuccess)
-      e = cudaMemcpyAsync(dB, B_host, (size_t)(N * row_bytes), cudaMemcpyHostToDevice, d->copy_in);
-    if (e == cudaSuccess) e = cudaEventRecord(ev_b, d->copy_in);
+      e = by_rows ? cudaMemcpyAsync(dB, B_host, (size_t)(N * row_bytes), cudaMemcpyHostToDevice,
+                                    d->copy_in)
+                  : cudaMemcpyAsync(dA, A_host, (size_t)(M * row_bytes), cudaMemcpyHostToDevice,
+                                    d->copy_in);
+    if (e == cudaSuccess) e = cudaEventRecord(ev_whole, d->copy_in);
     for (int64_t i = 0; e == cudaSuccess && i < nb; ++i) {
-      const int64_t r0 = i * rows, r = std::min(rows, M - r0);
-      e = cudaMemcpyAsync(dA + r0 * row_bytes, static_cast<const uint8_t*>(A_host) + r0 * row_bytes,
+      const int64_t r0 = i * rows, r = std::min(rows, cut - r0);
+      e = cudaMemcpyAsync(cut_dev + r0 * row_bytes, cut_host + r0 * row_bytes,
                           (size_t)(r * row_bytes), cudaMemcpyHostToDevice, d->copy_in);
       if (e == cudaSuccess) e = cudaEventRecord(ev[2 + i], d->copy_in);
     }
     if (e != cudaSuccess) return cuda_fail(e, "host-to-device copy");
-    e = cudaStreamWaitEvent(s, ev_b, 0);
+    e = cudaStreamWaitEvent(s, ev_whole, 0);
     for (int64_t i = 0; e == cudaSuccess && i < nb; ++i) {
-      const int64_t r0 = i * rows, r = std::min(rows, M - r0);
+      const int64_t r0 = i * rows, r = std::min(rows, cut - r0);
       e = cudaStreamWaitEvent(s, ev[2 + i], 0);
       if (e != cudaSuccess) break;
-      st = run_any(bits, r, N, K, dA + r0 * row_bytes, dB, dC + r0 * N, variant, nullptr, 0, true,
-                   s);
+      // a column block's C (M x r) is dense on the device at dC + r0 * M
+      st = by_rows ? run_any(bits, r, N, K, dA + r0 * row_bytes, dB, dC + r0 * N, variant,
+                             nullptr, 0, true, s)
+                   : run_any(bits, M, r, K, dA, dB + r0 * row_bytes, dC + r0 * M, variant,
+                             nullptr, 0, true, s);
       if (st != LBGEMM_OK) return st;
       e = cudaEventRecord(ev[2 + kHostMaxBlocks + i], s);
       if (e == cudaSuccess) e = cudaStreamWaitEvent(d->copy_out, ev[2 + kHostMaxBlocks + i], 0);
-      if (e == cudaSuccess)
-        e = cudaMemcpyAsync(C_host + r0 * N, dC + r0 * N, (size_t)(r * N * 4),
-                            cudaMemcpyDeviceToHost, d->copy_out);
+      if (e != cudaSuccess) break;
+      e = by_rows ? cudaMemcpyAsync(C_host + r0 * N, dC + r0 * N, (size_t)(r * N * 4),
+                                    cudaMemcpyDeviceToHost, d->copy_out)
+                  : cudaMemcpy2DAsync(C_host + r0, (size_t)(N * 4), dC + r0 * M, (size_t)(r * 4),
+                                      (size_t)(r * 4), (size_t)M, cudaMemcpyDeviceToHost,
+                                      d->copy_out);
     }
     if (e == cudaSuccess) e = cudaEventRecord(ev_out, d->copy_out);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(s, ev_out, 0);

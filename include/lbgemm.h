@@ -286,12 +286,13 @@ lbgemm_status lbgemm_time_variants(int bits, int64_t M, int64_t N, int64_t K, co
 /* Host-buffer convenience, for callers whose operands live in host memory:
  * copies A and B to device staging buffers that the library owns (grown with
  * cudaMalloc on demand), runs lbgemm_run_variant, copies C back to the host
- * buffer and synchronises `stream`.  When A or C passes 64 MB the problem runs
- * in blocks of rows of A and C (whole 256-row tiles, up to 8 blocks): B and
- * the blocks of A are copied in on one library-owned stream, the blocks of C
- * out on another, each block's GEMM on `stream` between its copies, so the
- * two copy directions and the GEMMs overlap.  Pinned host memory gives the
- * fastest copies.  Not for use under stream capture. */
+ * buffer and synchronises `stream`.  Problems that copy more than 8 MB run in
+ * blocks (up to 16) of the larger of M and N, each of whole 256-row (or
+ * 256-column) pieces: the other operand is copied in whole, then each block's
+ * rows of A (or B) on one library-owned stream, its GEMM on `stream`, and its
+ * rows (or columns, by a 2-D copy) of C out on another library-owned stream,
+ * so the two copy directions and the GEMMs overlap.  Pinned host memory gives
+ * the fastest copies.  Not for use under stream capture. */
 lbgemm_status lbgemm_run_host(int bits, int64_t M, int64_t N, int64_t K, const void* A_host,
                               const void* B_host, int32_t* C_host, int variant, void* stream);
 
