@@ -163,11 +163,18 @@ lbgemm_status scratch_acquire(Scratch& s, size_t bytes, cudaStream_t stream) {
   if (s.bytes < bytes) {
     cudaError_t e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize (scratch growth)");
+    // grow by at least half again, so that a run of ever larger problems
+    // reallocates a logarithmic number of times (exactly `bytes` if that fails)
+    size_t want = std::max<size_t>({bytes, size_t(1) << 20, s.bytes + s.bytes / 2});
     if (s.ptr) cudaFree(s.ptr);
     s.ptr = nullptr;
     s.bytes = 0;
-    size_t want = std::max<size_t>(bytes, size_t(1) << 20);
     e = cudaMalloc(&s.ptr, want);
+    if (e == cudaErrorMemoryAllocation && want > bytes) {
+      cudaGetLastError();  // clear the failed attempt
+      want = bytes;
+      e = cudaMalloc(&s.ptr, want);
+    }
     if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc (scratch)");
     s.bytes = want;
     s.used = false;

@@ -98,7 +98,8 @@ lbgemm_status lbgemm_variant_info(int bits, int variant, int* tile_m, int* tile_
  * large operand itself (lbgemm_run_fused), with only the small one
  * re-encoded ahead; and 1-bit problems with M*N*K < 2^30 on the
  * XOR-popcount kernel of lbgemm_run_popc.  Scratch memory for the re-encoding is
- * taken from a per-device buffer the library grows with cudaMalloc on demand;
+ * taken from a per-device buffer the library grows with cudaMalloc on demand
+ * (by at least half again each time);
  * calls from different streams are ordered on it with events.  A call that
  * grows the buffer synchronises the device, so make the first call of the
  * largest shape before capturing a CUDA graph, or use lbgemm_run_ws. */
