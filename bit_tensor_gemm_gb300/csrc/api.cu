@@ -620,14 +620,16 @@ lbgemm_status run_tc_fused(DeviceState& d, bool large_b, int tile_n, int64_t M, 
   CUtensorMap ml, ms;
   cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows_l};
   cuuint64_t strides[1] = {(cuuint64_t)K};
-  // the 256-wide kernel stages 128-element boxes (128-byte swizzle), the
-  // others 64-element boxes (64-byte swizzle)
+  // the int8 operand is staged in 128-element boxes (128-byte swizzle); the
+  // 256-wide kernel steps through K in 64-element slices, the others in
+  // 128-element slices
   const bool pairs = tile_n == 256;
-  cuuint32_t box[2] = {pairs ? 128u : 64u, 128};
+  const int slice = pairs ? 64 : 128;
+  cuuint32_t box[2] = {128u, 128};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = g_encode(&ml, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(opl), dims,
                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        pairs ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                        CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(LBGEMM_ERR_CUDA, "cuTensorMapEncodeTiled (int8) failed (%d)", (int)r);
   st = encode_kmajor(&ms, ws, rows_s, kp, true, tile_n);
@@ -636,8 +638,8 @@ lbgemm_status run_tc_fused(DeviceState& d, bool large_b, int tile_n, int64_t M, 
   p.M = (int)rows_l;
   p.N = (int)rows_s;
   p.K = (int)K;
-  p.num_kb = (int)((kp + 63) / 64);
-  p.chunk_kb = std::max(1, g_chunk_s8.load() / 64);
+  p.num_kb = (int)((kp + slice - 1) / slice);
+  p.chunk_kb = std::max(1, g_chunk_s8.load() / slice);
   if (pairs) p.chunk_kb = std::max(4, p.chunk_kb & ~3);  // whole groups of 4 slices
   p.tiles_m = (int)((rows_l + 127) / 128);
   p.tiles_n = (int)((rows_s + tile_n - 1) / tile_n);

@@ -14,20 +14,27 @@
 // 2 bytes by the GEMM: for a problem whose operands are large next to its
 // arithmetic that is most of the time.  Here the MMA's A operand (the "L"
 // operand, 128 rows per tile) stays int8 in global memory:
-//   - TMA copies each 64-element K slice of its 128 rows (8 KB, 64-byte rows
-//     with the 64-byte swizzle) into a deep staging ring in shared memory;
+//   - TMA copies each 128-element K slice of its 128 rows (16 KB, 128-byte
+//     rows with the 128-byte swizzle) into a staging ring in shared memory;
 //   - four converter warps, one per 32-lane quarter of tensor memory, read
 //     their rows (thread t of quarter q owns row 32q + t; with the swizzle the
-//     32 threads' 16-byte reads hit distinct banks), turn the 64 int8 values
-//     into 32 words of packed fp16 (exact: the fp16 with bits 0x6400 | (v+128)
+//     32 threads' 16-byte reads hit distinct banks), turn the 128 int8 values
+//     into 64 words of packed fp16 (exact: the fp16 with bits 0x6400 | (v+128)
 //     is 1024 + v + 128, minus 1152 gives v) and store them with tcgen05.st
-//     into a ring of 32-column slots of tensor memory;
+//     into a ring of 64-column slots of tensor memory;
 //   - the MMA thread issues tcgen05.mma with A read from tensor memory and B
 //     (the "S" operand, BN rows, re-encoded to fp16 ahead by the library's
 //     pass) read from shared memory.
 // Compared with converting into shared memory (the operand tile would be
 // written as fp16 and read again by the MMA), the tensor-memory route moves
-// 8 KB instead of 40 KB of shared memory per 128-row K slice.
+// 16 KB instead of 80 KB of shared memory per 128-row K slice.
+//
+// Slice size.  Every slice costs each role a fixed number of barrier
+// operations (a wait for the int8 data, a wait for the freed slot, arrivals,
+// a commit) of roughly 100 cycles each on GB300; instrumented, the roles of
+// the 64-element version spent ~1000 cycles per slice, of which the MMAs
+// (four of 128 x BN x 16) and the conversion were only a third.  128-element
+// slices halve those operations per byte.
 //
 // Output.  D's lane i and column j hold the sum for L-row i and S-row j.
 // TRANS = false: L is the GEMM's A, S its B, C[i][j] as in tc_gemm_kernel
@@ -37,7 +44,7 @@
 // of its stores writes 128 contiguous bytes (red.add under split K).
 //
 // Tensor memory: two fp32 accumulators of BN columns (alternating per K chunk,
-// as in tc_gemm_kernel), then STAGES slots of 32 columns for A.
+// as in tc_gemm_kernel), then STAGES slots of 64 columns for A.
 //
 // Roles (448 threads):
 //   warp 0 lane 0   TMA producer of the int8 staging ring (L operand)
@@ -56,7 +63,7 @@ namespace lbg {
 
 constexpr int kTsConvWarps = 4;
 constexpr int kTsThreads = 32 * (2 + kTcEpiWarps + kTsConvWarps);  // 448
-constexpr int kTsStgStages = 8;
+constexpr int kTsSliceK = 128;  // K elements per slice (one staging stage, one A slot)
 
 __host__ __device__ constexpr int ts_tmem_cols(int need) {
   return need <= 32 ? 32 : need <= 64 ? 64 : need <= 128 ? 128 : need <= 256 ? 256 : 512;
@@ -64,16 +71,20 @@ __host__ __device__ constexpr int ts_tmem_cols(int need) {
 
 template <int BN, int STAGES>
 struct TsLayout {
-  static constexpr int kSBytes = BN * 128;  // one 64-element fp16 K slice of BN rows
+  // one slice of the S operand: two 64-element fp16 boxes (128-byte rows,
+  // 128-byte swizzle) of BN rows each
+  static constexpr int kSBoxBytes = BN * 128;
+  static constexpr int kSBytes = 2 * kSBoxBytes;
   static constexpr int kRingBytes = kSBytes * STAGES;
   static constexpr int kEpiOffset = kRingBytes;
   static constexpr int kEpiBytes = kTcEpiWarps * 32 * 128;
   static constexpr int kStgOffset = kEpiOffset + kEpiBytes;
-  static constexpr int kStgStageBytes = kTcBM * 64;  // 128 rows x 64 int8
-  static constexpr int kStgBytes = kStgStageBytes * kTsStgStages;
+  static constexpr int kStgStages = STAGES;
+  static constexpr int kStgStageBytes = kTcBM * kTsSliceK;  // 128 rows x 128 int8
+  static constexpr int kStgBytes = kStgStageBytes * kStgStages;
   // barriers: full[S], empty[S], conv[S], acc_full[2], acc_empty[2], mma_done,
   // stg_full[SS], stg_empty[SS]
-  static constexpr int kNumBars = 3 * STAGES + 5 + 2 * kTsStgStages;
+  static constexpr int kNumBars = 3 * STAGES + 5 + 2 * kStgStages;
   static constexpr int kBarOffset = kStgOffset + kStgBytes;
   static constexpr int kTmemSlotOffset = kBarOffset + 8 * kNumBars;
   static constexpr int kAbortOffset = kTmemSlotOffset + 4;
@@ -81,8 +92,10 @@ struct TsLayout {
   static constexpr int kDynSmem = kUsedBytes + 1024;  // slack to align the ring to 1024
   static constexpr int kAccCols = 2 * BN;
   static constexpr int kACol0 = kAccCols;  // first column of the A slots
-  static constexpr int kTmemCols = ts_tmem_cols(kAccCols + 32 * STAGES);
-  static_assert(kAccCols + 32 * STAGES <= 512, "tensor memory holds 512 columns");
+  static constexpr int kASlotCols = kTsSliceK / 2;  // packed fp16 pairs per row
+  static constexpr int kTmemCols = ts_tmem_cols(kAccCols + kASlotCols * STAGES);
+  static_assert(kAccCols + kASlotCols * STAGES <= 512, "tensor memory holds 512 columns");
+  static_assert(kDynSmem <= 232448, "shared memory per CTA");
 };
 
 template <int BN, int STAGES, bool TRANS, bool LINEAR>
@@ -90,7 +103,7 @@ __global__ void __launch_bounds__(kTsThreads, 1)
     tc_ts_kernel(const __grid_constant__ CUtensorMap tmL, const __grid_constant__ CUtensorMap tmS,
                  const __grid_constant__ CUtensorMap tmC, const TcParams p) {
   using L = TsLayout<BN, STAGES>;
-  constexpr int SS = kTsStgStages;
+  constexpr int SS = L::kStgStages;
   constexpr uint32_t kIdesc = instr_desc(kTcBM, BN);
   constexpr int kGroups = BN / 2 / 32;  // 32-column groups per epilogue thread
 
@@ -161,7 +174,7 @@ __global__ void __launch_bounds__(kTsThreads, 1)
           }
           const uint32_t st = sbase + L::kStgOffset + stage * L::kStgStageBytes;
           mbar_arrive_expect_tx(stgf_bar(stage), L::kStgStageBytes);
-          tma_load_2d(st, &tmL, stgf_bar(stage), kb * 64, tm * kTcBM);
+          tma_load_2d(st, &tmL, stgf_bar(stage), kb * kTsSliceK, tm * kTcBM);
           ++issued;
           if (++stage == SS) {
             stage = 0;
@@ -211,13 +224,15 @@ __global__ void __launch_bounds__(kTsThreads, 1)
               break;
             }
             tc_fence_after();
-            const uint64_t bdesc = smem_desc_sw128(sbase + stage * L::kSBytes);
-            const uint32_t a_tmem = tmem_base + L::kACol0 + stage * 32;
+            const uint32_t s_addr = sbase + stage * L::kSBytes;
+            const uint32_t a_tmem = tmem_base + L::kACol0 + stage * L::kASlotCols;
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              // K = 16 per MMA: 8 columns of A, 32 bytes (2 x 16 B) of each B row
+            for (int k = 0; k < kTsSliceK / 16; ++k) {
+              // K = 16 per MMA: 8 columns of A, 32 bytes (2 x 16 B) of each B
+              // row, in the first or second 64-element box of the slice
+              const uint64_t bdesc = smem_desc_sw128(s_addr + (k >> 2) * L::kSBoxBytes);
               const uint32_t accumulate = (kb > kb0 || k > 0) ? 1u : 0u;
-              mma_f16_ts(d_tmem, a_tmem + 8 * k, bdesc + 2 * k, kIdesc, accumulate);
+              mma_f16_ts(d_tmem, a_tmem + 8 * k, bdesc + 2 * (k & 3), kIdesc, accumulate);
             }
             mma_commit(empty_bar(stage));
             if (++stage == STAGES) {
@@ -242,11 +257,12 @@ __global__ void __launch_bounds__(kTsThreads, 1)
       // been launched as a dependent of: wait for it before the first load.
       asm volatile("griddepcontrol.wait;" ::: "memory");
     }
-    // 64-byte swizzle: 16-byte chunk q of row r sits at chunk q ^ ((r / 2) % 4)
-    const int swz = (row >> 1) & 3;
-    // The slices this CTA converts, in order: (unit w, slice kb).  Software
-    // pipeline: slice i+1 is waited for, loaded and converted while the
-    // tensor-memory store of slice i is in flight.
+    // 128-byte swizzle: 16-byte chunk q of row r sits at chunk q ^ (r % 8)
+    const int swz = row & 7;
+    // The slices this CTA converts, in order: (unit w, slice kb), each in two
+    // halves of 64 elements.  Software pipeline: the next half is waited
+    // for (at a slice's start), loaded and converted while the tensor-memory
+    // store of the previous half is in flight.
     int w = (int)blockIdx.x - (int)gridDim.x;  // the unit before this CTA's first
     int kb = 0, kbe = 0, tn = 0;
     auto advance = [&]() -> bool {  // next slice into (kb, tn); false at the end
@@ -268,14 +284,16 @@ __global__ void __launch_bounds__(kTsThreads, 1)
     uint32_t lph = 0;
     int64_t issued = 0;
     // wait until slot (os, ss) may be written and its int8 data has landed;
-    // the loader also fills the S operand of stage os
+    // the loader also fills the S operand of stage os (two boxes)
     auto acquire = [&]() -> bool {
       int got = 1;
       if (lane == 0) {
         got = mbar_wait(empty_bar(os), oph ^ 1u, abort_flag, p.status);
         if (got && loader) {
+          const uint32_t dst = sbase + os * L::kSBytes;
           mbar_arrive_expect_tx(full_bar(os), L::kSBytes);
-          tma_load_2d(sbase + os * L::kSBytes, &tmS, full_bar(os), kb * 64, tn * BN);
+          tma_load_2d(dst, &tmS, full_bar(os), kb * kTsSliceK, tn * BN);
+          tma_load_2d(dst + L::kSBoxBytes, &tmS, full_bar(os), kb * kTsSliceK + 64, tn * BN);
           ++issued;
           if (++ls == STAGES) {
             ls = 0;
@@ -286,11 +304,12 @@ __global__ void __launch_bounds__(kTsThreads, 1)
       }
       return __shfl_sync(0xffffffffu, got, 0) != 0;
     };
-    auto convert = [&](uint32_t (&words)[32]) {
-      const uint8_t* src = smem + L::kStgOffset + ss * L::kStgStageBytes + row * 64;
+    // half h (64 elements, 32 words) of this thread's row of staging slot ss
+    auto convert = [&](int h, uint32_t (&words)[32]) {
+      const uint8_t* src = smem + L::kStgOffset + ss * L::kStgStageBytes + row * kTsSliceK;
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        const int4 v = *reinterpret_cast<const int4*>(src + ((q ^ swz) << 4));
+        const int4 v = *reinterpret_cast<const int4*>(src + (((4 * h + q) ^ swz) << 4));
         uint4 lo, hi;
         s8x16_to_f16(v, lo, hi);
         words[8 * q + 0] = lo.x;
@@ -308,11 +327,19 @@ __global__ void __launch_bounds__(kTsThreads, 1)
     uint32_t cur[32], nxt[32];
     if (have) {
       ok = acquire();
-      if (ok) convert(cur);
+      if (ok) convert(0, cur);
     }
     while (ok && have) {
+      // first half of the slice: store it, convert the second meanwhile
+      const uint32_t slot = tmem_base + lane_addr + L::kACol0 + os * L::kASlotCols;
+      tmem_st32(slot, cur);
+      convert(1, nxt);
+      tmem_st_wait();
+#pragma unroll
+      for (int j = 0; j < 32; ++j) cur[j] = nxt[j];
+      // second half: store it, start the next slice meanwhile
+      tmem_st32(slot + 32, cur);
       const int st_os = os, st_ss = ss;
-      tmem_st32(tmem_base + lane_addr + L::kACol0 + st_os * 32, cur);
       if (++os == STAGES) {
         os = 0;
         oph ^= 1u;
@@ -324,7 +351,7 @@ __global__ void __launch_bounds__(kTsThreads, 1)
       have = advance();
       if (have) {
         ok = acquire();
-        if (ok) convert(nxt);
+        if (ok) convert(0, nxt);
       }
       tmem_st_wait();
       tc_fence_before();
