@@ -56,7 +56,6 @@ constexpr int64_t kSmallMaxK = 512;
 // 8-bit problems on the in-kernel-conversion kernel (see fused_route).
 constexpr int64_t kFusedMaxSide = 512;
 constexpr int64_t kFusedMinOther = 1024;
-constexpr int64_t kFusedMinK = 2048;
 // Small side of the warp-level fp16 MMA kernel (hmma_skinny.cu): any problem
 // up to kWarpMmaMaxSide rows; with more rows (up to kWarpMmaMaxSideSmall,
 // each 32 rows re-reading the large operand) only small problems with
@@ -703,7 +702,9 @@ bool warpmma_ok(int64_t M, int64_t N, int64_t K, const void* A, const void* B) {
 // M*N*K <= 2^28).
 bool warpmma_small_ok(int64_t M, int64_t N, int64_t K, const void* A, const void* B) {
   const int64_t lo = std::min(M, N), hi = std::max(M, N);
-  const int64_t max_area = lo <= 64 && K <= 512 ? 2 * kWarpMmaMaxArea : kWarpMmaMaxArea;
+  // past 1024 of K, half the area: the in-kernel conversion kernel with
+  // 128-element slices is faster there (e.g. 64 x 8192 x 2048: 21.1 -> 17.1 us)
+  const int64_t max_area = K <= 1024 ? kWarpMmaMaxArea : kWarpMmaMaxArea / 2;
   const bool area = lo * hi <= max_area ||
                     (K <= kSmallMaxK && (double)M * (double)N * (double)K <= kSmallMaxWork);
   return lo <= kWarpMmaMaxSideSmall && K > 256 && K <= kWarpMmaMaxKSmall && area &&
@@ -712,27 +713,29 @@ bool warpmma_small_ok(int64_t M, int64_t N, int64_t K, const void* A, const void
 
 // Route of the in-kernel-conversion kernel for an 8-bit problem (1: B is
 // converted in the kernel, 2: A is; 0: re-encode both) and its tile width
-// along the re-encoded operand.  Measured on GB300 over the 729-shape grid:
-// with the small side <= 512, the large side >= 1024 and K >= 2048, skipping
-// the large operand's re-encoding pass wins (e.g. 512 x 8192 x 8192: 101 ->
-// 81 us; 256 x 16384 x 16384: 275 -> 146 us); the tile is the narrowest that
-// covers the small side (64, 128, else 256).
+// along the re-encoded operand.  Measured on GB300 over the grid of small
+// side 64-512, large side 1024-16384 and K 512-16384 (both orientations),
+// against re-encoding and the warp-MMA kernel: skipping the large operand's
+// re-encoding pass wins once the large side reaches 4096 rows, at K >= 4096
+// from 2048 rows, at K >= 8192 from 1024, and with at most 256 rows on the
+// small side from K = 2048 (e.g. 512 x 4096 x 1024: 17.0 -> 15.0 us;
+// 256 x 8192 x 2048: 27.3 -> 21.1 us; 256 x 16384 x 16384: 275 -> 146 us).
+// The tile: 64 up to 64 rows, else 128, but 256 (CTA pairs) for a small side
+// of 129-256 or 385-512 rows with the large side and K both large, where the
+// pairs' shared re-encoded tile pays.
 int fused_route(int64_t M, int64_t N, int64_t K, const void* A, const void* B, int* tile_n) {
   if (K % 16 || !aligned16(A) || !aligned16(B)) return 0;
   const int64_t lo = std::min(M, N), hi = std::max(M, N);
-  if (!(lo <= kFusedMaxSide && hi >= kFusedMinOther)) return 0;
-  // Re-measured on GB300 after the re-encoder got faster: with more than 256
-  // rows on the small side and a large side under 4096, K < 4096 runs faster
-  // re-encoded; with K of 1024-2047 the conversion pays once the large side
-  // reaches 8192 rows (16384 with 129-256 on the small side).
-  if (K >= kFusedMinK) {
-    if (lo > 256 && hi < 4096 && K < 4096) return 0;
-  } else if (K >= 1024) {
-    if (hi < 8192 || (lo > 128 && lo <= 256 && hi < 16384)) return 0;
-  } else {
-    return 0;
-  }
-  *tile_n = lo <= 64 ? 64 : lo <= 128 ? 128 : 256;
+  if (!(lo <= kFusedMaxSide && hi >= kFusedMinOther) || K < 512) return 0;
+  const bool go =
+      hi >= 4096 || K >= 8192 || (hi >= 2048 && K >= 4096) || (lo <= 256 && K >= 2048);
+  if (!go) return 0;
+  bool pairs = false;
+  if (lo > 128 && lo <= 256)
+    pairs = (hi >= 16384 && K >= 1024) || (hi >= 8192 && K >= 16384);
+  else if (lo > 384)
+    pairs = (hi >= 8192 && K >= 2048) || (hi >= 16384 && K >= 1024) || K >= 16384;
+  *tile_n = lo <= 64 ? 64 : pairs ? 256 : 128;
   return M <= N ? 1 : 2;
 }
 

@@ -87,16 +87,15 @@ lbgemm_status lbgemm_variant_info(int bits, int variant, int* tile_m, int* tile_
  * 8-bit problems with min(M, N) <= 32 (and K within the limit of
  * lbgemm_run_warpmma) on the warp-level fp16 MMA kernel, which streams the
  * large operand once; small 8-bit problems with min(M, N) <= 256,
- * 256 < K <= 2048 and either M*N <= 2^19 (2^20 with min(M, N) <= 64 and
- * K <= 512) or (K <= 512 and M*N*K <= 2^28) on
+ * 256 < K <= 2048 and either M*N <= 2^19 (2^18 with K > 1024) or
+ * (K <= 512 and M*N*K <= 2^28) on
  * the warp-level fp16 MMA kernel too (each 32 rows of the small side re-read
  * the large one); 8-bit problems with K <= 512 and M*N*K <= 2^28 on a
  * one-launch dp4a kernel; 8-bit problems with min(M, N) <= 512,
- * max(M, N) >= 1024 and K >= 2048 (but not min(M, N) > 256 with
- * max(M, N) < 4096 and K < 4096), or K >= 1024 with max(M, N) >= 8192 (16384
- * when 128 < min(M, N) <= 256), on a tensor-core kernel that converts the
- * large operand itself (lbgemm_run_fused), with only the small one
- * re-encoded ahead; and 1-bit problems with M*N*K < 2^30 on the
+ * max(M, N) >= 1024, K >= 512 and one of max(M, N) >= 4096, K >= 8192,
+ * (max(M, N) >= 2048 and K >= 4096) or (min(M, N) <= 256 and K >= 2048),
+ * on a tensor-core kernel that converts the large operand itself
+ * (lbgemm_run_fused), with only the small one re-encoded ahead; and 1-bit problems with M*N*K < 2^30 on the
  * XOR-popcount kernel of lbgemm_run_popc.  Scratch memory for the re-encoding is
  * taken from a per-device buffer the library grows with cudaMalloc on demand
  * (by at least half again each time);
@@ -206,8 +205,9 @@ lbgemm_status lbgemm_run_popc(int64_t M, int64_t N, int64_t K, const uint32_t* A
  * row-major, passed as void* (2 bytes per element).  The scale product is
  * formed in fp32, left to right.  K <= 131071.  The shape rules of
  * lbgemm_run apply: M <= 4 on the dp4a kernel that streams W once, M <= 32
- * on the warp-level fp16 MMA kernel, M <= 512 (N >= 1024, K >= 2048) on the
- * kernel that converts W itself, larger M on the tensor-core variant table. */
+ * on the warp-level fp16 MMA kernel, M <= 512 (with N >= 1024 and N, K as
+ * lbgemm_run says) on the kernel that converts W itself, larger M on the
+ * tensor-core variant table. */
 lbgemm_status lbgemm_linear(int64_t M, int64_t N, int64_t K, const int8_t* X, const float* sx,
                             const int8_t* W, const float* sw, void* Y, void* stream);
 

@@ -82,12 +82,16 @@ def test_int8_small_dp4a_path():
 
 @pytest.mark.parametrize("M,N,K", [(64, 4096, 2048), (200, 2500, 2064), (4096, 100, 4096),
                                    (3000, 256, 2064), (17, 2048, 4096), (500, 1100, 4096),
-                                   (1030, 512, 3008), (100, 9000, 1040), (8200, 400, 1024)])
+                                   (1030, 512, 3008), (100, 9000, 1040), (8200, 400, 1024),
+                                   (512, 4096, 512), (300, 5000, 1024), (64, 8192, 2048),
+                                   (400, 8192, 2048), (1100, 200, 8192)])
 def test_int8_fused_conversion_path(M, N, K):
-    """Default dispatch of problems with one side <= 512, the other >= 1024 and
-    K >= 2048 (or K >= 1024 with the large side >= 8192): the kernel converts
-    the large int8 operand itself (B when N >= M, giving C transposed from the
-    accumulator); ragged tiles and K tails included."""
+    """Default dispatch of problems with one side <= 512, the other >= 1024
+    and K >= 512 in the conversion kernel's domain (large side >= 4096, or
+    K >= 8192, or large side >= 2048 with K >= 4096, or small side <= 256
+    with K >= 2048): the kernel converts the large int8 operand itself (B
+    when N >= M, giving C transposed from the accumulator), on 64-, 128- or
+    256-wide tiles; ragged tiles and K tails included."""
     A, B = synth.operands(8, M, N, K, 7 * M + N + K)
     assert_exact(G().gemm(8, A, B, K), oracle.gemm(8, A, B, K), f"int8 fused {M}x{N}x{K}")
 
@@ -451,11 +455,12 @@ def test_linear_warpmma_route(M):
     check_linear(G().linear(X, sx, W, sw), ref, acc == 0, f"linear warp-MMA M={M}")
 
 
-@pytest.mark.parametrize("M", [33, 128, 300])
-def test_linear_fused_route(M):
-    """Token counts 17..512 with N >= 1024 and K >= 2048: the weights are
-    converted in the kernel and Y is written transposed from the accumulator."""
-    N, K = 2100, 4096
+@pytest.mark.parametrize("M,N,K", [(33, 2100, 4096), (128, 2100, 4096), (300, 2100, 4096),
+                                   (450, 8200, 2048)])
+def test_linear_fused_route(M, N, K):
+    """Token counts 33..512 in the conversion kernel's domain: the weights are
+    converted in the kernel and Y is written transposed from the accumulator
+    (128-wide tiles, and CTA pairs with 450 tokens)."""
     X, sx, W, sw = synth.linear_operands(M, N, K, 600 + M)
     X[1, :] = 0
     ref = oracle.linear(X, sx, W, sw)
