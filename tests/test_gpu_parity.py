@@ -456,11 +456,11 @@ def test_linear_warpmma_route(M):
 
 
 @pytest.mark.parametrize("M,N,K", [(33, 2100, 4096), (128, 2100, 4096), (300, 2100, 4096),
-                                   (450, 8200, 2048)])
+                                   (450, 8200, 2048), (40, 2102, 4096), (128, 11008, 4096)])
 def test_linear_fused_route(M, N, K):
     """Token counts 33..512 in the conversion kernel's domain: the weights are
     converted in the kernel and Y is written transposed from the accumulator
-    (128-wide tiles, and CTA pairs with 450 tokens)."""
+    (128-wide tiles, and CTA pairs with 450 tokens; N % 4 != 0 included)."""
     X, sx, W, sw = synth.linear_operands(M, N, K, 600 + M)
     X[1, :] = 0
     ref = oracle.linear(X, sx, W, sw)
