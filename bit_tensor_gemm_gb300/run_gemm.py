@@ -13,7 +13,8 @@ against a reference here; the tests do that.
 operand itself (lbgemm_run_fused); --warpmma the warp-level fp16 MMA kernel
 for a small side (lbgemm_run_warpmma); without these the library's own
 dispatch runs (lbgemm_run).  --encoded re-encodes A and B once and times only the GEMM
-kernel (lbgemm_run_encoded).  --linear runs lbgemm_linear (bits 8).
+kernel (lbgemm_run_encoded).  --linear runs lbgemm_linear (bits 8).  --popc
+runs the 1-bit XOR-popcount kernel (lbgemm_run_popc, bits 1).
 """
 from __future__ import annotations
 
@@ -34,6 +35,8 @@ def main(argv=None) -> int:
     ap.add_argument("--warpmma", action="store_true",
                     help="run lbgemm_run_warpmma (small side <= 32 rows)")
     ap.add_argument("--linear", action="store_true")
+    ap.add_argument("--popc", action="store_true",
+                    help="run lbgemm_run_popc (bits 1) with the default tile and stages")
     ap.add_argument("--reps", type=int, default=2)
     ap.add_argument("--seed", type=int, default=1)
     a = ap.parse_args(argv)
@@ -74,6 +77,12 @@ def main(argv=None) -> int:
         elif a.warpmma:
             def call():
                 L.lbgemm_run_warpmma(M, N, K, dA, dB, C)
+        elif a.popc:
+            if a.bits != 1:
+                ap.error("--popc needs --bits 1")
+
+            def call():
+                L.lbgemm_run_popc(M, N, K, dA, dB, C)
         elif a.fused:
             def call():
                 L.lbgemm_run_fused(M, N, K, dA, dB, C, a.fused)
