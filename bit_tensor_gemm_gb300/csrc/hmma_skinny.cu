@@ -110,6 +110,10 @@ __global__ void __launch_bounds__(kHmWarps * 32)
                        const float* __restrict__ sw, __nv_bfloat16* __restrict__ Y,
                        int chunk_steps, int U, int KP) {
   constexpr int NACC = 4 / MT;  // independent accumulators per (m tile, n8 tile)
+  // launched as a programmatic dependent: X (and its scales) may come from
+  // the grid before this one (the activation quantiser), which may still be
+  // running; wait for it before the first read
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   extern __shared__ int4 hm_smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
@@ -301,10 +305,18 @@ cudaError_t hmma_go(const int8_t* X, const int8_t* W, int MX, int NW, int K, int
   const int KP = kHmWarps / U;
   const int gx = (units + U - 1) / U < ctas ? (units + U - 1) / U : ctas;
   const int chunk_steps = chunk_elems / kHmStep > 0 ? chunk_elems / kHmStep : 1;
-  kern<<<dim3(gx, m_blocks), kHmWarps * 32, smem, s>>>(X, W, MX, NW, K, C, sx, sw,
-                                                        static_cast<__nv_bfloat16*>(Y),
-                                                        chunk_steps, U, KP);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(gx, m_blocks);
+  cfg.blockDim = dim3(kHmWarps * 32);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, X, W, MX, NW, K, C, sx, sw,
+                            static_cast<__nv_bfloat16*>(Y), chunk_steps, U, KP);
 }
 
 template <bool TRANS, bool LINEAR>

@@ -39,6 +39,32 @@ __device__ __forceinline__ void allow_dependent_launch() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// A kernel launched as a programmatic dependent may start while the grid
+// before it in the stream is still running: it waits for that grid (and its
+// memory operations) here before its first access to global memory.
+__device__ __forceinline__ void wait_prior_grid() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Launch with programmatic stream serialisation: the kernel may be scheduled
+// as soon as the previous grid in the stream has let dependents launch; the
+// kernel itself must call wait_prior_grid() before touching global memory.
+template <typename... KArgs, typename... Args>
+static cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                    cudaStream_t s, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // Clears the rectangle z of an int32 matrix, grid-stride over the whole grid;
 // 16-byte stores when the rows and columns allow.
 __device__ __forceinline__ void zero_rect(const ZeroRect& z) {
@@ -65,6 +91,7 @@ __device__ __forceinline__ void zero_rect(const ZeroRect& z) {
 // int8 -> fp16; each thread writes 8 halves (16 bytes).
 __global__ void cvt_s8_f16_kernel(CvtJob ja, CvtJob jb, int64_t K, int64_t Kp, ZeroRect z) {
   allow_dependent_launch();
+  wait_prior_grid();
   zero_rect(z);
   const int64_t vec_per_row = Kp / 8;
   const int64_t total_a = ja.rows * vec_per_row;
@@ -124,6 +151,7 @@ __global__ void cvt_s8_f16_flat_kernel(const int2* __restrict__ a, int64_t na, u
                                        const int2* __restrict__ b, int64_t nb, uint4* eb,
                                        ZeroRect z) {
   allow_dependent_launch();
+  wait_prior_grid();
   zero_rect(z);
   const int64_t total = na + nb;
   const int64_t nt = (int64_t)gridDim.x * blockDim.x;
@@ -158,6 +186,7 @@ __global__ void cvt_s8_f16_flat_kernel(const int2* __restrict__ a, int64_t na, u
 // table (byte -> two e4m3 codes) built per block with CUDA's fp8 conversion.
 __global__ void cvt_s4_e4m3_kernel(CvtJob ja, CvtJob jb, int64_t K, int64_t Kp, ZeroRect z) {
   allow_dependent_launch();
+  wait_prior_grid();
   zero_rect(z);
   __shared__ uint16_t table[256];
   for (int b = threadIdx.x; b < 256; b += blockDim.x) {
@@ -206,6 +235,7 @@ __global__ void cvt_s4_e4m3_kernel(CvtJob ja, CvtJob jb, int64_t K, int64_t Kp, 
 // conversion of +1 and -1.
 __global__ void cvt_b1_e4m3_kernel(CvtJob ja, CvtJob jb, int64_t W, ZeroRect z) {
   allow_dependent_launch();
+  wait_prior_grid();
   zero_rect(z);
   __shared__ uint32_t nib[16];
   if (threadIdx.x < 16) {
@@ -237,36 +267,51 @@ __global__ void cvt_b1_e4m3_kernel(CvtJob ja, CvtJob jb, int64_t W, ZeroRect z) 
 // Per-row symmetric int8 quantisation of bf16 activations (the step before a
 // quantised linear layer): s = max(absmax(row), 1e-12) / 127 and
 // q = clamp(round_half_even(x / s), -127, 127), all in fp32 with IEEE
-// division.  One warp per row; two passes over the row (max, then codes).
-__global__ void quant_rows_bf16_kernel(const __nv_bfloat16* __restrict__ X, int64_t M, int64_t K,
-                                       int8_t* __restrict__ Q, float* __restrict__ S, int vec) {
-  const int lane = threadIdx.x & 31;
-  const int64_t row = (int64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
-  if (row >= M) return;
+// division.  WPR warps per row (8 rows of one warp, or one row of eight
+// warps, per 256-thread block: few rows are spread over more threads); two
+// passes over the row (max, then codes).
+template <int WPR>
+__global__ void __launch_bounds__(256)
+    quant_rows_bf16_kernel(const __nv_bfloat16* __restrict__ X, int64_t M, int64_t K,
+                           int8_t* __restrict__ Q, float* __restrict__ S, int vec) {
+  constexpr int T = 32 * WPR;  // threads per row
+  // the GEMM launched after this grid waits for it to finish before reading
+  // Q and S, but may launch (and set up) meanwhile
+  allow_dependent_launch();
+  const int t = threadIdx.x % T;
+  const int64_t row = (int64_t)blockIdx.x * (256 / T) + threadIdx.x / T;
+  if (WPR == 1 && row >= M) return;  // (WPR > 1: one row per block, grid = M)
   const __nv_bfloat16* x = X + row * K;
   int8_t* q = Q + row * K;
   float amax = 0.0f;
   if (vec) {
-    for (int64_t k = (int64_t)lane * 8; k < K; k += 32 * 8) {
+    for (int64_t k = (int64_t)t * 8; k < K; k += T * 8) {
       const uint4 v = __ldg(reinterpret_cast<const uint4*>(x + k));
       const __nv_bfloat16* h = reinterpret_cast<const __nv_bfloat16*>(&v);
 #pragma unroll
       for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(__bfloat162float(h[j])));
     }
   } else {
-    for (int64_t k = lane; k < K; k += 32) amax = fmaxf(amax, fabsf(__bfloat162float(x[k])));
+    for (int64_t k = t; k < K; k += T) amax = fmaxf(amax, fabsf(__bfloat162float(x[k])));
   }
 #pragma unroll
   for (int off = 16; off >= 1; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+  if (WPR > 1) {
+    __shared__ float part[WPR];
+    if ((t & 31) == 0) part[t >> 5] = amax;
+    __syncthreads();
+#pragma unroll
+    for (int w = 0; w < WPR; ++w) amax = fmaxf(amax, part[w]);
+  }
   const float sc = __fdiv_rn(fmaxf(amax, 1e-12f), 127.0f);
-  if (lane == 0) S[row] = sc;
+  if (t == 0) S[row] = sc;
   auto code = [&](float v) -> int8_t {
     float r = rintf(__fdiv_rn(v, sc));
     r = fminf(fmaxf(r, -127.0f), 127.0f);
     return (int8_t)(int)r;
   };
   if (vec) {
-    for (int64_t k = (int64_t)lane * 8; k < K; k += 32 * 8) {
+    for (int64_t k = (int64_t)t * 8; k < K; k += T * 8) {
       const uint4 v = __ldg(reinterpret_cast<const uint4*>(x + k));
       const __nv_bfloat16* h = reinterpret_cast<const __nv_bfloat16*>(&v);
       uint32_t lo = 0, hi = 0;
@@ -278,7 +323,7 @@ __global__ void quant_rows_bf16_kernel(const __nv_bfloat16* __restrict__ X, int6
       *reinterpret_cast<uint2*>(q + k) = make_uint2(lo, hi);
     }
   } else {
-    for (int64_t k = lane; k < K; k += 32) q[k] = code(__bfloat162float(x[k]));
+    for (int64_t k = t; k < K; k += T) q[k] = code(__bfloat162float(x[k]));
   }
 }
 
@@ -357,6 +402,10 @@ __global__ void __launch_bounds__(kSkWarps * 32, MINB)
                      int K, int32_t* __restrict__ C, const float* __restrict__ sx,
                      const float* __restrict__ sw, __nv_bfloat16* __restrict__ Y) {
   constexpr int NV = MT * NR;
+  // launched as a programmatic dependent: A (and its scales) may come from
+  // the grid before this one (the activation quantiser), which may still be
+  // running; wait for it before the first read
+  wait_prior_grid();
   const int lane = threadIdx.x & 31;
   const int nwarps = gridDim.x * kSkWarps;
   const int groups = (N + NR - 1) / NR;
@@ -632,10 +681,17 @@ cudaError_t launch_quant_rows_bf16(const void* X, int64_t M, int64_t K, int8_t* 
   if (M == 0) return cudaSuccess;
   const int vec = (K % 8 == 0) && ((reinterpret_cast<uintptr_t>(X) & 15) == 0) &&
                   ((reinterpret_cast<uintptr_t>(Q) & 7) == 0);
-  const int rows_per_block = 8;
-  const unsigned grid = (unsigned)((M + rows_per_block - 1) / rows_per_block);
-  quant_rows_bf16_kernel<<<grid, 32 * rows_per_block, 0, s>>>(
-      static_cast<const __nv_bfloat16*>(X), M, K, Q, S, vec);
+  // eight warps per row while that leaves the rows' threads within a few
+  // waves of the GPU (a warp per row leaves it mostly idle: 2048 x 4096 took
+  // 19 us that way); beyond that one warp per row, eight rows per block
+  if (M <= 8192) {
+    quant_rows_bf16_kernel<8><<<(unsigned)M, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(X), M,
+                                                          K, Q, S, vec);
+  } else {
+    const unsigned grid = (unsigned)((M + 7) / 8);
+    quant_rows_bf16_kernel<1><<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(X), M, K, Q,
+                                                   S, vec);
+  }
   return cudaGetLastError();
 }
 
@@ -658,9 +714,9 @@ cudaError_t launch_encode_pair(int bits, const void* a, int64_t rows_a, void* en
   };
   if (bits == 1) {  // K % 32 == 0 and Kp == K: rows are contiguous words
     const int64_t W = K / 32;
-    cvt_b1_e4m3_kernel<<<with_zero(grid_for((rows_a + rows_b) * W, 256, sm_count)), 256, 0, s>>>(
-        ja, jb, W, zero);
-    return cudaGetLastError();
+    return launch_dependent(cvt_b1_e4m3_kernel,
+                            dim3(with_zero(grid_for((rows_a + rows_b) * W, 256, sm_count))),
+                            dim3(256), 0, s, ja, jb, W, zero);
   }
   auto aligned16 = [&](const void* p) {
     return p == nullptr || (reinterpret_cast<uintptr_t>(p) & 15) == 0;
@@ -670,18 +726,15 @@ cudaError_t launch_encode_pair(int bits, const void* a, int64_t rows_a, void* en
     const int64_t na = a ? rows_a * (K / 8) : 0, nb = b ? rows_b * (K / 8) : 0;
     int64_t blocks = (na + nb + 4 * 256 - 1) / (4 * 256);
     blocks = std::min<int64_t>(std::max<int64_t>(blocks, 1), (int64_t)sm_count * 8);
-    cvt_s8_f16_flat_kernel<<<with_zero((int)blocks), 256, 0, s>>>(
-        static_cast<const int2*>(a), na, static_cast<uint4*>(enc_a), static_cast<const int2*>(b),
-        nb, static_cast<uint4*>(enc_b), zero);
-    return cudaGetLastError();
+    return launch_dependent(cvt_s8_f16_flat_kernel, dim3(with_zero((int)blocks)), dim3(256), 0, s,
+                            static_cast<const int2*>(a), na, static_cast<uint4*>(enc_a),
+                            static_cast<const int2*>(b), nb, static_cast<uint4*>(enc_b), zero);
   }
   const int64_t vec = bits == 8 ? Kp / 8 : Kp / 16;
   const int grid = with_zero(grid_for((rows_a + rows_b) * vec, 256, sm_count));
   if (bits == 8)
-    cvt_s8_f16_kernel<<<grid, 256, 0, s>>>(ja, jb, K, Kp, zero);
-  else
-    cvt_s4_e4m3_kernel<<<grid, 256, 0, s>>>(ja, jb, K, Kp, zero);
-  return cudaGetLastError();
+    return launch_dependent(cvt_s8_f16_kernel, dim3(grid), dim3(256), 0, s, ja, jb, K, Kp, zero);
+  return launch_dependent(cvt_s4_e4m3_kernel, dim3(grid), dim3(256), 0, s, ja, jb, K, Kp, zero);
 }
 
 cudaError_t launch_small_s8(const int8_t* A, const int8_t* B, int64_t M, int64_t N, int64_t K,
@@ -699,9 +752,9 @@ static cudaError_t skinny_go(const int8_t* A, const int8_t* B, int M, int N, int
   const int groups = (N + NR - 1) / NR;
   const int want = (groups + kSkWarps - 1) / kSkWarps;
   const int grid = want < sm_count * MINB ? want : sm_count * MINB;
-  skinny_s8_kernel<MT, NR, PF, MINB, LINEAR><<<grid, kSkWarps * 32, 0, s>>>(
-      A, B, M, N, K, C, sx, sw, static_cast<__nv_bfloat16*>(Y));
-  return cudaGetLastError();
+  return launch_dependent(skinny_s8_kernel<MT, NR, PF, MINB, LINEAR>, dim3(grid),
+                          dim3(kSkWarps * 32), 0, s, A, B, M, N, K, C, sx, sw,
+                          static_cast<__nv_bfloat16*>(Y));
 }
 
 template <bool LINEAR>

@@ -487,8 +487,12 @@ def _bf16_rows(M, K, seed):
     return xt, xt.float().numpy()  # the exact values the GPU reads
 
 
-@pytest.mark.parametrize("M,K", [(37, 4096), (5, 100), (130, 1000), (1, 8)])
+@pytest.mark.parametrize("M,K", [(37, 4096), (5, 100), (130, 1000), (1, 8), (1100, 264),
+                                 (8200, 40), (8195, 30)])
 def test_quantize_rows_bit_exact(M, K):
+    """Eight warps per row up to 8192 rows, one warp per row beyond (with a
+    ragged last block); 16-byte loads when K % 8 == 0, else one element per
+    thread."""
     xt, xf = _bf16_rows(M, K, M + K)
     Q = torch.empty((M, K), dtype=torch.int8, device=G().DEV)
     S = torch.empty(M, dtype=torch.float32, device=G().DEV)
