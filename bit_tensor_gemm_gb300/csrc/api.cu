@@ -696,9 +696,8 @@ bool warpmma_ok(int64_t M, int64_t N, int64_t K, const void* A, const void* B) {
 }
 
 // The same kernel for a small problem with a side of up to
-// kWarpMmaMaxSideSmall rows and 256 < K <= 2048: M*N <= 2^19 (2^20 with a
-// side of at most 64 rows and K <= 512: 64 x 16384 x 512 measured 4 us
-// faster), or the one-launch dp4a kernel's problems (K <= 512,
+// kWarpMmaMaxSideSmall rows and 256 < K <= 2048: M*N <= 2^19 (2^18 past
+// K = 1024), or the one-launch dp4a kernel's problems (K <= 512,
 // M*N*K <= 2^28).
 bool warpmma_small_ok(int64_t M, int64_t N, int64_t K, const void* A, const void* B) {
   const int64_t lo = std::min(M, N), hi = std::max(M, N);
@@ -739,6 +738,40 @@ int fused_route(int64_t M, int64_t N, int64_t K, const void* A, const void* B, i
   return M <= N ? 1 : 2;
 }
 
+// The kernel lbgemm_run (linear = false) or lbgemm_linear (linear = true)
+// picks for a problem with the default dispatch; *tile_n is the in-kernel
+// conversion kernel's tile width (LBGEMM_ROUTE_FUSED) and *fuse which
+// operand it converts (1: B, 2: A).  The dispatchers call this, so the
+// introspection entry point cannot drift from them.
+int route_of(int bits, int64_t M, int64_t N, int64_t K, const void* A, const void* B, bool linear,
+             int* tile_n, int* fuse) {
+  *tile_n = 0;
+  *fuse = 0;
+  if (M == 0 || N == 0) return LBGEMM_ROUTE_NONE;
+  if (linear) {
+    if (skinny_ok(M, K, A, B)) return LBGEMM_ROUTE_SKINNY;
+    if (warpmma_ok(M, N, K, A, B)) return LBGEMM_ROUTE_WARPMMA;
+    if (fused_route(M, N, K, A, B, tile_n) == 1) {
+      *fuse = 1;
+      return LBGEMM_ROUTE_FUSED;
+    }
+    *tile_n = 0;
+    return LBGEMM_ROUTE_TABLE;
+  }
+  if (bits == 1) {
+    return (double)M * (double)N * (double)K < kPopcMaxWork ? LBGEMM_ROUTE_POPC
+                                                             : LBGEMM_ROUTE_TABLE;
+  }
+  if (bits != 8) return LBGEMM_ROUTE_TABLE;
+  if (skinny_ok(M, K, A, B)) return LBGEMM_ROUTE_SKINNY;
+  if (warpmma_ok(M, N, K, A, B) || warpmma_small_ok(M, N, K, A, B)) return LBGEMM_ROUTE_WARPMMA;
+  if (small_ok(M, N, K, A, B)) return LBGEMM_ROUTE_SMALL;
+  *fuse = fused_route(M, N, K, A, B, tile_n);
+  if (*fuse) return LBGEMM_ROUTE_FUSED;
+  *tile_n = 0;
+  return LBGEMM_ROUTE_TABLE;
+}
+
 lbgemm_status run_any(int bits, int64_t M, int64_t N, int64_t K, const void* A, const void* B,
                       int32_t* C, int variant, void* ws, size_t ws_bytes, bool internal_ws,
                       cudaStream_t stream) {
@@ -753,7 +786,10 @@ lbgemm_status run_any(int bits, int64_t M, int64_t N, int64_t K, const void* A, 
   const bool auto_pick = variant < 0;
   if (auto_pick) variant = table_select(d->sm_count, bits, M, N, K);
   cudaError_t e;
-  if (bits == 1 && auto_pick && (double)M * (double)N * (double)K < kPopcMaxWork) {
+  int fuse_tile = 0, fuse = 0;
+  const int route =
+      auto_pick ? route_of(bits, M, N, K, A, B, false, &fuse_tile, &fuse) : LBGEMM_ROUTE_TABLE;
+  if (route == LBGEMM_ROUTE_POPC) {
     // Small 1-bit problems: XOR + popcount on CUDA cores, no re-encoding.
     e = lbg::launch_b1_popc(kDefaultVariant / 3, kDefaultVariant % 3 + 2,
                             static_cast<const uint32_t*>(A), static_cast<const uint32_t*>(B), M, N,
@@ -762,29 +798,24 @@ lbgemm_status run_any(int bits, int64_t M, int64_t N, int64_t K, const void* A, 
     g_launches += 1;
     return LBGEMM_OK;
   }
-  if (bits == 8 && auto_pick && skinny_ok(M, K, A, B)) {
+  if (route == LBGEMM_ROUTE_SKINNY) {
     e = lbg::launch_skinny_s8(static_cast<const int8_t*>(A), static_cast<const int8_t*>(B), (int)M,
                               (int)N, (int)K, C, nullptr, nullptr, nullptr, d->sm_count, stream);
     if (e != cudaSuccess) return cuda_fail(e, "skinny GEMM launch");
     g_launches += 1;
     return LBGEMM_OK;
   }
-  if (bits == 8 && auto_pick && warpmma_ok(M, N, K, A, B))
+  if (route == LBGEMM_ROUTE_WARPMMA)
     return run_warpmma(*d, M, N, K, static_cast<const int8_t*>(A), static_cast<const int8_t*>(B),
                        C, nullptr, nullptr, nullptr, stream);
-  if (bits == 8 && auto_pick && warpmma_small_ok(M, N, K, A, B))
-    return run_warpmma(*d, M, N, K, static_cast<const int8_t*>(A), static_cast<const int8_t*>(B),
-                       C, nullptr, nullptr, nullptr, stream);
-  if (bits == 8 && auto_pick && small_ok(M, N, K, A, B)) {
+  if (route == LBGEMM_ROUTE_SMALL) {
     e = lbg::launch_small_s8(static_cast<const int8_t*>(A), static_cast<const int8_t*>(B), M, N, K,
                              C, stream);
     if (e != cudaSuccess) return cuda_fail(e, "small GEMM launch");
     g_launches += 1;
     return LBGEMM_OK;
   }
-  int fuse_tile = 0;
-  const int fuse = (bits == 8 && auto_pick) ? fused_route(M, N, K, A, B, &fuse_tile) : 0;
-  if (fuse) {
+  if (route == LBGEMM_ROUTE_FUSED) {
     const size_t need_f = enc_bytes(8, fuse == 1 ? M : N, K);
     if (!internal_ws) {
       if (!ws || ws_bytes < need_f)
@@ -830,17 +861,19 @@ lbgemm_status run_linear(int64_t M, int64_t N, int64_t K, const int8_t* X, const
   st = device_state(&d);
   if (st != LBGEMM_OK) return st;
   const bool auto_pick = variant < 0;
-  if (auto_pick && skinny_ok(M, K, X, W)) {
+  int fuse_tile = 0, fuse = 0;
+  const int route =
+      auto_pick ? route_of(8, M, N, K, X, W, true, &fuse_tile, &fuse) : LBGEMM_ROUTE_TABLE;
+  if (route == LBGEMM_ROUTE_SKINNY) {
     cudaError_t e =
         lbg::launch_skinny_s8(X, W, (int)M, (int)N, (int)K, nullptr, sx, sw, Y, d->sm_count, stream);
     if (e != cudaSuccess) return cuda_fail(e, "skinny linear launch");
     g_launches += 1;
     return LBGEMM_OK;
   }
-  if (auto_pick && warpmma_ok(M, N, K, X, W))
+  if (route == LBGEMM_ROUTE_WARPMMA)
     return run_warpmma(*d, M, N, K, X, W, nullptr, sx, sw, Y, stream);
-  int fuse_tile = 0;
-  if (auto_pick && fused_route(M, N, K, X, W, &fuse_tile) == 1) {
+  if (route == LBGEMM_ROUTE_FUSED) {
     // small token counts: only X is re-encoded; the kernel converts W itself
     std::lock_guard<std::mutex> lock(g_ws_mu);
     st = scratch_acquire(d->ws, enc_bytes(8, M, K), stream);
@@ -1092,6 +1125,18 @@ lbgemm_status lbgemm_linear_variant(int64_t M, int64_t N, int64_t K, const int8_
   } catch (...) {
     return fail(LBGEMM_ERR_CUDA, "internal error");
   }
+}
+
+int lbgemm_route(int bits, int64_t M, int64_t N, int64_t K, int linear, int* tile_n) {
+  if ((bits != 8 && bits != 4 && bits != 1) || (linear && bits != 8) || M < 0 || N < 0 || K < 1)
+    return -1;
+  // the route of 16-byte-aligned operands: any aligned address will do, the
+  // rules read only its alignment
+  const void* aligned = reinterpret_cast<const void*>(uintptr_t(256));
+  int t = 0, f = 0;
+  const int r = route_of(bits, M, N, K, aligned, aligned, linear != 0, &t, &f);
+  if (tile_n) *tile_n = t;
+  return r;
 }
 
 int lbgemm_select_for(int sm_count, int bits, int64_t M, int64_t N, int64_t K) {

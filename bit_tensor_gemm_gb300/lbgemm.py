@@ -24,6 +24,9 @@ ERR_UNSUPPORTED = 3
 ERR_CUDA = 4
 ERR_TIMEOUT = 5
 ERR_WORKSPACE = 6
+
+# kernels of the default dispatch (lbgemm_route)
+ROUTE_TABLE, ROUTE_POPC, ROUTE_SKINNY, ROUTE_WARPMMA, ROUTE_SMALL, ROUTE_FUSED, ROUTE_NONE = range(7)
 STATUS_NAMES = {0: "OK", 1: "INVALID_ARG", 2: "ALIGNMENT", 3: "UNSUPPORTED", 4: "CUDA",
                 5: "TIMEOUT", 6: "WORKSPACE"}
 
@@ -58,6 +61,7 @@ _SIGNATURES = {
     "lbgemm_select": (_i32, [_i32, _i64, _i64, _i64]),
     "lbgemm_table_set": (_i32, [_i32, _i64, _i64, _i64, _i32]),
     "lbgemm_select_for": (_i32, [_i32, _i32, _i64, _i64, _i64]),
+    "lbgemm_route": (_i32, [_i32, _i64, _i64, _i64, _i32, _vp]),
     "lbgemm_table_set_for": (_i32, [_i32, _i32, _i64, _i64, _i64, _i32]),
     "lbgemm_table_clear": (_i32, []),
     "lbgemm_table_size": (_i64, []),
@@ -236,6 +240,15 @@ def lbgemm_select(bits, M, N, K) -> int:
 
 def lbgemm_select_for(sm_count, bits, M, N, K) -> int:
     return load().lbgemm_select_for(sm_count, bits, M, N, K)
+
+
+def lbgemm_route(bits, M, N, K, linear=False):
+    """(route, tile_n) of the default dispatch for 16-byte-aligned operands."""
+    t = ctypes.c_int(0)
+    r = load().lbgemm_route(bits, M, N, K, int(bool(linear)), ctypes.byref(t))
+    if r < 0:
+        raise LbgemmError(ERR_INVALID_ARG, f"lbgemm_route({bits}, {M}, {N}, {K}): bad arguments")
+    return r, t.value
 
 
 def lbgemm_table_set(bits, M, N, K, variant) -> None:

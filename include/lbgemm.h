@@ -245,6 +245,25 @@ int lbgemm_select(int bits, int64_t M, int64_t N, int64_t K);
 lbgemm_status lbgemm_table_set(int bits, int64_t M, int64_t N, int64_t K, int variant);
 /* The same two for an explicit SM count (no device needed). */
 int lbgemm_select_for(int sm_count, int bits, int64_t M, int64_t N, int64_t K);
+
+/* The kernels of the default dispatch. */
+typedef enum {
+  LBGEMM_ROUTE_TABLE = 0,   /* re-encoding + the variant table's tensor-core kernel */
+  LBGEMM_ROUTE_POPC = 1,    /* 1-bit XOR-popcount kernel (lbgemm_run_popc)            */
+  LBGEMM_ROUTE_SKINNY = 2,  /* dp4a kernel streaming B once (M <= 4)                 */
+  LBGEMM_ROUTE_WARPMMA = 3, /* warp-level fp16 MMA kernel (lbgemm_run_warpmma)        */
+  LBGEMM_ROUTE_SMALL = 4,   /* one-launch dp4a kernel                                */
+  LBGEMM_ROUTE_FUSED = 5,   /* in-kernel conversion kernel (lbgemm_run_fused)         */
+  LBGEMM_ROUTE_NONE = 6     /* M == 0 or N == 0: nothing runs                        */
+} lbgemm_route_id;
+
+/* Which kernel lbgemm_run (linear = 0) or lbgemm_linear (linear != 0, bits
+ * 8) runs for a problem of these sizes with 16-byte-aligned operands, by the
+ * shape rules listed at lbgemm_run; with LBGEMM_ROUTE_FUSED, *tile_n (if
+ * not null) receives the kernel's tile width (64, 128 or 256), else 0.  The
+ * dispatchers use the same function.  Host only; -1 on bad bits or sizes
+ * (the alignment rules of K are not checked here). */
+int lbgemm_route(int bits, int64_t M, int64_t N, int64_t K, int linear, int* tile_n);
 lbgemm_status lbgemm_table_set_for(int sm_count, int bits, int64_t M, int64_t N, int64_t K,
                                    int variant);
 lbgemm_status lbgemm_table_clear(void);

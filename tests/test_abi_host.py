@@ -179,3 +179,77 @@ def test_workspace_size(lib):
     assert L.lbgemm_workspace_size(8, 3, 5, 9) == 256 + 256
     assert L.lbgemm_workspace_size(8, 256, 256, 256) == 2 * 256 * 256 * 2
     assert L.lbgemm_workspace_size(4, 256, 128, 256) == 256 * 256 + 128 * 256
+
+
+# ---- dispatch routes (host only) ----------------------------------------------
+
+def _pairs(lo, hi, K):
+    if 128 < lo <= 256:
+        return (hi >= 16384 and K >= 1024) or (hi >= 8192 and K >= 16384)
+    if lo > 384:
+        return (hi >= 8192 and K >= 2048) or (hi >= 16384 and K >= 1024) or K >= 16384
+    return False
+
+
+def _route8(M, N, K, linear=False):
+    """The shape rules that include/lbgemm.h states for lbgemm_run and
+    lbgemm_linear, written out from that text (16-byte-aligned operands)."""
+    if M == 0 or N == 0:
+        return L.ROUTE_NONE, 0
+    lo, hi = min(M, N), max(M, N)
+    k16 = K % 16 == 0
+    if M <= 4 and k16:
+        return L.ROUTE_SKINNY, 0
+    if lo <= 32 and k16 and K <= (4224 if lo <= 16 else 2048):
+        return L.ROUTE_WARPMMA, 0
+    if not linear:
+        cap = 2 ** 19 if K <= 1024 else 2 ** 18
+        if (lo <= 256 and 256 < K <= 2048 and k16
+                and (lo * hi <= cap or (K <= 512 and M * N * K <= 2 ** 28))):
+            return L.ROUTE_WARPMMA, 0
+        if K <= 512 and M * N * K <= 2 ** 28 and k16:
+            return L.ROUTE_SMALL, 0
+    if (k16 and lo <= 512 and hi >= 1024 and K >= 512 and (not linear or M <= N)
+            and (hi >= 4096 or K >= 8192 or (hi >= 2048 and K >= 4096)
+                 or (lo <= 256 and K >= 2048))):
+        return L.ROUTE_FUSED, 64 if lo <= 64 else 256 if _pairs(lo, hi, K) else 128
+    return L.ROUTE_TABLE, 0
+
+
+def test_routes_follow_the_stated_rules(lib):
+    sides = [1, 2, 4, 5, 16, 17, 32, 33, 64, 65, 100, 128, 129, 200, 256, 257, 300, 384, 385, 512,
+             513, 1024, 2048, 4096, 8192, 16384]
+    ks = [16, 48, 64, 256, 272, 512, 528, 1024, 1040, 2048, 2064, 4096, 4224, 4240, 8192, 16384]
+    for M in sides:
+        for N in sides:
+            for K in ks:
+                assert L.lbgemm_route(8, M, N, K) == _route8(M, N, K), (M, N, K)
+                assert L.lbgemm_route(8, M, N, K, linear=True) == _route8(M, N, K, True), (M, N, K)
+
+
+def test_routes_of_measured_examples(lib):
+    R = L
+    cases = [((8, 1, 11008, 4096), (R.ROUTE_SKINNY, 0)),
+             ((8, 16, 11008, 4096), (R.ROUTE_WARPMMA, 0)),
+             ((8, 64, 1024, 1024), (R.ROUTE_WARPMMA, 0)),
+             ((8, 256, 256, 256), (R.ROUTE_SMALL, 0)),
+             ((8, 64, 8192, 2048), (R.ROUTE_FUSED, 64)),
+             ((8, 512, 4096, 1024), (R.ROUTE_FUSED, 128)),
+             ((8, 8192, 256, 2048), (R.ROUTE_FUSED, 128)),
+             ((8, 256, 16384, 16384), (R.ROUTE_FUSED, 256)),
+             ((8, 8192, 8192, 8192), (R.ROUTE_TABLE, 0)),
+             ((8, 0, 5, 16), (R.ROUTE_NONE, 0)),
+             ((4, 8192, 8192, 8192), (R.ROUTE_TABLE, 0)),
+             ((1, 64, 64, 1024), (R.ROUTE_POPC, 0)),
+             ((1, 8192, 8192, 65536), (R.ROUTE_TABLE, 0))]
+    for args, want in cases:
+        assert L.lbgemm_route(*args) == want, args
+    # the linear layer on the 11008 x 4096 weights, token counts of the benchmark
+    for M, want in [(1, (R.ROUTE_SKINNY, 0)), (16, (R.ROUTE_WARPMMA, 0)),
+                    (128, (R.ROUTE_FUSED, 128)), (2048, (R.ROUTE_TABLE, 0))]:
+        assert L.lbgemm_route(8, M, 11008, 4096, linear=True) == want, M
+    for bad in [(3, 4, 4, 16), (8, -1, 4, 16), (8, 4, 4, 0)]:
+        with pytest.raises(L.LbgemmError):
+            L.lbgemm_route(*bad)
+    with pytest.raises(L.LbgemmError):
+        L.lbgemm_route(4, 16, 16, 32, linear=True)
