@@ -75,6 +75,27 @@ def ops_of(shapes):
     return float(sum(2 * m * n * k for m, n, k in shapes))
 
 
+ROUTE_NAMES = {0: "table", 1: "popcount", 2: "skinny_dp4a", 3: "warp_mma", 4: "small_dp4a",
+               5: "in_kernel_conversion", 6: "none"}
+
+
+def route_histogram(L, shapes, times_ms=None):
+    """Shapes (and, given per-shape times, milliseconds) per kernel of the
+    library's 8-bit default dispatch (lbgemm_route)."""
+    out = {}
+    for i, (m, n, k) in enumerate(shapes):
+        route, tile = L.lbgemm_route(8, m, n, k)
+        name = ROUTE_NAMES[route] + (f"_{tile}" if tile else "")
+        e = out.setdefault(name, {"shapes": 0, "ms": 0.0})
+        e["shapes"] += 1
+        if times_ms is not None:
+            e["ms"] += float(times_ms[i])
+    if times_ms is None:
+        for e in out.values():
+            del e["ms"]
+    return dict(sorted(out.items()))
+
+
 def max_over_ranks(x: float, device=None) -> float:
     """The largest x over all ranks (replicas time the same workload; the
     whole job takes as long as its slowest rank).  Identity without a
@@ -414,6 +435,7 @@ def run_ours(args):
         "sweep_tops_dispatch": ops_step / (s_ms.sum() / 1e3) / 1e12,
         "sweep_seconds": round(sweep_s, 1),
         "variant_histogram": [int(sum(v == i for v in chosen)) for i in range(9)],
+        "routes": route_histogram(L, shapes, s_ms),
     }
 
     # -- roofline of the dominant kernel: the tensor-core GEMM alone on encoded operands ------

@@ -253,3 +253,16 @@ def test_routes_of_measured_examples(lib):
             L.lbgemm_route(*bad)
     with pytest.raises(L.LbgemmError):
         L.lbgemm_route(4, 16, 16, 32, linear=True)
+
+
+def test_bench_route_histogram(lib):
+    """bench.py's per-route summary of the 729-shape sweep covers every shape
+    once and names the in-kernel conversion kernel with its tile."""
+    import bench  # noqa: PLC0415
+    h = bench.route_histogram(L, bench.SWEEP)
+    assert sum(e["shapes"] for e in h.values()) == 729
+    assert set(h) <= {"table", "skinny_dp4a", "warp_mma", "small_dp4a", "in_kernel_conversion_64",
+                      "in_kernel_conversion_128", "in_kernel_conversion_256"}
+    assert h["table"]["shapes"] > 200 and "ms" not in h["table"]
+    t = bench.route_histogram(L, bench.SWEEP[:3], [1.0, 2.0, 3.0])
+    assert sum(e["ms"] for e in t.values()) == 6.0
