@@ -95,7 +95,8 @@ lbgemm_status lbgemm_variant_info(int bits, int variant, int* tile_m, int* tile_
  * max(M, N) >= 1024, K >= 512 and one of max(M, N) >= 4096, K >= 8192,
  * (max(M, N) >= 2048 and K >= 4096) or (min(M, N) <= 256 and K >= 2048),
  * on a tensor-core kernel that converts the large operand itself
- * (lbgemm_run_fused), with only the small one re-encoded ahead; and 1-bit problems with M*N*K < 2^30 on the
+ * (lbgemm_run_fused), with only the small one re-encoded ahead; and 1-bit
+ * problems with M*N*K < 2^30 on the
  * XOR-popcount kernel of lbgemm_run_popc.  Scratch memory for the re-encoding is
  * taken from a per-device buffer the library grows with cudaMalloc on demand
  * (by at least half again each time);
