@@ -266,3 +266,40 @@ def test_bench_route_histogram(lib):
     assert h["table"]["shapes"] > 200 and "ms" not in h["table"]
     t = bench.route_histogram(L, bench.SWEEP[:3], [1.0, 2.0, 3.0])
     assert sum(e["ms"] for e in t.values()) == 6.0
+
+
+# every entry point rejects bad arguments before it touches a device
+P = 4096  # a 16-byte-aligned stand-in address (never dereferenced: the checks fail first)
+
+
+@pytest.mark.parametrize("call,status", [
+    (lambda: L.lbgemm_run_host(3, 4, 4, 16, P, P, P), L.ERR_INVALID_ARG),
+    (lambda: L.lbgemm_run_host(8, 4, 4, 0, P, P, P), L.ERR_INVALID_ARG),
+    (lambda: L.lbgemm_run_host(8, 4, 4, 16, None, P, P), L.ERR_INVALID_ARG),
+    (lambda: L.lbgemm_run_host(1, 4, 4, 48, P, P, P), L.ERR_ALIGNMENT),
+    (lambda: L.lbgemm_linear(4, 4, 16, P, None, P, P, P), L.ERR_INVALID_ARG),
+    (lambda: L.lbgemm_linear(4, 4, 131072, P, P, P, P, P), L.ERR_INVALID_ARG),
+    (lambda: L.lbgemm_linear_variant(4, 4, 16, P, P, P, P, P, 9), L.ERR_INVALID_ARG),
+    (lambda: L.lbgemm_linear_quant(4, 4, 16, P, P, None, P), L.ERR_INVALID_ARG),
+    (lambda: L.lbgemm_quantize_rows(-1, 16, P, P, P), L.ERR_INVALID_ARG),
+    (lambda: L.lbgemm_quantize_rows(4, 0, P, P, P), L.ERR_INVALID_ARG),
+    (lambda: L.lbgemm_quantize_rows(4, 16, P, None, P), L.ERR_INVALID_ARG),
+    (lambda: L.lbgemm_run_popc(4, 4, 48, P, P, P), L.ERR_ALIGNMENT),
+    (lambda: L.lbgemm_run_popc(4, 4, 64, P, P, P, 9), L.ERR_INVALID_ARG),
+    (lambda: L.lbgemm_run_encoded(2, 4, 4, 64, P, P, P), L.ERR_INVALID_ARG),
+    (lambda: L.lbgemm_run_encoded(8, 4, 4, 64, P, P, P, -2), L.ERR_INVALID_ARG),
+    (lambda: L.lbgemm_encode(3, 4, 64, P, P), L.ERR_INVALID_ARG),
+])
+def test_entry_points_reject_bad_arguments_without_a_device(lib, call, status):
+    with pytest.raises(L.LbgemmError) as e:
+        call()
+    assert e.value.status == status
+    assert L.lbgemm_last_error()
+
+
+def test_empty_problems_need_no_device(lib):
+    L.lbgemm_run_host(8, 0, 4, 16, P, P, P)
+    L.lbgemm_linear(0, 4, 16, P, P, P, P, P)
+    L.lbgemm_quantize_rows(0, 16, P, P, P)
+    L.lbgemm_run_popc(4, 0, 64, P, P, P)
+    L.lbgemm_run_encoded(8, 4, 0, 64, P, P, P)
