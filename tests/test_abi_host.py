@@ -303,3 +303,43 @@ def test_empty_problems_need_no_device(lib):
     L.lbgemm_quantize_rows(0, 16, P, P, P)
     L.lbgemm_run_popc(4, 0, 64, P, P, P)
     L.lbgemm_run_encoded(8, 4, 0, 64, P, P, P)
+
+
+C_PROGRAM = r"""
+#include <stdio.h>
+#include "lbgemm.h"
+int main(void) {
+  int tm = 0, tn = 0, tk = 0, st = 0, tile = -1;
+  if (lbgemm_num_variants() != 9) return 1;
+  if (lbgemm_variant_info(8, lbgemm_default_variant(), &tm, &tn, &tk, &st) != LBGEMM_OK) return 2;
+  int route = lbgemm_route(8, 16, 11008, 4096, 1, &tile);
+  lbgemm_status bad = lbgemm_run(3, 4, 4, 16, (const void*)0, (const void*)0, (int32_t*)0,
+                                 (void*)0);
+  const char* msg = lbgemm_last_error();
+  printf("%d %d %d %d %d %d %d %d\n", tm, tn, tk, st, route, tile, (int)bad, msg && msg[0] ? 1 : 0);
+  return 0;
+}
+"""
+
+
+def test_header_is_plain_c_and_links(lib, tmp_path):
+    """The boundary is a C ABI: a C99 program includes the header, links the
+    library and calls host-side entry points (no device needed)."""
+    import shutil  # noqa: PLC0415
+    import subprocess  # noqa: PLC0415
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "abi.c"
+    src.write_text(C_PROGRAM)
+    libdir = os.path.dirname(L.LIBRARY)
+    exe = tmp_path / "abi"
+    subprocess.run([cc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic", str(src),
+                    "-I", os.path.dirname(HEADER), "-L", libdir, "-llbgemm",
+                    f"-Wl,-rpath,{libdir}", "-o", str(exe)], check=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split()
+    tm, tn, tk, stages, route, tile, bad, has_msg = map(int, out)
+    info = L.lbgemm_variant_info(8, L.lbgemm_default_variant())
+    assert (tm, tn, tk, stages) == (info["tile_m"], info["tile_n"], info["tile_k"], info["stages"])
+    assert (route, tile) == (L.ROUTE_WARPMMA, 0)
+    assert bad == L.ERR_INVALID_ARG and has_msg == 1
