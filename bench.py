@@ -3,18 +3,21 @@
 
 Workload (one step): the 8-bit GEMM shape sweep -- M, N, K each in
 {64, 128, ..., 16384}, 729 shapes, operands uniform in [-127, 127] -- run once
-per shape through lbgemm_run with the variant the selection table picked.
-Before the timed steps the sweep itself runs: every shape is timed under all
-nine tile x stage variants (lbgemm_time_variants) and the table stores
-lbgemm_choose's pick, once a pick other than the default has won again head
-to head against it.  L2 is flushed before every GEMM, outside the timed
-intervals; the step time is the sum of the per-GEMM CUDA-event times.
+per shape through lbgemm_run with the kernel the selection table picked.
+Before the timed steps the sweep itself runs, for 8-, 4- and 1-bit operands
+(tune.py): every shape is timed under all nine tile x stage variants and the
+shape-route kernels that can run it (lbgemm_candidates), and the table
+stores the labelled variant and the dispatch's pick, each only once it has
+won again head to head against the default variant.  L2 is flushed before
+every GEMM, outside the timed intervals; the step time is the sum of the
+per-GEMM CUDA-event times.
 
 value = sum over the 729 shapes of 2*M*N*K / step time, in TOPS (integer
-operations, 2 per multiply-add).  The same line reports the selected-vs-
-default speedups, the other bit widths and the linear layer, the roofline of
-the dominant kernel, an end-to-end number through the host-buffer entry
-point, and the CPU oracle on a row sample.
+operations, 2 per multiply-add).  The same line reports, per bit width, the
+selected-vs-default speedups on an independent interleaved re-time with its
+measured noise floor; the other configurations and the linear layer; the
+roofline of the dominant kernel; an end-to-end number through the
+host-buffer entry point; and the CPU oracle on a row sample.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 """
@@ -41,6 +44,9 @@ SWEEP = [(m, n, k) for m in SIZES for n in SIZES for k in SIZES]
 E2E_SHAPES = [(SIZES[i], SIZES[j], SIZES[(-(i + j)) % 9]) for i in range(9) for j in range(9)]
 MAXD = SIZES[-1]
 METRIC = "int8 GEMM TOPS over the 729-shape sweep (selected variant)"
+BITS = (8, 4, 1)
+SEED_OF = {8: 2, 4: 3, 1: 4}  # workload numbers of the 8-, 4- and 1-bit configurations
+ROUTE_TABLE = 0
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
                   "sm_max_mhz": 2070.0}
 
@@ -51,7 +57,10 @@ def parse_args():
     p.add_argument("--steps", type=int, default=5)
     p.add_argument("--warmup", type=int, default=3)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--sweep-reps", type=int, default=5)
+    p.add_argument("--sweep-reps", type=int, default=10,
+                   help="runs per candidate and shape in the selection sweep (median)")
+    p.add_argument("--retime-reps", type=int, default=20,
+                   help="runs per arm and shape in the head-to-head checks and the re-time")
     p.add_argument("--shapes", type=int, default=0, help="debug: use only the first N shapes")
     p.add_argument("--no-cpu", action="store_true", help="debug: skip the CPU oracle sample")
     p.add_argument("--dump", default="", help="write per-shape sweep data (JSON) to this path")
@@ -79,13 +88,26 @@ ROUTE_NAMES = {0: "table", 1: "popcount", 2: "skinny_dp4a", 3: "warp_mma", 4: "s
                5: "in_kernel_conversion", 6: "none"}
 
 
-def route_histogram(L, shapes, times_ms=None):
-    """Shapes (and, given per-shape times, milliseconds) per kernel of the
-    library's 8-bit default dispatch (lbgemm_route)."""
+def route_name(route, param):
+    """Name of a (route, param) kernel: the route, with the tile width of the
+    in-kernel conversion kernel and the variant of the popcount kernel."""
+    if route == 5:
+        return f"{ROUTE_NAMES[route]}_{param}"
+    if route == 1:
+        return f"{ROUTE_NAMES[route]}_v{param}"
+    return ROUTE_NAMES[route]
+
+
+def route_histogram(L, shapes, times_ms=None, routes=None):
+    """Shapes (and, given per-shape times, milliseconds) per kernel: of the
+    given (route, param) list, else of the 8-bit shape rules (lbgemm_route)."""
     out = {}
     for i, (m, n, k) in enumerate(shapes):
-        route, tile = L.lbgemm_route(8, m, n, k)
-        name = ROUTE_NAMES[route] + (f"_{tile}" if tile else "")
+        if routes is not None:
+            name = route_name(*routes[i])
+        else:
+            route, tile = L.lbgemm_route(8, m, n, k)
+            name = route_name(route, tile)
         e = out.setdefault(name, {"shapes": 0, "ms": 0.0})
         e["shapes"] += 1
         if times_ms is not None:
@@ -94,6 +116,102 @@ def route_histogram(L, shapes, times_ms=None):
         for e in out.values():
             del e["ms"]
     return dict(sorted(out.items()))
+
+
+def geomean(x) -> float:
+    return float(np.exp(np.mean(np.log(np.asarray(x, dtype=np.float64)))))
+
+
+def shape_roofline_ms(bits, shapes, peaks):
+    """Per-shape roofline time (ms): the slower of the tensor pipe (sustained
+    bf16 peak for 8-bit operands encoded as fp16; twice that, the fp8 rate,
+    for 4- and 1-bit operands encoded as e4m3) and the HBM bytes of the
+    operation (A and B read once in their own format, int32 C written once)."""
+    rate = peaks["bf16_tflops_sustained"] * 1e12 * (1 if bits == 8 else 2)
+    per_elem = {8: 1.0, 4: 0.5, 1: 0.125}[bits]
+    return np.array([max(2.0 * m * n * k / rate,
+                         (per_elem * (m * k + n * k) + 4.0 * m * n) / (peaks["hbm_gbs"] * 1e9))
+                     for m, n, k in shapes]) * 1e3
+
+
+def selection_summary(bits, shapes, recs, disp, T, sweep_seconds, peaks, reps):
+    """Selected-vs-default figures of one bit width from the re-time T
+    [shape, arm]: arms default, label, dispatch, default again."""
+    d, t, s, d2 = T[:, 0], T[:, 1], T[:, 2], T[:, 3]
+    ops = ops_of(shapes)
+    noise = np.abs(d2 / d - 1.0)
+    noise_p95 = float(np.percentile(noise, 95))
+    speed, dspeed = d / t, d / s
+    labels = [r["label"] for r in recs]
+    picks = [tuple(r["pick"]) for r in recs]
+    dv = 7
+    t_roof = shape_roofline_ms(bits, shapes, peaks)
+    summ = {
+        "shapes": len(shapes),
+        "what": f"{bits}-bit: labelled vs default (variant 7) tile x stage variant, both on the "
+                "tensor-core kernel; dispatch_* = the kernel lbgemm_run runs (the table's pick "
+                "among the nine variants and the shape-route kernels) vs variant 7",
+        "retime": f"median of {reps} interleaved runs per arm and shape, L2 flushed before each",
+        "label_ne_default": int(sum(v != dv for v in labels)),
+        "pick_ne_default": int(sum(p != (ROUTE_TABLE, dv) for p in picks)),
+        "noise_floor_p95": noise_p95,
+        "noise_floor_max": float(noise.max()),
+        "noise_floor_what": "|t2 / t1 - 1| between two interleaved re-times of the default "
+                            "variant (the identical kernel)",
+        "speedup_geomean": geomean(speed),
+        "speedup_max": float(speed.max()),
+        "speedup_min": float(speed.min()),
+        "speedup_min_shape": list(shapes[int(np.argmin(speed))]),
+        "shapes_slower_beyond_noise": int((speed < 1.0 - noise_p95).sum()),
+        "shapes_slower_by_2pct": int((speed < 0.98).sum()),
+        "dispatch_speedup_geomean": geomean(dspeed),
+        "dispatch_speedup_max": float(dspeed.max()),
+        "dispatch_speedup_min": float(dspeed.min()),
+        "dispatch_speedup_min_shape": list(shapes[int(np.argmin(dspeed))]),
+        "dispatch_slower_beyond_noise": int((dspeed < 1.0 - noise_p95).sum()),
+        "dispatch_slower_by_2pct": int((dspeed < 0.98).sum()),
+        "sweep_tops_default": ops / (d.sum() / 1e3) / 1e12,
+        "sweep_tops_label": ops / (t.sum() / 1e3) / 1e12,
+        "sweep_tops_dispatch": ops / (s.sum() / 1e3) / 1e12,
+        "sweep_seconds": round(sweep_seconds, 1),
+        "variant_histogram": [int(sum(v == i for v in labels)) for i in range(9)],
+        "routes": route_histogram(None, shapes, s, disp),
+    }
+    roof = {"frac": float(t_roof.sum() / s.sum()),
+            "roofline_tops": ops / (t_roof.sum() / 1e3) / 1e12,
+            "definition": "sum over shapes of max(2MNK / tensor peak, operand and C bytes / HBM) "
+                          "divided by the sum of the dispatch's re-timed medians; tensor peak = "
+                          "sustained bf16 (8-bit, fp16 encoding) or twice it (4- and 1-bit, e4m3)"}
+    if bits == 8:
+        roof["frac_hbm_8tbs"] = float(np.sum([
+            max(2.0 * m * n * k / (peaks["bf16_tflops_sustained"] * 1e12),
+                (m * k + n * k + 4.0 * m * n) / 8.0e12) for m, n, k in shapes]) * 1e3 / s.sum())
+    return summ, roof
+
+
+def mlp_on_grid(L, bits, shapes, recs, sm):
+    """The shipped selector network of this bit width judged on this run's own
+    nine tensor-core medians of the grid shapes (None if none is shipped)."""
+    path = os.path.join(ROOT, "bit_tensor_gemm_gb300", "data", f"mlp_gb300_s{bits}.txt")
+    if not os.path.exists(path):
+        return None
+    L.lbgemm_mlp_load(path)
+    try:
+        T = np.array([r["ms"][:9] for r in recs])
+        pred = np.array([L.lbgemm_mlp_predict(bits, m, n, k, sm) for (m, n, k) in shapes])
+    finally:
+        L.lbgemm_mlp_clear()  # the timed steps use the measured table
+    best = T.argmin(axis=1)
+    t_pred = T[np.arange(len(T)), pred[:, 0]]
+    return {
+        "network": "log2 M, log2 N, log2 K, SM count -> 3 x 128 ReLU -> 9 variants",
+        "file": os.path.relpath(path, ROOT),
+        "top1_accuracy": float(np.mean(pred[:, 0] == best)),
+        "top2_accuracy": float(np.mean((pred[:, 0] == best) | (pred[:, 1] == best))),
+        "within_2pct_of_best": float(np.mean(t_pred <= T.min(axis=1) * 1.02)),
+        "time_pred_over_best": float(t_pred.sum() / T.min(axis=1).sum()),
+        "speedup_over_default": float(T[:, 7].sum() / t_pred.sum()),
+    }
 
 
 def max_over_ranks(x: float, device=None) -> float:
@@ -229,24 +347,44 @@ def source_hash():
     return h.hexdigest()[:16]
 
 
-def profiled_traffic():
-    """Per-launch DRAM bytes of the dominant kernel from the committed ncu summary,
-    when it was taken from the kernel source as it is now; else None."""
-    path = os.path.join(ROOT, "profiles", "tc_gemm_int8_sweep.txt")
+TRAFFIC_FILE = os.path.join("profiles", "tc_traffic_int8_sweep.md")
+TRAFFIC_SOURCE = (f"{TRAFFIC_FILE}: ncu dram__bytes_read.sum + dram__bytes_write.sum of single "
+                  "launches of representative sweep shapes; each sweep shape takes the ratio "
+                  "of DRAM bytes to the kernel's own operand and C bytes (fp16 A and B, int32 C) "
+                  "of its nearest representative (sum of |log2| differences of M, N, K)")
+
+
+def kernel_bytes(m, n, k):
+    """Bytes the tensor-core GEMM kernel must move for one launch: fp16 A and
+    B (the re-encoded operands) read once, int32 C written once."""
+    return 2.0 * (m + n) * k + 4.0 * m * n
+
+
+def profiled_traffic(shapes):
+    """Per-launch DRAM bytes of the dominant kernel averaged over the sweep's
+    launches, estimated from the committed single-launch ncu captures (when
+    they were taken from the kernel source as it is now); else None."""
+    import math  # noqa: PLC0415
+    path = os.path.join(ROOT, TRAFFIC_FILE)
     if not os.path.exists(path):
         return None
-    vals = {}
+    reps, src = [], None
     with open(path) as f:
         for line in f:
-            if ":" in line:
-                k, v = line.split(":", 1)
-                vals[k.strip()] = v.strip()
-    if vals.get("source_sha256_16") != source_hash():
+            w = line.split()
+            if len(w) == 2 and w[0] == "source_sha256_16":
+                src = w[1]
+            elif len(w) == 6 and w[0] == "capture":
+                m, n, k, dram = int(w[1]), int(w[2]), int(w[3]), float(w[5])
+                reps.append((m, n, k, dram / kernel_bytes(m, n, k)))
+    if src != source_hash() or not reps:
         return None
-    try:
-        return float(vals["dram_bytes_per_launch"])
-    except (KeyError, ValueError):
-        return None
+    total = 0.0
+    for m, n, k in shapes:
+        r = min(reps, key=lambda e: abs(math.log2(m / e[0])) + abs(math.log2(n / e[1])) +
+                abs(math.log2(k / e[2])))
+        total += r[3] * kernel_bytes(m, n, k)
+    return total / len(shapes)
 
 
 def run_ours(args):
@@ -255,6 +393,7 @@ def run_ours(args):
     from bit_tensor_gemm_gb300 import build as bld  # noqa: PLC0415
     from bit_tensor_gemm_gb300 import lbgemm as L  # noqa: PLC0415
     from bit_tensor_gemm_gb300 import synth  # noqa: PLC0415
+    from bit_tensor_gemm_gb300 import tune  # noqa: PLC0415
 
     rank, world, local = dist_env()
     if world > 1 and not torch.distributed.is_initialized():
@@ -272,72 +411,34 @@ def run_ours(args):
     C = torch.empty(MAXD * MAXD, dtype=torch.int32, device=dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
+    dev_ops = {8: (A, B)}
+
+    def operands_of(bits):
+        """Device operands of a bit width's sweep (seeded; kept for the re-time)."""
+        if bits not in dev_ops:
+            dev_ops[bits] = tune.device_operands(bits, shapes, dev,
+                                                 synth.config_seed(SEED_OF[bits]), with_c=False)
+        return dev_ops[bits]
 
     def barrier():
         torch.cuda.synchronize()
         if world > 1:
             torch.distributed.barrier()
 
-    def beats_default(m, n, k, v, keep, reps=5):
-        """Variant v against the default, interleaved, L2 flushed before each
-        run: is v's median faster by more than `keep` (relative)?"""
-        dv = L.lbgemm_default_variant()
-        pairs = []
-        for _ in range(reps):
-            for var in (v, dv):
-                flush.zero_()
-                e0 = torch.cuda.Event(enable_timing=True)
-                e1 = torch.cuda.Event(enable_timing=True)
-                e0.record(stream)
-                L.lbgemm_run_variant(8, m, n, k, A, B, C, var)
-                e1.record(stream)
-                pairs.append((var, e0, e1))
-        torch.cuda.synchronize()
-        tv = np.median([a.elapsed_time(b) for var, a, b in pairs if var == v])
-        td = np.median([a.elapsed_time(b) for var, a, b in pairs if var == dv])
-        return tv < td * (1.0 - keep)
+    sm = torch.cuda.get_device_properties(dev).multi_processor_count
 
-    # -- the sweep: nine variants per shape; the table keeps lbgemm_choose's pick ------------
-    t_sweep0 = time.perf_counter()
+    # -- the sweep, per bit width: every candidate kernel per shape; the table
+    #    keeps the label and the dispatch pick (tune.py) ---------------------------------------
     L.lbgemm_table_clear()
-    sweep_times = []
-    for (m, n, k) in shapes:
-        t = L.lbgemm_time_variants(8, m, n, k, A, B, C, warmup=1, reps=args.sweep_reps,
-                                   flush_l2=True)
-        sweep_times.append(t)
-        # keep the default unless another variant is faster by more than 2 %
-        # and by more than 2 us, the resolution of the event timings
-        keep = max(0.02, 0.002 / max(min(t), 1e-6))
-        v = L.lbgemm_choose(t, L.lbgemm_default_variant(), keep)
-        # a pick other than the default must win again head to head, in fresh
-        # interleaved timings, or the default stays: one noisy sweep sample
-        # must not make a shape slower than the default tile
-        if v != L.lbgemm_default_variant() and not beats_default(m, n, k, v, keep):
-            v = L.lbgemm_default_variant()
-        L.lbgemm_table_set(8, m, n, k, v)
-    sweep_s = time.perf_counter() - t_sweep0
-
-    # -- the learned selector (trained offline on a separate random-shape GB300
-    #    sweep) judged on this run's own timings of the 729 grid shapes --------------------
-    mlp_eval = None
-    mlp_path = os.path.join(ROOT, "bit_tensor_gemm_gb300", "data", "mlp_gb300_s8.txt")
-    if os.path.exists(mlp_path):
-        L.lbgemm_mlp_load(mlp_path)
-        sm = torch.cuda.get_device_properties(dev).multi_processor_count
-        T = np.array(sweep_times)
-        pred = np.array([L.lbgemm_mlp_predict(8, m, n, k, sm) for (m, n, k) in shapes])
-        best = T.argmin(axis=1)
-        t_pred = T[np.arange(len(T)), pred[:, 0]]
-        mlp_eval = {
-            "network": "log2 M, log2 N, log2 K, SM count -> 3 x 128 ReLU -> 9 variants",
-            "trained_on": "bit_tensor_gemm_gb300/data/sweep_gb300_s8.csv (3000 random shapes)",
-            "top1_accuracy": float(np.mean(pred[:, 0] == best)),
-            "top2_accuracy": float(np.mean((pred[:, 0] == best) | (pred[:, 1] == best))),
-            "within_2pct_of_best": float(np.mean(t_pred <= T.min(axis=1) * 1.02)),
-            "time_pred_over_best": float(t_pred.sum() / T.min(axis=1).sum()),
-            "speedup_over_default": float(T[:, 7].sum() / t_pred.sum()),
-        }
-        L.lbgemm_mlp_clear()  # the timed steps use the measured table
+    recs, sweep_s, mlp_eval = {}, {}, {}
+    for bits in BITS:
+        Ab, Bb = operands_of(bits)
+        t0 = time.perf_counter()
+        recs[bits] = tune.sweep(L, bits, shapes, Ab, Bb, C, sm, reps=args.sweep_reps,
+                                confirm_reps=args.retime_reps)
+        sweep_s[bits] = time.perf_counter() - t0
+        mlp_eval[bits] = mlp_on_grid(L, bits, shapes, recs[bits], sm)
+        del Ab, Bb
 
     def timed_pass(run_one, shp_list=shapes):
         """One pass: flush L2, event, GEMM, event, per shape.  Returns per-shape ms."""
@@ -355,9 +456,6 @@ def run_ours(args):
 
     def sel(m, n, k):
         L.lbgemm_run(8, m, n, k, A, B, C)
-
-    def dflt(m, n, k):
-        L.lbgemm_run_variant(8, m, n, k, A, B, C, L.lbgemm_default_variant())
 
     for _ in range(args.warmup):
         timed_pass(sel)
@@ -384,59 +482,31 @@ def run_ours(args):
     # The pages' comparison: the chosen tile x stage variant against the
     # default one, both forced on the tensor-core kernel.  Also the library's
     # full dispatch (which adds the shape rules) against the same default.
-    chosen = [L.lbgemm_select(8, *s) for s in shapes]
-    chosen_of = dict(zip(shapes, chosen))
-
-    def sel_tc(m, n, k):
-        L.lbgemm_run_variant(8, m, n, k, A, B, C, chosen_of[(m, n, k)])
-
-    d_runs, t_runs, s_runs = [], [], []
-    for _ in range(3):
-        d_runs.append(timed_pass(dflt))
-        t_runs.append(timed_pass(sel_tc))
-        s_runs.append(timed_pass(sel))
-    d_ms = np.median(np.array(d_runs), axis=0)
-    t_ms = np.median(np.array(t_runs), axis=0)
-    s_ms = np.median(np.array(s_runs), axis=0)
-    # a shape whose chosen variant is the default runs the identical kernel:
-    # its ratio is 1 by definition, not the noise between two timings
-    same = np.array([c == L.lbgemm_default_variant() for c in chosen])
-    speed = np.where(same, 1.0, d_ms / t_ms)
-    dspeed = d_ms / s_ms
-    # Per-shape roofline: the slower of the tensor pipe and the HBM bytes of
-    # the operation (int8 A and B read once, int32 C written once).
-    t_roof = np.array([max(2.0 * m * n * k / (peaks["bf16_tflops_sustained"] * 1e12),
-                           (m * k + n * k + 4.0 * m * n) / (peaks["hbm_gbs"] * 1e9))
-                       for m, n, k in shapes])
-    t_roof8 = np.array([max(2.0 * m * n * k / (peaks["bf16_tflops_sustained"] * 1e12),
-                            (m * k + n * k + 4.0 * m * n) / 8.0e12) for m, n, k in shapes])
-    sweep_roofline = {
-        "frac": float(t_roof.sum() / (s_ms.sum() / 1e3)),
-        "frac_hbm_8tbs": float(t_roof8.sum() / (s_ms.sum() / 1e3)),
-        "roofline_tops": ops_step / t_roof.sum() / 1e12,
-        "definition": "sum over shapes of max(2MNK / sustained bf16 peak, (MK+NK+4MN) bytes / "
-                      "HBM) divided by the sum of measured times (selected variants)"}
-    worst = int(np.argmin(speed))
-    selection = {
-        "shapes": len(shapes),
-        "selected_ne_default": int(sum(v != L.lbgemm_default_variant() for v in chosen)),
-        "what": "chosen vs default (variant 7) tile x stage variant, both on the tensor-core "
-                "kernel; dispatch_* adds the shape rules (lbgemm_run vs variant 7)",
-        "speedup_geomean": float(np.exp(np.mean(np.log(speed)))),
-        "speedup_max": float(speed.max()),
-        "speedup_min": float(speed.min()),
-        "speedup_min_shape": list(shapes[worst]),
-        "shapes_slower_than_default_by_2pct": int((speed < 0.98).sum()),
-        "dispatch_speedup_geomean": float(np.exp(np.mean(np.log(dspeed)))),
-        "dispatch_speedup_max": float(dspeed.max()),
-        "dispatch_speedup_min": float(dspeed.min()),
-        "sweep_tops_default": ops_step / (d_ms.sum() / 1e3) / 1e12,
-        "sweep_tops_chosen_variant": ops_step / (t_ms.sum() / 1e3) / 1e12,
-        "sweep_tops_dispatch": ops_step / (s_ms.sum() / 1e3) / 1e12,
-        "sweep_seconds": round(sweep_s, 1),
-        "variant_histogram": [int(sum(v == i for v in chosen)) for i in range(9)],
-        "routes": route_histogram(L, shapes, s_ms),
-    }
+    # The pages' comparison: the labelled tile x stage variant against the
+    # default one, both forced on the tensor-core kernel; and the library's
+    # dispatch (the kernel lbgemm_run runs: the table's pick) against the same
+    # default.  A second run of the default measures the noise floor: two
+    # timings of the identical kernel.
+    dv = (ROUTE_TABLE, L.lbgemm_default_variant())
+    selection_by_bits, rooflines = {}, {}
+    s_ms = None
+    for bits in BITS:
+        Ab, Bb = operands_of(bits)
+        label = [(ROUTE_TABLE, r["label"]) for r in recs[bits]]
+        disp = [tuple(L.lbgemm_dispatch_for(sm, bits, *sh)) for sh in shapes]
+        T = tune.retime(L, bits, shapes, [[dv] * len(shapes), label, disp, [dv] * len(shapes)],
+                        Ab, Bb, C, reps=args.retime_reps)
+        summ, roof = selection_summary(bits, shapes, recs[bits], disp, T, sweep_s[bits], peaks,
+                                       args.retime_reps)
+        summ["mlp_selector"] = mlp_eval[bits]
+        summ["sweep_roofline_frac"] = roof["frac"]
+        selection_by_bits[bits], rooflines[bits] = summ, roof
+        if bits == 8:
+            s_ms = T[:, 2]
+        del Ab, Bb
+    selection = dict(selection_by_bits[8])
+    selection["by_bits"] = {str(b): selection_by_bits[b] for b in BITS if b != 8}
+    sweep_roofline = rooflines[8]
 
     # -- roofline of the dominant kernel: the tensor-core GEMM alone on encoded operands ------
     encA = torch.empty(L.lbgemm_encoded_size(8, MAXD, MAXD), dtype=torch.uint8, device=dev)
@@ -456,15 +526,23 @@ def run_ours(args):
         enc_ms.append(e0.elapsed_time(e1))
     torch.cuda.nvtx.range_pop()
     kernel_tflops = ops_step / (sum(enc_ms) / 1e3) / 1e12
-    peak_tc = peaks["bf16_tflops_sustained"]
+    # each launch is timed alone (L2 flushed, synchronised): the burst peak
+    peak_tc = peaks["bf16_tflops"]
+    alg_bytes = sum(m * k + n * k + 4.0 * m * n for m, n, k in shapes) / len(shapes)
+    traffic = profiled_traffic(shapes)
     roofline = {"bound": "tensor", "achieved": kernel_tflops, "peak": peak_tc, "unit": "TFLOP/s",
-                "frac": kernel_tflops / peak_tc, "traffic": profiled_traffic(),
+                "frac": kernel_tflops / peak_tc, "traffic": traffic,
                 "kernel": "tensor-core GEMM: tc_gemm_kernel (small and medium tiles) and "
                           "tc_pair_kernel (large tile, CTA pairs); int8 encoded as fp16, "
                           "tcgen05 kind::f16",
-                "per": "launch average over the sweep's 729 launches (selected variants)",
-                "peak_source": f"{peak_kind} bf16 dense, sustained",
-                "frac_of_burst": kernel_tflops / peaks["bf16_tflops"]}
+                "per": "launch average over the sweep's 729 launches (the labelled variants), "
+                       "each launch timed alone with CUDA events, L2 flushed before it",
+                "peak_source": f"{peak_kind} bf16 dense, burst (launches timed alone)",
+                "frac_of_sustained": kernel_tflops / peaks["bf16_tflops_sustained"],
+                "algorithmic_bytes_per_launch": alg_bytes,
+                "traffic_over_algorithmic": traffic / alg_bytes if traffic else None,
+                "traffic_source": TRAFFIC_SOURCE if traffic else "no capture of the current "
+                                                                 "kernel source"}
     del encA, encB
 
     # -- the other bit widths and the linear layer ------------------------------------------------
@@ -501,13 +579,21 @@ def run_ours(args):
     B1 = torch.from_numpy(synth.b1(g1, 8192, 65536).view(np.int32)).to(dev)
     ops1 = 2 * 8192 * 8192 * 65536
     t = median_ms(lambda: L.lbgemm_run(1, 8192, 8192, 65536, A1, B1, C), 3)
+    clk_popc = Clocks(local)
+    clk_popc.start()
     tp = median_ms(lambda: L.lbgemm_run_popc(8192, 8192, 65536, A1, B1, C), 3)
-    popc_peak = 152 * 16 * peaks.get("sm_max_mhz", 2070.0) * 1e6 * 64 / 1e12
+    popc_clk = clk_popc.stop()
+    # ALU peak of the popcount route: 16 popcounts per clock per SM (the SM's
+    # integer pipe), the device's SM count, the SM clock sampled while it ran
+    popc_mhz = popc_clk.get("sm_mhz") or peaks.get("sm_max_mhz", 2070.0)
+    popc_peak = sm * 16 * popc_mhz * 1e6 * 64 / 1e12
     per_config["b1_8192x8192x65536"] = {
         "us": t * 1e3, "tops": ops1 / t / 1e9, "route": "tensor cores (+-1 as e4m3)",
         "frac_of_fp8_sustained": ops1 / t / 1e9 / (2 * peaks["bf16_tflops_sustained"]),
         "popc_us": tp * 1e3, "popc_tops": ops1 / tp / 1e9,
-        "popc_frac_of_alu_peak": ops1 / tp / 1e9 / popc_peak, "popc_alu_peak_tops": popc_peak}
+        "popc_frac_of_alu_peak": ops1 / tp / 1e9 / popc_peak, "popc_alu_peak_tops": popc_peak,
+        "popc_alu_peak_from": f"{sm} SMs x 16 popc/clk x {popc_mhz:.0f} MHz (median SM clock "
+                              "sampled during the popcount runs) x 64 ops per 32-bit word"}
     del A1, B1
     for M in (1, 16, 128, 2048):
         X, sx, W, sw = synth.linear_operands(M, 11008, 4096, synth.config_seed(5) + M)
@@ -582,17 +668,15 @@ def run_ours(args):
                        "timing": "sum of per-GEMM CUDA-event times on the launching stream",
                        "parallelism": "replicas" if world > 1 else "single GPU"},
             "clocks": clk, "gpu_launches": launches, "e2e": e2e, "roofline": roofline,
-            "cpu_baseline": cpu, "selection": selection, "mlp_selector": mlp_eval,
+            "cpu_baseline": cpu, "selection": selection,
             "sweep_roofline": sweep_roofline,
             "per_config": per_config,
         }), flush=True)
         if args.dump:
             with open(args.dump, "w") as f:
-                json.dump({"shapes": shapes, "variant_times_ms": sweep_times, "chosen": chosen,
-                           "selected_ms": s_ms.tolist(), "default_ms": d_ms.tolist(),
-                           "chosen_variant_ms": t_ms.tolist(),
-                           "kernel_only_ms": enc_ms, "roofline_ms": (t_roof * 1e3).tolist(),
-                           "sm_count": None}, f)
+                json.dump({"shapes": shapes, "sm_count": sm,
+                           "records": {str(b): r for b, r in recs.items()},
+                           "dispatch_ms_8bit": s_ms.tolist(), "kernel_only_ms": enc_ms}, f)
 
 
 def main():

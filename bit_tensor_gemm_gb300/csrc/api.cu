@@ -11,12 +11,14 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
+#include <dlfcn.h>
 
 #include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <map>
 #include <mutex>
@@ -46,6 +48,7 @@ constexpr int kMaxDevices = 64;
 // M <= 4 runs on the dp4a kernel that streams B once (measured on GB300: at
 // one to four rows it beats the warp-MMA kernel, which pays for 16-row MMAs)
 constexpr int kSkinnyMaxM = 4;
+constexpr int64_t kSkinnyKernelMaxM = 16;  // rows the dp4a streaming kernel takes at most
 constexpr int kGroupM = 16;  // M-tiles per group of the tile order (L2 reuse)
 // 1-bit problems below this many bit-MACs go to the popcount kernel: there
 // the expansion pass and the second launch cost more than they save.
@@ -263,16 +266,71 @@ bool small_ok(int64_t M, int64_t N, int64_t K, const void* A, const void* B) {
 
 // ---- selection table --------------------------------------------------------------------
 
+// One table entry: the tile x stage variant measured fastest on the
+// tensor-core kernel (the label of [LBG] section 2, used by lbgemm_select and
+// lbgemm_run_encoded), and the kernel the default dispatch runs for the shape
+// (route and its parameter: the variant for LBGEMM_ROUTE_TABLE and
+// LBGEMM_ROUTE_POPC, the tile width for LBGEMM_ROUTE_FUSED, else 0).
+// route < 0: no measured route (the shape rules decide).
+struct Choice {
+  int variant = kDefaultVariant;
+  int route = -1;
+  int param = 0;
+};
+
 using Key = std::tuple<int, int, int64_t, int64_t, int64_t>;  // sm, bits, M, N, K
 std::mutex g_table_mu;
-std::map<Key, int> g_table;
+std::map<Key, Choice> g_table;
+std::once_flag g_table_once;
+std::string g_table_default_path;  // the file loaded at first use ("" if none)
+
+lbgemm_status table_load_file(const char* path);
+
+// The table shipped beside the library (data/lbgemm_table_gb300.txt next to
+// its lib/ directory), or the file named by LBGEMM_TABLE ("" or "none": no
+// table), loaded once per process before the first use of the table.
+void ensure_default_table() {
+  std::call_once(g_table_once, [] {
+    std::string path;
+    const char* env = std::getenv("LBGEMM_TABLE");
+    if (env) {
+      if (env[0] == '\0' || std::strcmp(env, "none") == 0) return;
+      path = env;
+    } else {
+      Dl_info info;
+      if (!dladdr(reinterpret_cast<void*>(&ensure_default_table), &info) || !info.dli_fname)
+        return;
+      std::string so = info.dli_fname;
+      const size_t slash = so.rfind('/');
+      const std::string libdir = slash == std::string::npos ? "." : so.substr(0, slash);
+      path = libdir + "/../data/lbgemm_table_gb300.txt";
+      FILE* probe = fopen(path.c_str(), "r");
+      if (!probe) return;  // no shipped table: selection starts empty
+      fclose(probe);
+    }
+    const std::string saved = t_last_error;
+    if (table_load_file(path.c_str()) != LBGEMM_OK) {
+      fprintf(stderr, "lbgemm: selection table %s not loaded: %s\n", path.c_str(),
+              t_last_error.c_str());
+      t_last_error = saved;
+      return;
+    }
+    g_table_default_path = path;
+  });
+}
+
+bool table_exact(int sm, int bits, int64_t M, int64_t N, int64_t K, Choice* out) {
+  ensure_default_table();
+  std::lock_guard<std::mutex> lock(g_table_mu);
+  auto it = g_table.find(Key{sm, bits, M, N, K});
+  if (it == g_table.end()) return false;
+  *out = it->second;
+  return true;
+}
 
 int table_select(int sm, int bits, int64_t M, int64_t N, int64_t K) {
-  {
-    std::lock_guard<std::mutex> lock(g_table_mu);
-    auto it = g_table.find(Key{sm, bits, M, N, K});
-    if (it != g_table.end()) return it->second;
-  }
+  Choice c;
+  if (table_exact(sm, bits, M, N, K, &c)) return c.variant;
   // not swept: the learned selector when one is loaded for this bit width
   const int v = lbg::mlp_pick(bits, M, N, K, sm);
   if (v >= 0) return v;
@@ -289,7 +347,7 @@ int table_select(int sm, int bits, int64_t M, int64_t N, int64_t K) {
                      std::fabs(ln - std::log2((double)std::get<3>(lo->first))) +
                      std::fabs(lk - std::log2((double)std::get<4>(lo->first)));
     if (!have || d < best_d - 1e-12) {
-      best = lo->second;
+      best = lo->second.variant;
       best_d = d;
       have = true;
     }
@@ -772,6 +830,154 @@ int route_of(int bits, int64_t M, int64_t N, int64_t K, const void* A, const voi
   return LBGEMM_ROUTE_TABLE;
 }
 
+// Whether the kernel of (route, param) runs this problem: its size limits,
+// K alignment and operand alignment.  Every tensor-core variant runs every
+// problem (LBGEMM_ROUTE_TABLE, param = variant).
+bool route_runs(int bits, int64_t M, int64_t N, int64_t K, const void* A, const void* B, int route,
+                int param) {
+  const bool a16 = K % 16 == 0 && aligned16(A) && aligned16(B);
+  const int64_t lo = std::min(M, N);
+  switch (route) {
+    case LBGEMM_ROUTE_TABLE: return param >= 0 && param < kNumVariants;
+    case LBGEMM_ROUTE_POPC: return bits == 1 && param >= 0 && param < kNumVariants;
+    case LBGEMM_ROUTE_SKINNY: return bits == 8 && M <= kSkinnyKernelMaxM && a16;
+    case LBGEMM_ROUTE_WARPMMA:
+      return bits == 8 && lo <= kWarpMmaMaxSideSmall && a16 &&
+             K <= lbg::hmma_skinny_max_k((int)lo);
+    case LBGEMM_ROUTE_SMALL: return bits == 8 && a16;
+    case LBGEMM_ROUTE_FUSED: return bits == 8 && (param == 64 || param == 128 || param == 256) && a16;
+    default: return false;
+  }
+}
+
+// The candidates the timing sweep measures for a shape (16-byte-aligned
+// operands): the nine tensor-core variants, and each shape-route kernel that
+// runs the problem within the domain where it can plausibly win (kept small
+// so the sweep ends in minutes): the 1-bit popcount kernel's nine variants
+// below 2^34 bit-MACs; the dp4a kernel streaming B for M <= 16; the warp-MMA
+// kernel for a small side of up to 256 rows; the one-launch dp4a kernel up to
+// 2^31 MACs and K <= 4096; the in-kernel conversion kernel at tile widths 64
+// and 128 (and 256 once the small side exceeds 64 rows) for a small side of
+// up to 1024 rows.
+int candidate_list(int bits, int64_t M, int64_t N, int64_t K, int* routes, int* params, int max) {
+  const void* al = reinterpret_cast<const void*>(uintptr_t(256));
+  int n = 0;
+  auto add = [&](int r, int p) {
+    if (n < max) {
+      routes[n] = r;
+      params[n] = p;
+    }
+    ++n;
+  };
+  for (int v = 0; v < kNumVariants; ++v) add(LBGEMM_ROUTE_TABLE, v);
+  const double work = (double)M * (double)N * (double)K;
+  const int64_t lo = std::min(M, N);
+  if (bits == 1 && work < 17179869184.0)
+    for (int v = 0; v < kNumVariants; ++v) add(LBGEMM_ROUTE_POPC, v);
+  if (bits != 8 || K % 16) return n;
+  if (route_runs(8, M, N, K, al, al, LBGEMM_ROUTE_SKINNY, 0)) add(LBGEMM_ROUTE_SKINNY, 0);
+  if (route_runs(8, M, N, K, al, al, LBGEMM_ROUTE_WARPMMA, 0)) add(LBGEMM_ROUTE_WARPMMA, 0);
+  if (work <= 2147483648.0 && K <= 4096) add(LBGEMM_ROUTE_SMALL, 0);
+  if (lo <= 1024) {
+    add(LBGEMM_ROUTE_FUSED, 64);
+    add(LBGEMM_ROUTE_FUSED, 128);
+    if (lo > 64) add(LBGEMM_ROUTE_FUSED, 256);
+  }
+  return n;
+}
+
+// The kernel the default dispatch runs: the table's measured route for the
+// exact shape when it has one that runs these operands, else the shape rules
+// (route_of), with the variant from table_select on the tensor-core route.
+struct Pick {
+  int route = LBGEMM_ROUTE_NONE;
+  int param = 0;
+};
+
+Pick pick_route(int sm, int bits, int64_t M, int64_t N, int64_t K, const void* A, const void* B) {
+  Pick p;
+  if (M == 0 || N == 0) return p;
+  Choice c;
+  if (table_exact(sm, bits, M, N, K, &c) && c.route >= 0 &&
+      route_runs(bits, M, N, K, A, B, c.route, c.param)) {
+    p.route = c.route;
+    p.param = c.param;
+    return p;
+  }
+  int tile = 0, fuse = 0;
+  p.route = route_of(bits, M, N, K, A, B, false, &tile, &fuse);
+  p.param = p.route == LBGEMM_ROUTE_TABLE   ? table_select(sm, bits, M, N, K)
+            : p.route == LBGEMM_ROUTE_POPC  ? kDefaultVariant
+            : p.route == LBGEMM_ROUTE_FUSED ? tile
+                                            : 0;
+  return p;
+}
+
+// Scratch bytes of a route: both re-encoded operands on the tensor-core
+// route, the re-encoded smaller operand on the in-kernel conversion route,
+// none elsewhere.
+size_t route_scratch(int bits, int64_t M, int64_t N, int64_t K, const Pick& p) {
+  if (p.route == LBGEMM_ROUTE_TABLE) return enc_bytes(bits, M, K) + enc_bytes(bits, N, K);
+  if (p.route == LBGEMM_ROUTE_FUSED) return enc_bytes(8, std::min(M, N), K);
+  return 0;
+}
+
+// Runs one route on checked arguments.  Scratch: the caller's `ws` when
+// internal_ws is false (checked here), else the per-device buffer.
+lbgemm_status run_route(DeviceState& d, int bits, int64_t M, int64_t N, int64_t K, const void* A,
+                        const void* B, int32_t* C, const Pick& p, void* ws, size_t ws_bytes,
+                        bool internal_ws, cudaStream_t stream) {
+  cudaError_t e;
+  switch (p.route) {
+    case LBGEMM_ROUTE_NONE: return LBGEMM_OK;
+    case LBGEMM_ROUTE_POPC:
+      // XOR + popcount on CUDA cores, no re-encoding
+      e = lbg::launch_b1_popc(p.param / 3, p.param % 3 + 2, static_cast<const uint32_t*>(A),
+                              static_cast<const uint32_t*>(B), M, N, K, C, stream);
+      if (e != cudaSuccess) return cuda_fail(e, "1-bit popcount GEMM launch");
+      g_launches += 1;
+      return LBGEMM_OK;
+    case LBGEMM_ROUTE_SKINNY:
+      e = lbg::launch_skinny_s8(static_cast<const int8_t*>(A), static_cast<const int8_t*>(B),
+                                (int)M, (int)N, (int)K, C, nullptr, nullptr, nullptr, d.sm_count,
+                                stream);
+      if (e != cudaSuccess) return cuda_fail(e, "skinny GEMM launch");
+      g_launches += 1;
+      return LBGEMM_OK;
+    case LBGEMM_ROUTE_WARPMMA:
+      return run_warpmma(d, M, N, K, static_cast<const int8_t*>(A), static_cast<const int8_t*>(B),
+                         C, nullptr, nullptr, nullptr, stream);
+    case LBGEMM_ROUTE_SMALL:
+      e = lbg::launch_small_s8(static_cast<const int8_t*>(A), static_cast<const int8_t*>(B), M, N,
+                               K, C, stream);
+      if (e != cudaSuccess) return cuda_fail(e, "small GEMM launch");
+      g_launches += 1;
+      return LBGEMM_OK;
+    default: break;
+  }
+  const size_t need = route_scratch(bits, M, N, K, p);
+  if (!internal_ws) {
+    if (!ws || ws_bytes < need)
+      return fail(LBGEMM_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need, ws_bytes);
+    if ((reinterpret_cast<uintptr_t>(ws) & 255) != 0)
+      return fail(LBGEMM_ERR_ALIGNMENT, "workspace must be 256-byte aligned");
+    if (p.route == LBGEMM_ROUTE_FUSED)
+      return run_tc_fused(d, N >= M, p.param, M, N, K, A, B, C, nullptr, nullptr, nullptr, ws,
+                          stream);
+    return run_tc(d, bits, M, N, K, A, B, C, nullptr, nullptr, nullptr, p.param, ws, stream);
+  }
+  std::lock_guard<std::mutex> lock(g_ws_mu);
+  lbgemm_status st = scratch_acquire(d.ws, need, stream);
+  if (st != LBGEMM_OK) return st;
+  if (p.route == LBGEMM_ROUTE_FUSED)
+    st = run_tc_fused(d, N >= M, p.param, M, N, K, A, B, C, nullptr, nullptr, nullptr, d.ws.ptr,
+                      stream);
+  else
+    st = run_tc(d, bits, M, N, K, A, B, C, nullptr, nullptr, nullptr, p.param, d.ws.ptr, stream);
+  lbgemm_status st2 = scratch_release(d.ws, stream);
+  return st != LBGEMM_OK ? st : st2;
+}
+
 lbgemm_status run_any(int bits, int64_t M, int64_t N, int64_t K, const void* A, const void* B,
                       int32_t* C, int variant, void* ws, size_t ws_bytes, bool internal_ws,
                       cudaStream_t stream) {
@@ -783,69 +989,14 @@ lbgemm_status run_any(int bits, int64_t M, int64_t N, int64_t K, const void* A, 
   DeviceState* d = nullptr;
   st = device_state(&d);
   if (st != LBGEMM_OK) return st;
-  const bool auto_pick = variant < 0;
-  if (auto_pick) variant = table_select(d->sm_count, bits, M, N, K);
-  cudaError_t e;
-  int fuse_tile = 0, fuse = 0;
-  const int route =
-      auto_pick ? route_of(bits, M, N, K, A, B, false, &fuse_tile, &fuse) : LBGEMM_ROUTE_TABLE;
-  if (route == LBGEMM_ROUTE_POPC) {
-    // Small 1-bit problems: XOR + popcount on CUDA cores, no re-encoding.
-    e = lbg::launch_b1_popc(kDefaultVariant / 3, kDefaultVariant % 3 + 2,
-                            static_cast<const uint32_t*>(A), static_cast<const uint32_t*>(B), M, N,
-                            K, C, stream);
-    if (e != cudaSuccess) return cuda_fail(e, "1-bit popcount GEMM launch");
-    g_launches += 1;
-    return LBGEMM_OK;
+  Pick p;
+  if (variant < 0) {
+    p = pick_route(d->sm_count, bits, M, N, K, A, B);
+  } else {
+    p.route = LBGEMM_ROUTE_TABLE;
+    p.param = variant;
   }
-  if (route == LBGEMM_ROUTE_SKINNY) {
-    e = lbg::launch_skinny_s8(static_cast<const int8_t*>(A), static_cast<const int8_t*>(B), (int)M,
-                              (int)N, (int)K, C, nullptr, nullptr, nullptr, d->sm_count, stream);
-    if (e != cudaSuccess) return cuda_fail(e, "skinny GEMM launch");
-    g_launches += 1;
-    return LBGEMM_OK;
-  }
-  if (route == LBGEMM_ROUTE_WARPMMA)
-    return run_warpmma(*d, M, N, K, static_cast<const int8_t*>(A), static_cast<const int8_t*>(B),
-                       C, nullptr, nullptr, nullptr, stream);
-  if (route == LBGEMM_ROUTE_SMALL) {
-    e = lbg::launch_small_s8(static_cast<const int8_t*>(A), static_cast<const int8_t*>(B), M, N, K,
-                             C, stream);
-    if (e != cudaSuccess) return cuda_fail(e, "small GEMM launch");
-    g_launches += 1;
-    return LBGEMM_OK;
-  }
-  if (route == LBGEMM_ROUTE_FUSED) {
-    const size_t need_f = enc_bytes(8, fuse == 1 ? M : N, K);
-    if (!internal_ws) {
-      if (!ws || ws_bytes < need_f)
-        return fail(LBGEMM_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need_f,
-                    ws_bytes);
-      return run_tc_fused(*d, fuse == 1, fuse_tile, M, N, K, A, B, C, nullptr, nullptr, nullptr, ws,
-                          stream);
-    }
-    std::lock_guard<std::mutex> lock(g_ws_mu);
-    st = scratch_acquire(d->ws, need_f, stream);
-    if (st != LBGEMM_OK) return st;
-    st = run_tc_fused(*d, fuse == 1, fuse_tile, M, N, K, A, B, C, nullptr, nullptr, nullptr, d->ws.ptr,
-                      stream);
-    lbgemm_status st2 = scratch_release(d->ws, stream);
-    return st != LBGEMM_OK ? st : st2;
-  }
-  const size_t need = enc_bytes(bits, M, K) + enc_bytes(bits, N, K);
-  if (!internal_ws) {
-    if (!ws || ws_bytes < need)
-      return fail(LBGEMM_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need, ws_bytes);
-    if ((reinterpret_cast<uintptr_t>(ws) & 255) != 0)
-      return fail(LBGEMM_ERR_ALIGNMENT, "workspace must be 256-byte aligned");
-    return run_tc(*d, bits, M, N, K, A, B, C, nullptr, nullptr, nullptr, variant, ws, stream);
-  }
-  std::lock_guard<std::mutex> lock(g_ws_mu);
-  st = scratch_acquire(d->ws, need, stream);
-  if (st != LBGEMM_OK) return st;
-  st = run_tc(*d, bits, M, N, K, A, B, C, nullptr, nullptr, nullptr, variant, d->ws.ptr, stream);
-  lbgemm_status st2 = scratch_release(d->ws, stream);
-  return st != LBGEMM_OK ? st : st2;
+  return run_route(*d, bits, M, N, K, A, B, C, p, ws, ws_bytes, internal_ws, stream);
 }
 
 lbgemm_status run_linear(int64_t M, int64_t N, int64_t K, const int8_t* X, const float* sx,
@@ -890,6 +1041,52 @@ lbgemm_status run_linear(int64_t M, int64_t N, int64_t K, const int8_t* X, const
   st = run_tc(*d, 8, M, N, K, X, W, nullptr, sx, sw, Y, variant, d->ws.ptr, stream);
   lbgemm_status st2 = scratch_release(d->ws, stream);
   return st != LBGEMM_OK ? st : st2;
+}
+
+// A table entry's route must be one the dispatch can run at the entry's sizes
+// (16-byte-aligned operands; the 8-bit routes need K % 16 == 0).
+bool entry_route_ok(int bits, int64_t M, int64_t N, int64_t K, int route, int param) {
+  const void* al = reinterpret_cast<const void*>(uintptr_t(256));
+  return route >= 0 && route < LBGEMM_ROUTE_NONE && route_runs(bits, M, N, K, al, al, route, param);
+}
+
+// Reads "sm_count bits M N K variant [route param]" lines ('#' comments) and
+// merges them into the table; nothing is merged if any line is malformed.
+lbgemm_status table_load_file(const char* path) {
+  if (!path) return fail(LBGEMM_ERR_INVALID_ARG, "null path");
+  FILE* f = fopen(path, "r");
+  if (!f) return fail(LBGEMM_ERR_INVALID_ARG, "cannot open %s", path);
+  std::vector<std::pair<Key, Choice>> rows;
+  char line[256];
+  int lineno = 0;
+  while (fgets(line, sizeof line, f)) {
+    ++lineno;
+    const char* s = line;
+    while (*s == ' ' || *s == '\t') ++s;
+    if (*s == '#' || *s == '\n' || *s == '\0') continue;
+    int sm, bits, v, route = -1, param = 0;
+    long long M, N, K;
+    char extra[2];
+    const int got = sscanf(s, "%d %d %lld %lld %lld %d %d %d %1s", &sm, &bits, &M, &N, &K, &v,
+                           &route, &param, extra);
+    const bool shape_ok = (got == 6 || got == 8) && sm >= 1 &&
+                          (bits == 8 || bits == 4 || bits == 1) && M >= 1 && N >= 1 && K >= 1 &&
+                          v >= 0 && v < kNumVariants;
+    if (got == 6) route = -1;
+    if (!shape_ok || (got == 8 && !entry_route_ok(bits, M, N, K, route, param))) {
+      fclose(f);
+      return fail(LBGEMM_ERR_INVALID_ARG, "%s:%d: malformed table line", path, lineno);
+    }
+    Choice c;
+    c.variant = v;
+    c.route = route;
+    c.param = route >= 0 ? param : 0;
+    rows.push_back({Key{sm, bits, M, N, K}, c});
+  }
+  fclose(f);
+  std::lock_guard<std::mutex> lock(g_table_mu);
+  for (auto& r : rows) g_table[r.first] = r.second;
+  return LBGEMM_OK;
 }
 
 cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
@@ -1139,6 +1336,43 @@ int lbgemm_route(int bits, int64_t M, int64_t N, int64_t K, int linear, int* til
   return r;
 }
 
+int lbgemm_dispatch_for(int sm_count, int bits, int64_t M, int64_t N, int64_t K, int* param) {
+  if ((bits != 8 && bits != 4 && bits != 1) || M < 0 || N < 0 || K < 1 || sm_count < 1) return -1;
+  const void* aligned = reinterpret_cast<const void*>(uintptr_t(256));
+  const Pick p = pick_route(sm_count, bits, M, N, K, aligned, aligned);
+  if (param) *param = p.param;
+  return p.route;
+}
+
+int lbgemm_candidates(int bits, int64_t M, int64_t N, int64_t K, int* routes, int* params,
+                      int max) {
+  if ((bits != 8 && bits != 4 && bits != 1) || M < 1 || N < 1 || K < 1 || max < 0) return -1;
+  if (max > 0 && (!routes || !params)) return -1;
+  return candidate_list(bits, M, N, K, routes, params, max);
+}
+
+lbgemm_status lbgemm_run_candidate(int bits, int64_t M, int64_t N, int64_t K, const void* A,
+                                   const void* B, int32_t* C, int route, int param,
+                                   void* stream) {
+  try {
+    lbgemm_status st = check_gemm_args(bits, M, N, K, A, B, C);
+    if (st != LBGEMM_OK) return st;
+    if (!route_runs(bits, std::max<int64_t>(M, 1), std::max<int64_t>(N, 1), K, A, B, route, param))
+      return fail(LBGEMM_ERR_INVALID_ARG, "route %d (param %d) cannot run this problem", route,
+                  param);
+    if (M == 0 || N == 0) return LBGEMM_OK;
+    DeviceState* d = nullptr;
+    st = device_state(&d);
+    if (st != LBGEMM_OK) return st;
+    Pick p;
+    p.route = route;
+    p.param = param;
+    return run_route(*d, bits, M, N, K, A, B, C, p, nullptr, 0, true, as_stream(stream));
+  } catch (...) {
+    return fail(LBGEMM_ERR_CUDA, "internal error");
+  }
+}
+
 int lbgemm_select_for(int sm_count, int bits, int64_t M, int64_t N, int64_t K) {
   if ((bits != 8 && bits != 4 && bits != 1) || M < 1 || N < 1 || K < 1) return -1;
   return table_select(sm_count, bits, M, N, K);
@@ -1152,12 +1386,36 @@ int lbgemm_select(int bits, int64_t M, int64_t N, int64_t K) {
 
 lbgemm_status lbgemm_table_set_for(int sm_count, int bits, int64_t M, int64_t N, int64_t K,
                                    int variant) {
+  return lbgemm_table_set_choice_for(sm_count, bits, M, N, K, variant, -1, 0);
+}
+
+lbgemm_status lbgemm_table_set_choice_for(int sm_count, int bits, int64_t M, int64_t N, int64_t K,
+                                          int variant, int route, int param) {
   if ((bits != 8 && bits != 4 && bits != 1) || M < 1 || N < 1 || K < 1 || sm_count < 1 ||
       variant < 0 || variant >= kNumVariants)
     return fail(LBGEMM_ERR_INVALID_ARG, "bad table entry");
+  if (route >= 0 && !entry_route_ok(bits, M, N, K, route, param))
+    return fail(LBGEMM_ERR_INVALID_ARG, "route %d (param %d) cannot run %d-bit %lldx%lldx%lld",
+                route, param, bits, (long long)M, (long long)N, (long long)K);
+  ensure_default_table();
   std::lock_guard<std::mutex> lock(g_table_mu);
-  g_table[Key{sm_count, bits, M, N, K}] = variant;
+  Choice c;
+  c.variant = variant;
+  c.route = route >= 0 ? route : -1;
+  c.param = route >= 0 ? param : 0;
+  g_table[Key{sm_count, bits, M, N, K}] = c;
   return LBGEMM_OK;
+}
+
+int lbgemm_table_get_for(int sm_count, int bits, int64_t M, int64_t N, int64_t K, int* variant,
+                         int* route, int* param) {
+  if ((bits != 8 && bits != 4 && bits != 1) || M < 1 || N < 1 || K < 1 || sm_count < 1) return -1;
+  Choice c;
+  if (!table_exact(sm_count, bits, M, N, K, &c)) return 0;
+  if (variant) *variant = c.variant;
+  if (route) *route = c.route;
+  if (param) *param = c.param;
+  return 1;
 }
 
 lbgemm_status lbgemm_table_set(int bits, int64_t M, int64_t N, int64_t K, int variant) {
@@ -1168,114 +1426,146 @@ lbgemm_status lbgemm_table_set(int bits, int64_t M, int64_t N, int64_t K, int va
 }
 
 lbgemm_status lbgemm_table_clear(void) {
+  ensure_default_table();
   std::lock_guard<std::mutex> lock(g_table_mu);
   g_table.clear();
   return LBGEMM_OK;
 }
 
 int64_t lbgemm_table_size(void) {
+  ensure_default_table();
   std::lock_guard<std::mutex> lock(g_table_mu);
   return (int64_t)g_table.size();
 }
 
+const char* lbgemm_table_default_path(void) {
+  ensure_default_table();
+  return g_table_default_path.c_str();
+}
+
 lbgemm_status lbgemm_table_load(const char* path) {
-  if (!path) return fail(LBGEMM_ERR_INVALID_ARG, "null path");
-  FILE* f = fopen(path, "r");
-  if (!f) return fail(LBGEMM_ERR_INVALID_ARG, "cannot open %s", path);
-  std::vector<std::pair<Key, int>> rows;
-  char line[256];
-  int lineno = 0;
-  while (fgets(line, sizeof line, f)) {
-    ++lineno;
-    const char* s = line;
-    while (*s == ' ' || *s == '\t') ++s;
-    if (*s == '#' || *s == '\n' || *s == '\0') continue;
-    int sm, bits, v;
-    long long M, N, K;
-    if (sscanf(s, "%d %d %lld %lld %lld %d", &sm, &bits, &M, &N, &K, &v) != 6 || sm < 1 ||
-        (bits != 8 && bits != 4 && bits != 1) || M < 1 || N < 1 || K < 1 || v < 0 ||
-        v >= kNumVariants) {
-      fclose(f);
-      return fail(LBGEMM_ERR_INVALID_ARG, "%s:%d: malformed table line", path, lineno);
-    }
-    rows.push_back({Key{sm, bits, M, N, K}, v});
-  }
-  fclose(f);
-  std::lock_guard<std::mutex> lock(g_table_mu);
-  for (auto& r : rows) g_table[r.first] = r.second;
-  return LBGEMM_OK;
+  ensure_default_table();
+  return table_load_file(path);
 }
 
 lbgemm_status lbgemm_table_save(const char* path) {
   if (!path) return fail(LBGEMM_ERR_INVALID_ARG, "null path");
+  ensure_default_table();
   FILE* f = fopen(path, "w");
   if (!f) return fail(LBGEMM_ERR_INVALID_ARG, "cannot write %s", path);
-  fprintf(f, "# sm_count bits M N K variant\n");
+  fprintf(f, "# sm_count bits M N K variant [route param]\n");
   {
     std::lock_guard<std::mutex> lock(g_table_mu);
-    for (auto& kv : g_table)
-      fprintf(f, "%d %d %lld %lld %lld %d\n", std::get<0>(kv.first), std::get<1>(kv.first),
+    for (auto& kv : g_table) {
+      fprintf(f, "%d %d %lld %lld %lld %d", std::get<0>(kv.first), std::get<1>(kv.first),
               (long long)std::get<2>(kv.first), (long long)std::get<3>(kv.first),
-              (long long)std::get<4>(kv.first), kv.second);
+              (long long)std::get<4>(kv.first), kv.second.variant);
+      if (kv.second.route >= 0) fprintf(f, " %d %d", kv.second.route, kv.second.param);
+      fprintf(f, "\n");
+    }
   }
-  fclose(f);
-  return LBGEMM_OK;
+  const bool ok = fclose(f) == 0;
+  return ok ? LBGEMM_OK : fail(LBGEMM_ERR_INVALID_ARG, "cannot write %s", path);
 }
 
-int lbgemm_choose(const float* times, int default_variant, float keep_within) {
-  if (!times || default_variant < 0 || default_variant >= kNumVariants || keep_within < 0)
+int lbgemm_choose_candidate(const float* times, int count, int default_index,
+                            float keep_within) {
+  if (!times || count < 1 || default_index < 0 || default_index >= count || !(keep_within >= 0))
     return -1;
   int best = 0;
-  for (int i = 0; i < kNumVariants; ++i) {
+  for (int i = 0; i < count; ++i) {
     if (!(times[i] >= 0)) return -1;  // rejects NaN and negatives
     if (times[i] < times[best]) best = i;
   }
-  if (times[default_variant] <= times[best] * (1.0f + keep_within)) return default_variant;
+  if (times[default_index] <= times[best] * (1.0f + keep_within)) return default_index;
   return best;
+}
+
+int lbgemm_choose(const float* times, int default_variant, float keep_within) {
+  return lbgemm_choose_candidate(times, kNumVariants, default_variant, keep_within);
+}
+
+lbgemm_status lbgemm_time_candidates(int bits, int64_t M, int64_t N, int64_t K, const void* A,
+                                     const void* B, int32_t* C, int count, const int* routes,
+                                     const int* params, int warmup, int reps, int flush_l2,
+                                     float* times, void* stream) {
+  try {
+    if (!times || !routes || !params || count < 1 || reps < 1 || warmup < 0)
+      return fail(LBGEMM_ERR_INVALID_ARG, "bad timing args");
+    lbgemm_status st = check_gemm_args(bits, M, N, K, A, B, C);
+    if (st != LBGEMM_OK) return st;
+    if (M == 0 || N == 0) return fail(LBGEMM_ERR_INVALID_ARG, "nothing to time (M or N is 0)");
+    for (int c = 0; c < count; ++c)
+      if (!route_runs(bits, M, N, K, A, B, routes[c], params[c]))
+        return fail(LBGEMM_ERR_INVALID_ARG, "candidate %d (route %d, param %d) cannot run this "
+                    "problem", c, routes[c], params[c]);
+    cudaStream_t s = as_stream(stream);
+    DeviceState* d = nullptr;
+    st = device_state(&d);
+    if (st != LBGEMM_OK) return st;
+    if (flush_l2) {
+      std::lock_guard<std::mutex> lock(g_mu);
+      st = scratch_acquire(d->flush, kFlushBytes, s);
+      if (st != LBGEMM_OK) return st;
+    }
+    auto run = [&](int c) {
+      Pick p;
+      p.route = routes[c];
+      p.param = params[c];
+      return run_route(*d, bits, M, N, K, A, B, C, p, nullptr, 0, true, s);
+    };
+    for (int c = 0; c < count && st == LBGEMM_OK; ++c)
+      for (int w = 0; w < warmup && st == LBGEMM_OK; ++w) st = run(c);
+    if (st != LBGEMM_OK) return st;
+    // one event pair per candidate, reused every round; each round runs every
+    // candidate once (interleaved, so a drift of the clocks touches them all
+    // alike) and is read back before the next
+    std::vector<cudaEvent_t> ev(2 * (size_t)count, nullptr);
+    cudaError_t e = cudaSuccess;
+    for (auto& x : ev)
+      if (e == cudaSuccess) e = cudaEventCreate(&x);
+    std::vector<std::vector<float>> samples(count, std::vector<float>(reps));
+    for (int r = 0; r < reps && e == cudaSuccess && st == LBGEMM_OK; ++r) {
+      for (int c = 0; c < count && e == cudaSuccess && st == LBGEMM_OK; ++c) {
+        if (flush_l2) e = cudaMemsetAsync(d->flush.ptr, r & 0xFF, kFlushBytes, s);
+        if (e == cudaSuccess) e = cudaEventRecord(ev[2 * c], s);
+        if (e == cudaSuccess) st = run(c);
+        if (e == cudaSuccess && st == LBGEMM_OK) e = cudaEventRecord(ev[2 * c + 1], s);
+      }
+      if (e == cudaSuccess && st == LBGEMM_OK) e = cudaEventSynchronize(ev[2 * count - 1]);
+      for (int c = 0; c < count && e == cudaSuccess && st == LBGEMM_OK; ++c)
+        e = cudaEventElapsedTime(&samples[c][r], ev[2 * c], ev[2 * c + 1]);
+    }
+    for (auto& x : ev)
+      if (x) cudaEventDestroy(x);
+    if (e != cudaSuccess) return cuda_fail(e, "timing");
+    if (st != LBGEMM_OK) return st;
+    if (flush_l2) {
+      std::lock_guard<std::mutex> lock(g_mu);
+      st = scratch_release(d->flush, s);
+      if (st != LBGEMM_OK) return st;
+    }
+    for (int c = 0; c < count; ++c) {
+      std::sort(samples[c].begin(), samples[c].end());
+      times[c] = reps % 2 ? samples[c][reps / 2]
+                          : 0.5f * (samples[c][reps / 2 - 1] + samples[c][reps / 2]);
+    }
+    return LBGEMM_OK;
+  } catch (...) {
+    return fail(LBGEMM_ERR_CUDA, "internal error");
+  }
 }
 
 lbgemm_status lbgemm_time_variants(int bits, int64_t M, int64_t N, int64_t K, const void* A,
                                    const void* B, int32_t* C, int warmup, int reps, int flush_l2,
                                    float* times, void* stream) {
-  if (!times || reps < 1 || warmup < 0) return fail(LBGEMM_ERR_INVALID_ARG, "bad timing args");
-  cudaStream_t s = as_stream(stream);
-  DeviceState* d = nullptr;
-  lbgemm_status st0 = device_state(&d);
-  if (st0 != LBGEMM_OK) return st0;
-  if (flush_l2) {
-    std::lock_guard<std::mutex> lock(g_mu);
-    st0 = scratch_acquire(d->flush, kFlushBytes, s);
-    if (st0 != LBGEMM_OK) return st0;
+  int routes[kNumVariants], params[kNumVariants];
+  for (int v = 0; v < kNumVariants; ++v) {
+    routes[v] = LBGEMM_ROUTE_TABLE;
+    params[v] = v;
   }
-  cudaEvent_t e0, e1;
-  if (cudaEventCreate(&e0) != cudaSuccess || cudaEventCreate(&e1) != cudaSuccess)
-    return fail(LBGEMM_ERR_CUDA, "cudaEventCreate");
-  lbgemm_status st = LBGEMM_OK;
-  std::vector<float> samples(reps);
-  for (int v = 0; v < kNumVariants && st == LBGEMM_OK; ++v) {
-    for (int w = 0; w < warmup && st == LBGEMM_OK; ++w)
-      st = lbgemm_run_variant(bits, M, N, K, A, B, C, v, stream);
-    for (int r = 0; r < reps && st == LBGEMM_OK; ++r) {
-      if (flush_l2) cudaMemsetAsync(d->flush.ptr, r & 0xFF, kFlushBytes, s);
-      cudaEventRecord(e0, s);
-      st = lbgemm_run_variant(bits, M, N, K, A, B, C, v, stream);
-      cudaEventRecord(e1, s);
-      if (st != LBGEMM_OK) break;
-      cudaError_t e = cudaEventSynchronize(e1);
-      if (e != cudaSuccess) {
-        st = cuda_fail(e, "timing");
-        break;
-      }
-      cudaEventElapsedTime(&samples[r], e0, e1);
-    }
-    if (st == LBGEMM_OK) {
-      std::sort(samples.begin(), samples.end());
-      times[v] = samples[reps / 2];
-    }
-  }
-  cudaEventDestroy(e0);
-  cudaEventDestroy(e1);
-  return st;
+  return lbgemm_time_candidates(bits, M, N, K, A, B, C, kNumVariants, routes, params, warmup,
+                                reps, flush_l2, times, stream);
 }
 
 // Blocks of a host-buffer call: the larger of M and N is cut into blocks of
@@ -1483,6 +1773,31 @@ const char* lbgemm_last_error(void) { return t_last_error.c_str(); }
 namespace lbg {
 lbgemm_status report_error(lbgemm_status st, const char* message) {
   return fail(st, "%s", message);
+}
+
+// Scratch bytes that lbgemm_run_ws(bits, M, N, K, A, B, C, variant, ...)
+// needs: the route the dispatch takes (variant < 0) or the tensor-core
+// variant's.  Argument errors are reported as that call reports them.
+lbgemm_status scratch_for_call(int bits, int64_t M, int64_t N, int64_t K, const void* A,
+                               const void* B, const void* C, int variant, size_t* bytes) {
+  *bytes = 0;
+  lbgemm_status st = check_gemm_args(bits, M, N, K, A, B, C);
+  if (st != LBGEMM_OK) return st;
+  if (variant < -1 || variant >= kNumVariants)
+    return fail(LBGEMM_ERR_INVALID_ARG, "variant %d out of range", variant);
+  if (M == 0 || N == 0) return LBGEMM_OK;
+  DeviceState* d = nullptr;
+  st = device_state(&d);
+  if (st != LBGEMM_OK) return st;
+  Pick p;
+  if (variant < 0) {
+    p = pick_route(d->sm_count, bits, M, N, K, A, B);
+  } else {
+    p.route = LBGEMM_ROUTE_TABLE;
+    p.param = variant;
+  }
+  *bytes = route_scratch(bits, M, N, K, p);
+  return LBGEMM_OK;
 }
 }  // namespace lbg
 

@@ -11,6 +11,8 @@
 
 namespace lbg {
 lbgemm_status report_error(lbgemm_status st, const char* message);
+lbgemm_status scratch_for_call(int bits, int64_t M, int64_t N, int64_t K, const void* A,
+                               const void* B, const void* C, int variant, size_t* bytes);
 }
 
 namespace {
@@ -52,7 +54,12 @@ lbgemm_status scratch_address(void** out) {
 extern "C" lbgemm_status lbgemm_run_static(int bits, int64_t M, int64_t N, int64_t K,
                                            const void* A, const void* B, int32_t* C, int variant,
                                            void* stream) {
-  const size_t need = lbgemm_workspace_size(bits, M, N, K);
+  // the scratch of the route this call takes: both re-encoded operands on the
+  // tensor-core route, one on the in-kernel conversion route, none on the
+  // routes that read int8 directly
+  size_t need = 0;
+  lbgemm_status st = lbg::scratch_for_call(bits, M, N, K, A, B, C, variant, &need);
+  if (st != LBGEMM_OK) return st;
   if (need > kStaticScratchBytes) {
     char msg[256];
     snprintf(msg, sizeof msg,
@@ -61,11 +68,9 @@ extern "C" lbgemm_status lbgemm_run_static(int bits, int64_t M, int64_t N, int64
              need, kStaticScratchBytes);
     return lbg::report_error(LBGEMM_ERR_WORKSPACE, msg);
   }
-  if (need == 0) {  // no scratch needed (or arguments the checks below reject)
-    return lbgemm_run_ws(bits, M, N, K, A, B, C, variant, nullptr, 0, stream);
-  }
+  if (M == 0 || N == 0) return LBGEMM_OK;
   void* scratch = nullptr;
-  lbgemm_status st = scratch_address(&scratch);
+  st = scratch_address(&scratch);
   if (st != LBGEMM_OK) return st;
   return lbgemm_run_ws(bits, M, N, K, A, B, C, variant, scratch, kStaticScratchBytes, stream);
 }

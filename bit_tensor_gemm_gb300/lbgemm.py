@@ -62,12 +62,21 @@ _SIGNATURES = {
     "lbgemm_table_set": (_i32, [_i32, _i64, _i64, _i64, _i32]),
     "lbgemm_select_for": (_i32, [_i32, _i32, _i64, _i64, _i64]),
     "lbgemm_route": (_i32, [_i32, _i64, _i64, _i64, _i32, _vp]),
+    "lbgemm_dispatch_for": (_i32, [_i32, _i32, _i64, _i64, _i64, _vp]),
+    "lbgemm_candidates": (_i32, [_i32, _i64, _i64, _i64, _vp, _vp, _i32]),
+    "lbgemm_run_candidate": (_i32, [_i32, _i64, _i64, _i64, _vp, _vp, _vp, _i32, _i32, _vp]),
+    "lbgemm_time_candidates": (_i32, [_i32, _i64, _i64, _i64, _vp, _vp, _vp, _i32, _vp, _vp, _i32,
+                                      _i32, _i32, _vp, _vp]),
+    "lbgemm_table_set_choice_for": (_i32, [_i32, _i32, _i64, _i64, _i64, _i32, _i32, _i32]),
+    "lbgemm_table_get_for": (_i32, [_i32, _i32, _i64, _i64, _i64, _vp, _vp, _vp]),
+    "lbgemm_table_default_path": (ctypes.c_char_p, []),
     "lbgemm_table_set_for": (_i32, [_i32, _i32, _i64, _i64, _i64, _i32]),
     "lbgemm_table_clear": (_i32, []),
     "lbgemm_table_size": (_i64, []),
     "lbgemm_table_load": (_i32, [ctypes.c_char_p]),
     "lbgemm_table_save": (_i32, [ctypes.c_char_p]),
     "lbgemm_choose": (_i32, [_vp, _i32, _f32]),
+    "lbgemm_choose_candidate": (_i32, [_vp, _i32, _i32, _f32]),
     "lbgemm_mlp_load": (_i32, [ctypes.c_char_p]),
     "lbgemm_mlp_clear": (_i32, []),
     "lbgemm_mlp_predict": (_i32, [_i32, _i64, _i64, _i64, _i32, _vp]),
@@ -251,6 +260,63 @@ def lbgemm_route(bits, M, N, K, linear=False):
     return r, t.value
 
 
+def lbgemm_dispatch_for(sm_count, bits, M, N, K):
+    """(route, param) that lbgemm_run runs for 16-byte-aligned operands on a
+    device with sm_count SMs: the table's measured route, else the shape rules."""
+    prm = ctypes.c_int(0)
+    r = load().lbgemm_dispatch_for(sm_count, bits, M, N, K, ctypes.byref(prm))
+    if r < 0:
+        raise LbgemmError(ERR_INVALID_ARG, f"lbgemm_dispatch_for({bits}, {M}, {N}, {K}): bad arguments")
+    return r, prm.value
+
+
+def lbgemm_candidates(bits, M, N, K) -> list:
+    """The (route, param) candidates the timing sweep measures for a shape."""
+    n = load().lbgemm_candidates(bits, M, N, K, None, None, 0)
+    if n < 0:
+        raise LbgemmError(ERR_INVALID_ARG, f"lbgemm_candidates({bits}, {M}, {N}, {K}): bad arguments")
+    routes, params = (ctypes.c_int * n)(), (ctypes.c_int * n)()
+    load().lbgemm_candidates(bits, M, N, K, ctypes.addressof(routes), ctypes.addressof(params), n)
+    return list(zip(routes, params))
+
+
+def lbgemm_run_candidate(bits, M, N, K, A, B, C, route, param, stream=None) -> None:
+    _check(load().lbgemm_run_candidate(bits, M, N, K, _addr(A), _addr(B), _addr(C), route, param,
+                                       _stream(stream)))
+
+
+def lbgemm_time_candidates(bits, M, N, K, A, B, C, candidates, warmup=1, reps=5, flush_l2=True,
+                           stream=None) -> list:
+    """Median milliseconds of each (route, param) candidate, interleaved runs."""
+    n = len(candidates)
+    routes = (ctypes.c_int * n)(*[int(r) for r, _ in candidates])
+    params = (ctypes.c_int * n)(*[int(p) for _, p in candidates])
+    times = (ctypes.c_float * n)()
+    _check(load().lbgemm_time_candidates(bits, M, N, K, _addr(A), _addr(B), _addr(C), n,
+                                         ctypes.addressof(routes), ctypes.addressof(params),
+                                         warmup, reps, int(bool(flush_l2)),
+                                         ctypes.addressof(times), _stream(stream)))
+    return list(times)
+
+
+def lbgemm_table_set_choice_for(sm_count, bits, M, N, K, variant, route=-1, param=0) -> None:
+    _check(load().lbgemm_table_set_choice_for(sm_count, bits, M, N, K, variant, route, param))
+
+
+def lbgemm_table_get_for(sm_count, bits, M, N, K):
+    """(variant, route, param) of the exact entry (route -1: none), or None."""
+    v, r, p = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    got = load().lbgemm_table_get_for(sm_count, bits, M, N, K, ctypes.byref(v), ctypes.byref(r),
+                                      ctypes.byref(p))
+    if got < 0:
+        raise LbgemmError(ERR_INVALID_ARG, "lbgemm_table_get_for: bad arguments")
+    return (v.value, r.value, p.value) if got else None
+
+
+def lbgemm_table_default_path() -> str:
+    return (load().lbgemm_table_default_path() or b"").decode()
+
+
 def lbgemm_table_set(bits, M, N, K, variant) -> None:
     _check(load().lbgemm_table_set(bits, M, N, K, variant))
 
@@ -293,6 +359,12 @@ def lbgemm_mlp_predict(bits, M, N, K, sm_count) -> tuple[int, int]:
 def lbgemm_choose(times, default_variant: int = 7, keep_within: float = 0.02) -> int:
     arr = (ctypes.c_float * 9)(*[float(t) for t in times])
     return load().lbgemm_choose(ctypes.addressof(arr), default_variant, keep_within)
+
+
+def lbgemm_choose_candidate(times, default_index: int = 7, keep_within: float = 0.02) -> int:
+    arr = (ctypes.c_float * len(times))(*[float(t) for t in times])
+    return load().lbgemm_choose_candidate(ctypes.addressof(arr), len(times), default_index,
+                                          keep_within)
 
 
 def lbgemm_time_variants(bits, M, N, K, A, B, C, warmup=2, reps=5, flush_l2=True,

@@ -97,7 +97,11 @@ lbgemm_status lbgemm_variant_info(int bits, int variant, int* tile_m, int* tile_
  * on a tensor-core kernel that converts the large operand itself
  * (lbgemm_run_fused), with only the small one re-encoded ahead; and 1-bit
  * problems with M*N*K < 2^30 on the
- * XOR-popcount kernel of lbgemm_run_popc.  Scratch memory for the re-encoding is
+ * XOR-popcount kernel of lbgemm_run_popc.  These rules apply to shapes the
+ * selection table holds no measured route for; a table entry with a route
+ * (lbgemm_table_set_choice_for, or a route column in a loaded table file)
+ * runs that kernel instead, whenever it can run the given operands.
+ * Scratch memory for the re-encoding is
  * taken from a per-device buffer the library grows with cudaMalloc on demand
  * (by at least half again each time);
  * calls from different streams are ordered on it with events.  A call that
@@ -107,7 +111,7 @@ lbgemm_status lbgemm_run(int bits, int64_t M, int64_t N, int64_t K, const void* 
                          int32_t* C, void* stream);
 
 /* As lbgemm_run, forcing variant v (0..8) of the tensor-core kernel (no shape
- * rule applies); -1 means "use the table" (and the shape rules). */
+ * rule and no table route applies); -1 means "as lbgemm_run". */
 lbgemm_status lbgemm_run_variant(int bits, int64_t M, int64_t N, int64_t K, const void* A,
                                  const void* B, int32_t* C, int variant, void* stream);
 
@@ -160,12 +164,20 @@ lbgemm_status lbgemm_run_ws(int bits, int64_t M, int64_t N, int64_t K, const voi
  * compiled into the library: every GPU that loads the library holds it until
  * the process exits, and this call allocates nothing.  The caller still
  * passes A, B and C.  Problems whose scratch (lbgemm_workspace_size) exceeds
- * the array are rejected with LBGEMM_ERR_WORKSPACE before anything runs;
- * for 8-bit operands that is (M + N) * round_up(K, 8) * 2 bytes, e.g. M = N =
- * 2048 at K = 4096; for 1-bit operands (M + N) * K bytes.
+ * the array are rejected with LBGEMM_ERR_WORKSPACE before anything runs.
+ * The scratch is that of the kernel the call runs: on the tensor-core route
+ * both re-encoded operands (lbgemm_workspace_size: for 8-bit operands
+ * (M + N) * round_up(K, 8) * 2 bytes, e.g. M = N = 2048 at K = 4096; for
+ * 1-bit operands (M + N) * K bytes); on the in-kernel conversion route the
+ * smaller operand's fp16 copy only; none on the routes that read int8 (or
+ * 1-bit words) directly, so with variant -1 a linear-layer-shaped 16 x 11008
+ * x 4096 product runs whatever its size.
  *
  * The first call on each device looks up the array's device address (with
  * that device current); make that first call before any stream capture.
+ * The library caches per-device state (this address among it) for the life
+ * of the process: cudaDeviceReset while the library is in use is not
+ * supported.
  * Every call shares the one array: calls that can overlap on the GPU (other
  * streams, other threads) race on it and must be ordered by the caller.  The
  * array keeps whatever the last call wrote; each call rewrites every byte its
@@ -258,20 +270,45 @@ typedef enum {
   LBGEMM_ROUTE_NONE = 6     /* M == 0 or N == 0: nothing runs                        */
 } lbgemm_route_id;
 
-/* Which kernel lbgemm_run (linear = 0) or lbgemm_linear (linear != 0, bits
- * 8) runs for a problem of these sizes with 16-byte-aligned operands, by the
- * shape rules listed at lbgemm_run; with LBGEMM_ROUTE_FUSED, *tile_n (if
- * not null) receives the kernel's tile width (64, 128 or 256), else 0.  The
- * dispatchers use the same function.  Host only; -1 on bad bits or sizes
- * (the alignment rules of K are not checked here). */
+/* The shape rules listed at lbgemm_run: the kernel lbgemm_run (linear = 0)
+ * runs for a shape with no measured table route, or lbgemm_linear (linear
+ * != 0, bits 8) runs, for 16-byte-aligned operands; with LBGEMM_ROUTE_FUSED,
+ * *tile_n (if not null) receives the kernel's tile width (64, 128 or 256),
+ * else 0.  The dispatchers use the same function.  Host only; -1 on bad bits
+ * or sizes (the alignment rules of K are not checked here). */
 int lbgemm_route(int bits, int64_t M, int64_t N, int64_t K, int linear, int* tile_n);
+
+/* The kernel lbgemm_run runs for these sizes (16-byte-aligned operands) on a
+ * device with sm_count SMs: the table's measured route for the exact shape
+ * if it has one, else lbgemm_route's rule.  *param (if not null) receives
+ * the route's parameter: the variant for LBGEMM_ROUTE_TABLE (the table's
+ * choice) and LBGEMM_ROUTE_POPC, the tile width for LBGEMM_ROUTE_FUSED, else
+ * 0.  Host only; -1 on bad arguments. */
+int lbgemm_dispatch_for(int sm_count, int bits, int64_t M, int64_t N, int64_t K, int* param);
 lbgemm_status lbgemm_table_set_for(int sm_count, int bits, int64_t M, int64_t N, int64_t K,
                                    int variant);
+/* An entry with a measured route as well: variant is the tensor-core label
+ * (what lbgemm_select returns), (route, param) the kernel lbgemm_run runs for
+ * exactly this shape (param as lbgemm_dispatch_for gives it); route -1 stores
+ * no route.  LBGEMM_ERR_INVALID_ARG if that kernel cannot run the shape. */
+lbgemm_status lbgemm_table_set_choice_for(int sm_count, int bits, int64_t M, int64_t N, int64_t K,
+                                          int variant, int route, int param);
+/* The entry for exactly this shape: 1 (and its fields; route -1 when it has
+ * no route), 0 if there is none, -1 on bad arguments. */
+int lbgemm_table_get_for(int sm_count, int bits, int64_t M, int64_t N, int64_t K, int* variant,
+                         int* route, int* param);
 lbgemm_status lbgemm_table_clear(void);
 int64_t lbgemm_table_size(void);
-/* Text file, one entry per line: "sm_count bits M N K variant". */
+/* Text file, one entry per line: "sm_count bits M N K variant", optionally
+ * followed by "route param"; '#' starts a comment line.  Loading merges the
+ * file's entries into the table (none if any line is malformed). */
 lbgemm_status lbgemm_table_load(const char* path);
 lbgemm_status lbgemm_table_save(const char* path);
+/* The table is filled once per process, before its first use, from the file
+ * named by the environment variable LBGEMM_TABLE (unset: the GB300 table
+ * shipped with the library, data/lbgemm_table_gb300.txt beside its lib/
+ * directory; "" or "none": nothing).  The path loaded, or "" if none. */
+const char* lbgemm_table_default_path(void);
 
 /* ---- learned selector: [LBG] section 3 ------------------------------------------
  * A feed-forward network -- inputs log2(M), log2(N), log2(K) and the SM count,
@@ -293,16 +330,50 @@ int lbgemm_mlp_predict(int bits, int64_t M, int64_t N, int64_t K, int sm_count, 
  * (relative) of it, in which case the default is kept.  -1 on bad input. */
 int lbgemm_choose(const float* times, int default_variant, float keep_within);
 
+/* The same rule over `count` measured candidates (lbgemm_candidates order):
+ * the fastest (lowest index on ties), unless times[default_index] is within
+ * keep_within of it.  -1 on bad input. */
+int lbgemm_choose_candidate(const float* times, int count, int default_index, float keep_within);
+
 /* Timing step of the sweep, [LBG] section 2: runs every variant on the given
- * operands `warmup` times, then `reps` times, each rep timed with CUDA events
- * on `stream`, and writes the median milliseconds per variant to times[9].
+ * operands `warmup` times, then `reps` rounds in which each variant runs once
+ * (interleaved), each run timed with CUDA events on `stream`, and writes the
+ * median milliseconds per variant to times[9].
  * With flush_l2 != 0, a 256 MB library-owned buffer (allocated on first use)
- * is overwritten before each timed rep, outside the timed interval, so every
- * rep starts with operands out of L2.  Uses the internal workspace like
- * lbgemm_run.  Synchronises `stream`. */
+ * is overwritten before each timed run, outside the timed interval, so every
+ * run starts with operands out of L2.  Uses the internal workspace like
+ * lbgemm_run.  Synchronises `stream`; C holds the product afterwards. */
 lbgemm_status lbgemm_time_variants(int bits, int64_t M, int64_t N, int64_t K, const void* A,
                                    const void* B, int32_t* C, int warmup, int reps, int flush_l2,
                                    float* times, void* stream);
+
+/* The candidate kernels the timing sweep measures for a shape, as (route,
+ * param) pairs: the nine tensor-core variants (LBGEMM_ROUTE_TABLE, param =
+ * variant) first, then each shape-route kernel that runs the problem within
+ * the domain where it can plausibly win: for 1-bit below 2^34 bit-MACs the
+ * popcount kernel's nine variants (LBGEMM_ROUTE_POPC, param = its variant);
+ * for 8-bit with K % 16 == 0 the dp4a kernel streaming B (M <= 16), the
+ * warp-level fp16 MMA kernel (small side <= 256 within its K limit), the
+ * one-launch dp4a kernel (M*N*K <= 2^31, K <= 4096), and, for a small side
+ * of at most 1024 rows, the in-kernel conversion kernel at tile widths 64 and
+ * 128 (and 256 once the small side exceeds 64 rows).  Writes up to `max`
+ * pairs and returns how many there are (-1 on bad arguments).  Host only. */
+int lbgemm_candidates(int bits, int64_t M, int64_t N, int64_t K, int* routes, int* params,
+                      int max);
+
+/* C = A . B^T on one candidate kernel (route, param) as lbgemm_candidates
+ * lists them (any pair whose kernel runs the problem); scratch as
+ * lbgemm_run.  LBGEMM_ERR_INVALID_ARG if that kernel cannot run it. */
+lbgemm_status lbgemm_run_candidate(int bits, int64_t M, int64_t N, int64_t K, const void* A,
+                                   const void* B, int32_t* C, int route, int param, void* stream);
+
+/* As lbgemm_time_variants, for `count` candidates (routes[i], params[i]):
+ * the median milliseconds of each goes to times[i].  An even `reps` takes the
+ * mean of the two middle samples. */
+lbgemm_status lbgemm_time_candidates(int bits, int64_t M, int64_t N, int64_t K, const void* A,
+                                     const void* B, int32_t* C, int count, const int* routes,
+                                     const int* params, int warmup, int reps, int flush_l2,
+                                     float* times, void* stream);
 
 /* Host-buffer convenience, for callers whose operands live in host memory:
  * copies A and B to device staging buffers that the library owns (grown with

@@ -20,6 +20,10 @@ Readings where the page is silent:
   - label: the argmin of the measured times, the lowest index on exact ties.
   - the library's stored choice adds a no-regression guard: keep the default
     unless the label beats it by more than ``keep_within`` (2 %).
+  - the dispatch also measures the library's shape-route kernels as
+    candidates beside the nine variants and keeps the fastest under the same
+    guard; a shape with such a measured pick runs it, any other shape follows
+    the library's fixed shape rules.
   - a shape missing from the table takes the entry of the nearest swept
     shape of the same bit width and SM count, distance = sum over M, N, K of
     |log2(x) - log2(x')|, ties to the earlier entry in (M, N, K) order; an
@@ -61,6 +65,26 @@ def table_choice(times, default: int = DEFAULT_VARIANT, keep_within: float = 0.0
     if times[default] <= times[lab] * (1.0 + keep_within):
         return default
     return lab
+
+
+def candidate_choice(times, default_index: int = DEFAULT_VARIANT,
+                     keep_within: float = 0.02) -> int:
+    """The same guard over any list of measured candidates (the nine variants
+    first, then the shape-route kernels): the fastest, lowest index on exact
+    ties, unless the default is within keep_within of it."""
+    best = 0
+    for i, t in enumerate(times):
+        if t < times[best]:
+            best = i
+    if times[default_index] <= times[best] * (1.0 + keep_within):
+        return default_index
+    return best
+
+
+def dispatch(entry, rule):
+    """The kernel a call runs: the table's measured (route, param) for the
+    exact shape when there is one that runs the operands, else the rule's."""
+    return entry if entry is not None else rule
 
 
 def nearest(entries, M: int, N: int, K: int, default: int = DEFAULT_VARIANT) -> int:

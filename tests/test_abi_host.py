@@ -343,3 +343,175 @@ def test_header_is_plain_c_and_links(lib, tmp_path):
     assert (tm, tn, tk, stages) == (info["tile_m"], info["tile_n"], info["tile_k"], info["stages"])
     assert (route, tile) == (L.ROUTE_WARPMMA, 0)
     assert bad == L.ERR_INVALID_ARG and has_msg == 1
+
+
+# ---- measured routes in the table (host only) -------------------------------------
+
+def test_choose_candidate_matches_oracle(lib):
+    g = np.random.default_rng(31)
+    for trial in range(400):
+        n = int(g.integers(1, 20))
+        t = g.uniform(1.0, 2.0, n).astype(np.float32)
+        d = int(g.integers(0, n))
+        if trial % 3 == 0:  # ties and near-ties around the default
+            t[g.integers(0, n)] = t.min()
+            t[d] = t.min() * np.float32(1.0 + g.choice([0.0, 0.01, 0.019, 0.03]))
+        want = osel.candidate_choice([float(x) for x in t], d, 0.02)
+        assert L.lbgemm_choose_candidate(list(t), d, 0.02) == want, (t, d)
+    # the nine-variant rule is the same rule
+    t = [3.0, 2.0, 1.0, 1.5, 1.01, 4.0, 1.0, 1.02, 2.0]
+    assert L.lbgemm_choose(t, 7, 0.02) == L.lbgemm_choose_candidate(t, 7, 0.02) == 7
+    assert L.lbgemm_choose_candidate([1.0, float("nan")], 0, 0.02) == -1
+    assert L.lbgemm_choose_candidate([1.0, 2.0], 2, 0.02) == -1
+
+
+def test_candidates_cover_the_routes_that_run(lib):
+    T, POPC, SK, WM, SM, FU = (L.ROUTE_TABLE, L.ROUTE_POPC, L.ROUTE_SKINNY, L.ROUTE_WARPMMA,
+                               L.ROUTE_SMALL, L.ROUTE_FUSED)
+    tc = [(T, v) for v in range(9)]
+    assert L.lbgemm_candidates(4, 8192, 8192, 8192) == tc
+    assert L.lbgemm_candidates(1, 8192, 8192, 65536) == tc  # 2^42 bit-MACs: no popcount
+    assert L.lbgemm_candidates(1, 64, 64, 1024) == tc + [(POPC, v) for v in range(9)]
+    assert L.lbgemm_candidates(8, 16384, 16384, 16384) == tc
+    assert L.lbgemm_candidates(8, 64, 16384, 4096) == tc + [(FU, 64), (FU, 128)]
+    assert L.lbgemm_candidates(8, 8, 1024, 1024) == tc + [(SK, 0), (WM, 0), (SM, 0), (FU, 64),
+                                                          (FU, 128)]
+    assert L.lbgemm_candidates(8, 256, 512, 2048) == tc + [(WM, 0), (SM, 0), (FU, 64), (FU, 128),
+                                                           (FU, 256)]
+    assert L.lbgemm_candidates(8, 256, 512, 4096) == tc + [(SM, 0), (FU, 64), (FU, 128), (FU, 256)]
+    assert L.lbgemm_candidates(8, 100, 100, 100) == tc  # K % 16 != 0: the 8-bit routes need it
+    with pytest.raises(L.LbgemmError):
+        L.lbgemm_candidates(3, 64, 64, 64)
+
+
+def test_table_routes_drive_the_dispatch(lib, tmp_path):
+    sm = 4545  # an SM count no device has
+    T, POPC, WM, FU = L.ROUTE_TABLE, L.ROUTE_POPC, L.ROUTE_WARPMMA, L.ROUTE_FUSED
+    # no entry: the shape rules (lbgemm_route), the variant from selection
+    for bits, shape in [(8, (16, 11008, 4096)), (8, (4096, 4096, 4096)), (1, (64, 64, 1024))]:
+        r, p = L.lbgemm_dispatch_for(sm, bits, *shape)
+        rule, tile = L.lbgemm_route(bits, *shape)
+        assert r == rule
+        if r == T:
+            assert p == L.lbgemm_select_for(sm, bits, *shape)
+        if r == FU:
+            assert p == tile
+    # measured entries take over for their exact shape only
+    L.lbgemm_table_set_choice_for(sm, 8, 4096, 4096, 4096, 3, T, 5)
+    L.lbgemm_table_set_choice_for(sm, 8, 256, 8192, 2048, 1, FU, 256)
+    L.lbgemm_table_set_choice_for(sm, 8, 128, 1024, 1024, 4, WM, 0)
+    L.lbgemm_table_set_choice_for(sm, 1, 64, 64, 1024, 2, POPC, 4)
+    L.lbgemm_table_set_for(sm, 4, 512, 512, 512, 6)  # a label without a route
+    assert L.lbgemm_dispatch_for(sm, 8, 4096, 4096, 4096) == (T, 5)
+    assert L.lbgemm_select_for(sm, 8, 4096, 4096, 4096) == 3  # the label stays the variant
+    assert L.lbgemm_dispatch_for(sm, 8, 256, 8192, 2048) == (FU, 256)
+    assert L.lbgemm_dispatch_for(sm, 8, 128, 1024, 1024) == (WM, 0)
+    assert L.lbgemm_dispatch_for(sm, 1, 64, 64, 1024) == (POPC, 4)
+    assert L.lbgemm_dispatch_for(sm, 4, 512, 512, 512) == (T, 6)
+    assert L.lbgemm_table_get_for(sm, 8, 256, 8192, 2048) == (1, FU, 256)
+    assert L.lbgemm_table_get_for(sm, 4, 512, 512, 512) == (6, -1, 0)
+    assert L.lbgemm_table_get_for(sm, 4, 512, 512, 1024) is None
+    # a neighbour of a measured shape follows the rules again
+    assert L.lbgemm_dispatch_for(sm, 8, 256, 8192, 4096)[0] == L.lbgemm_route(8, 256, 8192, 4096)[0]
+    # routes that cannot run the shape are refused
+    for bad in [(8, 512, 512, 512, 0, WM, 0),      # warp-MMA: small side above 256
+                (4, 64, 64, 64, 0, FU, 128),       # 8-bit routes only
+                (8, 64, 64, 40, 0, FU, 128),       # K % 16
+                (8, 64, 64, 64, 0, FU, 96),        # no such tile
+                (8, 64, 64, 64, 0, POPC, 1),       # popcount: 1-bit only
+                (8, 64, 64, 64, 0, T, 9),
+                (8, 64, 64, 64, 0, 6, 0)]:
+        with pytest.raises(L.LbgemmError):
+            L.lbgemm_table_set_choice_for(sm, *bad)
+    # the file keeps the routes; old six-column lines still load
+    p = str(tmp_path / "t.txt")
+    L.lbgemm_table_save(p)
+    text = open(p).read()
+    assert f"{sm} 8 256 8192 2048 1 {FU} 256\n" in text and f"{sm} 4 512 512 512 6\n" in text
+    L.lbgemm_table_clear()
+    L.lbgemm_table_load(p)
+    assert L.lbgemm_dispatch_for(sm, 8, 256, 8192, 2048) == (FU, 256)
+    assert L.lbgemm_table_get_for(sm, 4, 512, 512, 512) == (6, -1, 0)
+    n = L.lbgemm_table_size()
+    for bad_line in [f"{sm} 8 64 64 64 7 {WM}\n",            # route without its parameter
+                     f"{sm} 8 512 512 512 7 {WM} 0\n",      # a route that cannot run it
+                     f"{sm} 8 64 64 64 7 0 7 1\n"]:         # trailing field
+        bad = tmp_path / "bad.txt"
+        bad.write_text("# header\n" + bad_line)
+        with pytest.raises(L.LbgemmError):
+            L.lbgemm_table_load(str(bad))
+        assert L.lbgemm_table_size() == n  # nothing merged
+    L.lbgemm_table_clear()
+
+
+def test_oracle_dispatch_rule():
+    assert osel.dispatch(None, (3, 0)) == (3, 0)
+    assert osel.dispatch((5, 128), (0, 7)) == (5, 128)
+
+
+# ---- the GB300 table shipped with the library ----------------------------------------
+
+SHIPPED = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                       "bit_tensor_gemm_gb300", "data", "lbgemm_table_gb300.txt")
+
+PROBE = r"""
+import json, sys
+sys.path.insert(0, {root!r})
+from bit_tensor_gemm_gb300 import lbgemm as L
+L.load()
+out = {{"path": L.lbgemm_table_default_path(), "size": L.lbgemm_table_size(), "q": []}}
+for sm, bits, m, n, k in json.loads(sys.argv[1]):
+    out["q"].append([L.lbgemm_select_for(sm, bits, m, n, k),
+                     list(L.lbgemm_dispatch_for(sm, bits, m, n, k))])
+print(json.dumps(out))
+"""
+
+
+def _fresh_process(queries, env_table=None):
+    """Answers of a fresh process (the table is loaded at first use)."""
+    import json  # noqa: PLC0415
+    import subprocess  # noqa: PLC0415
+    import sys  # noqa: PLC0415
+    env = dict(os.environ)
+    env.pop("LBGEMM_TABLE", None)
+    if env_table is not None:
+        env["LBGEMM_TABLE"] = env_table
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "-c", PROBE.format(root=root), json.dumps(queries)],
+                       env=env, capture_output=True, text=True, check=True)
+    return json.loads(r.stdout)
+
+
+def _shipped_entries():
+    rows = []
+    for line in open(SHIPPED):
+        w = line.split()
+        if w and not w[0].startswith("#"):
+            rows.append([int(x) for x in w])
+    return rows
+
+
+def test_shipped_table_is_loaded_by_default(lib):
+    rows = _shipped_entries()
+    assert len(rows) == 3 * 729  # the 729-shape grid for 8-, 4- and 1-bit operands
+    assert {r[1] for r in rows} == {8, 4, 1} and all(len(r) == 8 for r in rows)
+    g = np.random.default_rng(5)
+    picks = [rows[i] for i in g.choice(len(rows), 60, replace=False)]
+    picks += [r for r in rows if r[1] in (4, 1)][:20]
+    queries = [r[:5] for r in picks]
+    got = _fresh_process(queries)
+    assert os.path.realpath(got["path"]) == os.path.realpath(SHIPPED)
+    assert got["size"] == len(rows)
+    for r, (sel, disp) in zip(picks, got["q"]):
+        assert sel == r[5], r  # lbgemm_select gives the stored label
+        assert disp == [r[6], r[7]], r  # and lbgemm_run the stored route
+
+
+def test_table_file_from_the_environment(lib, tmp_path):
+    assert _fresh_process([], env_table="none")["size"] == 0
+    assert _fresh_process([], env_table="")["size"] == 0
+    p = tmp_path / "mine.txt"
+    p.write_text("# mine\n4242 4 100 200 300 5\n4242 8 64 4096 1024 2 5 64\n")
+    got = _fresh_process([[4242, 4, 100, 200, 300], [4242, 8, 64, 4096, 1024]], env_table=str(p))
+    assert got["size"] == 2 and got["path"] == str(p)
+    assert got["q"] == [[5, [L.ROUTE_TABLE, 5]], [2, [L.ROUTE_FUSED, 64]]]
