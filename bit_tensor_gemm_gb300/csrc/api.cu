@@ -234,8 +234,13 @@ int variant_stages(int variant) {
   return variant / 3 == 2 ? variant % 3 + 4 : variant % 3 + 2;
 }
 
-TcKernel tc_kernel(int variant, bool f8, bool linear) {
-  const int tile = variant / 3, stages = variant_stages(variant);
+// A tensor-core kernel instantiation: tile class (0 small, 1 medium, 2
+// large) and stage count, packed as tile * 8 + stages.  The nine variants
+// are nine of them; lbgemm_run_tile reaches the others the library compiles.
+int spec_of(int variant) { return (variant / 3) * 8 + variant_stages(variant); }
+
+TcKernel tc_kernel(int spec, bool f8, bool linear) {
+  const int tile = spec / 8, stages = spec % 8;
   switch (tile) {
     case 0: return lbg::tc_kernel_small(stages, f8, linear);
     case 1: return lbg::tc_kernel_medium(stages, f8, linear);
@@ -521,12 +526,13 @@ lbgemm_status clear_split_tiles(const TcKernel& k, const KPlan& kp, int64_t M, i
 
 lbgemm_status run_tc_encoded(DeviceState& d, int bits, int64_t M, int64_t N, int64_t K,
                              const void* encA, const void* encB, int32_t* C, const float* sx,
-                             const float* sw, void* Y, int variant, bool after_encode,
+                             const float* sw, void* Y, int spec, bool after_encode,
                              const KPlan* planned, cudaStream_t stream) {
   const bool f8 = bits != 8;  // 4-bit and 1-bit operands are e4m3-encoded
   const bool linear = Y != nullptr;
-  TcKernel k = tc_kernel(variant, f8, linear);
-  if (!k.launch) return fail(LBGEMM_ERR_UNSUPPORTED, "no kernel for variant %d", variant);
+  TcKernel k = tc_kernel(spec, f8, linear);
+  if (!k.launch)
+    return fail(LBGEMM_ERR_UNSUPPORTED, "no kernel for tile %d with %d stages", spec / 8, spec % 8);
   const int64_t kp = enc_kp(bits, K);
   CUtensorMap ma, mb;
   lbgemm_status st = encode_kmajor(&ma, encA, M, kp, !f8, 128);
@@ -596,14 +602,14 @@ lbgemm_status run_tc_encoded(DeviceState& d, int bits, int64_t M, int64_t N, int
 
 lbgemm_status run_tc(DeviceState& d, int bits, int64_t M, int64_t N, int64_t K, const void* A,
                      const void* B, int32_t* C, const float* sx, const float* sw, void* Y,
-                     int variant, void* ws, cudaStream_t stream) {
+                     int spec, void* ws, cudaStream_t stream) {
   uint8_t* encA = static_cast<uint8_t*>(ws);
   uint8_t* encB = encA + enc_bytes(bits, M, K);
   // Plan K splits first: the encoder launch clears the part of C that split
   // tiles add into, and the GEMM is launched as its dependent.
   KPlan plan;
   const bool linear = Y != nullptr;
-  TcKernel k = tc_kernel(variant, bits != 8, linear);
+  TcKernel k = tc_kernel(spec, bits != 8, linear);
   if (k.launch) {
     plan = plan_k(d, k, bits, M, N, K, linear, (N % 4 == 0) && aligned16(C));
   }
@@ -611,7 +617,7 @@ lbgemm_status run_tc(DeviceState& d, int bits, int64_t M, int64_t N, int64_t K, 
   lbgemm_status st = encode_operands(d, bits, A, M, encA, B, N, encB, K, stream,
                                      split_rect(k, plan, M, N, C));
   if (st != LBGEMM_OK) return st;
-  return run_tc_encoded(d, bits, M, N, K, encA, encB, C, sx, sw, Y, variant, true, &plan, stream);
+  return run_tc_encoded(d, bits, M, N, K, encA, encB, C, sx, sw, Y, spec, true, &plan, stream);
 }
 
 // 8-bit problems with one operand converted in the kernel: only the other
@@ -892,7 +898,10 @@ int candidate_list(int bits, int64_t M, int64_t N, int64_t K, int* routes, int* 
 struct Pick {
   int route = LBGEMM_ROUTE_NONE;
   int param = 0;
+  int spec = -1;  // LBGEMM_ROUTE_TABLE: an explicit kernel spec instead of variant `param`
 };
+
+int tc_spec(const Pick& p) { return p.spec >= 0 ? p.spec : spec_of(p.param); }
 
 Pick pick_route(int sm, int bits, int64_t M, int64_t N, int64_t K, const void* A, const void* B) {
   Pick p;
@@ -964,7 +973,7 @@ lbgemm_status run_route(DeviceState& d, int bits, int64_t M, int64_t N, int64_t 
     if (p.route == LBGEMM_ROUTE_FUSED)
       return run_tc_fused(d, N >= M, p.param, M, N, K, A, B, C, nullptr, nullptr, nullptr, ws,
                           stream);
-    return run_tc(d, bits, M, N, K, A, B, C, nullptr, nullptr, nullptr, p.param, ws, stream);
+    return run_tc(d, bits, M, N, K, A, B, C, nullptr, nullptr, nullptr, tc_spec(p), ws, stream);
   }
   std::lock_guard<std::mutex> lock(g_ws_mu);
   lbgemm_status st = scratch_acquire(d.ws, need, stream);
@@ -973,7 +982,8 @@ lbgemm_status run_route(DeviceState& d, int bits, int64_t M, int64_t N, int64_t 
     st = run_tc_fused(d, N >= M, p.param, M, N, K, A, B, C, nullptr, nullptr, nullptr, d.ws.ptr,
                       stream);
   else
-    st = run_tc(d, bits, M, N, K, A, B, C, nullptr, nullptr, nullptr, p.param, d.ws.ptr, stream);
+    st = run_tc(d, bits, M, N, K, A, B, C, nullptr, nullptr, nullptr, tc_spec(p), d.ws.ptr,
+                stream);
   lbgemm_status st2 = scratch_release(d.ws, stream);
   return st != LBGEMM_OK ? st : st2;
 }
@@ -1038,7 +1048,7 @@ lbgemm_status run_linear(int64_t M, int64_t N, int64_t K, const int8_t* X, const
   const size_t need = enc_bytes(8, M, K) + enc_bytes(8, N, K);
   st = scratch_acquire(d->ws, need, stream);
   if (st != LBGEMM_OK) return st;
-  st = run_tc(*d, 8, M, N, K, X, W, nullptr, sx, sw, Y, variant, d->ws.ptr, stream);
+  st = run_tc(*d, 8, M, N, K, X, W, nullptr, sx, sw, Y, spec_of(variant), d->ws.ptr, stream);
   lbgemm_status st2 = scratch_release(d->ws, stream);
   return st != LBGEMM_OK ? st : st2;
 }
@@ -1298,7 +1308,8 @@ lbgemm_status lbgemm_run_encoded(int bits, int64_t M, int64_t N, int64_t K, cons
     st = device_state(&d);
     if (st != LBGEMM_OK) return st;
     if (variant < 0) variant = table_select(d->sm_count, bits, M, N, K);
-    return run_tc_encoded(*d, bits, M, N, K, A_enc, B_enc, C, nullptr, nullptr, nullptr, variant,
+    return run_tc_encoded(*d, bits, M, N, K, A_enc, B_enc, C, nullptr, nullptr, nullptr,
+                          spec_of(variant),
                           false, nullptr, as_stream(stream));
   } catch (...) {
     return fail(LBGEMM_ERR_CUDA, "internal error");
@@ -1367,6 +1378,27 @@ lbgemm_status lbgemm_run_candidate(int bits, int64_t M, int64_t N, int64_t K, co
     Pick p;
     p.route = route;
     p.param = param;
+    return run_route(*d, bits, M, N, K, A, B, C, p, nullptr, 0, true, as_stream(stream));
+  } catch (...) {
+    return fail(LBGEMM_ERR_CUDA, "internal error");
+  }
+}
+
+lbgemm_status lbgemm_run_tile(int bits, int64_t M, int64_t N, int64_t K, const void* A,
+                              const void* B, int32_t* C, int tile, int stages, void* stream) {
+  try {
+    lbgemm_status st = check_gemm_args(bits, M, N, K, A, B, C);
+    if (st != LBGEMM_OK) return st;
+    if (tile < 0 || tile > 2 || stages < 2 || stages > (tile == 2 ? 6 : 4))
+      return fail(LBGEMM_ERR_UNSUPPORTED, "no tensor-core kernel for tile %d with %d stages", tile,
+                  stages);
+    if (M == 0 || N == 0) return LBGEMM_OK;
+    DeviceState* d = nullptr;
+    st = device_state(&d);
+    if (st != LBGEMM_OK) return st;
+    Pick p;
+    p.route = LBGEMM_ROUTE_TABLE;
+    p.spec = tile * 8 + stages;
     return run_route(*d, bits, M, N, K, A, B, C, p, nullptr, 0, true, as_stream(stream));
   } catch (...) {
     return fail(LBGEMM_ERR_CUDA, "internal error");

@@ -46,6 +46,7 @@ _SIGNATURES = {
     "lbgemm_run_variant": (_i32, [_i32, _i64, _i64, _i64, _vp, _vp, _vp, _i32, _vp]),
     "lbgemm_run_fused": (_i32, [_i64, _i64, _i64, _vp, _vp, _vp, _i32, _vp]),
     "lbgemm_run_warpmma": (_i32, [_i64, _i64, _i64, _vp, _vp, _vp, _vp]),
+    "lbgemm_run_tile": (_i32, [_i32, _i64, _i64, _i64, _vp, _vp, _vp, _i32, _i32, _vp]),
     "lbgemm_workspace_size": (ctypes.c_size_t, [_i32, _i64, _i64, _i64]),
     "lbgemm_run_ws": (_i32, [_i32, _i64, _i64, _i64, _vp, _vp, _vp, _i32, _vp, ctypes.c_size_t,
                              _vp]),
@@ -186,6 +187,11 @@ def lbgemm_run_fused(M, N, K, A, B, C, tile_n=128, stream=None) -> None:
 
 def lbgemm_run_warpmma(M, N, K, A, B, C, stream=None) -> None:
     _check(load().lbgemm_run_warpmma(M, N, K, _addr(A), _addr(B), _addr(C), _stream(stream)))
+
+
+def lbgemm_run_tile(bits, M, N, K, A, B, C, tile, stages, stream=None) -> None:
+    _check(load().lbgemm_run_tile(bits, M, N, K, _addr(A), _addr(B), _addr(C), tile, stages,
+                                  _stream(stream)))
 
 
 def lbgemm_workspace_size(bits, M, N, K) -> int:

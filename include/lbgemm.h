@@ -142,6 +142,16 @@ lbgemm_status lbgemm_run_fused(int64_t M, int64_t N, int64_t K, const int8_t* A,
 lbgemm_status lbgemm_run_warpmma(int64_t M, int64_t N, int64_t K, const int8_t* A,
                                  const int8_t* B, int32_t* C, void* stream);
 
+/* C = A . B^T on one tensor-core kernel named by tile class (0 small
+ * 128 x 64, 1 medium 128 x 128, 2 large 256 x 256 on a CTA pair) and stage
+ * count: 2..4 for the small and medium tiles, 2..6 for the large one (2 and
+ * 3 beyond the variant table's levels, for measurements of the stage
+ * dimension).  Re-encoding and scratch as lbgemm_run_variant;
+ * LBGEMM_ERR_UNSUPPORTED for a pair the library does not compile.  [LBG]
+ * sections 1-2 (tile shape and stage count). */
+lbgemm_status lbgemm_run_tile(int bits, int64_t M, int64_t N, int64_t K, const void* A,
+                              const void* B, int32_t* C, int tile, int stages, void* stream);
+
 /* Bytes of scratch that lbgemm_run_ws needs for this problem on the
  * tensor-core route (0 for bad arguments): the re-encoded A and B. */
 size_t lbgemm_workspace_size(int bits, int64_t M, int64_t N, int64_t K);

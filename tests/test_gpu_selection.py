@@ -129,3 +129,24 @@ def test_tuning_one_shape_stores_a_valid_entry():
             L.lbgemm_table_set_choice_for(sm, 8, M, N, K, 7, -1, 0)
         else:
             L.lbgemm_table_set_choice_for(sm, 8, M, N, K, *saved)
+
+
+@pytest.mark.parametrize("bits", [8, 4, 1])
+def test_every_compiled_tile_and_stage_count_is_exact(bits):
+    """lbgemm_run_tile: the nine variants and the large tile's 2- and 3-stage
+    kernels (measurement only), on a ragged shape, a split-K shape and a
+    shape of more than one wave of small and medium tiles."""
+    for i, (M, N, K) in enumerate([(300, 200, 1040), (129, 65, 4160), (2500, 2000, 1040)]):
+        if bits == 1:
+            K = (K + 31) // 32 * 32
+        A, B, dA, dB, dC = _setup(bits, M, N, K, 61 + i + bits)
+        want = oracle.gemm(bits, A, B, K)
+        for tile in range(3):
+            for stages in range(2, 7 if tile == 2 else 5):
+                dC.fill_(-7)
+                L.lbgemm_run_tile(bits, M, N, K, dA, dB, dC, tile, stages)
+                L.lbgemm_device_status()
+                assert np.array_equal(dC.cpu().numpy(), want), (bits, M, N, K, tile, stages)
+    with pytest.raises(L.LbgemmError) as e:
+        L.lbgemm_run_tile(bits, 64, 64, 256, dA, dB, dC, 1, 5)
+    assert e.value.status == L.ERR_UNSUPPORTED
