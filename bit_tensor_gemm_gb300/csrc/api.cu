@@ -68,6 +68,8 @@ constexpr int64_t kFusedMinOther = 1024;
 // does (K of 272-512: 8.8-10.9 us against 12.9 us; at K <= 256 the dp4a
 // kernel is as fast or faster).
 constexpr int64_t kWarpMmaMaxSide = 32;
+// Small side of the streaming warp-MMA kernel (stream_mma.cu).
+constexpr int64_t kStreamMaxSide = 16;
 constexpr int64_t kWarpMmaMaxSideSmall = 256;
 constexpr int64_t kWarpMmaMaxArea = int64_t(1) << 19;  // min(M, N) * max(M, N)
 constexpr int64_t kWarpMmaMaxKSmall = 2048;
@@ -751,6 +753,15 @@ lbgemm_status run_warpmma(DeviceState& d, int64_t M, int64_t N, int64_t K, const
   return LBGEMM_OK;
 }
 
+// The streaming kernel takes a problem with a small side of at most 16 rows
+// against at least 1024 (measured on GB300, 5-16 rows x 11008 x 4096, back to
+// back over rotating weights: 12.6-13.3 us against 14.2 on the warp-MMA
+// kernel; the dp4a kernel stays ahead up to 4 rows), K <= 4096.
+bool stream_ok(int64_t M, int64_t N, int64_t K, const void* A, const void* B) {
+  return std::min(M, N) <= kStreamMaxSide && std::max(M, N) >= 1024 && K % 16 == 0 &&
+         K <= lbg::stream_mma_max_k() && aligned16(A) && aligned16(B);
+}
+
 // The warp-MMA kernel takes the problem: small side <= kWarpMmaMaxSide rows,
 // X fits its shared memory, K % 16 == 0, aligned operands.
 bool warpmma_ok(int64_t M, int64_t N, int64_t K, const void* A, const void* B) {
@@ -814,6 +825,7 @@ int route_of(int bits, int64_t M, int64_t N, int64_t K, const void* A, const voi
   if (M == 0 || N == 0) return LBGEMM_ROUTE_NONE;
   if (linear) {
     if (skinny_ok(M, K, A, B)) return LBGEMM_ROUTE_SKINNY;
+    if (M <= kStreamMaxSide && stream_ok(M, N, K, A, B)) return LBGEMM_ROUTE_STREAM;
     if (warpmma_ok(M, N, K, A, B)) return LBGEMM_ROUTE_WARPMMA;
     if (fused_route(M, N, K, A, B, tile_n) == 1) {
       *fuse = 1;
@@ -828,6 +840,7 @@ int route_of(int bits, int64_t M, int64_t N, int64_t K, const void* A, const voi
   }
   if (bits != 8) return LBGEMM_ROUTE_TABLE;
   if (skinny_ok(M, K, A, B)) return LBGEMM_ROUTE_SKINNY;
+  if (stream_ok(M, N, K, A, B)) return LBGEMM_ROUTE_STREAM;
   if (warpmma_ok(M, N, K, A, B) || warpmma_small_ok(M, N, K, A, B)) return LBGEMM_ROUTE_WARPMMA;
   if (small_ok(M, N, K, A, B)) return LBGEMM_ROUTE_SMALL;
   *fuse = fused_route(M, N, K, A, B, tile_n);
@@ -852,6 +865,28 @@ bool route_runs(int bits, int64_t M, int64_t N, int64_t K, const void* A, const 
              K <= lbg::hmma_skinny_max_k((int)lo);
     case LBGEMM_ROUTE_SMALL: return bits == 8 && a16;
     case LBGEMM_ROUTE_FUSED: return bits == 8 && (param == 64 || param == 128 || param == 256) && a16;
+    case LBGEMM_ROUTE_STREAM:
+      return bits == 8 && lo <= kStreamMaxSide && a16 && K <= lbg::stream_mma_max_k();
+    default: return false;
+  }
+}
+
+// The routes of the linear layer (X = A is the token side; Y is M x N bf16):
+// the tensor-core variants, the dp4a and streaming kernels for few tokens,
+// the warp-MMA kernel, and the in-kernel conversion of W.
+bool linear_route_runs(int64_t M, int64_t N, int64_t K, const void* X, const void* W, int route,
+                       int param) {
+  const bool a16 = K % 16 == 0 && aligned16(X) && aligned16(W);
+  switch (route) {
+    case LBGEMM_ROUTE_TABLE: return param >= 0 && param < kNumVariants;
+    case LBGEMM_ROUTE_SKINNY: return M <= kSkinnyKernelMaxM && a16;
+    case LBGEMM_ROUTE_STREAM:
+      return M <= kStreamMaxSide && a16 && K <= lbg::stream_mma_max_k();
+    case LBGEMM_ROUTE_WARPMMA:
+      return std::min(M, N) <= kWarpMmaMaxSide && a16 &&
+             K <= lbg::hmma_skinny_max_k((int)std::min(M, N));
+    case LBGEMM_ROUTE_FUSED:
+      return (param == 64 || param == 128 || param == 256) && M <= N && a16;
     default: return false;
   }
 }
@@ -882,6 +917,7 @@ int candidate_list(int bits, int64_t M, int64_t N, int64_t K, int* routes, int* 
     for (int v = 0; v < kNumVariants; ++v) add(LBGEMM_ROUTE_POPC, v);
   if (bits != 8 || K % 16) return n;
   if (route_runs(8, M, N, K, al, al, LBGEMM_ROUTE_SKINNY, 0)) add(LBGEMM_ROUTE_SKINNY, 0);
+  if (route_runs(8, M, N, K, al, al, LBGEMM_ROUTE_STREAM, 0)) add(LBGEMM_ROUTE_STREAM, 0);
   if (route_runs(8, M, N, K, al, al, LBGEMM_ROUTE_WARPMMA, 0)) add(LBGEMM_ROUTE_WARPMMA, 0);
   if (work <= 2147483648.0 && K <= 4096) add(LBGEMM_ROUTE_SMALL, 0);
   if (lo <= 1024) {
@@ -962,6 +998,20 @@ lbgemm_status run_route(DeviceState& d, int bits, int64_t M, int64_t N, int64_t 
       if (e != cudaSuccess) return cuda_fail(e, "small GEMM launch");
       g_launches += 1;
       return LBGEMM_OK;
+    case LBGEMM_ROUTE_STREAM:
+      // the small side is X; C is written transposed from its point of view
+      // when that side is B
+      e = M <= N ? lbg::launch_stream_mma(static_cast<const int8_t*>(A),
+                                          static_cast<const int8_t*>(B), (int)M, (int)N, (int)K,
+                                          false, C, nullptr, nullptr, nullptr, false, d.sm_count,
+                                          d.status, stream)
+                 : lbg::launch_stream_mma(static_cast<const int8_t*>(B),
+                                          static_cast<const int8_t*>(A), (int)N, (int)M, (int)K,
+                                          true, C, nullptr, nullptr, nullptr, false, d.sm_count,
+                                          d.status, stream);
+      if (e != cudaSuccess) return cuda_fail(e, "streaming GEMM launch");
+      g_launches += 1;
+      return LBGEMM_OK;
     default: break;
   }
   const size_t need = route_scratch(bits, M, N, K, p);
@@ -1009,26 +1059,47 @@ lbgemm_status run_any(int bits, int64_t M, int64_t N, int64_t K, const void* A, 
   return run_route(*d, bits, M, N, K, A, B, C, p, ws, ws_bytes, internal_ws, stream);
 }
 
+// The linear layer.  route < 0: by the shape rules (variant < 0) or the
+// tensor-core variant `variant`; else that route with its parameter (the
+// variant of LBGEMM_ROUTE_TABLE, the tile width of LBGEMM_ROUTE_FUSED).
+// early_w: W is not written by the grid launched before this call on the
+// stream (the caller's own quantiser), so the streaming kernel may start
+// reading it before that grid ends.
 lbgemm_status run_linear(int64_t M, int64_t N, int64_t K, const int8_t* X, const float* sx,
                          const int8_t* W, const float* sw, void* Y, int variant,
-                         cudaStream_t stream) {
+                         cudaStream_t stream, int route = -1, int param = 0,
+                         bool early_w = false) {
   lbgemm_status st = check_gemm_args(8, M, N, K, X, W, Y);
   if (st != LBGEMM_OK) return st;
   if (variant < -1 || variant >= kNumVariants)
     return fail(LBGEMM_ERR_INVALID_ARG, "variant %d out of range", variant);
+  if (route >= 0 && !linear_route_runs(M, N, K, X, W, route, param))
+    return fail(LBGEMM_ERR_INVALID_ARG, "route %d (param %d) cannot run this linear layer", route,
+                param);
   if (M == 0 || N == 0) return LBGEMM_OK;
   if (!sx || !sw) return fail(LBGEMM_ERR_INVALID_ARG, "null scale pointer");
   DeviceState* d = nullptr;
   st = device_state(&d);
   if (st != LBGEMM_OK) return st;
-  const bool auto_pick = variant < 0;
-  int fuse_tile = 0, fuse = 0;
-  const int route =
-      auto_pick ? route_of(8, M, N, K, X, W, true, &fuse_tile, &fuse) : LBGEMM_ROUTE_TABLE;
+  int fuse_tile = param, fuse = 0;
+  if (route < 0) {
+    route = variant < 0 ? route_of(8, M, N, K, X, W, true, &fuse_tile, &fuse) : LBGEMM_ROUTE_TABLE;
+    if (route == LBGEMM_ROUTE_TABLE)
+      variant = variant < 0 ? table_select(d->sm_count, 8, M, N, K) : variant;
+  } else if (route == LBGEMM_ROUTE_TABLE) {
+    variant = param;
+  }
   if (route == LBGEMM_ROUTE_SKINNY) {
     cudaError_t e =
         lbg::launch_skinny_s8(X, W, (int)M, (int)N, (int)K, nullptr, sx, sw, Y, d->sm_count, stream);
     if (e != cudaSuccess) return cuda_fail(e, "skinny linear launch");
+    g_launches += 1;
+    return LBGEMM_OK;
+  }
+  if (route == LBGEMM_ROUTE_STREAM) {
+    cudaError_t e = lbg::launch_stream_mma(X, W, (int)M, (int)N, (int)K, false, nullptr, sx, sw, Y,
+                                           early_w, d->sm_count, d->status, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "streaming linear launch");
     g_launches += 1;
     return LBGEMM_OK;
   }
@@ -1043,7 +1114,6 @@ lbgemm_status run_linear(int64_t M, int64_t N, int64_t K, const int8_t* X, const
     lbgemm_status st2 = scratch_release(d->ws, stream);
     return st != LBGEMM_OK ? st : st2;
   }
-  if (auto_pick) variant = table_select(d->sm_count, 8, M, N, K);
   std::lock_guard<std::mutex> lock(g_ws_mu);
   const size_t need = enc_bytes(8, M, K) + enc_bytes(8, N, K);
   st = scratch_acquire(d->ws, need, stream);
@@ -1057,7 +1127,7 @@ lbgemm_status run_linear(int64_t M, int64_t N, int64_t K, const int8_t* X, const
 // (16-byte-aligned operands; the 8-bit routes need K % 16 == 0).
 bool entry_route_ok(int bits, int64_t M, int64_t N, int64_t K, int route, int param) {
   const void* al = reinterpret_cast<const void*>(uintptr_t(256));
-  return route >= 0 && route < LBGEMM_ROUTE_NONE && route_runs(bits, M, N, K, al, al, route, param);
+  return route >= 0 && route != LBGEMM_ROUTE_NONE && route_runs(bits, M, N, K, al, al, route, param);
 }
 
 // Reads "sm_count bits M N K variant [route param]" lines ('#' comments) and
@@ -1265,7 +1335,8 @@ lbgemm_status lbgemm_linear_quant(int64_t M, int64_t N, int64_t K, const void* X
     cudaError_t e = lbg::launch_quant_rows_bf16(X, M, K, Q, S, s);
     if (e != cudaSuccess) return cuda_fail(e, "quantize launch");
     g_launches += 1;
-    st = run_linear(M, N, K, Q, S, W, sw, Y, -1, s);
+    // W is the caller's, not written by the quantiser launched just before
+    st = run_linear(M, N, K, Q, S, W, sw, Y, -1, s, -1, 0, true);
     lbgemm_status st2 = scratch_release(d->quant, s);
     return st != LBGEMM_OK ? st : st2;
   } catch (...) {
@@ -1330,6 +1401,17 @@ lbgemm_status lbgemm_linear_variant(int64_t M, int64_t N, int64_t K, const int8_
                                     int variant, void* stream) {
   try {
     return run_linear(M, N, K, X, sx, W, sw, Y, variant, as_stream(stream));
+  } catch (...) {
+    return fail(LBGEMM_ERR_CUDA, "internal error");
+  }
+}
+
+lbgemm_status lbgemm_linear_candidate(int64_t M, int64_t N, int64_t K, const int8_t* X,
+                                      const float* sx, const int8_t* W, const float* sw, void* Y,
+                                      int route, int param, void* stream) {
+  try {
+    if (route < 0) return fail(LBGEMM_ERR_INVALID_ARG, "route %d out of range", route);
+    return run_linear(M, N, K, X, sx, W, sw, Y, -1, as_stream(stream), route, param);
   } catch (...) {
     return fail(LBGEMM_ERR_CUDA, "internal error");
   }

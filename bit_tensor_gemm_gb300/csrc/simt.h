@@ -34,6 +34,16 @@ int64_t hmma_skinny_max_k(int MX);
 cudaError_t launch_hmma_skinny(const int8_t* X, const int8_t* W, int MX, int NW, int K,
                                bool trans, int32_t* C, const float* sx, const float* sw, void* Y,
                                int chunk_elems, int sm_count, cudaStream_t s);
+// 8-bit GEMM with a small side X (1 <= MX <= 16 rows) against W (NW rows),
+// K % 16 == 0, K <= stream_mma_max_k(), 16-byte-aligned rows: W streamed once
+// through a bulk-copy ring, warp-level fp16 MMAs; out[x][w] (or out[w][x]
+// when trans); the linear layer when Y is given (not trans).  early_w: W is
+// not written by the grid launched before (its copies may start at once).
+// Wait time-outs set *status.  stream_mma.cu.
+int64_t stream_mma_max_k();
+cudaError_t launch_stream_mma(const int8_t* X, const int8_t* W, int MX, int NW, int K, bool trans,
+                              int32_t* C, const float* sx, const float* sw, void* Y, bool early_w,
+                              int sm_count, int* status, cudaStream_t s);
 cudaError_t launch_quant_rows_bf16(const void* X, int64_t M, int64_t K, int8_t* Q, float* S,
                                    cudaStream_t s);
 // Small 8-bit GEMM on dp4a, one launch; K % 16 == 0, A and B 16-byte aligned.

@@ -27,6 +27,7 @@ ERR_WORKSPACE = 6
 
 # kernels of the default dispatch (lbgemm_route)
 ROUTE_TABLE, ROUTE_POPC, ROUTE_SKINNY, ROUTE_WARPMMA, ROUTE_SMALL, ROUTE_FUSED, ROUTE_NONE = range(7)
+ROUTE_STREAM = 7
 STATUS_NAMES = {0: "OK", 1: "INVALID_ARG", 2: "ALIGNMENT", 3: "UNSUPPORTED", 4: "CUDA",
                 5: "TIMEOUT", 6: "WORKSPACE"}
 
@@ -59,6 +60,8 @@ _SIGNATURES = {
     "lbgemm_quantize_rows": (_i32, [_i64, _i64, _vp, _vp, _vp, _vp]),
     "lbgemm_linear_quant": (_i32, [_i64, _i64, _i64, _vp, _vp, _vp, _vp, _vp]),
     "lbgemm_linear_variant": (_i32, [_i64, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _i32, _vp]),
+    "lbgemm_linear_candidate": (_i32, [_i64, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _i32, _i32,
+                                       _vp]),
     "lbgemm_select": (_i32, [_i32, _i64, _i64, _i64]),
     "lbgemm_table_set": (_i32, [_i32, _i64, _i64, _i64, _i32]),
     "lbgemm_select_for": (_i32, [_i32, _i32, _i64, _i64, _i64]),
@@ -247,6 +250,11 @@ def lbgemm_linear_quant(M, N, K, X, W, sw, Y, stream=None) -> None:
 def lbgemm_linear_variant(M, N, K, X, sx, W, sw, Y, variant, stream=None) -> None:
     _check(load().lbgemm_linear_variant(M, N, K, _addr(X), _addr(sx), _addr(W), _addr(sw),
                                         _addr(Y), variant, _stream(stream)))
+
+
+def lbgemm_linear_candidate(M, N, K, X, sx, W, sw, Y, route, param=0, stream=None) -> None:
+    _check(load().lbgemm_linear_candidate(M, N, K, _addr(X), _addr(sx), _addr(W), _addr(sw),
+                                          _addr(Y), route, param, _stream(stream)))
 
 
 def lbgemm_select(bits, M, N, K) -> int:

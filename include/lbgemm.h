@@ -84,6 +84,9 @@ lbgemm_status lbgemm_variant_info(int bits, int variant, int* tile_m, int* tile_
  * (int8 -> fp16, int4 -> e4m3, +-1 -> e4m3), except these shape rules, in
  * order (the 8-bit ones need K % 16 == 0 and 16-byte-aligned operands):
  * 8-bit problems with M <= 4 run on a dp4a kernel that streams B once;
+ * 8-bit problems with min(M, N) <= 16, max(M, N) >= 1024 and K <= 4096 on
+ * a warp-level fp16 MMA kernel that streams the large operand once through a
+ * bulk-copy ring (LBGEMM_ROUTE_STREAM);
  * 8-bit problems with min(M, N) <= 32 (and K within the limit of
  * lbgemm_run_warpmma) on the warp-level fp16 MMA kernel, which streams the
  * large operand once; small 8-bit problems with min(M, N) <= 256,
@@ -227,8 +230,9 @@ lbgemm_status lbgemm_run_popc(int64_t M, int64_t N, int64_t K, const uint32_t* A
  * [M]); W: int8 N x K (per-output-channel scale sw, fp32 [N]); Y: bf16 M x N
  * row-major, passed as void* (2 bytes per element).  The scale product is
  * formed in fp32, left to right.  K <= 131071.  The shape rules of
- * lbgemm_run apply: M <= 4 on the dp4a kernel that streams W once, M <= 32
- * on the warp-level fp16 MMA kernel, M <= 512 (with N >= 1024 and N, K as
+ * lbgemm_run apply: M <= 4 on the dp4a kernel that streams W once, M <= 16
+ * (N >= 1024, K <= 4096) on the streaming warp-MMA kernel, M <= 32 on the
+ * warp-level fp16 MMA kernel, M <= 512 (with N >= 1024 and N, K as
  * lbgemm_run says) on the kernel that converts W itself, larger M on the
  * tensor-core variant table. */
 lbgemm_status lbgemm_linear(int64_t M, int64_t N, int64_t K, const int8_t* X, const float* sx,
@@ -238,6 +242,16 @@ lbgemm_status lbgemm_linear(int64_t M, int64_t N, int64_t K, const int8_t* X, co
 lbgemm_status lbgemm_linear_variant(int64_t M, int64_t N, int64_t K, const int8_t* X,
                                     const float* sx, const int8_t* W, const float* sw, void* Y,
                                     int variant, void* stream);
+
+/* As lbgemm_linear, forced onto one kernel: route LBGEMM_ROUTE_TABLE (param =
+ * variant), LBGEMM_ROUTE_SKINNY (M <= 16), LBGEMM_ROUTE_STREAM (M <= 16,
+ * K <= 4096), LBGEMM_ROUTE_WARPMMA (min(M, N) <= 32) or LBGEMM_ROUTE_FUSED
+ * (param = tile width 64, 128 or 256); the 8-bit routes need K % 16 == 0 and
+ * 16-byte-aligned X and W.  LBGEMM_ERR_INVALID_ARG if that kernel cannot run
+ * the layer.  For tests and timing. */
+lbgemm_status lbgemm_linear_candidate(int64_t M, int64_t N, int64_t K, const int8_t* X,
+                                      const float* sx, const int8_t* W, const float* sw, void* Y,
+                                      int route, int param, void* stream);
 
 /* Per-token (per-row) symmetric int8 quantisation of activations, the step in
  * front of a quantised linear layer ([LBG] section 4 and conclusion: low-bit
@@ -277,7 +291,9 @@ typedef enum {
   LBGEMM_ROUTE_WARPMMA = 3, /* warp-level fp16 MMA kernel (lbgemm_run_warpmma)        */
   LBGEMM_ROUTE_SMALL = 4,   /* one-launch dp4a kernel                                */
   LBGEMM_ROUTE_FUSED = 5,   /* in-kernel conversion kernel (lbgemm_run_fused)         */
-  LBGEMM_ROUTE_NONE = 6     /* M == 0 or N == 0: nothing runs                        */
+  LBGEMM_ROUTE_NONE = 6,    /* M == 0 or N == 0: nothing runs                        */
+  LBGEMM_ROUTE_STREAM = 7   /* small side <= 16, K <= 4096: warp-level fp16 MMAs on the
+                               large operand streamed once through a bulk-copy ring    */
 } lbgemm_route_id;
 
 /* The shape rules listed at lbgemm_run: the kernel lbgemm_run (linear = 0)

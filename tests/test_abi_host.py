@@ -200,6 +200,8 @@ def _route8(M, N, K, linear=False):
     k16 = K % 16 == 0
     if M <= 4 and k16:
         return L.ROUTE_SKINNY, 0
+    if lo <= 16 and hi >= 1024 and k16 and K <= 4096 and (not linear or M <= 16):
+        return L.ROUTE_STREAM, 0
     if lo <= 32 and k16 and K <= (4224 if lo <= 16 else 2048):
         return L.ROUTE_WARPMMA, 0
     if not linear:
@@ -230,7 +232,9 @@ def test_routes_follow_the_stated_rules(lib):
 def test_routes_of_measured_examples(lib):
     R = L
     cases = [((8, 1, 11008, 4096), (R.ROUTE_SKINNY, 0)),
-             ((8, 16, 11008, 4096), (R.ROUTE_WARPMMA, 0)),
+             ((8, 16, 11008, 4096), (R.ROUTE_STREAM, 0)),
+             ((8, 11008, 5, 4096), (R.ROUTE_STREAM, 0)),
+             ((8, 16, 11008, 4224), (R.ROUTE_WARPMMA, 0)),
              ((8, 64, 1024, 1024), (R.ROUTE_WARPMMA, 0)),
              ((8, 256, 256, 256), (R.ROUTE_SMALL, 0)),
              ((8, 64, 8192, 2048), (R.ROUTE_FUSED, 64)),
@@ -245,7 +249,7 @@ def test_routes_of_measured_examples(lib):
     for args, want in cases:
         assert L.lbgemm_route(*args) == want, args
     # the linear layer on the 11008 x 4096 weights, token counts of the benchmark
-    for M, want in [(1, (R.ROUTE_SKINNY, 0)), (16, (R.ROUTE_WARPMMA, 0)),
+    for M, want in [(1, (R.ROUTE_SKINNY, 0)), (16, (R.ROUTE_STREAM, 0)), (17, (R.ROUTE_FUSED, 64)),
                     (128, (R.ROUTE_FUSED, 128)), (2048, (R.ROUTE_TABLE, 0))]:
         assert L.lbgemm_route(8, M, 11008, 4096, linear=True) == want, M
     for bad in [(3, 4, 4, 16), (8, -1, 4, 16), (8, 4, 4, 0)]:
@@ -261,7 +265,8 @@ def test_bench_route_histogram(lib):
     import bench  # noqa: PLC0415
     h = bench.route_histogram(L, bench.SWEEP)
     assert sum(e["shapes"] for e in h.values()) == 729
-    assert set(h) <= {"table", "skinny_dp4a", "warp_mma", "small_dp4a", "in_kernel_conversion_64",
+    assert set(h) <= {"table", "skinny_dp4a", "stream_mma", "warp_mma", "small_dp4a",
+                      "in_kernel_conversion_64",
                       "in_kernel_conversion_128", "in_kernel_conversion_256"}
     assert h["table"]["shapes"] > 200 and "ms" not in h["table"]
     t = bench.route_histogram(L, bench.SWEEP[:3], [1.0, 2.0, 3.0])
@@ -341,7 +346,7 @@ def test_header_is_plain_c_and_links(lib, tmp_path):
     tm, tn, tk, stages, route, tile, bad, has_msg = map(int, out)
     info = L.lbgemm_variant_info(8, L.lbgemm_default_variant())
     assert (tm, tn, tk, stages) == (info["tile_m"], info["tile_n"], info["tile_k"], info["stages"])
-    assert (route, tile) == (L.ROUTE_WARPMMA, 0)
+    assert (route, tile) == (L.ROUTE_STREAM, 0)
     assert bad == L.ERR_INVALID_ARG and has_msg == 1
 
 
@@ -374,8 +379,11 @@ def test_candidates_cover_the_routes_that_run(lib):
     assert L.lbgemm_candidates(1, 64, 64, 1024) == tc + [(POPC, v) for v in range(9)]
     assert L.lbgemm_candidates(8, 16384, 16384, 16384) == tc
     assert L.lbgemm_candidates(8, 64, 16384, 4096) == tc + [(FU, 64), (FU, 128)]
-    assert L.lbgemm_candidates(8, 8, 1024, 1024) == tc + [(SK, 0), (WM, 0), (SM, 0), (FU, 64),
-                                                          (FU, 128)]
+    assert L.lbgemm_candidates(8, 8, 1024, 1024) == tc + [(SK, 0), (L.ROUTE_STREAM, 0), (WM, 0),
+                                                          (SM, 0), (FU, 64), (FU, 128)]
+    assert (L.ROUTE_STREAM, 0) in L.lbgemm_candidates(8, 4096, 16, 4096)
+    assert (L.ROUTE_STREAM, 0) not in L.lbgemm_candidates(8, 4096, 16, 4112)  # K <= 4096
+    assert (L.ROUTE_STREAM, 0) not in L.lbgemm_candidates(8, 17, 4096, 1024)
     assert L.lbgemm_candidates(8, 256, 512, 2048) == tc + [(WM, 0), (SM, 0), (FU, 64), (FU, 128),
                                                            (FU, 256)]
     assert L.lbgemm_candidates(8, 256, 512, 4096) == tc + [(SM, 0), (FU, 64), (FU, 128), (FU, 256)]
