@@ -32,6 +32,7 @@
 
 namespace lbg {
 int mlp_pick(int bits, int64_t M, int64_t N, int64_t K, int sm_count);
+lbgemm_status mlp_load_file(const char* path);
 }
 
 // Device status word: kernels OR error bits into it (see lbgemm_device_status).
@@ -293,36 +294,55 @@ std::string g_table_default_path;  // the file loaded at first use ("" if none)
 
 lbgemm_status table_load_file(const char* path);
 
-// The table shipped beside the library (data/lbgemm_table_gb300.txt next to
-// its lib/ directory), or the file named by LBGEMM_TABLE ("" or "none": no
-// table), loaded once per process before the first use of the table.
+bool file_exists(const std::string& path) {
+  FILE* f = fopen(path.c_str(), "r");
+  if (!f) return false;
+  fclose(f);
+  return true;
+}
+
+// The data directory shipped beside the library (data/ next to its lib/).
+std::string shipped_data_dir() {
+  Dl_info info;
+  if (!dladdr(reinterpret_cast<void*>(&shipped_data_dir), &info) || !info.dli_fname) return "";
+  std::string so = info.dli_fname;
+  const size_t slash = so.rfind('/');
+  return (slash == std::string::npos ? std::string(".") : so.substr(0, slash)) + "/../data/";
+}
+
+// Loaded once per process, before the first use of the table: the table
+// named by LBGEMM_TABLE ("" or "none": no table), else the GB300 table
+// shipped beside the library (data/lbgemm_table_gb300.txt); and the selector
+// networks shipped there (data/mlp_gb300_s<bits>.txt) unless LBGEMM_MLP is
+// "" or "none".  A file that fails to load is reported on stderr and skipped.
 void ensure_default_table() {
   std::call_once(g_table_once, [] {
+    const std::string saved = t_last_error;
+    const std::string dir = shipped_data_dir();
     std::string path;
     const char* env = std::getenv("LBGEMM_TABLE");
     if (env) {
-      if (env[0] == '\0' || std::strcmp(env, "none") == 0) return;
-      path = env;
-    } else {
-      Dl_info info;
-      if (!dladdr(reinterpret_cast<void*>(&ensure_default_table), &info) || !info.dli_fname)
-        return;
-      std::string so = info.dli_fname;
-      const size_t slash = so.rfind('/');
-      const std::string libdir = slash == std::string::npos ? "." : so.substr(0, slash);
-      path = libdir + "/../data/lbgemm_table_gb300.txt";
-      FILE* probe = fopen(path.c_str(), "r");
-      if (!probe) return;  // no shipped table: selection starts empty
-      fclose(probe);
+      if (env[0] != '\0' && std::strcmp(env, "none") != 0) path = env;
+    } else if (!dir.empty() && file_exists(dir + "lbgemm_table_gb300.txt")) {
+      path = dir + "lbgemm_table_gb300.txt";
     }
-    const std::string saved = t_last_error;
-    if (table_load_file(path.c_str()) != LBGEMM_OK) {
-      fprintf(stderr, "lbgemm: selection table %s not loaded: %s\n", path.c_str(),
-              t_last_error.c_str());
-      t_last_error = saved;
-      return;
+    if (!path.empty()) {
+      if (table_load_file(path.c_str()) == LBGEMM_OK)
+        g_table_default_path = path;
+      else
+        fprintf(stderr, "lbgemm: selection table %s not loaded: %s\n", path.c_str(),
+                t_last_error.c_str());
     }
-    g_table_default_path = path;
+    const char* envm = std::getenv("LBGEMM_MLP");
+    const bool nets = !envm || (envm[0] != '\0' && std::strcmp(envm, "none") != 0);
+    for (int bits : {8, 4, 1}) {
+      const std::string net = dir + "mlp_gb300_s" + std::to_string(bits) + ".txt";
+      if (!nets || dir.empty() || !file_exists(net)) continue;
+      if (lbg::mlp_load_file(net.c_str()) != LBGEMM_OK)
+        fprintf(stderr, "lbgemm: selector network %s not loaded: %s\n", net.c_str(),
+                t_last_error.c_str());
+    }
+    t_last_error = saved;
   });
 }
 
@@ -1888,6 +1908,8 @@ namespace lbg {
 lbgemm_status report_error(lbgemm_status st, const char* message) {
   return fail(st, "%s", message);
 }
+
+void ensure_defaults() { ensure_default_table(); }
 
 // Scratch bytes that lbgemm_run_ws(bits, M, N, K, A, B, C, variant, ...)
 // needs: the route the dispatch takes (variant < 0) or the tensor-core

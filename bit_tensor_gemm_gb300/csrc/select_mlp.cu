@@ -127,6 +127,9 @@ int mlp_pick(int bits, int64_t M, int64_t N, int64_t K, int sm_count) {
   std::lock_guard<std::mutex> lock(g_mu);
   const Mlp& m = g_models[bits];
   if (!m.loaded || m.layers.back().n_out != 9) return -1;
+  // a network trained on one SM count (its SM feature constant: standard
+  // deviation stored as 1) answers for that SM count only
+  if (m.stdv[3] == 1.0f && std::fabs((float)sm_count - m.mean[3]) > 0.5f) return -1;
   const float x[4] = {(float)std::log2((double)M), (float)std::log2((double)N),
                       (float)std::log2((double)K), (float)sm_count};
   int a, b;
@@ -134,26 +137,37 @@ int mlp_pick(int bits, int64_t M, int64_t N, int64_t K, int sm_count) {
   return a;
 }
 
+// Loads a network file (no default loading first: the defaults use this).
+lbgemm_status mlp_load_file(const char* path) {
+  if (!path) return report_error(LBGEMM_ERR_INVALID_ARG, "null path");
+  FILE* f = fopen(path, "r");
+  if (!f) return report_error(LBGEMM_ERR_INVALID_ARG, "cannot open the network file");
+  Mlp m;
+  int bits = 0;
+  std::string why;
+  const bool ok = parse(f, m, bits, why);
+  fclose(f);
+  if (!ok) return report_error(LBGEMM_ERR_INVALID_ARG, ("network file: " + why).c_str());
+  std::lock_guard<std::mutex> lock(g_mu);
+  g_models[bits] = std::move(m);
+  return LBGEMM_OK;
+}
+
+// The shipped table and networks are loaded before any change the caller
+// makes (api.cu).
+void ensure_defaults();
+
 }  // namespace lbg
 
 extern "C" {
 
 lbgemm_status lbgemm_mlp_load(const char* path) {
-  if (!path) return lbg::report_error(LBGEMM_ERR_INVALID_ARG, "null path");
-  FILE* f = fopen(path, "r");
-  if (!f) return lbg::report_error(LBGEMM_ERR_INVALID_ARG, "cannot open the network file");
-  lbg::Mlp m;
-  int bits = 0;
-  std::string why;
-  const bool ok = lbg::parse(f, m, bits, why);
-  fclose(f);
-  if (!ok) return lbg::report_error(LBGEMM_ERR_INVALID_ARG, ("network file: " + why).c_str());
-  std::lock_guard<std::mutex> lock(lbg::g_mu);
-  lbg::g_models[bits] = std::move(m);
-  return LBGEMM_OK;
+  lbg::ensure_defaults();
+  return lbg::mlp_load_file(path);
 }
 
 lbgemm_status lbgemm_mlp_clear(void) {
+  lbg::ensure_defaults();
   std::lock_guard<std::mutex> lock(lbg::g_mu);
   for (auto& m : lbg::g_models) m = lbg::Mlp();
   return LBGEMM_OK;
@@ -161,6 +175,7 @@ lbgemm_status lbgemm_mlp_clear(void) {
 
 int lbgemm_mlp_predict(int bits, int64_t M, int64_t N, int64_t K, int sm_count, int* second) {
   if ((bits != 1 && bits != 4 && bits != 8) || M < 1 || N < 1 || K < 1) return -1;
+  lbg::ensure_defaults();
   std::lock_guard<std::mutex> lock(lbg::g_mu);
   const lbg::Mlp& m = lbg::g_models[bits];
   if (!m.loaded) return -1;

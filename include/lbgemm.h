@@ -333,7 +333,9 @@ lbgemm_status lbgemm_table_save(const char* path);
 /* The table is filled once per process, before its first use, from the file
  * named by the environment variable LBGEMM_TABLE (unset: the GB300 table
  * shipped with the library, data/lbgemm_table_gb300.txt beside its lib/
- * directory; "" or "none": nothing).  The path loaded, or "" if none. */
+ * directory; "" or "none": nothing); at the same moment the selector
+ * networks shipped there (data/mlp_gb300_s<bits>.txt) are loaded unless
+ * LBGEMM_MLP is "" or "none".  The table path loaded, or "" if none. */
 const char* lbgemm_table_default_path(void);
 
 /* ---- learned selector: [LBG] section 3 ------------------------------------------
@@ -342,9 +344,12 @@ const char* lbgemm_table_default_path(void);
  * offline on sweep timings (bit_tensor_gemm_gb300/selector_mlp.py writes the
  * text file).  Once a nine-class network is loaded for a bit width,
  * lbgemm_select answers shapes that have no table entry with the network's
- * top class (before the nearest-entry rule).  The network runs on the host in
- * float32.  lbgemm_mlp_load replaces the network of the file's bit width;
- * LBGEMM_ERR_INVALID_ARG for a missing or malformed file. */
+ * top class (before the nearest-entry rule); a network trained on a single
+ * SM count (the file's SM standard deviation is 1) answers for that SM count
+ * only.  The network runs on the host in float32.  lbgemm_mlp_load replaces
+ * the network of the file's bit width; LBGEMM_ERR_INVALID_ARG for a missing
+ * or malformed file.  The shipped GB300 networks load by default (see
+ * lbgemm_table_default_path). */
 lbgemm_status lbgemm_mlp_load(const char* path);
 lbgemm_status lbgemm_mlp_clear(void);
 /* Top class of the network loaded for `bits` (and the second one in *second

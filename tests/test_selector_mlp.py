@@ -35,6 +35,7 @@ def test_oracle_forward_hand_worked():
 
 
 def test_library_matches_hand_worked(lib):
+    L.lbgemm_mlp_clear()  # the shipped networks load by default
     L.lbgemm_mlp_load(TINY)
     assert L.lbgemm_mlp_predict(8, 8, 4, 2, 5) == (2, 0)
     assert L.lbgemm_mlp_predict(8, 2, 16, 2, 1) == (2, 1)
@@ -108,3 +109,29 @@ def test_save_load_roundtrip(tmp_path):
     X = S.features([100, 7], [300, 9000], [64, 4096], 152)
     assert np.allclose(back.logits(X), net.logits(X), rtol=1e-6, atol=1e-6)
     assert back.bits == 4
+
+
+def test_shipped_networks_load_by_default_and_answer_their_sm_count(lib):
+    """A fresh process has the GB300 networks of every bit width; a network
+    trained on one SM count does not answer for another."""
+    import json  # noqa: PLC0415
+    import subprocess  # noqa: PLC0415
+    import sys  # noqa: PLC0415
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    code = ("import sys, json; sys.path.insert(0, %r)\n"
+            "from bit_tensor_gemm_gb300 import lbgemm as L\n"
+            "print(json.dumps([L.lbgemm_mlp_predict(b, 300, 5000, 700, 152)[0] for b in (8, 4, 1)]"
+            " + [L.lbgemm_select_for(150, 8, 300, 5000, 700)]))" % root)
+    env = {k: v for k, v in os.environ.items() if k not in ("LBGEMM_MLP", "LBGEMM_TABLE")}
+    got = json.loads(subprocess.run([sys.executable, "-c", code], env=env, capture_output=True,
+                                    text=True, check=True).stdout)
+    for bits, v in zip((8, 4, 1), got[:3]):
+        net = S.MLP.load(os.path.join(root, "bit_tensor_gemm_gb300", "data",
+                                      f"mlp_gb300_s{bits}.txt"))
+        assert v == int(net.predict_top2(S.features([300], [5000], [700], 152))[0, 0]), bits
+    # SM count 150: no table entries, the network does not apply: the default
+    assert got[3] == 7
+    env["LBGEMM_MLP"] = "none"
+    got = json.loads(subprocess.run([sys.executable, "-c", code], env=env, capture_output=True,
+                                    text=True, check=True).stdout)
+    assert got[:3] == [-1, -1, -1]
