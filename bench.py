@@ -64,6 +64,9 @@ def parse_args():
     p.add_argument("--shapes", type=int, default=0, help="debug: use only the first N shapes")
     p.add_argument("--no-cpu", action="store_true", help="debug: skip the CPU oracle sample")
     p.add_argument("--dump", default="", help="write per-shape sweep data (JSON) to this path")
+    p.add_argument("--table", default="",
+                   help="profiling: load this selection table instead of running the sweep "
+                        "(no selection re-time in the line)")
     return p.parse_args()
 
 
@@ -438,7 +441,9 @@ def run_ours(args):
     #    keeps the label and the dispatch pick (tune.py) ---------------------------------------
     L.lbgemm_table_clear()
     recs, sweep_s, mlp_eval = {}, {}, {}
-    for bits in BITS:
+    if args.table:
+        L.lbgemm_table_load(args.table)
+    for bits in ([] if args.table else BITS):
         Ab, Bb = operands_of(bits)
         t0 = time.perf_counter()
         recs[bits] = tune.sweep(L, bits, shapes, Ab, Bb, C, sm, reps=args.sweep_reps,
@@ -497,7 +502,7 @@ def run_ours(args):
     dv = (ROUTE_TABLE, L.lbgemm_default_variant())
     selection_by_bits, rooflines = {}, {}
     s_ms = None
-    for bits in BITS:
+    for bits in ([] if args.table else BITS):
         Ab, Bb = operands_of(bits)
         label = [(ROUTE_TABLE, r["label"]) for r in recs[bits]]
         disp = [tuple(L.lbgemm_dispatch_for(sm, bits, *sh)) for sh in shapes]
@@ -511,9 +516,13 @@ def run_ours(args):
         if bits == 8:
             s_ms = T[:, 2]
         del Ab, Bb
-    selection = dict(selection_by_bits[8])
-    selection["by_bits"] = {str(b): selection_by_bits[b] for b in BITS if b != 8}
-    sweep_roofline = rooflines[8]
+    if args.table:
+        selection = {"table": args.table, "note": "loaded, not measured in this run"}
+        sweep_roofline = None
+    else:
+        selection = dict(selection_by_bits[8])
+        selection["by_bits"] = {str(b): selection_by_bits[b] for b in BITS if b != 8}
+        sweep_roofline = rooflines[8]
 
     # -- roofline of the dominant kernel: the tensor-core GEMM alone on encoded operands ------
     encA = torch.empty(L.lbgemm_encoded_size(8, MAXD, MAXD), dtype=torch.uint8, device=dev)
@@ -719,7 +728,8 @@ def run_ours(args):
             with open(args.dump, "w") as f:
                 json.dump({"shapes": shapes, "sm_count": sm,
                            "records": {str(b): r for b, r in recs.items()},
-                           "dispatch_ms_8bit": s_ms.tolist(), "kernel_only_ms": enc_ms}, f)
+                           "dispatch_ms_8bit": None if s_ms is None else s_ms.tolist(),
+                           "kernel_only_ms": enc_ms}, f)
 
 
 def main():
