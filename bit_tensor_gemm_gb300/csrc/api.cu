@@ -83,6 +83,17 @@ std::atomic<int> g_chunk_s8{1024};
 std::atomic<int> g_chunk_s4{131072};
 std::atomic<int> g_chunk_b1{1 << 23};
 std::atomic<int> g_tail_split{1};  // 0 whole-problem splits only, 1 also a last partial wave, 2 forced
+// K elements per slice of the 64/128-wide conversion kernels; 0: by tile
+// (measured on GB300 over the grid shapes the dispatch gives these kernels:
+// 256-element slices make the 64-wide kernel up to 10 % faster, e.g. 64 x
+// 16384 x 16384 81.9 -> 74.3 us, and the 128-wide one up to 14 % slower, its
+// tensor memory then holding only two slots)
+std::atomic<int> g_fused_slice{0};
+
+int fused_slice(int tile_n) {
+  const int s = g_fused_slice.load();
+  return s ? s : tile_n == 64 ? 256 : 128;
+}
 
 lbgemm_status fail(lbgemm_status st, const char* fmt, ...) {
   char buf[512];
@@ -650,7 +661,7 @@ lbgemm_status run_tc_fused(DeviceState& d, bool large_b, int tile_n, int64_t M, 
                            int64_t K, const void* A, const void* B, int32_t* C, const float* sx,
                            const float* sw, void* Y, void* ws, cudaStream_t stream) {
   const bool linear = Y != nullptr;
-  TcKernel k = lbg::tc_kernel_ts(tile_n, large_b, linear);
+  TcKernel k = lbg::tc_kernel_ts(tile_n, large_b, linear, fused_slice(tile_n));
   if (!k.launch) return fail(LBGEMM_ERR_UNSUPPORTED, "no fused kernel (tile %d)", tile_n);
   // rows of the converted (L) and of the re-encoded (S) operand
   const int64_t rows_l = large_b ? N : M, rows_s = large_b ? M : N;
@@ -709,7 +720,7 @@ lbgemm_status run_tc_fused(DeviceState& d, bool large_b, int tile_n, int64_t M, 
   // 256-wide kernel steps through K in 64-element slices, the others in
   // 128-element slices
   const bool pairs = tile_n == 256;
-  const int slice = pairs ? 64 : 128;
+  const int slice = pairs ? 64 : k.slice;
   cuuint32_t box[2] = {128u, 128};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = g_encode(&ml, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(opl), dims,
@@ -1855,6 +1866,15 @@ lbgemm_status lbgemm_set_exact_chunk(int bits, int k_elems) {
   }
   return fail(LBGEMM_ERR_INVALID_ARG, "bits must be 8, 4 or 1");
 }
+
+lbgemm_status lbgemm_set_fused_slice(int k_elems) {
+  if (k_elems != 0 && k_elems != 128 && k_elems != 256)
+    return fail(LBGEMM_ERR_INVALID_ARG, "the fused slice must be 0, 128 or 256 (got %d)", k_elems);
+  g_fused_slice = k_elems;
+  return LBGEMM_OK;
+}
+
+int lbgemm_get_fused_slice(void) { return g_fused_slice.load(); }
 
 lbgemm_status lbgemm_set_tail_split(int mode) {
   if (mode < 0 || mode > 2) return fail(LBGEMM_ERR_INVALID_ARG, "tail split mode must be 0, 1 or 2");

@@ -42,6 +42,7 @@ struct TcKernel {
   int cluster = 1;      // CTAs per tile: 2 for the cta_group::2 kernel
   int stages = 0;
   int threads = 320;
+  int slice = 0;  // K elements per slice of the in-kernel-conversion kernels (0: others)
 };
 
 // Dynamic shared memory to request so that the CTAs that fit on one SM by
@@ -59,8 +60,9 @@ TcKernel tc_kernel_small(int stages, bool f8, bool linear);
 TcKernel tc_kernel_medium(int stages, bool f8, bool linear);
 TcKernel tc_kernel_pair(int stages, bool f8, bool linear);
 // One operand converted from int8 in the kernel and fed to the MMA from tensor
-// memory (8-bit only, 6 stages): trans = false converts A, trans = true
-// converts B (C is written transposed from the accumulator); tile_n 64, 128 or 256.
-TcKernel tc_kernel_ts(int tile_n, bool trans, bool linear);
+// memory (8-bit only): trans = false converts A, trans = true converts B (C is
+// written transposed from the accumulator); tile_n 64, 128 or 256; slice: K
+// elements per pipeline slice of the 64- and 128-wide kernels (128 or 256).
+TcKernel tc_kernel_ts(int tile_n, bool trans, bool linear, int slice = 128);
 
 }  // namespace lbg

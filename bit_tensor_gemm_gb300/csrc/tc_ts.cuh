@@ -14,12 +14,13 @@
 // 2 bytes by the GEMM: for a problem whose operands are large next to its
 // arithmetic that is most of the time.  Here the MMA's A operand (the "L"
 // operand, 128 rows per tile) stays int8 in global memory:
-//   - TMA copies each 128-element K slice of its 128 rows (16 KB, 128-byte
-//     rows with the 128-byte swizzle) into a staging ring in shared memory;
+//   - TMA copies each K slice of its 128 rows (SK / 128 boxes of 16 KB,
+//     128-byte rows with the 128-byte swizzle) into a staging ring in shared
+//     memory;
 //   - four converter warps, one per 32-lane quarter of tensor memory, read
 //     their rows (thread t of quarter q owns row 32q + t; with the swizzle the
-//     32 threads' 16-byte reads hit distinct banks), turn the 128 int8 values
-//     into 64 words of packed fp16 (exact: the fp16 with bits 0x6400 | (v+128)
+//     32 threads' 16-byte reads hit distinct banks), turn each 64 int8 values
+//     into 32 words of packed fp16 (exact: the fp16 with bits 0x6400 | (v+128)
 //     is 1024 + v + 128, minus 1152 gives v) and store them with tcgen05.st
 //     into a ring of 64-column slots of tensor memory;
 //   - the MMA thread issues tcgen05.mma with A read from tensor memory and B
@@ -29,12 +30,16 @@
 // written as fp16 and read again by the MMA), the tensor-memory route moves
 // 16 KB instead of 80 KB of shared memory per 128-row K slice.
 //
-// Slice size.  Every slice costs each role a fixed number of barrier
-// operations (a wait for the int8 data, a wait for the freed slot, arrivals,
-// a commit) of roughly 100 cycles each on GB300; instrumented, the roles of
-// the 64-element version spent ~1000 cycles per slice, of which the MMAs
-// (four of 128 x BN x 16) and the conversion were only a third.  128-element
-// slices halve those operations per byte.
+// Slice size (template parameter SK: 128 or 256 elements).  Every slice
+// costs each role a fixed number of barrier operations (a wait for the int8
+// data, a wait for the freed slot, arrivals, a commit) of roughly 100 cycles
+// each on GB300; instrumented, the roles of a 64-element version spent ~1000
+// cycles per slice, of which the MMAs (four of 128 x BN x 16) and the
+// conversion were only a third.  Longer slices cut those operations per
+// byte, but a slice's A slot takes SK / 2 columns of tensor memory: beside
+// two 128-column accumulators only two 256-element slots fit, too shallow a
+// pipeline (measured: the 64-wide kernel is up to 10 % faster with 256, the
+// 128-wide one up to 14 % slower).
 //
 // Output.  D's lane i and column j hold the sum for L-row i and S-row j.
 // TRANS = false: L is the GEMM's A, S its B, C[i][j] as in tc_gemm_kernel
@@ -44,7 +49,7 @@
 // of its stores writes 128 contiguous bytes (red.add under split K).
 //
 // Tensor memory: two fp32 accumulators of BN columns (alternating per K chunk,
-// as in tc_gemm_kernel), then STAGES slots of 64 columns for A.
+// as in tc_gemm_kernel), then STAGES slots of SK / 2 columns for A.
 //
 // Roles (448 threads):
 //   warp 0 lane 0   TMA producer of the int8 staging ring (L operand)
@@ -63,24 +68,29 @@ namespace lbg {
 
 constexpr int kTsConvWarps = 4;
 constexpr int kTsThreads = 32 * (2 + kTcEpiWarps + kTsConvWarps);  // 448
-constexpr int kTsSliceK = 128;  // K elements per slice (one staging stage, one A slot)
 
 __host__ __device__ constexpr int ts_tmem_cols(int need) {
   return need <= 32 ? 32 : need <= 64 ? 64 : need <= 128 ? 128 : need <= 256 ? 256 : 512;
 }
 
-template <int BN, int STAGES>
+// SK: K elements per slice (one staging stage, one A slot), 128 or 256.
+template <int BN, int STAGES, int SK>
 struct TsLayout {
-  // one slice of the S operand: two 64-element fp16 boxes (128-byte rows,
-  // 128-byte swizzle) of BN rows each
+  static_assert(SK == 128 || SK == 256, "K slices of 128 or 256 elements");
+  // one slice of the S operand: SK / 64 fp16 boxes of 64 elements (128-byte
+  // rows, 128-byte swizzle) of BN rows each
   static constexpr int kSBoxBytes = BN * 128;
-  static constexpr int kSBytes = 2 * kSBoxBytes;
+  static constexpr int kSBoxes = SK / 64;
+  static constexpr int kSBytes = kSBoxes * kSBoxBytes;
   static constexpr int kRingBytes = kSBytes * STAGES;
   static constexpr int kEpiOffset = kRingBytes;
   static constexpr int kEpiBytes = kTcEpiWarps * 32 * 128;
   static constexpr int kStgOffset = kEpiOffset + kEpiBytes;
   static constexpr int kStgStages = STAGES;
-  static constexpr int kStgStageBytes = kTcBM * kTsSliceK;  // 128 rows x 128 int8
+  // SK / 128 TMA boxes of 128 rows x 128 int8 (128-byte swizzle)
+  static constexpr int kStgBoxBytes = kTcBM * 128;
+  static constexpr int kStgBoxes = SK / 128;
+  static constexpr int kStgStageBytes = kStgBoxBytes * kStgBoxes;
   static constexpr int kStgBytes = kStgStageBytes * kStgStages;
   // barriers: full[S], empty[S], conv[S], acc_full[2], acc_empty[2], mma_done,
   // stg_full[SS], stg_empty[SS]
@@ -92,17 +102,18 @@ struct TsLayout {
   static constexpr int kDynSmem = kUsedBytes + 1024;  // slack to align the ring to 1024
   static constexpr int kAccCols = 2 * BN;
   static constexpr int kACol0 = kAccCols;  // first column of the A slots
-  static constexpr int kASlotCols = kTsSliceK / 2;  // packed fp16 pairs per row
+  static constexpr int kASlotCols = SK / 2;  // packed fp16 pairs per row
   static constexpr int kTmemCols = ts_tmem_cols(kAccCols + kASlotCols * STAGES);
   static_assert(kAccCols + kASlotCols * STAGES <= 512, "tensor memory holds 512 columns");
   static_assert(kDynSmem <= 232448, "shared memory per CTA");
 };
 
-template <int BN, int STAGES, bool TRANS, bool LINEAR>
+template <int BN, int STAGES, int SK, bool TRANS, bool LINEAR>
 __global__ void __launch_bounds__(kTsThreads, 1)
     tc_ts_kernel(const __grid_constant__ CUtensorMap tmL, const __grid_constant__ CUtensorMap tmS,
                  const __grid_constant__ CUtensorMap tmC, const TcParams p) {
-  using L = TsLayout<BN, STAGES>;
+  using L = TsLayout<BN, STAGES, SK>;
+  constexpr int kQuarters = SK / 64;  // 64-element pieces a converter handles per slice
   constexpr int SS = L::kStgStages;
   constexpr uint32_t kIdesc = instr_desc(kTcBM, BN);
   constexpr int kGroups = BN / 2 / 32;  // 32-column groups per epilogue thread
@@ -174,7 +185,10 @@ __global__ void __launch_bounds__(kTsThreads, 1)
           }
           const uint32_t st = sbase + L::kStgOffset + stage * L::kStgStageBytes;
           mbar_arrive_expect_tx(stgf_bar(stage), L::kStgStageBytes);
-          tma_load_2d(st, &tmL, stgf_bar(stage), kb * kTsSliceK, tm * kTcBM);
+#pragma unroll
+          for (int b = 0; b < L::kStgBoxes; ++b)
+            tma_load_2d(st + b * L::kStgBoxBytes, &tmL, stgf_bar(stage), kb * SK + 128 * b,
+                        tm * kTcBM);
           ++issued;
           if (++stage == SS) {
             stage = 0;
@@ -227,9 +241,9 @@ __global__ void __launch_bounds__(kTsThreads, 1)
             const uint32_t s_addr = sbase + stage * L::kSBytes;
             const uint32_t a_tmem = tmem_base + L::kACol0 + stage * L::kASlotCols;
 #pragma unroll
-            for (int k = 0; k < kTsSliceK / 16; ++k) {
+            for (int k = 0; k < SK / 16; ++k) {
               // K = 16 per MMA: 8 columns of A, 32 bytes (2 x 16 B) of each B
-              // row, in the first or second 64-element box of the slice
+              // row, in 64-element box k / 4 of the slice
               const uint64_t bdesc = smem_desc_sw128(s_addr + (k >> 2) * L::kSBoxBytes);
               const uint32_t accumulate = (kb > kb0 || k > 0) ? 1u : 0u;
               mma_f16_ts(d_tmem, a_tmem + 8 * k, bdesc + 2 * (k & 3), kIdesc, accumulate);
@@ -292,8 +306,9 @@ __global__ void __launch_bounds__(kTsThreads, 1)
         if (got && loader) {
           const uint32_t dst = sbase + os * L::kSBytes;
           mbar_arrive_expect_tx(full_bar(os), L::kSBytes);
-          tma_load_2d(dst, &tmS, full_bar(os), kb * kTsSliceK, tn * BN);
-          tma_load_2d(dst + L::kSBoxBytes, &tmS, full_bar(os), kb * kTsSliceK + 64, tn * BN);
+#pragma unroll
+          for (int b = 0; b < L::kSBoxes; ++b)
+            tma_load_2d(dst + b * L::kSBoxBytes, &tmS, full_bar(os), kb * SK + 64 * b, tn * BN);
           ++issued;
           if (++ls == STAGES) {
             ls = 0;
@@ -304,12 +319,14 @@ __global__ void __launch_bounds__(kTsThreads, 1)
       }
       return __shfl_sync(0xffffffffu, got, 0) != 0;
     };
-    // half h (64 elements, 32 words) of this thread's row of staging slot ss
+    // piece h (64 elements, 32 words) of this thread's row of staging slot ss:
+    // box h / 2, 16-byte chunks 4 (h % 2) .. 4 (h % 2) + 3 of the row
     auto convert = [&](int h, uint32_t (&words)[32]) {
-      const uint8_t* src = smem + L::kStgOffset + ss * L::kStgStageBytes + row * kTsSliceK;
+      const uint8_t* src = smem + L::kStgOffset + ss * L::kStgStageBytes +
+                           (h >> 1) * L::kStgBoxBytes + row * 128;
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        const int4 v = *reinterpret_cast<const int4*>(src + (((4 * h + q) ^ swz) << 4));
+        const int4 v = *reinterpret_cast<const int4*>(src + (((4 * (h & 1) + q) ^ swz) << 4));
         uint4 lo, hi;
         s8x16_to_f16(v, lo, hi);
         words[8 * q + 0] = lo.x;
@@ -330,15 +347,18 @@ __global__ void __launch_bounds__(kTsThreads, 1)
       if (ok) convert(0, cur);
     }
     while (ok && have) {
-      // first half of the slice: store it, convert the second meanwhile
+      // every piece but the last: store it, convert the next meanwhile
       const uint32_t slot = tmem_base + lane_addr + L::kACol0 + os * L::kASlotCols;
-      tmem_st32(slot, cur);
-      convert(1, nxt);
-      tmem_st_wait();
 #pragma unroll
-      for (int j = 0; j < 32; ++j) cur[j] = nxt[j];
-      // second half: store it, start the next slice meanwhile
-      tmem_st32(slot + 32, cur);
+      for (int h = 0; h + 1 < kQuarters; ++h) {
+        tmem_st32(slot + 32 * h, cur);
+        convert(h + 1, nxt);
+        tmem_st_wait();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) cur[j] = nxt[j];
+      }
+      // the last piece: store it, start the next slice meanwhile
+      tmem_st32(slot + 32 * (kQuarters - 1), cur);
       const int st_os = os, st_ss = ss;
       if (++os == STAGES) {
         os = 0;
@@ -484,10 +504,10 @@ __global__ void __launch_bounds__(kTsThreads, 1)
   }
 }
 
-template <int BN, int STAGES, bool TRANS, bool LINEAR>
+template <int BN, int STAGES, int SK, bool TRANS, bool LINEAR>
 cudaError_t tc_ts_launch(const CUtensorMap* l, const CUtensorMap* s, const CUtensorMap* c,
                          const TcParams* p, int grid, bool pdl, cudaStream_t stream) {
-  using L = TsLayout<BN, STAGES>;
+  using L = TsLayout<BN, STAGES, SK>;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kTsThreads);
@@ -498,20 +518,21 @@ cudaError_t tc_ts_launch(const CUtensorMap* l, const CUtensorMap* s, const CUten
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, tc_ts_kernel<BN, STAGES, TRANS, LINEAR>, *l, *s, *c, *p);
+  return cudaLaunchKernelEx(&cfg, tc_ts_kernel<BN, STAGES, SK, TRANS, LINEAR>, *l, *s, *c, *p);
 }
 
-template <int BN, int STAGES, bool TRANS, bool LINEAR>
+template <int BN, int STAGES, int SK, bool TRANS, bool LINEAR>
 TcKernel tc_ts_entry() {
-  using L = TsLayout<BN, STAGES>;
+  using L = TsLayout<BN, STAGES, SK>;
   TcKernel k;
-  k.launch = &tc_ts_launch<BN, STAGES, TRANS, LINEAR>;
-  k.func = reinterpret_cast<const void*>(&tc_ts_kernel<BN, STAGES, TRANS, LINEAR>);
+  k.launch = &tc_ts_launch<BN, STAGES, SK, TRANS, LINEAR>;
+  k.func = reinterpret_cast<const void*>(&tc_ts_kernel<BN, STAGES, SK, TRANS, LINEAR>);
   k.threads = kTsThreads;
   k.smem = tc_smem_request(L::kDynSmem, L::kTmemCols);
   k.tmem_cols = L::kTmemCols;
   k.tile_n = BN;
   k.stages = STAGES;
+  k.slice = SK;
   return k;
 }
 

@@ -90,6 +90,8 @@ _SIGNATURES = {
     "lbgemm_set_exact_chunk": (_i32, [_i32, _i32]),
     "lbgemm_get_exact_chunk": (_i32, [_i32]),
     "lbgemm_set_tail_split": (_i32, [_i32]),
+    "lbgemm_set_fused_slice": (_i32, [_i32]),
+    "lbgemm_get_fused_slice": (_i32, []),
     "lbgemm_get_tail_split": (_i32, []),
     "lbgemm_device_status": (_i32, [_vp]),
     "lbgemm_selftest_timeout": (_i32, [_vp]),
@@ -406,6 +408,16 @@ def lbgemm_get_exact_chunk(bits: int) -> int:
 def lbgemm_set_tail_split(mode: int) -> None:
     """0 whole-problem splits only, 1 also a partial last wave (default), 2 forced."""
     _check(load().lbgemm_set_tail_split(mode))
+
+
+def lbgemm_set_fused_slice(k_elems: int) -> None:
+    """K elements per slice of the 64/128-wide in-kernel-conversion kernels
+    (128 or 256; 0 = by tile width, the default)."""
+    _check(load().lbgemm_set_fused_slice(k_elems))
+
+
+def lbgemm_get_fused_slice() -> int:
+    return load().lbgemm_get_fused_slice()
 
 
 def lbgemm_get_tail_split() -> int:

@@ -448,6 +448,19 @@ int lbgemm_get_exact_chunk(int bits);
 lbgemm_status lbgemm_set_tail_split(int mode);
 int lbgemm_get_tail_split(void);
 
+/* ---- K slices of the in-kernel conversion kernels -------------------------------
+ * The 64- and 128-wide in-kernel-conversion kernels (LBGEMM_ROUTE_FUSED with
+ * tile 64 or 128, lbgemm_run_fused) step through K in slices of 128 or 256
+ * elements: each slice costs the kernel's roles a fixed number of barrier
+ * operations, and longer slices leave fewer slots in tensor memory (6 or 4
+ * slots of 128, 3 or 2 of 256).  0 (the default): 256 for the 64-wide
+ * kernel, 128 for the 128-wide one (measured fastest on GB300); 128 or 256:
+ * that size for both.  A scheduling choice only: C is the same exact int32
+ * result.  Process-wide; affects calls launched afterwards;
+ * LBGEMM_ERR_INVALID_ARG for another value. */
+lbgemm_status lbgemm_set_fused_slice(int k_elems);
+int lbgemm_get_fused_slice(void);
+
 /* ---- status ------------------------------------------------------------------ */
 
 /* Synchronises `stream`, then returns LBGEMM_ERR_TIMEOUT if any kernel of this

@@ -523,3 +523,15 @@ def test_table_file_from_the_environment(lib, tmp_path):
     got = _fresh_process([[4242, 4, 100, 200, 300], [4242, 8, 64, 4096, 1024]], env_table=str(p))
     assert got["size"] == 2 and got["path"] == str(p)
     assert got["q"] == [[5, [L.ROUTE_TABLE, 5]], [2, [L.ROUTE_FUSED, 64]]]
+
+
+def test_fused_slice_setting(lib):
+    assert L.lbgemm_get_fused_slice() == 0
+    for v in (128, 256, 0):
+        L.lbgemm_set_fused_slice(v)
+        assert L.lbgemm_get_fused_slice() == v
+    for bad in (64, 512, -1):
+        with pytest.raises(L.LbgemmError) as e:
+            L.lbgemm_set_fused_slice(bad)
+        assert e.value.status == L.ERR_INVALID_ARG
+    assert L.lbgemm_get_fused_slice() == 0

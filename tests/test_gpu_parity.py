@@ -104,14 +104,20 @@ FUSED_SHAPES = [(300, 520, 1040), (520, 300, 1040), (129, 4100, 2048), (4100, 12
                 (100, 1100, 16384), (1, 1, 16), (256, 256, 3008)]
 
 
+@pytest.mark.parametrize("slice_k", [0, 128, 256])
 @pytest.mark.parametrize("tile_n", [64, 128, 256])
-def test_int8_fused_every_tile(tile_n):
+def test_int8_fused_every_tile(tile_n, slice_k):
     """lbgemm_run_fused with each tile width (64 and 128: double-buffered
-    accumulators; 256: one accumulator, K in groups of 4 slices)."""
-    for i, (M, N, K) in enumerate(FUSED_SHAPES):
-        A, B = synth.operands(8, M, N, K, 900 + 17 * i + tile_n)
-        assert_exact(G().fused(A, B, K, tile_n), oracle.gemm(8, A, B, K),
-                     f"fused tile {tile_n} {M}x{N}x{K}")
+    accumulators, K slices of 128 or 256 elements; 256: one accumulator, K in
+    groups of 4 slices of 64)."""
+    try:
+        L.lbgemm_set_fused_slice(slice_k)
+        for i, (M, N, K) in enumerate(FUSED_SHAPES):
+            A, B = synth.operands(8, M, N, K, 900 + 17 * i + tile_n)
+            assert_exact(G().fused(A, B, K, tile_n), oracle.gemm(8, A, B, K),
+                         f"fused tile {tile_n} slice {slice_k} {M}x{N}x{K}")
+    finally:
+        L.lbgemm_set_fused_slice(0)
 
 
 @pytest.mark.parametrize("tile_n", [64, 128, 256])
@@ -143,8 +149,39 @@ def test_int8_fused_short_chunks():
         L.lbgemm_set_exact_chunk(8, 512)
         for tile_n in (64, 256):
             assert_exact(G().fused(A, B, K, tile_n), want, f"fused chunk 512 tile {tile_n}")
+        L.lbgemm_set_fused_slice(256)
+        for tile_n in (64, 128):
+            assert_exact(G().fused(A, B, K, tile_n), want, f"fused chunk 512 slice 256 {tile_n}")
     finally:
         L.lbgemm_set_exact_chunk(8, 1024)
+        L.lbgemm_set_fused_slice(0)
+
+
+@pytest.mark.parametrize("tile_n", [64, 128])
+def test_int8_fused_slice_256_extremes(tile_n):
+    """256-element slices: every value -128 and the adversarial order."""
+    try:
+        L.lbgemm_set_fused_slice(256)
+        K = 4096
+        A = np.full((200, K), -128, np.int8)
+        B = np.full((300, K), -128, np.int8)
+        assert np.all(G().fused(A, B, K, tile_n) == 16384 * K)
+        A = np.ones((128, K), np.int8)
+        B = np.ones((64, K), np.int8)
+        A[:, :511] = -128
+        B[:, :511] = -128
+        A[:, 1024:2047] = -128
+        B[:, 1024:2047] = -128
+        B[1::2, 600:1000] = -1
+        assert_exact(G().fused(A, B, K, tile_n), oracle.gemm(8, A, B, K), "slice 256 adversarial")
+        assert_exact(G().fused(B, A, K, tile_n), oracle.gemm(8, B, A, K), "slice 256 adv. (T)")
+        # the linear layer through the same kernel
+        X, sx, W, sw = synth.linear_operands(128, 2100, 4096, 640)
+        ref = oracle.linear(X, sx, W, sw)
+        acc = oracle.gemm(8, X, W, 4096)
+        check_linear(G().linear(X, sx, W, sw), ref, acc == 0, "linear fused slice 256")
+    finally:
+        L.lbgemm_set_fused_slice(0)
 
 
 # (M, N, K): small side 1..32 on either operand, ragged W tiles (N % 16 != 0),
