@@ -152,6 +152,8 @@ def main(argv=None) -> int:
     ap.add_argument("--csv-dir", default="", help="write grid_<gpu>_s<bits>.csv here")
     ap.add_argument("--dump", default="", help="write every record (JSON) here")
     ap.add_argument("--shapes", type=int, default=0, help="debug: only the first N grid shapes")
+    ap.add_argument("--merge", action="store_true",
+                    help="keep the loaded table's entries of the bit widths not swept")
     a = ap.parse_args(argv)
     import json  # noqa: PLC0415
 
@@ -165,7 +167,8 @@ def main(argv=None) -> int:
     dev = torch.device("cuda", torch.cuda.current_device())
     sm = torch.cuda.get_device_properties(dev).multi_processor_count
     shapes = GRID[: a.shapes] if a.shapes else GRID
-    L.lbgemm_table_clear()
+    if not a.merge:
+        L.lbgemm_table_clear()
     dump = {}
     for bits in a.bits:
         A, B, C = device_operands(bits, shapes, dev, synth.config_seed({8: 2, 4: 3, 1: 4}[bits]))
