@@ -894,7 +894,9 @@ bool route_runs(int bits, int64_t M, int64_t N, int64_t K, const void* A, const 
     case LBGEMM_ROUTE_WARPMMA:
       return bits == 8 && lo <= kWarpMmaMaxSideSmall && a16 &&
              K <= lbg::hmma_skinny_max_k((int)lo);
-    case LBGEMM_ROUTE_SMALL: return bits == 8 && a16;
+    case LBGEMM_ROUTE_SMALL:
+      return (bits == 8 && a16) ||
+             (bits == 4 && K % 32 == 0 && aligned16(A) && aligned16(B));
     case LBGEMM_ROUTE_FUSED: return bits == 8 && (param == 64 || param == 128 || param == 256) && a16;
     case LBGEMM_ROUTE_STREAM:
       return bits == 8 && lo <= kStreamMaxSide && a16 && K <= lbg::stream_mma_max_k();
@@ -946,6 +948,7 @@ int candidate_list(int bits, int64_t M, int64_t N, int64_t K, int* routes, int* 
   const int64_t lo = std::min(M, N);
   if (bits == 1 && work < 17179869184.0)
     for (int v = 0; v < kNumVariants; ++v) add(LBGEMM_ROUTE_POPC, v);
+  if (bits == 4 && K % 32 == 0 && work <= 2147483648.0 && K <= 8192) add(LBGEMM_ROUTE_SMALL, 0);
   if (bits != 8 || K % 16) return n;
   if (route_runs(8, M, N, K, al, al, LBGEMM_ROUTE_SKINNY, 0)) add(LBGEMM_ROUTE_SKINNY, 0);
   if (route_runs(8, M, N, K, al, al, LBGEMM_ROUTE_STREAM, 0)) add(LBGEMM_ROUTE_STREAM, 0);
@@ -1024,8 +1027,10 @@ lbgemm_status run_route(DeviceState& d, int bits, int64_t M, int64_t N, int64_t 
       return run_warpmma(d, M, N, K, static_cast<const int8_t*>(A), static_cast<const int8_t*>(B),
                          C, nullptr, nullptr, nullptr, stream);
     case LBGEMM_ROUTE_SMALL:
-      e = lbg::launch_small_s8(static_cast<const int8_t*>(A), static_cast<const int8_t*>(B), M, N,
-                               K, C, stream);
+      e = bits == 4 ? lbg::launch_small_s4(static_cast<const uint8_t*>(A),
+                                           static_cast<const uint8_t*>(B), M, N, K, C, stream)
+                    : lbg::launch_small_s8(static_cast<const int8_t*>(A),
+                                           static_cast<const int8_t*>(B), M, N, K, C, stream);
       if (e != cudaSuccess) return cuda_fail(e, "small GEMM launch");
       g_launches += 1;
       return LBGEMM_OK;

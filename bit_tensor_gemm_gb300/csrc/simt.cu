@@ -446,12 +446,15 @@ __global__ void __launch_bounds__(kSkWarps * 32, MINB)
 }
 
 // ---------------------------------------------------------------------------
-// Small 8-bit GEMM on CUDA cores (dp4a), for problems too small to pay for the
-// re-encoding pass and a second launch: one launch, int8 read directly.  CTA
-// tile 64 x 64, 256 threads as a 16 x 16 grid, thread (ty, tx) owning rows
-// ty + 16 i and columns tx + 16 j; K staged 64 bytes at a time through a
-// two-stage cp.async ring.  Out-of-range rows and K bytes load as zero.
-// Requires K % 16 == 0 and 16-byte aligned A and B.
+// Small 8-bit (and 4-bit) GEMM on CUDA cores (dp4a), for problems too small
+// to pay for the re-encoding pass and a second launch: one launch, the
+// packed operands read directly (nibbles sign-extended to int8 in
+// registers).  CTA tile 64 x 64, 256 threads as a 16 x 16 grid, thread
+// (ty, tx) owning rows ty + 16 i and columns tx + 16 j; K staged 64 bytes at
+// a time through a two-stage cp.async ring.  Out-of-range rows and K bytes
+// load as zero (a zero nibble is the value 0).  Requires rows of a multiple
+// of 16 bytes (K % 16 == 0 for int8, K % 32 == 0 for nibbles) and 16-byte
+// aligned A and B.
 constexpr int kSmKS = 64;           // bytes of K per stage
 constexpr int kSmStride = kSmKS + 16;  // padded smem row, 16-byte aligned
 
@@ -467,9 +470,22 @@ __device__ __forceinline__ void small_load_tile(int8_t* dst, const int8_t* src, 
                : "memory");
 }
 
+// Signed nibbles (two per byte, element 2j in the low nibble of byte j) of a
+// 32-bit word into two words of four signed int8: the low nibbles (elements
+// 0, 2, 4, 6) and the high ones (1, 3, 5, 7).  A nibble n is (n ^ 8) - 8.
+__device__ __forceinline__ void s4x8_to_s8(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  lo = __vsub4((w & 0x0F0F0F0Fu) ^ 0x08080808u, 0x08080808u);
+  hi = __vsub4(((w >> 4) & 0x0F0F0F0Fu) ^ 0x08080808u, 0x08080808u);
+}
+
+// S4: the operands are packed signed nibbles; KB is the row length in bytes
+// (K for int8, K / 2 for nibbles).  A dot product does not depend on the
+// order of K, so the low and the high nibbles of the same bytes of A and B
+// are paired as two dp4a terms.
+template <bool S4>
 __global__ void __launch_bounds__(256)
-    small_s8_kernel(const int8_t* __restrict__ A, const int8_t* __restrict__ B, int64_t M,
-                    int64_t N, int64_t K, int32_t* __restrict__ C) {
+    small_dp4a_kernel(const int8_t* __restrict__ A, const int8_t* __restrict__ B, int64_t M,
+                      int64_t N, int64_t K, int32_t* __restrict__ C) {
   __shared__ __align__(16) int8_t sA[2][64 * kSmStride];
   __shared__ __align__(16) int8_t sB[2][64 * kSmStride];
   const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
@@ -502,10 +518,25 @@ __global__ void __launch_bounds__(256)
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           int s = acc[i][j];
-          s = __dp4a(a[i].x, b[j].x, s);
-          s = __dp4a(a[i].y, b[j].y, s);
-          s = __dp4a(a[i].z, b[j].z, s);
-          s = __dp4a(a[i].w, b[j].w, s);
+          if (S4) {
+            const uint32_t av[4] = {(uint32_t)a[i].x, (uint32_t)a[i].y, (uint32_t)a[i].z,
+                                    (uint32_t)a[i].w};
+            const uint32_t bv[4] = {(uint32_t)b[j].x, (uint32_t)b[j].y, (uint32_t)b[j].z,
+                                    (uint32_t)b[j].w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              uint32_t al, ah, bl, bh;
+              s4x8_to_s8(av[q], al, ah);
+              s4x8_to_s8(bv[q], bl, bh);
+              s = __dp4a((int)al, (int)bl, s);
+              s = __dp4a((int)ah, (int)bh, s);
+            }
+          } else {
+            s = __dp4a(a[i].x, b[j].x, s);
+            s = __dp4a(a[i].y, b[j].y, s);
+            s = __dp4a(a[i].z, b[j].z, s);
+            s = __dp4a(a[i].w, b[j].w, s);
+          }
           acc[i][j] = s;
         }
     }
@@ -741,7 +772,16 @@ cudaError_t launch_small_s8(const int8_t* A, const int8_t* B, int64_t M, int64_t
                             int32_t* C, cudaStream_t s) {
   if (M == 0 || N == 0) return cudaSuccess;
   const dim3 grid((unsigned)((N + 63) / 64), (unsigned)((M + 63) / 64));
-  small_s8_kernel<<<grid, 256, 0, s>>>(A, B, M, N, K, C);
+  small_dp4a_kernel<false><<<grid, 256, 0, s>>>(A, B, M, N, K, C);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_small_s4(const uint8_t* A, const uint8_t* B, int64_t M, int64_t N, int64_t K,
+                            int32_t* C, cudaStream_t s) {
+  if (M == 0 || N == 0) return cudaSuccess;
+  const dim3 grid((unsigned)((N + 63) / 64), (unsigned)((M + 63) / 64));
+  small_dp4a_kernel<true><<<grid, 256, 0, s>>>(reinterpret_cast<const int8_t*>(A),
+                                               reinterpret_cast<const int8_t*>(B), M, N, K / 2, C);
   return cudaGetLastError();
 }
 

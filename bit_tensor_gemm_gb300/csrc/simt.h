@@ -49,6 +49,9 @@ cudaError_t launch_quant_rows_bf16(const void* X, int64_t M, int64_t K, int8_t* 
 // Small 8-bit GEMM on dp4a, one launch; K % 16 == 0, A and B 16-byte aligned.
 cudaError_t launch_small_s8(const int8_t* A, const int8_t* B, int64_t M, int64_t N, int64_t K,
                             int32_t* C, cudaStream_t s);
+// The same for packed signed nibbles (K elements per row, K % 32 == 0).
+cudaError_t launch_small_s4(const uint8_t* A, const uint8_t* B, int64_t M, int64_t N, int64_t K,
+                            int32_t* C, cudaStream_t s);
 // 1-bit GEMM, tile class 0..2 and 2..4 stages; K % 32 == 0.
 cudaError_t launch_b1_popc(int tile, int stages, const uint32_t* A, const uint32_t* B, int64_t M,
                            int64_t N, int64_t K, int32_t* C, cudaStream_t s);

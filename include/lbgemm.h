@@ -289,7 +289,7 @@ typedef enum {
   LBGEMM_ROUTE_POPC = 1,    /* 1-bit XOR-popcount kernel (lbgemm_run_popc)            */
   LBGEMM_ROUTE_SKINNY = 2,  /* dp4a kernel streaming B once (M <= 4)                 */
   LBGEMM_ROUTE_WARPMMA = 3, /* warp-level fp16 MMA kernel (lbgemm_run_warpmma)        */
-  LBGEMM_ROUTE_SMALL = 4,   /* one-launch dp4a kernel                                */
+  LBGEMM_ROUTE_SMALL = 4,   /* one-launch dp4a kernel (8-bit, or 4-bit nibbles)      */
   LBGEMM_ROUTE_FUSED = 5,   /* in-kernel conversion kernel (lbgemm_run_fused)         */
   LBGEMM_ROUTE_NONE = 6,    /* M == 0 or N == 0: nothing runs                        */
   LBGEMM_ROUTE_STREAM = 7   /* small side <= 16, K <= 4096: warp-level fp16 MMAs on the
@@ -383,6 +383,8 @@ lbgemm_status lbgemm_time_variants(int bits, int64_t M, int64_t N, int64_t K, co
  * variant) first, then each shape-route kernel that runs the problem within
  * the domain where it can plausibly win: for 1-bit below 2^34 bit-MACs the
  * popcount kernel's nine variants (LBGEMM_ROUTE_POPC, param = its variant);
+ * for 4-bit with K % 32 == 0, M*N*K <= 2^31 and K <= 8192 the one-launch dp4a
+ * kernel on the packed nibbles (LBGEMM_ROUTE_SMALL);
  * for 8-bit with K % 16 == 0 the dp4a kernel streaming B (M <= 16), the
  * warp-level fp16 MMA kernel (small side <= 256 within its K limit), the
  * one-launch dp4a kernel (M*N*K <= 2^31, K <= 4096), and, for a small side

@@ -375,6 +375,8 @@ def test_candidates_cover_the_routes_that_run(lib):
                                L.ROUTE_SMALL, L.ROUTE_FUSED)
     tc = [(T, v) for v in range(9)]
     assert L.lbgemm_candidates(4, 8192, 8192, 8192) == tc
+    assert L.lbgemm_candidates(4, 256, 512, 1024) == tc + [(SM, 0)]
+    assert L.lbgemm_candidates(4, 256, 512, 1040) == tc  # K % 32 != 0
     assert L.lbgemm_candidates(1, 8192, 8192, 65536) == tc  # 2^42 bit-MACs: no popcount
     assert L.lbgemm_candidates(1, 64, 64, 1024) == tc + [(POPC, v) for v in range(9)]
     assert L.lbgemm_candidates(8, 16384, 16384, 16384) == tc

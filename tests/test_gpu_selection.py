@@ -54,7 +54,8 @@ def test_time_variants_medians_and_product(flush):
 
 
 @pytest.mark.parametrize("bits,M,N,K", [(8, 96, 3000, 1040), (1, 100, 70, 1024),
-                                        (4, 130, 250, 514), (8, 8, 1000, 512)])
+                                        (4, 130, 250, 514), (4, 130, 250, 512),
+                                        (8, 8, 1000, 512)])
 def test_every_candidate_is_exact(bits, M, N, K):
     """Each (route, param) the sweep times computes the oracle's product, via
     lbgemm_run_candidate and inside lbgemm_time_candidates."""
@@ -150,3 +151,29 @@ def test_every_compiled_tile_and_stage_count_is_exact(bits):
     with pytest.raises(L.LbgemmError) as e:
         L.lbgemm_run_tile(bits, 64, 64, 256, dA, dB, dC, 1, 5)
     assert e.value.status == L.ERR_UNSUPPORTED
+
+
+def test_small_dp4a_on_nibbles():
+    """The one-launch dp4a kernel on packed 4-bit operands: ragged tiles, one
+    16-byte K chunk, K tails inside a 64-byte stage, extremes and a mixed
+    pattern, bit-exact."""
+    for i, (M, N, K) in enumerate([(1, 1, 32), (65, 70, 32), (130, 250, 96), (64, 64, 128),
+                                   (300, 200, 1024), (1000, 17, 2016), (77, 513, 4096)]):
+        A, B = synth.operands(4, M, N, K, 2100 + i)
+        dA, dB = G().to_dev(A), G().to_dev(B)
+        dC = torch.full((M, N), -7, dtype=torch.int32, device="cuda")
+        L.lbgemm_run_candidate(4, M, N, K, dA, dB, dC, L.ROUTE_SMALL, 0)
+        L.lbgemm_device_status()
+        want = oracle.gemm(4, A, B, K)
+        assert np.array_equal(dC.cpu().numpy(), want), (M, N, K)
+    K = 4096
+    A = np.full((40, K // 2), 0x88, np.uint8)  # every nibble -8
+    B = np.full((30, K // 2), 0x88, np.uint8)
+    dC = torch.empty((40, 30), dtype=torch.int32, device="cuda")
+    L.lbgemm_run_candidate(4, 40, 30, K, G().to_dev(A), G().to_dev(B), dC, L.ROUTE_SMALL, 0)
+    assert np.all(dC.cpu().numpy() == 64 * K)
+    A = np.full((40, K // 2), 0x78, np.uint8)  # low nibble -8, high nibble 7
+    B = np.full((30, K // 2), 0x87, np.uint8)  # low 7, high -8
+    L.lbgemm_run_candidate(4, 40, 30, K, G().to_dev(A), G().to_dev(B), dC, L.ROUTE_SMALL, 0)
+    assert np.all(dC.cpu().numpy() == oracle.gemm(4, A, B, K))
+    assert np.all(dC.cpu().numpy() == -112 * K // 2 * 1)
