@@ -87,7 +87,10 @@ def select_shape(L, bits, m, n, k, A, B, C, reps=10, confirm_reps=20):
                                  flush_l2=True)
     keep = keep_margin(min(t))
     label = L.lbgemm_choose(t[:9], DEFAULT, keep)
-    pick = tuple(cands[L.lbgemm_choose_candidate(t, DEFAULT, keep)])
+    best = L.lbgemm_choose_candidate(t, DEFAULT, keep)
+    if label < 0 or best < 0:
+        raise RuntimeError(f"{bits}-bit {m}x{n}x{k}: unusable timings {t}")
+    pick = tuple(cands[best])
     confirmed = {}
 
     def wins(c):

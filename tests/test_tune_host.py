@@ -112,3 +112,11 @@ def test_route_names():
                               [(L.ROUTE_FUSED, 128), (L.ROUTE_TABLE, 7)])
     assert h == {"in_kernel_conversion_128": {"shapes": 1, "ms": 1.0},
                  "table": {"shapes": 1, "ms": 2.0}}
+
+
+def test_unusable_timings_stop_the_sweep():
+    ms = [1.0] * 8 + [float("nan"), 0.5, 0.9]
+    lib = FakeLib(CANDS, ms, {})
+    with pytest.raises(RuntimeError):
+        tune.sweep(lib, 8, [(64, 64, 64)], None, None, None, 152)
+    assert lib.table == {}
