@@ -35,9 +35,13 @@ class FakeLib:
         return list(self.sweep_ms)
 
     def lbgemm_choose(self, times, default, keep):
+        if not all(t >= 0 for t in times):  # the library rejects NaN and negatives with -1
+            return -1
         return osel.table_choice(list(times), default, keep)
 
     def lbgemm_choose_candidate(self, times, default, keep):
+        if not all(t >= 0 for t in times):
+            return -1
         return osel.candidate_choice(list(times), default, keep)
 
     def lbgemm_table_set_choice_for(self, sm, bits, m, n, k, label, route, param):
