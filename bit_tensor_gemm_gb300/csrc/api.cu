@@ -51,9 +51,20 @@ constexpr int kMaxDevices = 64;
 constexpr int kSkinnyMaxM = 4;
 constexpr int64_t kSkinnyKernelMaxM = 16;  // rows the dp4a streaming kernel takes at most
 constexpr int kGroupM = 16;  // M-tiles per group of the tile order (L2 reuse)
-// 1-bit problems below this many bit-MACs go to the popcount kernel: there
-// the expansion pass and the second launch cost more than they save.
-constexpr double kPopcMaxWork = 1073741824.0;
+// 1-bit problems below this many bit-MACs go to the popcount kernel, with
+// its 64 x 64 tile and 3 stages: there the expansion pass and the second
+// launch cost more than they save.  Measured on GB300 over the 729-shape
+// grid: the popcount kernel takes most shapes up to 2^26 bit-MACs and the
+// tensor cores most from 2^27, and 113 of its 177 wins are this variant
+// (the 128 x 128 tile leaves most SMs idle on such problems).
+constexpr double kPopcMaxWork = 134217728.0;
+constexpr int kPopcRuleVariant = 1;
+// 4-bit problems with K <= kSmallS4MaxK and at most kSmallS4MaxWork MACs go
+// to the one-launch dp4a kernel on the packed nibbles (measured on GB300 over
+// the grid: it wins most shapes with K <= 256 up to 2^26 MACs and none with
+// K >= 512).
+constexpr int64_t kSmallS4MaxK = 256;
+constexpr double kSmallS4MaxWork = 67108864.0;
 // 8-bit problems with K <= kSmallMaxK and at most kSmallMaxWork MACs go to the
 // one-launch dp4a kernel.
 constexpr int64_t kSmallMaxK = 512;
@@ -849,6 +860,9 @@ int fused_route(int64_t M, int64_t N, int64_t K, const void* A, const void* B, i
 // conversion kernel's tile width (LBGEMM_ROUTE_FUSED) and *fuse which
 // operand it converts (1: B, 2: A).  The dispatchers call this, so the
 // introspection entry point cannot drift from them.
+bool route_runs(int bits, int64_t M, int64_t N, int64_t K, const void* A, const void* B, int route,
+                int param);
+
 int route_of(int bits, int64_t M, int64_t N, int64_t K, const void* A, const void* B, bool linear,
              int* tile_n, int* fuse) {
   *tile_n = 0;
@@ -868,6 +882,12 @@ int route_of(int bits, int64_t M, int64_t N, int64_t K, const void* A, const voi
   if (bits == 1) {
     return (double)M * (double)N * (double)K < kPopcMaxWork ? LBGEMM_ROUTE_POPC
                                                              : LBGEMM_ROUTE_TABLE;
+  }
+  if (bits == 4) {
+    return K <= kSmallS4MaxK && (double)M * (double)N * (double)K <= kSmallS4MaxWork &&
+                   route_runs(4, M, N, K, A, B, LBGEMM_ROUTE_SMALL, 0)
+               ? LBGEMM_ROUTE_SMALL
+               : LBGEMM_ROUTE_TABLE;
   }
   if (bits != 8) return LBGEMM_ROUTE_TABLE;
   if (skinny_ok(M, K, A, B)) return LBGEMM_ROUTE_SKINNY;
@@ -986,7 +1006,7 @@ Pick pick_route(int sm, int bits, int64_t M, int64_t N, int64_t K, const void* A
   int tile = 0, fuse = 0;
   p.route = route_of(bits, M, N, K, A, B, false, &tile, &fuse);
   p.param = p.route == LBGEMM_ROUTE_TABLE   ? table_select(sm, bits, M, N, K)
-            : p.route == LBGEMM_ROUTE_POPC  ? kDefaultVariant
+            : p.route == LBGEMM_ROUTE_POPC  ? kPopcRuleVariant
             : p.route == LBGEMM_ROUTE_FUSED ? tile
                                             : 0;
   return p;

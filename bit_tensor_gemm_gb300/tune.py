@@ -28,6 +28,10 @@ table (lbgemm_table_set_choice_for).
 
 writes the table file that the library loads by default, and one CSV of the
 nine tensor-core medians per bit width (the selector network's grid data).
+
+    python -m bit_tensor_gemm_gb300.tune --bits 8 4 1 --offgrid 300 --out unused
+
+judges the loaded table's fallback on random shapes it does not hold.
 """
 from __future__ import annotations
 
@@ -137,6 +141,41 @@ def retime(L, bits, shapes, arms, A, B, C, reps=20):
     return out
 
 
+def random_shapes(count, seed, max_work=2.0 ** 37):
+    """Log-uniform shapes in [64, 16384] per dimension, multiples of 16 (32
+    along K), at most max_work MACs: shapes the grid table does not hold."""
+    g = np.random.default_rng(seed)
+    out = []
+    while len(out) < count:
+        m, n, k = (int(round(2 ** g.uniform(6, 14))) for _ in range(3))
+        m, n, k = max(16, m // 16 * 16), max(16, n // 16 * 16), max(32, k // 32 * 32)
+        if float(m) * n * k <= max_work and (m, n, k) not in GRID:
+            out.append((m, n, k))
+    return out
+
+
+def offgrid_check(L, bits, shapes, A, B, C, sm_count, reps=10):
+    """How the dispatch does on shapes without a table entry: every candidate
+    timed per shape; the time of the kernel lbgemm_run picks (the shape rules,
+    with the selector network's variant on the tensor-core route) against the
+    fastest candidate and the default variant."""
+    t_pick = t_best = t_default = 0.0
+    over = 0
+    for m, n, k in shapes:
+        cands = L.lbgemm_candidates(bits, m, n, k)
+        t = L.lbgemm_time_candidates(bits, m, n, k, A, B, C, cands, warmup=1, reps=reps,
+                                     flush_l2=True)
+        pick = tuple(L.lbgemm_dispatch_for(sm_count, bits, m, n, k))
+        tp = t[cands.index(pick)] if pick in cands else t[DEFAULT]
+        t_pick += tp
+        t_best += min(t)
+        t_default += t[DEFAULT]
+        over += tp > min(t) * 1.10
+    return {"shapes": len(shapes), "pick_over_best": t_pick / t_best,
+            "default_over_best": t_default / t_best, "pick_speedup_over_default": t_default / t_pick,
+            "shapes_over_best_by_10pct": over}
+
+
 def write_grid_csv(path, bits, recs, sm_count):
     """The nine tensor-core medians per shape (the selector network's data)."""
     with open(path, "w") as f:
@@ -157,6 +196,9 @@ def main(argv=None) -> int:
     ap.add_argument("--shapes", type=int, default=0, help="debug: only the first N grid shapes")
     ap.add_argument("--merge", action="store_true",
                     help="keep the loaded table's entries of the bit widths not swept")
+    ap.add_argument("--offgrid", type=int, default=0, metavar="COUNT",
+                    help="instead of tuning: judge the dispatch on COUNT random shapes the "
+                         "loaded table does not hold (prints one JSON line per bit width)")
     a = ap.parse_args(argv)
     import json  # noqa: PLC0415
 
@@ -170,6 +212,16 @@ def main(argv=None) -> int:
     dev = torch.device("cuda", torch.cuda.current_device())
     sm = torch.cuda.get_device_properties(dev).multi_processor_count
     shapes = GRID[: a.shapes] if a.shapes else GRID
+    if a.offgrid:
+        for bits in a.bits:
+            shp = random_shapes(a.offgrid, 2027 + bits)
+            A, B, C = device_operands(bits, shp, dev,
+                                      synth.config_seed({8: 2, 4: 3, 1: 4}[bits]))
+            print(json.dumps({"bits": bits, **offgrid_check(L, bits, shp, A, B, C, sm)}),
+                  flush=True)
+            del A, B, C
+        L.lbgemm_device_status()
+        return 0
     if not a.merge:
         L.lbgemm_table_clear()
     dump = {}

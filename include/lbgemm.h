@@ -98,9 +98,11 @@ lbgemm_status lbgemm_variant_info(int bits, int variant, int* tile_m, int* tile_
  * max(M, N) >= 1024, K >= 512 and one of max(M, N) >= 4096, K >= 8192,
  * (max(M, N) >= 2048 and K >= 4096) or (min(M, N) <= 256 and K >= 2048),
  * on a tensor-core kernel that converts the large operand itself
- * (lbgemm_run_fused), with only the small one re-encoded ahead; and 1-bit
- * problems with M*N*K < 2^30 on the
- * XOR-popcount kernel of lbgemm_run_popc.  These rules apply to shapes the
+ * (lbgemm_run_fused), with only the small one re-encoded ahead; 4-bit
+ * problems with K <= 256 (K % 32 == 0) and M*N*K <= 2^26 on the one-launch
+ * dp4a kernel over the packed nibbles; and 1-bit problems with M*N*K < 2^27
+ * on the XOR-popcount kernel of lbgemm_run_popc (variant 1: 64 x 64 tile, 3
+ * stages).  These rules apply to shapes the
  * selection table holds no measured route for; a table entry with a route
  * (lbgemm_table_set_choice_for, or a route column in a loaded table file)
  * runs that kernel instead, whenever it can run the given operands.

@@ -245,6 +245,13 @@ def test_routes_of_measured_examples(lib):
              ((8, 0, 5, 16), (R.ROUTE_NONE, 0)),
              ((4, 8192, 8192, 8192), (R.ROUTE_TABLE, 0)),
              ((1, 64, 64, 1024), (R.ROUTE_POPC, 0)),
+             ((1, 256, 256, 1024), (R.ROUTE_POPC, 0)),      # 2^26 bit-MACs
+             ((1, 512, 512, 512), (R.ROUTE_TABLE, 0)),      # 2^27: the tensor cores
+             ((4, 256, 256, 256), (R.ROUTE_SMALL, 0)),      # 2^24 MACs, K <= 256
+             ((4, 512, 512, 256), (R.ROUTE_SMALL, 0)),      # 2^26 exactly
+             ((4, 1024, 512, 256), (R.ROUTE_TABLE, 0)),     # 2^27 > 2^26
+             ((4, 256, 256, 512), (R.ROUTE_TABLE, 0)),      # K > 256
+             ((4, 64, 64, 48), (R.ROUTE_TABLE, 0)),         # K % 32 != 0
              ((1, 8192, 8192, 65536), (R.ROUTE_TABLE, 0))]
     for args, want in cases:
         assert L.lbgemm_route(*args) == want, args
@@ -398,7 +405,9 @@ def test_table_routes_drive_the_dispatch(lib, tmp_path):
     sm = 4545  # an SM count no device has
     T, POPC, WM, FU = L.ROUTE_TABLE, L.ROUTE_POPC, L.ROUTE_WARPMMA, L.ROUTE_FUSED
     # no entry: the shape rules (lbgemm_route), the variant from selection
-    for bits, shape in [(8, (16, 11008, 4096)), (8, (4096, 4096, 4096)), (1, (64, 64, 1024))]:
+    assert L.lbgemm_dispatch_for(sm, 1, 64, 64, 1024) == (POPC, 1)  # the rule's 64 x 64 variant
+    for bits, shape in [(8, (16, 11008, 4096)), (8, (4096, 4096, 4096)), (1, (64, 64, 1024)),
+                        (4, (256, 256, 256))]:
         r, p = L.lbgemm_dispatch_for(sm, bits, *shape)
         rule, tile = L.lbgemm_route(bits, *shape)
         assert r == rule

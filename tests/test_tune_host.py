@@ -124,3 +124,11 @@ def test_unusable_timings_stop_the_sweep():
     with pytest.raises(RuntimeError):
         tune.sweep(lib, 8, [(64, 64, 64)], None, None, None, 152)
     assert lib.table == {}
+
+
+def test_random_shapes_are_off_the_grid():
+    shp = tune.random_shapes(200, 5)
+    assert len(shp) == 200 and len(set(shp)) > 190
+    for m, n, k in shp:
+        assert (m, n, k) not in tune.GRID and m % 16 == 0 and n % 16 == 0 and k % 32 == 0
+        assert 16 <= min(m, n) and max(m, n, k) <= 16384 and m * n * k <= 2 ** 37
