@@ -61,6 +61,8 @@ def parse_args():
                    help="runs per candidate and shape in the selection sweep (median)")
     p.add_argument("--retime-reps", type=int, default=20,
                    help="runs per arm and shape in the head-to-head checks and the re-time")
+    p.add_argument("--offgrid", type=int, default=100,
+                   help="random shapes per bit width off the grid for the fallback check")
     p.add_argument("--shapes", type=int, default=0, help="debug: use only the first N shapes")
     p.add_argument("--no-cpu", action="store_true", help="debug: skip the CPU oracle sample")
     p.add_argument("--dump", default="", help="write per-shape sweep data (JSON) to this path")
@@ -198,12 +200,9 @@ def mlp_on_grid(L, bits, shapes, recs, sm):
     path = os.path.join(ROOT, "bit_tensor_gemm_gb300", "data", f"mlp_gb300_s{bits}.txt")
     if not os.path.exists(path):
         return None
-    L.lbgemm_mlp_load(path)
-    try:
-        T = np.array([r["ms"][:9] for r in recs])
-        pred = np.array([L.lbgemm_mlp_predict(bits, m, n, k, sm) for (m, n, k) in shapes])
-    finally:
-        L.lbgemm_mlp_clear()  # the timed steps use the measured table
+    L.lbgemm_mlp_load(path)  # (the library loads it by default too; grid shapes hit the table)
+    T = np.array([r["ms"][:9] for r in recs])
+    pred = np.array([L.lbgemm_mlp_predict(bits, m, n, k, sm) for (m, n, k) in shapes])
     best = T.argmin(axis=1)
     idx = np.arange(len(T))
     t_pred = T[idx, pred[:, 0]]
@@ -512,6 +511,17 @@ def run_ours(args):
                                        args.retime_reps)
         summ["mlp_selector"] = mlp_eval[bits]
         summ["sweep_roofline_frac"] = roof["frac"]
+        if args.offgrid:
+            # shapes the table does not hold: the kernel lbgemm_run picks there
+            # (the shape rules, the network's variant) against every candidate
+            shp = tune.random_shapes(args.offgrid, 2027 + bits)
+            Ao, Bo, Co = tune.device_operands(bits, shp, dev, synth.config_seed(SEED_OF[bits]))
+            summ["offgrid"] = tune.offgrid_check(L, bits, shp, Ao, Bo, Co, sm, reps=10)
+            summ["offgrid"]["what"] = ("random shapes without a table entry (log-uniform in "
+                                       "64-16384, at most 2^37 MACs): time of the kernel "
+                                       "lbgemm_run picks over the fastest candidate, and of "
+                                       "the default variant 7")
+            del Ao, Bo, Co
         selection_by_bits[bits], rooflines[bits] = summ, roof
         if bits == 8:
             s_ms = T[:, 2]
