@@ -71,6 +71,13 @@ constexpr int64_t kSmallMaxK = 512;
 // 8-bit problems on the in-kernel-conversion kernel (see fused_route).
 constexpr int64_t kFusedMaxSide = 512;
 constexpr int64_t kFusedMinOther = 1024;
+// The linear layer on that kernel splits K only when the split plan's waves
+// of units cost at most this share of the unsplit grid's: the split runs a
+// second grid to scale the int32 sums (measured on GB300, 64 tokens x 4096 x
+// 4096, 32 tiles on 152 SMs, 26.9 -> 19.5 us; 64 x 4096 x 11008, 50.2 ->
+// 25.6 us; 64 x 11008 x 4096, 86 tiles, split plan at 0.79 of the grid: no
+// gain).
+constexpr double kLinearSplitGain = 0.7;
 // Small side of the warp-level fp16 MMA kernel (hmma_skinny.cu): any problem
 // up to kWarpMmaMaxSide rows; with more rows (up to kWarpMmaMaxSideSmall,
 // each 32 rows re-reading the large operand) only small problems with
@@ -279,6 +286,15 @@ int64_t enc_kp(int bits, int64_t K) { return bits == 8 ? round_up(K, 8) : round_
 size_t enc_bytes(int bits, int64_t rows, int64_t K) {
   const int64_t kp = enc_kp(bits, K);
   return (size_t)round_up(rows * kp * (bits == 8 ? 2 : 1), 256);
+}
+
+// Scratch of the linear layer on the in-kernel-conversion route: the
+// re-encoded X, then room for the int32 sums of a split K (64- and 128-wide
+// tiles).
+size_t fused_linear_scratch(int64_t M, int64_t N, int64_t K, int tile_n) {
+  size_t b = enc_bytes(8, M, K);
+  if (tile_n != 256) b += (size_t)round_up(M * N * 4, 256);
+  return b;
 }
 
 bool skinny_ok(int64_t M, int64_t K, const void* A, const void* B) {
@@ -692,8 +708,15 @@ lbgemm_status run_tc_fused(DeviceState& d, bool large_b, int tile_n, int64_t M, 
   // tiles on 152 slots at K = 16384: 7 pieces (896 units in 6 waves, 6/7 of a
   // tile each) instead of one wave with 128 of the 152 slots busy (measured
   // on GB300: 64 x 16384 x 16384, 114 -> 106 us).
+  // The linear layer splits K only when converting W (the transposed kernel)
+  // with the 64- or 128-wide tile, and only where the split plan's waves cost
+  // at most kLinearSplitGain of the unsplit grid's: it then runs as the plain
+  // GEMM kernel adding int32 partial sums into a workspace after the
+  // re-encoded operand in `ws` (fused_linear_scratch), and a second grid
+  // scales the sums into Y.
+  const bool linear_split = linear && large_b && tile_n != 256;
   int splits = 1;
-  if (!linear && (vec_ok || large_b)) {
+  if ((!linear && (vec_ok || large_b)) || linear_split) {
     if (tile_n == 256) {
       KPlan kpl = plan_k(d, k, 8, rows_l, rows_s, K, linear, true);
       splits = kpl.dp_tiles == 0 ? kpl.splits : 1;
@@ -712,12 +735,22 @@ lbgemm_status run_tc_fused(DeviceState& d, bool large_b, int tile_n, int64_t M, 
           splits = sp;
         }
       }
+      if (linear && best > kLinearSplitGain * (double)((tiles + slots - 1) / slots)) splits = 1;
     }
   }
-  // the encoder also clears C when K is split (partial tiles are added into it)
+  // the split linear layer: the plain kernel into int32 sums
+  int32_t* sums = nullptr;
+  if (linear && splits > 1) {
+    sums = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + enc_bytes(8, rows_s, K));
+    k = lbg::tc_kernel_ts(tile_n, large_b, false, fused_slice(tile_n));
+    if (!k.launch) return fail(LBGEMM_ERR_UNSUPPORTED, "no fused kernel (tile %d)", tile_n);
+  }
+  int32_t* Cout = sums ? sums : C;
+  // the encoder also clears C (or the sums) when K is split: partial tiles
+  // are added into it
   lbg::ZeroRect zero;
   if (splits > 1) {
-    zero.C = C;
+    zero.C = Cout;
     zero.ld = N;
     zero.r1 = M;
     zero.c1 = N;
@@ -754,10 +787,10 @@ lbgemm_status run_tc_fused(DeviceState& d, bool large_b, int tile_n, int64_t M, 
   p.group_m = kGroupM;
   p.splits = splits;
   p.num_units = p.num_tiles * splits;
-  p.C = C;
+  p.C = Cout;
   p.sx = sx;
   p.sw = sw;
-  p.Y = static_cast<__nv_bfloat16*>(Y);
+  p.Y = sums ? nullptr : static_cast<__nv_bfloat16*>(Y);
   p.status = d.status;
   p.vec_ok = vec_ok;
   CUtensorMap mc;
@@ -775,6 +808,11 @@ lbgemm_status run_tc_fused(DeviceState& d, bool large_b, int tile_n, int64_t M, 
   cudaError_t e = k.launch(&ml, &ms, &mc, &p, grid, true, stream);
   if (e != cudaSuccess) return cuda_fail(e, "fused tensor-core GEMM launch");
   g_launches += 1;
+  if (sums) {
+    e = lbg::launch_scale_sums(sums, M, N, sx, sw, Y, d.sm_count, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "linear-layer scaling launch");
+    g_launches += 1;
+  }
   return LBGEMM_OK;
 }
 
@@ -873,6 +911,10 @@ int route_of(int bits, int64_t M, int64_t N, int64_t K, const void* A, const voi
     if (M <= kStreamMaxSide && stream_ok(M, N, K, A, B)) return LBGEMM_ROUTE_STREAM;
     if (warpmma_ok(M, N, K, A, B)) return LBGEMM_ROUTE_WARPMMA;
     if (fused_route(M, N, K, A, B, tile_n) == 1) {
+      // no CTA pairs for the linear layer: the 128-wide tile, K split where
+      // the grid is short, is as fast or faster (measured on GB300: 512
+      // tokens x 11008 x 4096, 92 -> 72 us; 256 tokens, equal)
+      if (*tile_n == 256) *tile_n = 128;
       *fuse = 1;
       return LBGEMM_ROUTE_FUSED;
     }
@@ -1164,7 +1206,7 @@ lbgemm_status run_linear(int64_t M, int64_t N, int64_t K, const int8_t* X, const
   if (route == LBGEMM_ROUTE_FUSED) {
     // small token counts: only X is re-encoded; the kernel converts W itself
     std::lock_guard<std::mutex> lock(g_ws_mu);
-    st = scratch_acquire(d->ws, enc_bytes(8, M, K), stream);
+    st = scratch_acquire(d->ws, fused_linear_scratch(M, N, K, fuse_tile), stream);
     if (st != LBGEMM_OK) return st;
     st = run_tc_fused(*d, true, fuse_tile, M, N, K, X, W, nullptr, sx, sw, Y, d->ws.ptr, stream);
     lbgemm_status st2 = scratch_release(d->ws, stream);

@@ -693,7 +693,51 @@ __global__ void wait_selftest_kernel(int* status, uint64_t limit_ns) {
 }
 
 // ---------------------------------------------------------------------------
+// The linear layer's scaling of int32 sums: Y[m][n] = bf16(S[m][n] * sx[m] *
+// sw[n]), the products in the order of the GEMM kernels' linear epilogues.
+// Four elements per thread when rows are whole 16-byte groups.
+__global__ void scale_sums_kernel(const int32_t* S, int64_t M, int64_t N, const float* sx,
+                                  const float* sw, __nv_bfloat16* Y, int vec) {
+  allow_dependent_launch();
+  wait_prior_grid();
+  const int64_t nt = (int64_t)gridDim.x * blockDim.x;
+  const int64_t t0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (vec) {
+    const int64_t nq = N / 4;
+    for (int64_t q = t0; q < M * nq; q += nt) {
+      const int64_t m = q / nq, n = (q - m * nq) * 4;
+      const int4 v = __ldcs(reinterpret_cast<const int4*>(S + m * N + n));
+      const float a = sx[m];
+      const float4 w = *reinterpret_cast<const float4*>(sw + n);
+      __nv_bfloat162 lo = __floats2bfloat162_rn((float)v.x * a * w.x, (float)v.y * a * w.y);
+      __nv_bfloat162 hi = __floats2bfloat162_rn((float)v.z * a * w.z, (float)v.w * a * w.w);
+      uint2 o;
+      o.x = *reinterpret_cast<const uint32_t*>(&lo);
+      o.y = *reinterpret_cast<const uint32_t*>(&hi);
+      *reinterpret_cast<uint2*>(Y + m * N + n) = o;
+    }
+  } else {
+    for (int64_t e = t0; e < M * N; e += nt) {
+      const int64_t m = e / N, n = e - m * N;
+      Y[e] = __float2bfloat16_rn((float)S[e] * sx[m] * sw[n]);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
 // host launchers
+
+cudaError_t launch_scale_sums(const int32_t* S, int64_t M, int64_t N, const float* sx,
+                              const float* sw, void* Y, int sm_count, cudaStream_t s) {
+  if (M == 0 || N == 0) return cudaSuccess;
+  auto al = [](const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; };
+  const int vec = N % 4 == 0 && al(S, 16) && al(sw, 16) && al(Y, 8);
+  const int64_t work = vec ? M * (N / 4) : M * N;
+  int64_t blocks = (work + 255) / 256;
+  blocks = std::min<int64_t>(std::max<int64_t>(blocks, 1), (int64_t)sm_count * 8);
+  return launch_dependent(scale_sums_kernel, dim3((unsigned)blocks), dim3(256), 0, s, S, M, N, sx,
+                          sw, static_cast<__nv_bfloat16*>(Y), vec);
+}
 
 cudaError_t launch_wait_selftest(int* status, uint64_t limit_ns, cudaStream_t s) {
   wait_selftest_kernel<<<1, 32, 0, s>>>(status, limit_ns);

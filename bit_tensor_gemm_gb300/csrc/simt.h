@@ -47,6 +47,11 @@ cudaError_t launch_stream_mma(const int8_t* X, const int8_t* W, int MX, int NW, 
 cudaError_t launch_quant_rows_bf16(const void* X, int64_t M, int64_t K, int8_t* Q, float* S,
                                    cudaStream_t s);
 // Small 8-bit GEMM on dp4a, one launch; K % 16 == 0, A and B 16-byte aligned.
+// The linear layer's scaling of int32 sums S (M x N, row-major) into bf16 Y
+// with row scales sx (M) and column scales sw (N); launched as a
+// programmatic dependent of the grid that computed S.
+cudaError_t launch_scale_sums(const int32_t* S, int64_t M, int64_t N, const float* sx,
+                              const float* sw, void* Y, int sm_count, cudaStream_t s);
 cudaError_t launch_small_s8(const int8_t* A, const int8_t* B, int64_t M, int64_t N, int64_t K,
                             int32_t* C, cudaStream_t s);
 // The same for packed signed nibbles (K elements per row, K % 32 == 0).

@@ -273,10 +273,8 @@ __global__ void __launch_bounds__(kTsThreads, 1)
     }
     // 128-byte swizzle: 16-byte chunk q of row r sits at chunk q ^ (r % 8)
     const int swz = row & 7;
-    // The slices this CTA converts, in order: (unit w, slice kb), each in two
-    // halves of 64 elements.  Software pipeline: the next half is waited
-    // for (at a slice's start), loaded and converted while the tensor-memory
-    // store of the previous half is in flight.
+    // The slices this CTA converts, in order: (unit w, slice kb), each in
+    // pieces of 64 elements.
     int w = (int)blockIdx.x - (int)gridDim.x;  // the unit before this CTA's first
     int kb = 0, kbe = 0, tn = 0;
     auto advance = [&]() -> bool {  // next slice into (kb, tn); false at the end
@@ -341,25 +339,30 @@ __global__ void __launch_bounds__(kTsThreads, 1)
     };
     bool have = advance();
     bool ok = true;
-    uint32_t cur[32], nxt[32];
+    uint32_t cur[32];
     if (have) {
       ok = acquire();
       if (ok) convert(0, cur);
     }
     while (ok && have) {
-      // every piece but the last: store it, convert the next meanwhile
+      // Store each piece as soon as it is converted: tcgen05.st reads its
+      // registers when it issues, so the next piece is converted into the
+      // same registers while the stores are in flight, and the slice waits
+      // for its stores once.  Its A slot and staging slot are handed on
+      // before the next slice's wait (a slot and its int8 data) begins.
       const uint32_t slot = tmem_base + lane_addr + L::kACol0 + os * L::kASlotCols;
 #pragma unroll
-      for (int h = 0; h + 1 < kQuarters; ++h) {
+      for (int h = 0; h < kQuarters; ++h) {
+        if (h > 0) convert(h, cur);
         tmem_st32(slot + 32 * h, cur);
-        convert(h + 1, nxt);
-        tmem_st_wait();
-#pragma unroll
-        for (int j = 0; j < 32; ++j) cur[j] = nxt[j];
       }
-      // the last piece: store it, start the next slice meanwhile
-      tmem_st32(slot + 32 * (kQuarters - 1), cur);
-      const int st_os = os, st_ss = ss;
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(conv_bar(os));
+        mbar_arrive(stge_bar(ss));
+      }
       if (++os == STAGES) {
         os = 0;
         oph ^= 1u;
@@ -371,17 +374,8 @@ __global__ void __launch_bounds__(kTsThreads, 1)
       have = advance();
       if (have) {
         ok = acquire();
-        if (ok) convert(0, nxt);
+        if (ok) convert(0, cur);
       }
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(conv_bar(st_os));
-        mbar_arrive(stge_bar(st_ss));
-      }
-#pragma unroll
-      for (int j = 0; j < 32; ++j) cur[j] = nxt[j];
     }
     if (!ok && loader) {
       // Wind-down: wait for the S copies this thread still has in flight.

@@ -214,7 +214,8 @@ def _route8(M, N, K, linear=False):
     if (k16 and lo <= 512 and hi >= 1024 and K >= 512 and (not linear or M <= N)
             and (hi >= 4096 or K >= 8192 or (hi >= 2048 and K >= 4096)
                  or (lo <= 256 and K >= 2048))):
-        return L.ROUTE_FUSED, 64 if lo <= 64 else 256 if _pairs(lo, hi, K) else 128
+        # CTA pairs only for the GEMM
+        return L.ROUTE_FUSED, 64 if lo <= 64 else 256 if _pairs(lo, hi, K) and not linear else 128
     return L.ROUTE_TABLE, 0
 
 
@@ -257,8 +258,11 @@ def test_routes_of_measured_examples(lib):
         assert L.lbgemm_route(*args) == want, args
     # the linear layer on the 11008 x 4096 weights, token counts of the benchmark
     for M, want in [(1, (R.ROUTE_SKINNY, 0)), (16, (R.ROUTE_STREAM, 0)), (17, (R.ROUTE_FUSED, 64)),
-                    (128, (R.ROUTE_FUSED, 128)), (2048, (R.ROUTE_TABLE, 0))]:
+                    (128, (R.ROUTE_FUSED, 128)), (512, (R.ROUTE_FUSED, 128)),
+                    (2048, (R.ROUTE_TABLE, 0))]:
         assert L.lbgemm_route(8, M, 11008, 4096, linear=True) == want, M
+    # the GEMM of the same shape takes CTA pairs, the linear layer does not
+    assert L.lbgemm_route(8, 512, 11008, 4096) == (R.ROUTE_FUSED, 256)
     for bad in [(3, 4, 4, 16), (8, -1, 4, 16), (8, 4, 4, 0)]:
         with pytest.raises(L.LbgemmError):
             L.lbgemm_route(*bad)

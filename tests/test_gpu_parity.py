@@ -497,12 +497,61 @@ def test_linear_warpmma_route(M):
 def test_linear_fused_route(M, N, K):
     """Token counts 33..512 in the conversion kernel's domain: the weights are
     converted in the kernel and Y is written transposed from the accumulator
-    (128-wide tiles, and CTA pairs with 450 tokens; N % 4 != 0 included)."""
+    (64- and 128-wide tiles by the dispatch, CTA pairs forced with 450 tokens;
+    N % 4 != 0 included)."""
     X, sx, W, sw = synth.linear_operands(M, N, K, 600 + M)
     X[1, :] = 0
     ref = oracle.linear(X, sx, W, sw)
     acc = oracle.gemm(8, X, W, K)
     check_linear(G().linear(X, sx, W, sw), ref, acc == 0, f"linear fused M={M}")
+    if M > 384:
+        dY = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device=G().DEV)
+        L.lbgemm_linear_candidate(M, N, K, G().to_dev(X), G().to_dev(sx), G().to_dev(W),
+                                  G().to_dev(sw), dY, L.ROUTE_FUSED, 256)
+        L.lbgemm_device_status()
+        got = dY.float().cpu().numpy().astype(np.float64)
+        check_linear(got, ref, acc == 0, f"linear fused pairs M={M}")
+
+
+@pytest.mark.parametrize("tile", [64, 128])
+@pytest.mark.parametrize("M,N,K", [(24, 4096, 4096), (64, 4096, 4096), (100, 2102, 4096),
+                                   (17, 11008, 4096), (200, 1030, 8192), (64, 1000, 512)])
+def test_linear_fused_split_k(tile, M, N, K):
+    """The conversion kernel's linear layer, K split over CTAs where the
+    unsplit grid would leave most SMs idle: partial sums added into an int32
+    workspace, then scaled into Y by a second grid (ragged tiles of W rows and
+    tokens; N % 4 != 0 on the scalar scaling path); unsplit where the split
+    would not pay (11008 rows, 512-long K).  A second call right after the
+    first must not see the first one's sums."""
+    for rep in range(2):
+        X, sx, W, sw = synth.linear_operands(M, N, K, 610 + M + 7 * rep)
+        X[1, :] = 0
+        ref = oracle.linear(X, sx, W, sw)
+        acc = oracle.gemm(8, X, W, K)
+        dY = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device=G().DEV)
+        L.lbgemm_linear_candidate(M, N, K, G().to_dev(X), G().to_dev(sx), G().to_dev(W),
+                                  G().to_dev(sw), dY, L.ROUTE_FUSED, tile)
+        L.lbgemm_device_status()
+        got = dY.float().cpu().numpy().astype(np.float64)
+        check_linear(got, ref, acc == 0, f"linear split-K tile {tile} {M}x{N}x{K} call {rep}")
+
+
+def test_linear_fused_split_k_extremes():
+    """Sums of K products of -128 x -128 (2^14 each) summed over K pieces in
+    int32: 16384 * 8192 = 2^27, exact in the workspace and in fp32."""
+    M, N, K = 40, 4096, 8192
+    X = np.full((M, K), -128, np.int8)
+    W = np.full((N, K), -128, np.int8)
+    W[::3] = 127
+    sx = np.full(M, 2.0 ** -20, np.float32)
+    sw = np.full(N, 0.5, np.float32)
+    dY = torch.empty((M, N), dtype=torch.bfloat16, device=G().DEV)
+    L.lbgemm_linear_candidate(M, N, K, G().to_dev(X), G().to_dev(sx), G().to_dev(W),
+                              G().to_dev(sw), dY, L.ROUTE_FUSED, 64)
+    L.lbgemm_device_status()
+    got = dY.float().cpu().numpy().astype(np.float64)
+    ref = oracle.linear(X, sx, W, sw)
+    np.testing.assert_array_equal(got, ref)
 
 
 @pytest.mark.parametrize("variant", [0, 4, 8])
