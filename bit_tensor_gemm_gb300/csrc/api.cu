@@ -107,6 +107,9 @@ std::atomic<int> g_tail_split{1};  // 0 whole-problem splits only, 1 also a last
 // 16384 x 16384 81.9 -> 74.3 us, and the 128-wide one up to 14 % slower, its
 // tensor memory then holding only two slots)
 std::atomic<int> g_fused_slice{0};
+// in-kernel-conversion schedule: 0 split K by the cost model, 1 stream-K
+// wherever every CTA gets two slices
+std::atomic<int> g_stream_k{0};
 
 int fused_slice(int tile_n) {
   const int s = g_fused_slice.load();
@@ -714,8 +717,16 @@ lbgemm_status run_tc_fused(DeviceState& d, bool large_b, int tile_n, int64_t M, 
   // GEMM kernel adding int32 partial sums into a workspace after the
   // re-encoded operand in `ws` (fused_linear_scratch), and a second grid
   // scales the sums into Y.
+  // Stream-K (64- and 128-wide kernels, opt-in by lbgemm_set_fused_stream_k):
+  // every CTA slot takes an equal run of the tile-major order of all K
+  // slices, cut at tile ends into pieces that each add a partial tile.
+  // Measured on GB300 no faster than the split plan (e.g. 128 x 11008 x
+  // 4096: 33.8 against 32.8 us; 256 x 11008 x 4096: 48.3 against 52.2; 512 x
+  // 4096 x 1024: 21.5 against 15.4): a slice costs the kernel the same ~1200
+  // cycles either way, bound by the SM's shared- and tensor-memory traffic,
+  // so a shorter run per CTA buys little against the extra partial tiles.
   const bool linear_split = linear && large_b && tile_n != 256;
-  int splits = 1;
+  int splits = 1, stream_pieces = 0;
   if ((!linear && (vec_ok || large_b)) || linear_split) {
     if (tile_n == 256) {
       KPlan kpl = plan_k(d, k, 8, rows_l, rows_s, K, linear, true);
@@ -735,12 +746,24 @@ lbgemm_status run_tc_fused(DeviceState& d, bool large_b, int tile_n, int64_t M, 
           splits = sp;
         }
       }
-      if (linear && best > kLinearSplitGain * (double)((tiles + slots - 1) / slots)) splits = 1;
+      const int64_t kslices = (kp + k.slice - 1) / k.slice;
+      const int64_t total = tiles * kslices;
+      if (g_stream_k.load() && total >= 2 * slots) {
+        const int64_t run = (total + slots - 1) / slots;
+        splits = 1;
+        stream_pieces = (int)((run + kslices - 1) / kslices + 1);
+      }
+      if (linear && stream_pieces == 0 &&
+          best > kLinearSplitGain * (double)((tiles + slots - 1) / slots)) {
+        splits = 1;
+        stream_pieces = 0;
+      }
     }
   }
+  const bool partial = splits > 1 || stream_pieces > 0;
   // the split linear layer: the plain kernel into int32 sums
   int32_t* sums = nullptr;
-  if (linear && splits > 1) {
+  if (linear && partial) {
     sums = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + enc_bytes(8, rows_s, K));
     k = lbg::tc_kernel_ts(tile_n, large_b, false, fused_slice(tile_n));
     if (!k.launch) return fail(LBGEMM_ERR_UNSUPPORTED, "no fused kernel (tile %d)", tile_n);
@@ -749,7 +772,7 @@ lbgemm_status run_tc_fused(DeviceState& d, bool large_b, int tile_n, int64_t M, 
   // the encoder also clears C (or the sums) when K is split: partial tiles
   // are added into it
   lbg::ZeroRect zero;
-  if (splits > 1) {
+  if (partial) {
     zero.C = Cout;
     zero.ld = N;
     zero.r1 = M;
@@ -787,6 +810,10 @@ lbgemm_status run_tc_fused(DeviceState& d, bool large_b, int tile_n, int64_t M, 
   p.group_m = kGroupM;
   p.splits = splits;
   p.num_units = p.num_tiles * splits;
+  if (stream_pieces > 0) {
+    p.stream_k = stream_pieces;
+    p.num_units = (int)unit_slots(d, k) * stream_pieces;
+  }
   p.C = Cout;
   p.sx = sx;
   p.sw = sw;
@@ -1942,6 +1969,15 @@ lbgemm_status lbgemm_set_fused_slice(int k_elems) {
 }
 
 int lbgemm_get_fused_slice(void) { return g_fused_slice.load(); }
+
+lbgemm_status lbgemm_set_fused_stream_k(int mode) {
+  if (mode < 0 || mode > 1)
+    return fail(LBGEMM_ERR_INVALID_ARG, "the stream-K mode must be 0 or 1 (got %d)", mode);
+  g_stream_k = mode;
+  return LBGEMM_OK;
+}
+
+int lbgemm_get_fused_stream_k(void) { return g_stream_k.load(); }
 
 lbgemm_status lbgemm_set_tail_split(int mode) {
   if (mode < 0 || mode > 2) return fail(LBGEMM_ERR_INVALID_ARG, "tail split mode must be 0, 1 or 2");

@@ -17,7 +17,11 @@ struct TcParams {
   int dp_tiles;   // leading tiles (in tile order) computed whole, one unit each
   int splits;     // K pieces of each remaining tile (> 1: its partial tiles are
                   // added into C, zeroed there beforehand)
-  int num_units;  // dp_tiles + (num_tiles - dp_tiles) * splits
+  int num_units;  // dp_tiles + (num_tiles - dp_tiles) * splits; grid * stream_k
+  int stream_k;   // in-kernel-conversion kernels only: > 0 shares the tile-major
+                  // order of all K slices out evenly, CTA b taking the b-th
+                  // contiguous run, cut at tile ends into up to stream_k units,
+                  // every one added into C (zeroed there beforehand)
   int vec_ok;    // rows of C/Y are 16-byte aligned: C goes out by TMA stores,
                  // Y by 16-byte vector stores
   int32_t* C;

@@ -108,6 +108,30 @@ struct TsLayout {
   static_assert(kDynSmem <= 232448, "shared memory per CTA");
 };
 
+// Unit w of this CTA (w % gridDim.x == blockIdx.x): a tile t and its K
+// slices [kb0, kb1) (kb0 == kb1: nothing to do).  With stream_k the CTA's
+// run of the tile-major slice order is cut at tile ends; the i-th piece is
+// unit blockIdx.x + i * gridDim.x.
+__device__ __forceinline__ void ts_unit(int w, const TcParams& p, int& t, int& kb0, int& kb1) {
+  if (!p.stream_k) {
+    unit_range(w, p, t, kb0, kb1);
+    return;
+  }
+  const int g = (int)gridDim.x;
+  const int b = w % g, i = w / g;
+  const int64_t total = (int64_t)p.num_tiles * p.num_kb;
+  const int64_t s0 = (int64_t)b * total / g, s1 = (int64_t)(b + 1) * total / g;
+  const int64_t a = i == 0 ? s0 : (s0 / p.num_kb + i) * p.num_kb;
+  if (a >= s1) {
+    t = kb0 = kb1 = 0;
+    return;
+  }
+  const int64_t e = min(s1, (a / p.num_kb + 1) * p.num_kb);
+  t = (int)(a / p.num_kb);
+  kb0 = (int)(a - (int64_t)t * p.num_kb);
+  kb1 = kb0 + (int)(e - a);
+}
+
 template <int BN, int STAGES, int SK, bool TRANS, bool LINEAR>
 __global__ void __launch_bounds__(kTsThreads, 1)
     tc_ts_kernel(const __grid_constant__ CUtensorMap tmL, const __grid_constant__ CUtensorMap tmS,
@@ -176,7 +200,7 @@ __global__ void __launch_bounds__(kTsThreads, 1)
       bool ok = true;
       for (int w = blockIdx.x; ok && w < p.num_units; w += gridDim.x) {
         int t, kbb, kbe, tm, tn;
-        unit_range(w, p, t, kbb, kbe);
+        ts_unit(w, p, t, kbb, kbe);
         tile_coords(t, p, tm, tn);
         for (int kb = kbb; kb < kbe; ++kb) {
           if (!mbar_wait(stge_bar(stage), phase ^ 1u, abort_flag, p.status)) {
@@ -219,7 +243,7 @@ __global__ void __launch_bounds__(kTsThreads, 1)
       bool ok = true;
       for (int w = blockIdx.x; ok && w < p.num_units; w += gridDim.x) {
         int t, kbb, kbe;
-        unit_range(w, p, t, kbb, kbe);
+        ts_unit(w, p, t, kbb, kbe);
         const int num_chunks = (kbe - kbb + p.chunk_kb - 1) / p.chunk_kb;
         for (int c = 0; ok && c < num_chunks; ++c, ++u) {
           const int buf = u & 1;
@@ -281,7 +305,7 @@ __global__ void __launch_bounds__(kTsThreads, 1)
       if (++kb < kbe) return true;
       for (w += gridDim.x; w < p.num_units; w += gridDim.x) {
         int t, kbb, tm;
-        unit_range(w, p, t, kbb, kbe);
+        ts_unit(w, p, t, kbb, kbe);
         tile_coords(t, p, tm, tn);
         if (kbb < kbe) {
           kb = kbb;
@@ -404,11 +428,14 @@ __global__ void __launch_bounds__(kTsThreads, 1)
     uint32_t u = 0;
     int32_t acc[kGroups][32];
     bool ok = true;
+    // partial tiles (split K, stream-K) are added into C, cleared beforehand
+    const bool adds = p.splits > 1 || p.stream_k > 0;
     for (int w = blockIdx.x; ok && w < p.num_units; w += gridDim.x) {
       int t, kbb, kbe, tm, tn;
-      unit_range(w, p, t, kbb, kbe);
+      ts_unit(w, p, t, kbb, kbe);
       tile_coords(t, p, tm, tn);
       const int num_chunks = (kbe - kbb + p.chunk_kb - 1) / p.chunk_kb;
+      if (num_chunks == 0) continue;  // an empty stream-K unit
       for (int c = 0; c < num_chunks; ++c, ++u) {
         const int buf = u & 1;
         int got = 0;
@@ -449,7 +476,7 @@ __global__ void __launch_bounds__(kTsThreads, 1)
                 const int64_t off = (int64_t)jj * p.M + i;
                 if (LINEAR) {
                   p.Y[off] = __float2bfloat16_rn((float)acc[g][j] * p.sx[jj] * p.sw[i]);
-                } else if (p.splits > 1) {
+                } else if (adds) {
                   atomicAdd(p.C + off, acc[g][j]);
                 } else {
                   p.C[off] = acc[g][j];
@@ -473,7 +500,7 @@ __global__ void __launch_bounds__(kTsThreads, 1)
           __syncwarp();
           if (lane == 0) {
             const int x = tn * BN + col0 + g * 32, y = tm * kTcBM + quarter * 32;
-            if (p.splits > 1)
+            if (adds)
               tma_reduce_add_2d(&tmC, stage_addr, x, y);
             else
               tma_store_2d(&tmC, stage_addr, x, y);

@@ -92,6 +92,8 @@ _SIGNATURES = {
     "lbgemm_set_tail_split": (_i32, [_i32]),
     "lbgemm_set_fused_slice": (_i32, [_i32]),
     "lbgemm_get_fused_slice": (_i32, []),
+    "lbgemm_set_fused_stream_k": (_i32, [_i32]),
+    "lbgemm_get_fused_stream_k": (_i32, []),
     "lbgemm_get_tail_split": (_i32, []),
     "lbgemm_device_status": (_i32, [_vp]),
     "lbgemm_selftest_timeout": (_i32, [_vp]),
@@ -418,6 +420,16 @@ def lbgemm_set_fused_slice(k_elems: int) -> None:
 
 def lbgemm_get_fused_slice() -> int:
     return load().lbgemm_get_fused_slice()
+
+
+def lbgemm_set_fused_stream_k(mode: int) -> None:
+    """Work schedule of the 64/128-wide in-kernel-conversion kernels: 0 split
+    K by the cost model (default), 1 stream-K where possible."""
+    _check(load().lbgemm_set_fused_stream_k(mode))
+
+
+def lbgemm_get_fused_stream_k() -> int:
+    return load().lbgemm_get_fused_stream_k()
 
 
 def lbgemm_get_tail_split() -> int:

@@ -467,6 +467,21 @@ int lbgemm_get_tail_split(void);
 lbgemm_status lbgemm_set_fused_slice(int k_elems);
 int lbgemm_get_fused_slice(void);
 
+/* ---- work schedule of the in-kernel conversion kernels --------------------------
+ * How the 64- and 128-wide in-kernel-conversion kernels share K out over the
+ * CTAs when the output tiles alone would not keep the GPU busy: split K
+ * (every tile cut into the same number of pieces) or stream-K (every CTA
+ * takes an equal run of the tile-major order of all K slices, cut at tile
+ * ends; the pieces of a tile are added into C, cleared beforehand).
+ * 0 (the default): split K by the library's cost model of waves and partial
+ * tiles; 1: stream-K wherever every CTA gets at least two slices (measured
+ * on GB300 no faster than the split plan: the kernel's per-slice cost does
+ * not fall with a shorter run).  A scheduling choice only: C is the same
+ * exact int32 result, Y the same scaled values.  Process-wide; affects calls
+ * launched afterwards; LBGEMM_ERR_INVALID_ARG for another value. */
+lbgemm_status lbgemm_set_fused_stream_k(int mode);
+int lbgemm_get_fused_stream_k(void);
+
 /* ---- status ------------------------------------------------------------------ */
 
 /* Synchronises `stream`, then returns LBGEMM_ERR_TIMEOUT if any kernel of this

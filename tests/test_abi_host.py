@@ -550,3 +550,17 @@ def test_fused_slice_setting(lib):
             L.lbgemm_set_fused_slice(bad)
         assert e.value.status == L.ERR_INVALID_ARG
     assert L.lbgemm_get_fused_slice() == 0
+
+
+def test_fused_stream_k_setting(lib):
+    """The conversion kernels' schedule knob: 0 (split K, the default) or 1
+    (stream-K); anything else is rejected and leaves the setting alone."""
+    assert L.lbgemm_get_fused_stream_k() == 0
+    for v in (1, 0):
+        L.lbgemm_set_fused_stream_k(v)
+        assert L.lbgemm_get_fused_stream_k() == v
+    for bad in (2, -1):
+        with pytest.raises(L.LbgemmError) as e:
+            L.lbgemm_set_fused_stream_k(bad)
+        assert e.value.status == L.ERR_INVALID_ARG
+    assert L.lbgemm_get_fused_stream_k() == 0

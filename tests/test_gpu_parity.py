@@ -139,6 +139,40 @@ def test_int8_fused_extremes(tile_n):
     assert_exact(G().fused(B, A, K, tile_n), oracle.gemm(8, B, A, K), "fused adversarial (T)")
 
 
+@pytest.mark.parametrize("tile_n", [64, 128])
+def test_int8_fused_stream_k(tile_n):
+    """Stream-K forced on the 64/128-wide conversion kernels: every CTA takes
+    an equal run of the tile-major K slices, cut at tile ends, the pieces of a
+    tile added into C.  B converted (C written transposed by atomics) and A
+    converted (TMA reduce-adds), ragged tiles, K not a multiple of the slice;
+    bit-exact.  The linear layer on the same schedule (int32 sums, then the
+    scaling grid) within 1e-2."""
+    L.lbgemm_set_fused_stream_k(1)
+    try:
+        assert L.lbgemm_get_fused_stream_k() == 1
+        for i, (M, N, K) in enumerate([(64, 4100, 4096), (4096, 100, 2064), (200, 3000, 1040),
+                                       (33, 16384, 1024)]):
+            A, B = synth.operands(8, M, N, K, 2100 + i)
+            dC = torch.full((M, N), -7, dtype=torch.int32, device="cuda")
+            L.lbgemm_run_candidate(8, M, N, K, G().to_dev(A), G().to_dev(B), dC, L.ROUTE_FUSED,
+                                   tile_n)
+            L.lbgemm_device_status()
+            assert_exact(dC.cpu().numpy(), oracle.gemm(8, A, B, K),
+                         f"stream-K tile {tile_n} {M}x{N}x{K}")
+        for i, (M, N, K) in enumerate([(100, 4096, 4096), (40, 11008, 2048)]):
+            X, sx, W, sw = synth.linear_operands(M, N, K, 2200 + i)
+            X[1, :] = 0
+            dY = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+            L.lbgemm_linear_candidate(M, N, K, G().to_dev(X), G().to_dev(sx), G().to_dev(W),
+                                      G().to_dev(sw), dY, L.ROUTE_FUSED, tile_n)
+            L.lbgemm_device_status()
+            got = dY.float().cpu().numpy().astype(np.float64)
+            check_linear(got, oracle.linear(X, sx, W, sw), oracle.gemm(8, X, W, K) == 0,
+                         f"stream-K linear tile {tile_n} {M}x{N}x{K}")
+    finally:
+        L.lbgemm_set_fused_stream_k(0)
+
+
 def test_int8_fused_short_chunks():
     """A shorter exact chunk (512 elements) changes where the accumulator is
     read out; the result must not change."""
