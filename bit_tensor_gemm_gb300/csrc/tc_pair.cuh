@@ -62,6 +62,9 @@ struct PairLayout {
   static constexpr int kDynSmem = kUsedBytes + 1024;  // slack to align the ring to 1024
   static constexpr int kTmemCols = 512;              // two 256-column fp32 accumulators
   static_assert(kDynSmem <= 232448, "shared memory of one CTA");
+  // the stage ring holds a whole C tile of this CTA (8 warps x 4 groups of
+  // 32 x 128 bytes) from 4 stages on
+  static constexpr bool kRingHoldsC = kEpiOffset >= kTcEpiWarps * 4 * 32 * 128;
 };
 
 // ---- cluster and cta_group::2 forms ------------------------------------------------------
@@ -362,6 +365,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
       const bool adds = unit_range(w, p, t, kbb, kbe);
       tile_coords(t, p, tm, tn);
       const int num_chunks = (kbe - kbb + p.chunk_kb - 1) / p.chunk_kb;
+      // The cluster's last unit: once its final accumulator is complete no
+      // copy or MMA touches either CTA's stage ring any more, so each warp
+      // stages all its groups of C there (where the ring is large enough) and
+      // issues their stores back to back.
+      const bool last_unit = L::kRingHoldsC && w + ncl >= p.num_units;
       for (int c = 0; c < num_chunks; ++c, ++u) {
         const int buf = u & 1;
         int got = 0;
@@ -372,15 +380,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
           break;
         }
         tc_fence_after();
+        if (c == 0) {
+          // the first chunk lands in acc itself: all loads, then one wait
 #pragma unroll
-        for (int g = 0; g < kGroups; ++g) {
-          uint32_t v[32];
-          tmem_ld32(tmem_base + lane_addr + buf * kPairTile + col0 + g * 32, v);
+          for (int g = 0; g < kGroups; ++g)
+            tmem_ld32(tmem_base + lane_addr + buf * kPairTile + col0 + g * 32,
+                      reinterpret_cast<uint32_t(&)[32]>(acc[g]));
           tmem_ld_wait();
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int32_t x = __float2int_rn(__uint_as_float(v[j]));
-            acc[g][j] = (c == 0) ? x : acc[g][j] + x;
+          for (int g = 0; g < kGroups; ++g)
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              acc[g][j] = __float2int_rn(__uint_as_float((uint32_t)acc[g][j]));
+        } else {
+#pragma unroll
+          for (int g = 0; g < kGroups; ++g) {
+            uint32_t v[32];
+            tmem_ld32(tmem_base + lane_addr + buf * kPairTile + col0 + g * 32, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) acc[g][j] += __float2int_rn(__uint_as_float(v[j]));
           }
         }
         tc_fence_before();
@@ -397,10 +416,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
       if (!LINEAR && p.vec_ok) {
 #pragma unroll
         for (int g = 0; g < kGroups; ++g, ++stores) {
-          // the store that last used this buffer has read it
-          if (lane == 0) bulk_wait_read<L::kEpiBufs - 1>();
-          __syncwarp();
-          const uint32_t buf = stage_addr + (stores % L::kEpiBufs) * (32 * 128);
+          uint32_t buf;
+          if (last_unit) {
+            buf = sbase + (e * kGroups + g) * (32 * 128);
+          } else {
+            // the store that last used this buffer has read it
+            if (lane == 0) bulk_wait_read<L::kEpiBufs - 1>();
+            __syncwarp();
+            buf = stage_addr + (stores % L::kEpiBufs) * (32 * 128);
+          }
 #pragma unroll
           for (int q = 0; q < 8; ++q)
             st_shared_v4(buf + lane * 128 + ((q ^ (lane & 7)) << 4), acc[g][4 * q],
