@@ -934,14 +934,23 @@ int route_of(int bits, int64_t M, int64_t N, int64_t K, const void* A, const voi
   *fuse = 0;
   if (M == 0 || N == 0) return LBGEMM_ROUTE_NONE;
   if (linear) {
-    if (skinny_ok(M, K, A, B)) return LBGEMM_ROUTE_SKINNY;
+    // 5-8 tokens past the streaming kernel's K: the dp4a kernel still wins up
+    // to K = 8192 (measured on GB300: 8 x 28672 x 8192, 77.8 -> 71.7 us; 8 x
+    // 8192 x 8192, 32.3 -> 31.0; at K = 11008 and beyond it loses to the
+    // in-kernel-conversion kernel, 26.9 against 34.8 us for 8 x 4096 x 11008)
+    if (skinny_ok(M, K, A, B) ||
+        (M <= 2 * kSkinnyMaxM && K > lbg::stream_mma_max_k() && K <= 8192 &&
+         skinny_ok(1, K, A, B)))
+      return LBGEMM_ROUTE_SKINNY;
     if (M <= kStreamMaxSide && stream_ok(M, N, K, A, B)) return LBGEMM_ROUTE_STREAM;
     if (warpmma_ok(M, N, K, A, B)) return LBGEMM_ROUTE_WARPMMA;
     if (fused_route(M, N, K, A, B, tile_n) == 1) {
-      // no CTA pairs for the linear layer: the 128-wide tile, K split where
-      // the grid is short, is as fast or faster (measured on GB300: 512
-      // tokens x 11008 x 4096, 92 -> 72 us; 256 tokens, equal)
-      if (*tile_n == 256) *tile_n = 128;
+      // CTA pairs for the linear layer only past 384 tokens with K >= 8192;
+      // elsewhere the 128-wide tile, K split where the grid is short, is as
+      // fast or faster (measured on GB300: 512 tokens x 11008 x 4096, 92 ->
+      // 72 us; 256 tokens, equal or faster up to 28672 x 8192; but 512 x
+      // 8192 x 28672, 280 against 252 us on the pairs)
+      if (*tile_n == 256 && !(std::min(M, N) > 384 && K >= 8192)) *tile_n = 128;
       *fuse = 1;
       return LBGEMM_ROUTE_FUSED;
     }

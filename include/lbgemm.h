@@ -232,13 +232,15 @@ lbgemm_status lbgemm_run_popc(int64_t M, int64_t N, int64_t K, const uint32_t* A
  * [M]); W: int8 N x K (per-output-channel scale sw, fp32 [N]); Y: bf16 M x N
  * row-major, passed as void* (2 bytes per element).  The scale product is
  * formed in fp32, left to right.  K <= 131071.  The shape rules of
- * lbgemm_run apply: M <= 4 on the dp4a kernel that streams W once, M <= 16
- * (N >= 1024, K <= 4096) on the streaming warp-MMA kernel, M <= 32 on the
- * warp-level fp16 MMA kernel, M <= 512 (with N >= 1024 and N, K as
- * lbgemm_run says) on the kernel that converts W itself (64- or 128-wide
- * tiles, never the CTA-pair tile; where its tiles would leave most SMs idle,
- * K is split over CTAs into int32 sums in library scratch and a second grid
- * scales them into Y), larger M on the tensor-core variant table. */
+ * lbgemm_run apply: M <= 4 (M <= 8 when 4096 < K <= 8192) on the dp4a
+ * kernel that streams W once, M <= 16 (N >= 1024, K <= 4096) on the
+ * streaming warp-MMA kernel, M <= 32 on the warp-level fp16 MMA kernel,
+ * M <= 512 (with N >= 1024 and N, K as lbgemm_run says) on the kernel that
+ * converts W itself (64- or 128-wide tiles; the CTA-pair tile only past 384
+ * tokens with K >= 8192 where lbgemm_run takes it; where its tiles would
+ * leave most SMs idle, K is split over CTAs into int32 sums in library
+ * scratch and a second grid scales them into Y), larger M on the
+ * tensor-core variant table. */
 lbgemm_status lbgemm_linear(int64_t M, int64_t N, int64_t K, const int8_t* X, const float* sx,
                             const int8_t* W, const float* sw, void* Y, void* stream);
 

@@ -198,7 +198,7 @@ def _route8(M, N, K, linear=False):
         return L.ROUTE_NONE, 0
     lo, hi = min(M, N), max(M, N)
     k16 = K % 16 == 0
-    if M <= 4 and k16:
+    if k16 and (M <= 4 or (linear and M <= 8 and 4096 < K <= 8192)):
         return L.ROUTE_SKINNY, 0
     if lo <= 16 and hi >= 1024 and k16 and K <= 4096 and (not linear or M <= 16):
         return L.ROUTE_STREAM, 0
@@ -214,8 +214,9 @@ def _route8(M, N, K, linear=False):
     if (k16 and lo <= 512 and hi >= 1024 and K >= 512 and (not linear or M <= N)
             and (hi >= 4096 or K >= 8192 or (hi >= 2048 and K >= 4096)
                  or (lo <= 256 and K >= 2048))):
-        # CTA pairs only for the GEMM
-        return L.ROUTE_FUSED, 64 if lo <= 64 else 256 if _pairs(lo, hi, K) and not linear else 128
+        # CTA pairs for the linear layer only past 384 rows with K >= 8192
+        pairs = _pairs(lo, hi, K) and (not linear or (lo > 384 and K >= 8192))
+        return L.ROUTE_FUSED, 64 if lo <= 64 else 256 if pairs else 128
     return L.ROUTE_TABLE, 0
 
 
