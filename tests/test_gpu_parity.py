@@ -549,13 +549,14 @@ def test_linear_fused_route(M, N, K):
 
 @pytest.mark.parametrize("tile", [64, 128])
 @pytest.mark.parametrize("M,N,K", [(24, 4096, 4096), (64, 4096, 4096), (100, 2102, 4096),
-                                   (17, 11008, 4096), (200, 1030, 8192), (64, 1000, 512)])
+                                   (17, 11008, 4096), (200, 1030, 8192), (64, 1000, 512),
+                                   (100, 2102, 1040)])
 def test_linear_fused_split_k(tile, M, N, K):
     """The conversion kernel's linear layer, K split over CTAs where the
     unsplit grid would leave most SMs idle: partial sums added into an int32
     workspace, then scaled into Y by a second grid (ragged tiles of W rows and
-    tokens; N % 4 != 0 on the scalar scaling path); unsplit where the split
-    would not pay (11008 rows, 512-long K).  A second call right after the
+    tokens; N % 4 != 0 on the scalar scaling path; a K with a ragged last
+    slice); unsplit where the split would not pay (11008 rows, 512-long K).  A second call right after the
     first must not see the first one's sums."""
     for rep in range(2):
         X, sx, W, sw = synth.linear_operands(M, N, K, 610 + M + 7 * rep)
