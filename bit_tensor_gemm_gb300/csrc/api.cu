@@ -78,6 +78,13 @@ constexpr int64_t kFusedMinOther = 1024;
 // 25.6 us; 64 x 11008 x 4096, 86 tiles, split plan at 0.79 of the grid: no
 // gain).
 constexpr double kLinearSplitGain = 0.7;
+// ... and takes stream-K instead where that schedule's cost model (each CTA's
+// run of K slices plus one partial tile) is at most this share of the plan
+// chosen so far: where the tiles make a fractional number of waves
+// (measured on GB300: 192 tokens x 11008 x 4096, 172 tiles on 152 SMs, 53.2
+// -> 46.1 us; 128 x 28672 x 8192, 92.2 -> 82.5 us; where it predicts less
+// it measured no gain or a loss, e.g. 256 x 14336 x 4096, 53.2 -> 55.9 us).
+constexpr double kLinearStreamGain = 0.85;
 // Small side of the warp-level fp16 MMA kernel (hmma_skinny.cu): any problem
 // up to kWarpMmaMaxSide rows; with more rows (up to kWarpMmaMaxSideSmall,
 // each 32 rows re-reading the large operand) only small problems with
@@ -717,14 +724,15 @@ lbgemm_status run_tc_fused(DeviceState& d, bool large_b, int tile_n, int64_t M, 
   // GEMM kernel adding int32 partial sums into a workspace after the
   // re-encoded operand in `ws` (fused_linear_scratch), and a second grid
   // scales the sums into Y.
-  // Stream-K (64- and 128-wide kernels, opt-in by lbgemm_set_fused_stream_k):
-  // every CTA slot takes an equal run of the tile-major order of all K
-  // slices, cut at tile ends into pieces that each add a partial tile.
-  // Measured on GB300 no faster than the split plan (e.g. 128 x 11008 x
-  // 4096: 33.8 against 32.8 us; 256 x 11008 x 4096: 48.3 against 52.2; 512 x
-  // 4096 x 1024: 21.5 against 15.4): a slice costs the kernel the same ~1200
-  // cycles either way, bound by the SM's shared- and tensor-memory traffic,
-  // so a shorter run per CTA buys little against the extra partial tiles.
+  // Stream-K (64- and 128-wide kernels; the linear layer by its cost model,
+  // the GEMM only when lbgemm_set_fused_stream_k asks): every CTA slot takes
+  // an equal run of the tile-major order of all K slices, cut at tile ends
+  // into pieces that each add a partial tile.  For the GEMM it measured no
+  // faster than the split plan (e.g. 512 x 4096 x 1024: 21.5 against 15.4
+  // us): a slice costs the kernel the same ~1200 cycles either way, bound by
+  // the SM's shared- and tensor-memory traffic, so a shorter run per CTA buys
+  // little against the extra partial tiles; the linear layer gains where its
+  // tiles make a fractional number of waves (kLinearStreamGain).
   const bool linear_split = linear && large_b && tile_n != 256;
   int splits = 1, stream_pieces = 0;
   if ((!linear && (vec_ok || large_b)) || linear_split) {
@@ -746,17 +754,26 @@ lbgemm_status run_tc_fused(DeviceState& d, bool large_b, int tile_n, int64_t M, 
           splits = sp;
         }
       }
+      const double whole = (double)((tiles + slots - 1) / slots);
       const int64_t kslices = (kp + k.slice - 1) / k.slice;
       const int64_t total = tiles * kslices;
-      if (g_stream_k.load() && total >= 2 * slots) {
-        const int64_t run = (total + slots - 1) / slots;
+      // stream-K: each CTA's run of slices plus about one partial tile more
+      // than its whole tiles
+      const int64_t run = total >= 2 * slots ? (total + slots - 1) / slots : 0;
+      const double sk_cost =
+          run ? (double)run / kslices + ((double)run / kslices + 1.0) * c_share : 1e30;
+      bool stream = g_stream_k.load() && run > 0;
+      if (linear && !stream) {
+        double chosen = best;
+        if (best > kLinearSplitGain * whole) {
+          splits = 1;
+          chosen = whole;
+        }
+        stream = sk_cost <= kLinearStreamGain * chosen;
+      }
+      if (stream) {
         splits = 1;
         stream_pieces = (int)((run + kslices - 1) / kslices + 1);
-      }
-      if (linear && stream_pieces == 0 &&
-          best > kLinearSplitGain * (double)((tiles + slots - 1) / slots)) {
-        splits = 1;
-        stream_pieces = 0;
       }
     }
   }
