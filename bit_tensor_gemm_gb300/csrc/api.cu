@@ -690,6 +690,62 @@ lbgemm_status run_tc(DeviceState& d, int bits, int64_t M, int64_t N, int64_t K, 
   return run_tc_encoded(d, bits, M, N, K, encA, encB, C, sx, sw, Y, spec, true, &plan, stream);
 }
 
+// Work schedule of the 64- and 128-wide in-kernel-conversion kernels for
+// rows_l rows converted in the kernel (128 per tile), rows_s re-encoded rows
+// (tile_n per tile), K slices of `slice` elements, on `slots` CTA slots: K
+// pieces per tile (splits), or stream-K (stream_pieces > 0: units per CTA).
+// The cost of a plan is counted in whole-tile times: waves of units, a unit
+// costing its share of the tile's K plus, when split, its partial tile of C
+// (4 tile_n bytes per row against K).  The GEMM takes the cheapest split (up
+// to 16 pieces, at least 4 slices of 64 each), stream-K only when forced;
+// the linear layer splits only at kLinearSplitGain of the whole grid's cost
+// and takes stream-K (each CTA's run plus one partial tile) at
+// kLinearStreamGain of the plan chosen so far.
+struct FusedSchedule {
+  int splits = 1;
+  int stream_pieces = 0;
+};
+
+FusedSchedule fused_schedule(int64_t rows_l, int64_t rows_s, int64_t K, int tile_n, int slice,
+                             bool linear, int64_t slots, bool force_stream) {
+  FusedSchedule fs;
+  const int64_t tiles = ((rows_l + 127) / 128) * ((rows_s + tile_n - 1) / tile_n);
+  const int64_t kp = enc_kp(8, K);
+  const int64_t num_kb = (kp + 63) / 64;
+  const double c_share = 4.0 * tile_n / (double)K;
+  double best = 1e30;
+  for (int sp = 1; sp <= 16 && (sp == 1 || num_kb / sp >= 4); ++sp) {
+    const int64_t waves = (tiles * sp + slots - 1) / slots;
+    const double cost = (double)waves * (1.0 / sp + (sp > 1 ? c_share : 0.0));
+    if (cost < best - 1e-9) {
+      best = cost;
+      fs.splits = sp;
+    }
+  }
+  const double whole = (double)((tiles + slots - 1) / slots);
+  const int64_t kslices = (kp + slice - 1) / slice;
+  const int64_t total = tiles * kslices;
+  // stream-K: each CTA's run of slices plus about one partial tile more than
+  // its whole tiles
+  const int64_t run = total >= 2 * slots ? (total + slots - 1) / slots : 0;
+  const double sk_cost =
+      run ? (double)run / kslices + ((double)run / kslices + 1.0) * c_share : 1e30;
+  bool stream = force_stream && run > 0;
+  if (linear && !stream) {
+    double chosen = best;
+    if (best > kLinearSplitGain * whole) {
+      fs.splits = 1;
+      chosen = whole;
+    }
+    stream = sk_cost <= kLinearStreamGain * chosen;
+  }
+  if (stream) {
+    fs.splits = 1;
+    fs.stream_pieces = (int)((run + kslices - 1) / kslices + 1);
+  }
+  return fs;
+}
+
 // 8-bit problems with one operand converted in the kernel: only the other
 // operand is re-encoded ahead.  large_b: B is converted (the kernel computes
 // C transposed, rows of B on the tensor-memory A side); else A is converted.
@@ -740,41 +796,10 @@ lbgemm_status run_tc_fused(DeviceState& d, bool large_b, int tile_n, int64_t M, 
       KPlan kpl = plan_k(d, k, 8, rows_l, rows_s, K, linear, true);
       splits = kpl.dp_tiles == 0 ? kpl.splits : 1;
     } else {
-      const int64_t tiles =
-          ((rows_l + k.tile_m - 1) / k.tile_m) * ((rows_s + tile_n - 1) / tile_n);
-      const int64_t slots = unit_slots(d, k);
-      const int64_t num_kb = (enc_kp(8, K) + 63) / 64;
-      const double c_share = 4.0 * tile_n / (double)K;
-      double best = 1e30;
-      for (int sp = 1; sp <= 16 && (sp == 1 || num_kb / sp >= 4); ++sp) {
-        const int64_t waves = (tiles * sp + slots - 1) / slots;
-        const double cost = (double)waves * (1.0 / sp + (sp > 1 ? c_share : 0.0));
-        if (cost < best - 1e-9) {
-          best = cost;
-          splits = sp;
-        }
-      }
-      const double whole = (double)((tiles + slots - 1) / slots);
-      const int64_t kslices = (kp + k.slice - 1) / k.slice;
-      const int64_t total = tiles * kslices;
-      // stream-K: each CTA's run of slices plus about one partial tile more
-      // than its whole tiles
-      const int64_t run = total >= 2 * slots ? (total + slots - 1) / slots : 0;
-      const double sk_cost =
-          run ? (double)run / kslices + ((double)run / kslices + 1.0) * c_share : 1e30;
-      bool stream = g_stream_k.load() && run > 0;
-      if (linear && !stream) {
-        double chosen = best;
-        if (best > kLinearSplitGain * whole) {
-          splits = 1;
-          chosen = whole;
-        }
-        stream = sk_cost <= kLinearStreamGain * chosen;
-      }
-      if (stream) {
-        splits = 1;
-        stream_pieces = (int)((run + kslices - 1) / kslices + 1);
-      }
+      const FusedSchedule fs = fused_schedule(rows_l, rows_s, K, tile_n, k.slice, linear,
+                                              unit_slots(d, k), g_stream_k.load() != 0);
+      splits = fs.splits;
+      stream_pieces = fs.stream_pieces;
     }
   }
   const bool partial = splits > 1 || stream_pieces > 0;
@@ -1995,6 +2020,21 @@ lbgemm_status lbgemm_set_fused_slice(int k_elems) {
 }
 
 int lbgemm_get_fused_slice(void) { return g_fused_slice.load(); }
+
+lbgemm_status lbgemm_fused_schedule(int64_t M, int64_t N, int64_t K, int tile_n, int linear,
+                                    int sm_count, int* splits, int* stream_pieces) {
+  if ((tile_n != 64 && tile_n != 128) || M < 1 || N < 1 || K < 1 || sm_count < 1 ||
+      (linear && M > N))
+    return fail(LBGEMM_ERR_INVALID_ARG, "bad fused-schedule query");
+  const bool large_b = linear || N >= M;
+  FusedSchedule fs;
+  if (linear || large_b || N % 4 == 0)
+    fs = fused_schedule(large_b ? N : M, large_b ? M : N, K, tile_n, fused_slice(tile_n),
+                        linear != 0, sm_count, g_stream_k.load() != 0);
+  if (splits) *splits = fs.splits;
+  if (stream_pieces) *stream_pieces = fs.stream_pieces;
+  return LBGEMM_OK;
+}
 
 lbgemm_status lbgemm_set_fused_stream_k(int mode) {
   if (mode < 0 || mode > 1)

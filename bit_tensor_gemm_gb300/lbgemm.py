@@ -93,6 +93,8 @@ _SIGNATURES = {
     "lbgemm_set_fused_slice": (_i32, [_i32]),
     "lbgemm_get_fused_slice": (_i32, []),
     "lbgemm_set_fused_stream_k": (_i32, [_i32]),
+    "lbgemm_fused_schedule": (_i32, [_i64, _i64, _i64, _i32, _i32, _i32, ctypes.POINTER(ctypes.c_int),
+                                     ctypes.POINTER(ctypes.c_int)]),
     "lbgemm_get_fused_stream_k": (_i32, []),
     "lbgemm_get_tail_split": (_i32, []),
     "lbgemm_device_status": (_i32, [_vp]),
@@ -430,6 +432,15 @@ def lbgemm_set_fused_stream_k(mode: int) -> None:
 
 def lbgemm_get_fused_stream_k() -> int:
     return load().lbgemm_get_fused_stream_k()
+
+
+def lbgemm_fused_schedule(M, N, K, tile_n, linear=False, sm_count=152):
+    """(splits, stream_pieces) of the 64/128-wide in-kernel-conversion kernel
+    for this GEMM or linear layer on sm_count SMs (host only)."""
+    sp, pc = ctypes.c_int(0), ctypes.c_int(0)
+    _check(load().lbgemm_fused_schedule(M, N, K, tile_n, int(bool(linear)), sm_count,
+                                        ctypes.byref(sp), ctypes.byref(pc)))
+    return sp.value, pc.value
 
 
 def lbgemm_get_tail_split() -> int:

@@ -488,6 +488,28 @@ int lbgemm_get_fused_slice(void);
 lbgemm_status lbgemm_set_fused_stream_k(int mode);
 int lbgemm_get_fused_stream_k(void);
 
+/* The schedule the 64- or 128-wide in-kernel-conversion kernel takes for an
+ * 8-bit GEMM (linear = 0) or linear layer (linear != 0, M <= N) on a device
+ * with sm_count SMs (one CTA per SM), 16-byte-aligned operands, under the
+ * current slice and stream-K settings: *splits K pieces per tile (1: whole
+ * tiles), or *stream_pieces > 0 for stream-K (units per CTA; *splits = 1).
+ * Host only.  The converted operand is the larger one (B when N >= M; W for
+ * the linear layer), R its rows, S the other's; tiles = ceil(R/128) *
+ * ceil(S/tile_n); costs are in whole-tile times on `sm_count` slots:
+ * split p (1 <= p <= 16, p = 1 or ceil(K/64)/p >= 4) costs
+ * ceil(tiles*p/sm_count) * (1/p + (p > 1 ? 4*tile_n/K : 0)), the cheapest p
+ * wins (the first on ties); stream-K, possible when tiles*k >= 2*sm_count
+ * with k = ceil(ceil8(K)/slice), costs r/k + (r/k + 1) * 4*tile_n/K with
+ * r = ceil(tiles*k/sm_count) and takes r/k rounded up plus 1 pieces.  A GEMM
+ * converting A (N < M) with N % 4 != 0 runs whole tiles.  The GEMM takes the
+ * cheapest split (stream-K only when lbgemm_set_fused_stream_k forces it);
+ * the linear layer keeps a split only if its cost is at most 0.7 of
+ * ceil(tiles/sm_count), else whole tiles, and then takes stream-K if its
+ * cost is at most 0.85 of the plan kept (or when forced).
+ * LBGEMM_ERR_INVALID_ARG for another tile_n or bad sizes. */
+lbgemm_status lbgemm_fused_schedule(int64_t M, int64_t N, int64_t K, int tile_n, int linear,
+                                    int sm_count, int* splits, int* stream_pieces);
+
 /* ---- status ------------------------------------------------------------------ */
 
 /* Synchronises `stream`, then returns LBGEMM_ERR_TIMEOUT if any kernel of this

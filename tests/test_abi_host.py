@@ -565,3 +565,80 @@ def test_fused_stream_k_setting(lib):
             L.lbgemm_set_fused_stream_k(bad)
         assert e.value.status == L.ERR_INVALID_ARG
     assert L.lbgemm_get_fused_stream_k() == 0
+
+
+def _fused_schedule(M, N, K, tile_n, linear, sm, slice_, force=False):
+    """The schedule include/lbgemm.h states for lbgemm_fused_schedule, written
+    out from that text."""
+    import math  # noqa: PLC0415
+    large_b = linear or N >= M
+    if not linear and not large_b and N % 4:
+        return 1, 0
+    R, S = (N, M) if large_b else (M, N)
+    tiles = math.ceil(R / 128) * math.ceil(S / tile_n)
+    c = 4 * tile_n / K
+    nkb = math.ceil(K / 64)
+    best, splits = None, 1
+    for p in range(1, 17):
+        if p > 1 and nkb // p < 4:
+            break
+        cost = math.ceil(tiles * p / sm) * (1 / p + (c if p > 1 else 0))
+        if best is None or cost < best - 1e-9:
+            best, splits = cost, p
+    k = math.ceil((K + 7) // 8 * 8 / slice_)
+    r = math.ceil(tiles * k / sm) if tiles * k >= 2 * sm else 0
+    sk = r / k + (r / k + 1) * c if r else None
+    stream = force and r > 0
+    if linear and not stream:
+        chosen = best
+        if best > 0.7 * math.ceil(tiles / sm):
+            splits, chosen = 1, math.ceil(tiles / sm)
+        stream = sk is not None and sk <= 0.85 * chosen
+    if stream:
+        return 1, math.ceil(r / k) + 1
+    return splits, 0
+
+
+def test_fused_schedule_follows_the_stated_model(lib):
+    """The split / stream-K plan of the 64- and 128-wide conversion kernels,
+    against the header's formula on a grid of GEMM and linear shapes and SM
+    counts, plus the measured cases the model was fitted on."""
+    assert L.lbgemm_get_fused_slice() == 0 and L.lbgemm_get_fused_stream_k() == 0
+    sides = [1, 16, 64, 100, 128, 192, 256, 512, 1024, 4096, 11008, 28672]
+    for M in sides:
+        for N in sides:
+            for K in (256, 1040, 4096, 16384):
+                for tile in (64, 128):
+                    for linear in (False, True):
+                        if linear and M > N:
+                            continue
+                        for sm in (152, 148):
+                            want = _fused_schedule(M, N, K, tile, linear, sm, 256 if tile == 64 else 128)
+                            assert L.lbgemm_fused_schedule(M, N, K, tile, linear, sm) == want, \
+                                (M, N, K, tile, linear, sm)
+    # measured on GB300 (152 SMs): 64 x 16384 x 16384 GEMM in 7 pieces (114 ->
+    # 106 us); the linear layer split where the grid is short (64 x 4096 x
+    # 4096: 27 -> 19.5 us), stream-K where the tiles make a fractional wave
+    # (192 x 11008 x 4096: 53 -> 45 us), whole tiles where neither pays
+    # (256 x 28672 x 8192)
+    assert L.lbgemm_fused_schedule(64, 16384, 16384, 64) == (7, 0)
+    assert L.lbgemm_fused_schedule(64, 4096, 4096, 64, True) == (4, 0)
+    assert L.lbgemm_fused_schedule(192, 11008, 4096, 128, True)[1] > 0
+    assert L.lbgemm_fused_schedule(256, 28672, 8192, 128, True) == (1, 0)
+    # forced stream-K, and the slice setting feeding the slice count
+    L.lbgemm_set_fused_stream_k(1)
+    try:
+        assert L.lbgemm_fused_schedule(64, 16384, 16384, 64) == \
+            _fused_schedule(64, 16384, 16384, 64, False, 152, 256, force=True)
+    finally:
+        L.lbgemm_set_fused_stream_k(0)
+    L.lbgemm_set_fused_slice(256)
+    try:
+        assert L.lbgemm_fused_schedule(128, 11008, 4096, 128, True) == \
+            _fused_schedule(128, 11008, 4096, 128, True, 152, 256)
+    finally:
+        L.lbgemm_set_fused_slice(0)
+    for bad in [(64, 64, 64, 256, False, 152), (0, 64, 64, 64, False, 152),
+                (64, 64, 64, 64, False, 0), (128, 64, 64, 64, True, 152)]:
+        with pytest.raises(L.LbgemmError):
+            L.lbgemm_fused_schedule(*bad)
