@@ -201,9 +201,27 @@ lbgemm_status device_state(DeviceState** out) {
   return LBGEMM_OK;
 }
 
-// Grows `s` to at least `bytes` (synchronising the device when it must
-// reallocate) and orders this use after the previous one on another stream.
-lbgemm_status scratch_acquire(Scratch& s, size_t bytes, cudaStream_t stream) {
+// Whether `stream` is being captured into a CUDA graph.
+bool capturing(cudaStream_t stream) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  return cudaStreamIsCapturing(stream, &cs) == cudaSuccess && cs == cudaStreamCaptureStatusActive;
+}
+
+// Scratch for one call, in *ptr.  Normally the per-device buffer `s`, grown
+// to at least `bytes` (synchronising the device when it must reallocate),
+// this use ordered after the previous one on another stream by its event.
+// While `stream` is being captured into a CUDA graph, a stream-ordered
+// allocation instead (an allocation node of the graph, freed again by
+// scratch_release within it): the graph then holds no address of the shared
+// buffer, which a later call may reallocate, and no dependency on work
+// outside the capture.
+lbgemm_status scratch_acquire(Scratch& s, size_t bytes, cudaStream_t stream, void** ptr) {
+  *ptr = nullptr;
+  if (capturing(stream)) {
+    cudaError_t e = cudaMallocAsync(ptr, std::max<size_t>(bytes, 256), stream);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMallocAsync (scratch, stream capture)");
+    return LBGEMM_OK;
+  }
   if (s.bytes < bytes) {
     cudaError_t e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize (scratch growth)");
@@ -231,10 +249,16 @@ lbgemm_status scratch_acquire(Scratch& s, size_t bytes, cudaStream_t stream) {
     cudaError_t e = cudaStreamWaitEvent(stream, s.done, 0);
     if (e != cudaSuccess) return cuda_fail(e, "cudaStreamWaitEvent");
   }
+  *ptr = s.ptr;
   return LBGEMM_OK;
 }
 
-lbgemm_status scratch_release(Scratch& s, cudaStream_t stream) {
+// Ends a use of the scratch that scratch_acquire handed out as `ptr`.
+lbgemm_status scratch_release(Scratch& s, cudaStream_t stream, void* ptr) {
+  if (ptr && ptr != s.ptr) {  // the graph's own allocation
+    cudaError_t e = cudaFreeAsync(ptr, stream);
+    return e == cudaSuccess ? LBGEMM_OK : cuda_fail(e, "cudaFreeAsync (scratch)");
+  }
   cudaError_t e = cudaEventRecord(s.done, stream);
   if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
   s.used = true;
@@ -1202,15 +1226,16 @@ lbgemm_status run_route(DeviceState& d, int bits, int64_t M, int64_t N, int64_t 
     return run_tc(d, bits, M, N, K, A, B, C, nullptr, nullptr, nullptr, tc_spec(p), ws, stream);
   }
   std::lock_guard<std::mutex> lock(g_ws_mu);
-  lbgemm_status st = scratch_acquire(d.ws, need, stream);
+  void* scratch = nullptr;
+  lbgemm_status st = scratch_acquire(d.ws, need, stream, &scratch);
   if (st != LBGEMM_OK) return st;
   if (p.route == LBGEMM_ROUTE_FUSED)
-    st = run_tc_fused(d, N >= M, p.param, M, N, K, A, B, C, nullptr, nullptr, nullptr, d.ws.ptr,
+    st = run_tc_fused(d, N >= M, p.param, M, N, K, A, B, C, nullptr, nullptr, nullptr, scratch,
                       stream);
   else
-    st = run_tc(d, bits, M, N, K, A, B, C, nullptr, nullptr, nullptr, tc_spec(p), d.ws.ptr,
+    st = run_tc(d, bits, M, N, K, A, B, C, nullptr, nullptr, nullptr, tc_spec(p), scratch,
                 stream);
-  lbgemm_status st2 = scratch_release(d.ws, stream);
+  lbgemm_status st2 = scratch_release(d.ws, stream, scratch);
   return st != LBGEMM_OK ? st : st2;
 }
 
@@ -1284,18 +1309,20 @@ lbgemm_status run_linear(int64_t M, int64_t N, int64_t K, const int8_t* X, const
   if (route == LBGEMM_ROUTE_FUSED) {
     // small token counts: only X is re-encoded; the kernel converts W itself
     std::lock_guard<std::mutex> lock(g_ws_mu);
-    st = scratch_acquire(d->ws, fused_linear_scratch(M, N, K, fuse_tile), stream);
+    void* scratch = nullptr;
+    st = scratch_acquire(d->ws, fused_linear_scratch(M, N, K, fuse_tile), stream, &scratch);
     if (st != LBGEMM_OK) return st;
-    st = run_tc_fused(*d, true, fuse_tile, M, N, K, X, W, nullptr, sx, sw, Y, d->ws.ptr, stream);
-    lbgemm_status st2 = scratch_release(d->ws, stream);
+    st = run_tc_fused(*d, true, fuse_tile, M, N, K, X, W, nullptr, sx, sw, Y, scratch, stream);
+    lbgemm_status st2 = scratch_release(d->ws, stream, scratch);
     return st != LBGEMM_OK ? st : st2;
   }
   std::lock_guard<std::mutex> lock(g_ws_mu);
   const size_t need = enc_bytes(8, M, K) + enc_bytes(8, N, K);
-  st = scratch_acquire(d->ws, need, stream);
+  void* scratch = nullptr;
+  st = scratch_acquire(d->ws, need, stream, &scratch);
   if (st != LBGEMM_OK) return st;
-  st = run_tc(*d, 8, M, N, K, X, W, nullptr, sx, sw, Y, spec_of(variant), d->ws.ptr, stream);
-  lbgemm_status st2 = scratch_release(d->ws, stream);
+  st = run_tc(*d, 8, M, N, K, X, W, nullptr, sx, sw, Y, spec_of(variant), scratch, stream);
+  lbgemm_status st2 = scratch_release(d->ws, stream, scratch);
   return st != LBGEMM_OK ? st : st2;
 }
 
@@ -1400,11 +1427,12 @@ lbgemm_status lbgemm_run_fused(int64_t M, int64_t N, int64_t K, const int8_t* A,
     if (st != LBGEMM_OK) return st;
     const bool large_b = N >= M;
     std::lock_guard<std::mutex> lock(g_ws_mu);
-    st = scratch_acquire(d->ws, enc_bytes(8, large_b ? M : N, K), as_stream(stream));
+    void* scratch = nullptr;
+    st = scratch_acquire(d->ws, enc_bytes(8, large_b ? M : N, K), as_stream(stream), &scratch);
     if (st != LBGEMM_OK) return st;
-    st = run_tc_fused(*d, large_b, tile_n, M, N, K, A, B, C, nullptr, nullptr, nullptr, d->ws.ptr,
+    st = run_tc_fused(*d, large_b, tile_n, M, N, K, A, B, C, nullptr, nullptr, nullptr, scratch,
                       as_stream(stream));
-    lbgemm_status st2 = scratch_release(d->ws, as_stream(stream));
+    lbgemm_status st2 = scratch_release(d->ws, as_stream(stream), scratch);
     return st != LBGEMM_OK ? st : st2;
   } catch (...) {
     return fail(LBGEMM_ERR_CUDA, "internal error");
@@ -1504,16 +1532,20 @@ lbgemm_status lbgemm_linear_quant(int64_t M, int64_t N, int64_t K, const void* X
     static std::mutex quant_mu;
     std::lock_guard<std::mutex> lock(quant_mu);
     const size_t qbytes = (size_t)round_up(M * K, 256);
-    st = scratch_acquire(d->quant, qbytes + (size_t)M * sizeof(float), s);
+    void* scratch = nullptr;
+    st = scratch_acquire(d->quant, qbytes + (size_t)M * sizeof(float), s, &scratch);
     if (st != LBGEMM_OK) return st;
-    int8_t* Q = static_cast<int8_t*>(d->quant.ptr);
-    float* S = reinterpret_cast<float*>(static_cast<uint8_t*>(d->quant.ptr) + qbytes);
+    int8_t* Q = static_cast<int8_t*>(scratch);
+    float* S = reinterpret_cast<float*>(static_cast<uint8_t*>(scratch) + qbytes);
     cudaError_t e = lbg::launch_quant_rows_bf16(X, M, K, Q, S, s);
-    if (e != cudaSuccess) return cuda_fail(e, "quantize launch");
+    if (e != cudaSuccess) {
+      scratch_release(d->quant, s, scratch);
+      return cuda_fail(e, "quantize launch");
+    }
     g_launches += 1;
     // W is the caller's, not written by the quantiser launched just before
     st = run_linear(M, N, K, Q, S, W, sw, Y, -1, s, -1, 0, true);
-    lbgemm_status st2 = scratch_release(d->quant, s);
+    lbgemm_status st2 = scratch_release(d->quant, s, scratch);
     return st != LBGEMM_OK ? st : st2;
   } catch (...) {
     return fail(LBGEMM_ERR_CUDA, "internal error");
@@ -1793,9 +1825,10 @@ lbgemm_status lbgemm_time_candidates(int bits, int64_t M, int64_t N, int64_t K, 
     DeviceState* d = nullptr;
     st = device_state(&d);
     if (st != LBGEMM_OK) return st;
+    void* flush_buf = nullptr;
     if (flush_l2) {
       std::lock_guard<std::mutex> lock(g_mu);
-      st = scratch_acquire(d->flush, kFlushBytes, s);
+      st = scratch_acquire(d->flush, kFlushBytes, s, &flush_buf);
       if (st != LBGEMM_OK) return st;
     }
     auto run = [&](int c) {
@@ -1817,7 +1850,7 @@ lbgemm_status lbgemm_time_candidates(int bits, int64_t M, int64_t N, int64_t K, 
     std::vector<std::vector<float>> samples(count, std::vector<float>(reps));
     for (int r = 0; r < reps && e == cudaSuccess && st == LBGEMM_OK; ++r) {
       for (int c = 0; c < count && e == cudaSuccess && st == LBGEMM_OK; ++c) {
-        if (flush_l2) e = cudaMemsetAsync(d->flush.ptr, r & 0xFF, kFlushBytes, s);
+        if (flush_l2) e = cudaMemsetAsync(flush_buf, r & 0xFF, kFlushBytes, s);
         if (e == cudaSuccess) e = cudaEventRecord(ev[2 * c], s);
         if (e == cudaSuccess) st = run(c);
         if (e == cudaSuccess && st == LBGEMM_OK) e = cudaEventRecord(ev[2 * c + 1], s);
@@ -1832,7 +1865,7 @@ lbgemm_status lbgemm_time_candidates(int bits, int64_t M, int64_t N, int64_t K, 
     if (st != LBGEMM_OK) return st;
     if (flush_l2) {
       std::lock_guard<std::mutex> lock(g_mu);
-      st = scratch_release(d->flush, s);
+      st = scratch_release(d->flush, s, flush_buf);
       if (st != LBGEMM_OK) return st;
     }
     for (int c = 0; c < count; ++c) {
@@ -1897,9 +1930,10 @@ lbgemm_status lbgemm_run_host(int bits, int64_t M, int64_t N, int64_t K, const v
     std::lock_guard<std::mutex> lock(host_mu);
     st = host_streams(*d);
     if (st != LBGEMM_OK) return st;
-    st = scratch_acquire(d->host_stage, a_bytes + b_bytes + round_up(c_bytes, 256), s);
+    void* stage = nullptr;
+    st = scratch_acquire(d->host_stage, a_bytes + b_bytes + round_up(c_bytes, 256), s, &stage);
     if (st != LBGEMM_OK) return st;
-    uint8_t* dA = static_cast<uint8_t*>(d->host_stage.ptr);
+    uint8_t* dA = static_cast<uint8_t*>(stage);
     uint8_t* dB = dA + a_bytes;
     int32_t* dC = reinterpret_cast<int32_t*>(dB + b_bytes);
     // Cut M (rows of A and C) or N (rows of B, columns of C): the operand
@@ -1929,7 +1963,7 @@ lbgemm_status lbgemm_run_host(int bits, int64_t M, int64_t N, int64_t K, const v
       if (st != LBGEMM_OK) return st;
       e = cudaMemcpyAsync(C_host, dC, c_bytes, cudaMemcpyDeviceToHost, s);
       if (e != cudaSuccess) return cuda_fail(e, "device-to-host copy");
-      st = scratch_release(d->host_stage, s);
+      st = scratch_release(d->host_stage, s, stage);
       if (st != LBGEMM_OK) return st;
       e = cudaStreamSynchronize(s);
       return e == cudaSuccess ? LBGEMM_OK : cuda_fail(e, "cudaStreamSynchronize");
@@ -1980,7 +2014,7 @@ lbgemm_status lbgemm_run_host(int bits, int64_t M, int64_t N, int64_t K, const v
     if (e == cudaSuccess) e = cudaEventRecord(ev_out, d->copy_out);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(s, ev_out, 0);
     if (e != cudaSuccess) return cuda_fail(e, "pipelined host copies");
-    st = scratch_release(d->host_stage, s);
+    st = scratch_release(d->host_stage, s, stage);
     if (st != LBGEMM_OK) return st;
     e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");

@@ -109,9 +109,14 @@ lbgemm_status lbgemm_variant_info(int bits, int variant, int* tile_m, int* tile_
  * Scratch memory for the re-encoding is
  * taken from a per-device buffer the library grows with cudaMalloc on demand
  * (by at least half again each time);
- * calls from different streams are ordered on it with events.  A call that
- * grows the buffer synchronises the device, so make the first call of the
- * largest shape before capturing a CUDA graph, or use lbgemm_run_ws. */
+ * calls from different streams are ordered on it with events; a call that
+ * grows the buffer synchronises the device.  While `stream` is being
+ * captured into a CUDA graph, a call takes its scratch from stream-ordered
+ * allocations instead (cudaMallocAsync / cudaFreeAsync, which become
+ * allocation nodes of the graph): the graph needs no warm-up of the buffer,
+ * depends on nothing outside the capture and stays valid when a later call
+ * reallocates the buffer.  The library's per-device state must exist before
+ * the first capture on a device (any one call made outside capture). */
 lbgemm_status lbgemm_run(int bits, int64_t M, int64_t N, int64_t K, const void* A, const void* B,
                          int32_t* C, void* stream);
 
