@@ -130,3 +130,22 @@ def test_quantised_linear_captured():
     got = Y.float().cpu().numpy().astype(np.float64)
     nz = acc != 0
     assert np.all(np.abs(got[nz] - ref[nz]) <= 1e-2 * np.abs(ref[nz]))
+
+
+def test_caller_workspace_entry_captured():
+    """lbgemm_run_ws inside a graph: the caller's workspace, no library
+    scratch at all."""
+    bits, M, N, K = 8, 512, 768, 2048
+    A, B = synth.operands(bits, M, N, K, 51)
+    dA, dB = _dev(A), _dev(B)
+    C = torch.full((M, N), -7, dtype=torch.int32, device="cuda")
+    need = L.lbgemm_workspace_size(bits, M, N, K)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        L.lbgemm_run_ws(bits, M, N, K, dA, dB, C, -1, ws, need, stream=s)
+    g.replay()
+    torch.cuda.synchronize()
+    L.lbgemm_device_status()
+    assert np.array_equal(C.cpu().numpy(), oracle.gemm(bits, A, B, K))
