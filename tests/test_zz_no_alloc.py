@@ -73,9 +73,12 @@ def test_static_matches_oracle_two_calls_in_a_row_and_allocates_nothing(routed_e
     assert L.lbgemm_workspace_size(8, 256, 8192, 2048) > L.STATIC_SCRATCH_BYTES
     probs = _problems()
     # the first call of each kernel may load its code into the device (lazy
-    # module loading); device memory is compared from the second call on
+    # module loading, the library's and torch's fill and copy kernels alike);
+    # device memory is compared from the second round of calls on
     for bits, M, N, K, v, dA, dB, want, dC in probs:
+        dC.fill_(-2)
         L.lbgemm_run_static(bits, M, N, K, dA, dB, dC, v)
+        dC.cpu()
     L.lbgemm_device_status()
     torch.cuda.synchronize()
     free0 = torch.cuda.mem_get_info()[0]
@@ -99,3 +102,25 @@ def test_static_limit_is_enforced_before_running():
         L.lbgemm_run_static(8, M, N, K, dummy, dummy, dummy, 7)
     assert e.value.status == L.ERR_WORKSPACE
     assert "static" in L.lbgemm_last_error()
+
+
+def test_static_entry_captured_in_a_graph():
+    """Captured into a CUDA graph after one call outside capture (the array's
+    address is looked up then), the static entry replays exactly; the graph
+    holds no allocation node, as the call allocates nothing."""
+    bits, M, N, K = 8, 1024, 768, 4104
+    A, B = synth.operands(bits, M, N, K, 911)
+    dA, dB = _dev(A), _dev(B)
+    dC = torch.full((M, N), -5, dtype=torch.int32, device="cuda")
+    L.lbgemm_run_static(bits, M, N, K, dA, dB, dC, 8)
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        L.lbgemm_run_static(bits, M, N, K, dA, dB, dC, 8, stream=s)
+    for call in range(2):
+        dC.fill_(-5 - call)
+        g.replay()
+        torch.cuda.synchronize()
+        L.lbgemm_device_status()
+        assert np.array_equal(dC.cpu().numpy(), oracle.gemm(bits, A, B, K)), call
