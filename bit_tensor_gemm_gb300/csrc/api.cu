@@ -827,7 +827,8 @@ lbgemm_status run_tc_fused(DeviceState& d, bool large_b, int tile_n, int64_t M, 
     }
   }
   const bool partial = splits > 1 || stream_pieces > 0;
-  // the split linear layer: the plain kernel into int32 sums
+  // the linear layer with K shared out (split or stream-K): the plain kernel
+  // adds into int32 sums, scaled into Y by a second grid below
   int32_t* sums = nullptr;
   if (linear && partial) {
     sums = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + enc_bytes(8, rows_s, K));
