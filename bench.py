@@ -43,6 +43,7 @@ SWEEP = [(m, n, k) for m in SIZES for n in SIZES for k in SIZES]
 # Balanced ninth of the sweep: every (M, N) pair once, each K value nine times.
 E2E_SHAPES = [(SIZES[i], SIZES[j], SIZES[(-(i + j)) % 9]) for i in range(9) for j in range(9)]
 MAXD = SIZES[-1]
+E2E_PASSES = 5
 METRIC = "int8 GEMM TOPS over the 729-shape sweep (selected variant)"
 BITS = (8, 4, 1)
 SEED_OF = {8: 2, 4: 3, 1: 4}  # workload numbers of the 8-, 4- and 1-bit configurations
@@ -698,21 +699,30 @@ def run_ours(args):
     # the host pages and copy paths are warm, as for the timed steps' warm-up
     for (m, n, k) in e2e_shapes:
         L.lbgemm_run_host(8, m, n, k, A_pin, B_pin, C_pin, -1, stream)
-    e2e_s, h2d, d2h = 0.0, 0, 0
-    for (m, n, k) in e2e_shapes:
-        t0 = time.perf_counter()
-        L.lbgemm_run_host(8, m, n, k, A_pin, B_pin, C_pin, -1, stream)
-        e2e_s += time.perf_counter() - t0
-        h2d += m * k + n * k
-        d2h += 4 * m * n
-    dev_same = np.median(np.array([timed_pass(sel, e2e_shapes) for _ in range(2)]), axis=0)
+    # E2E_PASSES timed passes, each call timed on the host clock; the median
+    # pass is the value (a single pass once read 2.4x slower than its
+    # neighbours on the same box), every pass is reported
+    h2d = sum(m * k + n * k for m, n, k in e2e_shapes)
+    d2h = sum(4 * m * n for m, n, k in e2e_shapes)
     e2e_ops = ops_of(e2e_shapes)
+    pass_s = []
+    for _ in range(E2E_PASSES):
+        e2e_s = 0.0
+        for (m, n, k) in e2e_shapes:
+            t0 = time.perf_counter()
+            L.lbgemm_run_host(8, m, n, k, A_pin, B_pin, C_pin, -1, stream)
+            e2e_s += time.perf_counter() - t0
+        pass_s.append(e2e_s)
+    e2e_s = float(np.median(pass_s))
+    dev_same = np.median(np.array([timed_pass(sel, e2e_shapes) for _ in range(2)]), axis=0)
     e2e = {"value": e2e_ops * world / e2e_s / 1e12, "unit": "TOPS",
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+           "passes_tops": [round(e2e_ops * world / t / 1e12, 1) for t in pass_s],
            "shapes": f"{len(e2e_shapes)} of the sweep: every (M, N) pair once, each K nine times",
            "device_value_same_shapes": e2e_ops / (dev_same.sum() / 1e3) / 1e12,
            "entry": "lbgemm_run_host: pinned host buffers, copies and a sync inside the call; "
-                    "one untimed pass over the shapes before the timed one"}
+                    "one untimed pass over the shapes, then the median of "
+                    f"{E2E_PASSES} timed passes"}
     del A_pin, B_pin, C_pin
 
     # -- the CPU oracle on a row sample -------------------------------------------------------------

@@ -416,6 +416,7 @@ def test_int8_host_buffers():
 
 
 @pytest.mark.parametrize("bits,M,N,K", [(8, 4500, 4000, 256), (8, 20000, 64, 4096),
+                                        (8, 9000, 4000, 64),
                                         (8, 300, 9000, 1024), (8, 2000, 2100, 512),
                                         (4, 4500, 4000, 128), (4, 300, 6000, 4096),
                                         (1, 5000, 4000, 64), (1, 300, 9000, 8192)])
@@ -423,7 +424,8 @@ def test_host_buffers_in_blocks(bits, M, N, K):
     """Problems that copy more than 8 MB run in blocks of the larger side
     (copies in and out on their own streams, overlapping the blocks' GEMMs):
     row blocks and column blocks (C out by 2-D copies), ragged last blocks,
-    a large A with a small C, and every bit width."""
+    the block count at its cap (9000 x 4000 x 64: 144 MB of copies in twelve
+    blocks of 768 rows), a large A with a small C, and every bit width."""
     A, B = synth.operands(bits, M, N, K, 80 + bits)
     C = np.zeros((M, N), np.int32)
     L.lbgemm_run_host(bits, M, N, K, A, B, C, -1, 0)
