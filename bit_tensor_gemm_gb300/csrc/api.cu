@@ -108,19 +108,22 @@ std::atomic<int> g_chunk_s8{1024};
 std::atomic<int> g_chunk_s4{131072};
 std::atomic<int> g_chunk_b1{1 << 23};
 std::atomic<int> g_tail_split{1};  // 0 whole-problem splits only, 1 also a last partial wave, 2 forced
-// K elements per slice of the 64/128-wide conversion kernels; 0: by tile
-// (measured on GB300 over the grid shapes the dispatch gives these kernels:
-// 256-element slices make the 64-wide kernel up to 10 % faster, e.g. 64 x
-// 16384 x 16384 81.9 -> 74.3 us, and the 128-wide one up to 14 % slower, its
-// tensor memory then holding only two slots)
+// K elements per slice of the 64/128-wide conversion kernels; 0: by tile and
+// use (measured on GB300 over the grid shapes the dispatch gives these
+// kernels: 256-element slices make the 64-wide kernel up to 10 % faster, e.g.
+// 64 x 16384 x 16384 81.9 -> 74.3 us, and the 128-wide one up to 14 % slower
+// for the GEMM, its tensor memory then holding only two slots; for the linear
+// layer the 128-wide kernel is 8 % faster with them over 35 layers of 96-512
+// tokens on 4096-28672 x 4096-11008 weights, up to 16 % at 384 tokens, and
+// within 4 % of its 128-element time on each of them)
 std::atomic<int> g_fused_slice{0};
 // in-kernel-conversion schedule: 0 split K by the cost model, 1 stream-K
 // wherever every CTA gets two slices
 std::atomic<int> g_stream_k{0};
 
-int fused_slice(int tile_n) {
+int fused_slice(int tile_n, bool linear) {
   const int s = g_fused_slice.load();
-  return s ? s : tile_n == 64 ? 256 : 128;
+  return s ? s : (tile_n == 64 || linear) ? 256 : 128;
 }
 
 lbgemm_status fail(lbgemm_status st, const char* fmt, ...) {
@@ -778,7 +781,7 @@ lbgemm_status run_tc_fused(DeviceState& d, bool large_b, int tile_n, int64_t M, 
                            int64_t K, const void* A, const void* B, int32_t* C, const float* sx,
                            const float* sw, void* Y, void* ws, cudaStream_t stream) {
   const bool linear = Y != nullptr;
-  TcKernel k = lbg::tc_kernel_ts(tile_n, large_b, linear, fused_slice(tile_n));
+  TcKernel k = lbg::tc_kernel_ts(tile_n, large_b, linear, fused_slice(tile_n, linear));
   if (!k.launch) return fail(LBGEMM_ERR_UNSUPPORTED, "no fused kernel (tile %d)", tile_n);
   // rows of the converted (L) and of the re-encoded (S) operand
   const int64_t rows_l = large_b ? N : M, rows_s = large_b ? M : N;
@@ -832,7 +835,7 @@ lbgemm_status run_tc_fused(DeviceState& d, bool large_b, int tile_n, int64_t M, 
   int32_t* sums = nullptr;
   if (linear && partial) {
     sums = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + enc_bytes(8, rows_s, K));
-    k = lbg::tc_kernel_ts(tile_n, large_b, false, fused_slice(tile_n));
+    k = lbg::tc_kernel_ts(tile_n, large_b, false, fused_slice(tile_n, true));
     if (!k.launch) return fail(LBGEMM_ERR_UNSUPPORTED, "no fused kernel (tile %d)", tile_n);
   }
   int32_t* Cout = sums ? sums : C;
@@ -2064,8 +2067,9 @@ lbgemm_status lbgemm_fused_schedule(int64_t M, int64_t N, int64_t K, int tile_n,
   const bool large_b = linear || N >= M;
   FusedSchedule fs;
   if (linear || large_b || N % 4 == 0)
-    fs = fused_schedule(large_b ? N : M, large_b ? M : N, K, tile_n, fused_slice(tile_n),
-                        linear != 0, sm_count, g_stream_k.load() != 0);
+    fs = fused_schedule(large_b ? N : M, large_b ? M : N, K, tile_n,
+                        fused_slice(tile_n, linear != 0), linear != 0, sm_count,
+                        g_stream_k.load() != 0);
   if (splits) *splits = fs.splits;
   if (stream_pieces) *stream_pieces = fs.stream_pieces;
   return LBGEMM_OK;

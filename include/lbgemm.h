@@ -468,8 +468,9 @@ int lbgemm_get_tail_split(void);
  * elements: each slice costs the kernel's roles a fixed number of barrier
  * operations, and longer slices leave fewer slots in tensor memory (6 or 4
  * slots of 128, 3 or 2 of 256).  0 (the default): 256 for the 64-wide
- * kernel, 128 for the 128-wide one (measured fastest on GB300); 128 or 256:
- * that size for both.  A scheduling choice only: C is the same exact int32
+ * kernel and for the linear layer on the 128-wide one, 128 for the GEMM on
+ * the 128-wide one (measured fastest on GB300); 128 or 256: that size for
+ * both, GEMM and linear layer.  A scheduling choice only: C is the same exact int32
  * result.  Process-wide; affects calls launched afterwards;
  * LBGEMM_ERR_INVALID_ARG for another value. */
 lbgemm_status lbgemm_set_fused_slice(int k_elems);

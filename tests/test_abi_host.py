@@ -613,7 +613,8 @@ def test_fused_schedule_follows_the_stated_model(lib):
                         if linear and M > N:
                             continue
                         for sm in (152, 148):
-                            want = _fused_schedule(M, N, K, tile, linear, sm, 256 if tile == 64 else 128)
+                            want = _fused_schedule(M, N, K, tile, linear, sm,
+                                                   256 if tile == 64 or linear else 128)
                             assert L.lbgemm_fused_schedule(M, N, K, tile, linear, sm) == want, \
                                 (M, N, K, tile, linear, sm)
     # measured on GB300 (152 SMs): 64 x 16384 x 16384 GEMM in 7 pieces (114 ->
@@ -632,10 +633,12 @@ def test_fused_schedule_follows_the_stated_model(lib):
             _fused_schedule(64, 16384, 16384, 64, False, 152, 256, force=True)
     finally:
         L.lbgemm_set_fused_stream_k(0)
-    L.lbgemm_set_fused_slice(256)
+    L.lbgemm_set_fused_slice(128)
     try:
         assert L.lbgemm_fused_schedule(128, 11008, 4096, 128, True) == \
-            _fused_schedule(128, 11008, 4096, 128, True, 152, 256)
+            _fused_schedule(128, 11008, 4096, 128, True, 152, 128)
+        assert L.lbgemm_fused_schedule(512, 4096, 4096, 64) == \
+            _fused_schedule(512, 4096, 4096, 64, False, 152, 128)
     finally:
         L.lbgemm_set_fused_slice(0)
     for bad in [(64, 64, 64, 256, False, 152), (0, 64, 64, 64, False, 152),

@@ -573,6 +573,29 @@ def test_linear_fused_split_k(tile, M, N, K):
         check_linear(got, ref, acc == 0, f"linear split-K tile {tile} {M}x{N}x{K} call {rep}")
 
 
+@pytest.mark.parametrize("slice_k", [128, 256])
+@pytest.mark.parametrize("M,N,K", [(128, 2100, 4096), (200, 1030, 8192), (192, 4100, 2064),
+                                   (300, 9800, 1040)])
+def test_linear_fused_slice_forced(slice_k, M, N, K):
+    """The 128-wide conversion kernel's linear layer with either K slice
+    forced (256 elements is its default for the linear layer, 128 for the
+    GEMM): whole tiles, split and stream-K schedules, a ragged last slice."""
+    X, sx, W, sw = synth.linear_operands(M, N, K, 680 + M + slice_k)
+    X[2, :] = 0
+    ref = oracle.linear(X, sx, W, sw)
+    acc = oracle.gemm(8, X, W, K)
+    L.lbgemm_set_fused_slice(slice_k)
+    try:
+        dY = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device=G().DEV)
+        L.lbgemm_linear_candidate(M, N, K, G().to_dev(X), G().to_dev(sx), G().to_dev(W),
+                                  G().to_dev(sw), dY, L.ROUTE_FUSED, 128)
+        L.lbgemm_device_status()
+    finally:
+        L.lbgemm_set_fused_slice(0)
+    got = dY.float().cpu().numpy().astype(np.float64)
+    check_linear(got, ref, acc == 0, f"linear slice {slice_k} {M}x{N}x{K}")
+
+
 def test_linear_fused_split_k_extremes():
     """Sums of K products of -128 x -128 (2^14 each) summed over K pieces in
     int32: 16384 * 8192 = 2^27, exact in the workspace and in fp32."""
