@@ -1015,12 +1015,13 @@ int route_of(int bits, int64_t M, int64_t N, int64_t K, const void* A, const voi
     if (M <= kStreamMaxSide && stream_ok(M, N, K, A, B)) return LBGEMM_ROUTE_STREAM;
     if (warpmma_ok(M, N, K, A, B)) return LBGEMM_ROUTE_WARPMMA;
     if (fused_route(M, N, K, A, B, tile_n) == 1) {
-      // CTA pairs for the linear layer only past 384 tokens with K >= 8192;
-      // elsewhere the 128-wide tile, K split where the grid is short, is as
-      // fast or faster (measured on GB300: 512 tokens x 11008 x 4096, 92 ->
-      // 72 us; 256 tokens, equal or faster up to 28672 x 8192; but 512 x
-      // 8192 x 28672, 280 against 252 us on the pairs)
-      if (*tile_n == 256 && !(std::min(M, N) > 384 && K >= 8192)) *tile_n = 128;
+      // the linear layer keeps the 128-wide tile where the GEMM would take
+      // CTA pairs: with its 256-element K slices and K shared out where the
+      // grid is short it is faster on every layer measured on GB300 (400-512
+      // tokens: 512 x 28672 x 8192, 230 -> 200 us; 512 x 8192 x 28672, 250 ->
+      // 230 us; 512 x 4096 x 16384, 150 -> 78 us; 256 tokens, equal or faster
+      // up to 28672 x 8192)
+      if (*tile_n == 256) *tile_n = 128;
       *fuse = 1;
       return LBGEMM_ROUTE_FUSED;
     }

@@ -241,9 +241,8 @@ lbgemm_status lbgemm_run_popc(int64_t M, int64_t N, int64_t K, const uint32_t* A
  * kernel that streams W once, M <= 16 (N >= 1024, K <= 4096) on the
  * streaming warp-MMA kernel, M <= 32 on the warp-level fp16 MMA kernel,
  * M <= 512 (with N >= 1024 and N, K as lbgemm_run says) on the kernel that
- * converts W itself (64- or 128-wide tiles; the CTA-pair tile only past 384
- * tokens with K >= 8192 where lbgemm_run takes it; where its tiles would
- * leave most SMs idle or make a fractional number of waves, K is shared out
+ * converts W itself (64-wide tiles up to 64 tokens, else 128-wide, never
+ * the CTA-pair tile; where its tiles would leave most SMs idle or make a fractional number of waves, K is shared out
  * over CTAs (split or stream-K) into int32 sums in library scratch and a
  * second grid scales them into Y), larger M on the tensor-core variant
  * table. */

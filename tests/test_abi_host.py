@@ -214,8 +214,8 @@ def _route8(M, N, K, linear=False):
     if (k16 and lo <= 512 and hi >= 1024 and K >= 512 and (not linear or M <= N)
             and (hi >= 4096 or K >= 8192 or (hi >= 2048 and K >= 4096)
                  or (lo <= 256 and K >= 2048))):
-        # CTA pairs for the linear layer only past 384 rows with K >= 8192
-        pairs = _pairs(lo, hi, K) and (not linear or (lo > 384 and K >= 8192))
+        # the linear layer never on CTA pairs
+        pairs = _pairs(lo, hi, K) and not linear
         return L.ROUTE_FUSED, 64 if lo <= 64 else 256 if pairs else 128
     return L.ROUTE_TABLE, 0
 
