@@ -529,11 +529,13 @@ def test_linear_warpmma_route(M):
 
 
 @pytest.mark.parametrize("M,N,K", [(33, 2100, 4096), (128, 2100, 4096), (300, 2100, 4096),
-                                   (450, 8200, 2048), (40, 2102, 4096), (128, 11008, 4096)])
+                                   (450, 8200, 2048), (40, 2102, 4096), (128, 11008, 4096),
+                                   (400, 8200, 8192)])
 def test_linear_fused_route(M, N, K):
     """Token counts 33..512 in the conversion kernel's domain: the weights are
     converted in the kernel and Y is written transposed from the accumulator
-    (64- and 128-wide tiles by the dispatch, CTA pairs forced with 450 tokens;
+    (64- and 128-wide tiles by the dispatch, also past 384 tokens at K = 8192;
+    CTA pairs forced with 400 and 450 tokens;
     N % 4 != 0 included)."""
     X, sx, W, sw = synth.linear_operands(M, N, K, 600 + M)
     X[1, :] = 0
